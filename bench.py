@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the deterministic Mamba2 SSD backward on GB300.
+
+One step = one backward pass (mamba2_ssd_bwd: every kernel of the backward)
+over the workload's synthetic batch; the forward that produces the saved
+chunk states runs once, untimed.  Default workload: bf16, batch 1, seqlen
+16384, 256 heads of headdim 64, 8 groups, dstate 128, chunk 128 -- the
+long-sequence row of the per-kernel breakdown in "Deterministic bwd kernel
+for mamba2" (Mamba PR #827), with the model dimensions of this library's
+specification.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle instead (on the host cores, bounded samples of the same workload).
+Under torchrun each rank runs an independent replica (the backward does not
+shard across GPUs here): value = all ranks' tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "SSD bwd tokens/s @ seqlen 16K; % of roofline; bitwise repeat over 20 runs"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bf16_T16384")
+    ap.add_argument("--config", type=int, default=0)
+    ap.add_argument("--variant", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------ clocks ----
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------ byte models ----
+def api_bytes(w, es):
+    """Algorithmic bytes of one backward: its API inputs read once and its
+    outputs written once (x, dout, B, C in the input dtype; dt and the saved
+    chunk states fp32; dx, ddt, dB, dC fp32; init/dinit when present)."""
+    b, T, H, P, G, N, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk
+    nc = -(-T // Q)
+    rd = 2 * b * T * H * P * es + 2 * b * T * G * N * es + b * T * H * 4 + b * nc * H * P * N * 4 + 3 * H * 4
+    wr = b * T * H * P * 4 + 2 * b * T * G * N * 4 + b * T * H * 4 + 2 * H * 4
+    if w.with_init:
+        nseq = len(w.seq_lens) if w.seq_lens else b
+        rd += nseq * H * P * N * 4
+        wr += nseq * H * P * N * 4
+    return rd + wr
+
+
+def kernel_bytes(name, w, es):
+    """Algorithmic bytes of one launch of a kernel of the general path: the
+    arrays it must read and write, each once."""
+    b, T, H, P, G, N, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk
+    nc = -(-T // Q)
+    f4 = 4
+    x = b * T * H * P * es
+    bc = b * T * G * N * es
+    dt = b * T * H * f4
+    acs = 2 * b * H * nc * Q * f4
+    qq = b * nc * H * Q * Q * f4
+    cbq = b * nc * G * Q * Q * f4
+    st = b * nc * H * P * N * f4
+    slots = b * T * H * N * f4
+    tab = {
+        "cumsum_fwd": dt + acs,
+        "cb": 2 * bc + cbq,
+        "mwg": 2 * x + cbq + acs + dt + 3 * qq,
+        "dhscan": x + bc + acs + st,
+        "state_passing_bwd": 3 * st + acs,
+        "dx": x + bc + dt + qq + st + acs + b * T * H * P * f4,
+        "dbdc": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * slots,
+        "dbdc_atomic": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * b * T * G * N * f4,
+        "ddt_dacs": 2 * x + 2 * bc + dt + qq + 2 * st + acs + dt + 3 * b * H * nc * Q * f4,
+        "cumsum_bwd": 2 * dt + 4 * b * H * nc * Q * f4,
+        "cumsum_bwd_atomic": 2 * dt + 4 * b * H * nc * Q * f4,
+        "reduce_heads": 2 * slots + 2 * b * T * G * N * f4,
+        "reduce_heads_scalars": 2 * b * nc * H * f4,
+    }
+    return tab.get(name)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------- CPU oracle ----
+def oracle_tokens_per_s(w, sample_tokens, nthreads=None):
+    """Times the fp64 CPU oracle (forward + backward: its backward recomputes
+    the forward) on the first ``sample_tokens`` tokens of the workload, all
+    heads.  Returns (tokens/s, seconds, threads)."""
+    import oracle
+    from deterministic_mamba2_ssd_gb300.inputs import workload_inputs
+    T = min(sample_tokens, w.seqlen)
+    d = workload_inputs(w.name, seqlen=T)
+    if w.with_init:
+        d["init"] = d["init"][:1].contiguous()
+    nt = nthreads or oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], init=d["init"], nthreads=nt)
+    oracle.bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dout"], init=d["init"], nthreads=nt)
+    dt = time.perf_counter() - t0
+    return w.batch * T / dt, dt, nt
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    sample = 256
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, sample)
+    times = []
+    nt = None
+    for _ in range(args.steps):
+        _, dt, nt = oracle_tokens_per_s(w, sample)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = w.batch * min(sample, w.seqlen) / (ms / 1e3)
+    desc = "first %d tokens of the workload, all %d heads, fwd+bwd in fp64 per step" % (min(sample, w.seqlen),
+                                                                                         w.nheads)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": w.seqlen, "global_batch": w.batch,
+                       "sample_tokens_per_step": min(sample, w.seqlen)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------- ours ----
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import __graft_entry__
+    __graft_entry__.build()
+    import deterministic_mamba2_ssd_gb300 as ssd
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS, workload_inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = WORKLOADS[args.workload]
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    d = workload_inputs(w.name)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
+                       seq_idx=g["seq_idx"], init_states=g["init"])
+    out = ssd.bwd(saved, g["dout"], config=args.config, variant=args.variant)
+    ws = torch.empty(max(16, ssd.bwd_workspace_size(saved.dims, args.config, args.variant)), dtype=torch.uint8,
+                     device=dev)
+    names = ssd.bwd_launch_names(saved.dims, args.config, args.variant)
+    nl = len(names)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def new_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)     # materialise the event objects
+        return evs
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        ssd.bwd(saved, g["dout"], config=args.config, variant=args.variant, out=out, workspace=ws)
+    traces = [new_events(2 * nl) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(1.0)   # evict L2 between steps (outside the traced region)
+        ssd.bwd(saved, g["dout"], config=args.config, variant=args.variant, out=out, workspace=ws,
+                events=traces[k])
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    wall = time.perf_counter() - t0
+    clocks = clk.stop()
+
+    step_ms = [traces[k][0].elapsed_time(traces[k][-1]) for k in range(args.steps)]
+    per_kernel = {}
+    for k in range(args.steps):
+        for j, n in enumerate(names):
+            per_kernel.setdefault((j, n), []).append(traces[k][2 * j].elapsed_time(traces[k][2 * j + 1]))
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, dev)
+    tokens = w.batch * w.seqlen
+    value = world * tokens / (ms_max / 1e3)
+
+    # dominant kernel and its roofline
+    tot = {key: sum(v) for key, v in per_kernel.items()}
+    (jdom, ndom), tdom = max(tot.items(), key=lambda kv: kv[1])
+    dom_ms = tdom / args.steps
+    peak, peak_kind = load_peaks()
+    if nl == 1:
+        alg = api_bytes(w, es)
+    else:
+        alg = kernel_bytes(ndom, w, es)
+    achieved = alg / (dom_ms / 1e3) / 1e9 if alg else None
+    shares = {n: round(tot[(j, n)] / sum(tot.values()), 4) for (j, n) in tot}
+
+    # determinism overhead: the same kernels with atomic accumulation
+    atomic_ms = None
+    if not args.no_atomic and args.variant == 0:
+        ws_a = torch.empty(max(16, ssd.bwd_workspace_size(saved.dims, args.config, 1)), dtype=torch.uint8,
+                           device=dev)
+        out_a = {k: torch.empty_like(v) for k, v in out.items()}
+        for _ in range(2):
+            ssd.bwd(saved, g["dout"], config=args.config, variant=1, out=out_a, workspace=ws_a)
+        na = len(ssd.bwd_launch_names(saved.dims, args.config, 1))
+        ta = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            ev = new_events(2 * na)
+            ssd.bwd(saved, g["dout"], config=args.config, variant=1, out=out_a, workspace=ws_a, events=ev)
+            torch.cuda.synchronize()
+            ta.append(ev[0].elapsed_time(ev[-1]))
+        atomic_ms = statistics.mean(ta)
+        del ws_a, out_a
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.pin_memory() for k, v in d.items() if v is not None}
+        host["states"] = saved.states.cpu().pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in out.values())
+        # saved struct that points at the freshly copied device inputs
+        _, saved_e = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
+                             chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"))
+        saved_e.struct.states = dev_in["states"].data_ptr()
+        saved_e.tensors["states"] = dev_in["states"]
+        e_ms = []
+        for k in range(args.warmup + args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for key, v in host.items():
+                dev_in[key].copy_(v, non_blocking=True)
+            ssd.bwd(saved_e, dev_in["dout"], config=args.config, out=out, workspace=ws)
+            for key, v in out.items():
+                host_out[key].copy_(v, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if k >= args.warmup:
+                e_ms.append(e0.elapsed_time(e1))
+        em = max_over_ranks(statistics.mean(e_ms), world, dev)
+        e2e = {"value": world * tokens / (em / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": em}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, secs, nt = oracle_tokens_per_s(w, args.cpu_sample_tokens)
+            cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle",
+                   "sample": "first %d tokens of the workload, all %d heads, fp64 forward+backward, %.1f s" %
+                             (min(args.cpu_sample_tokens, w.seqlen), w.nheads, secs)}
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if es == 2 else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.batch * world, "seq_len": w.seqlen,
+                       "nheads": w.nheads, "headdim": w.headdim, "ngroups": w.ngroups, "dstate": w.dstate,
+                       "chunk_size": w.chunk, "parallelism": "replicas" if world > 1 else "single",
+                       "launch_config": ssd.config_name(saved.dims, args.config),
+                       "l2": "flushed between steps (256 MB write) and inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": ndom, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg, "launch_ms": dom_ms},
+            "bwd_roofline_8TBps_frac": (api_bytes(w, es) / 8e12) / (ms_max / 1e3),
+            "kernel_share": shares,
+            "gpu_launches": nl * args.steps,
+            "deterministic_vs_atomic": {"det_ms": ms_max, "atomic_ms": atomic_ms,
+                                        "overhead": (ms_max / atomic_ms - 1.0) if atomic_ms else None},
+            "wall_s_timed_region": wall,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

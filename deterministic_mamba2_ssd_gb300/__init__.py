@@ -1,0 +1,218 @@
+"""Deterministic Mamba2 SSD chunked scan for GB300 -- thin Python binding.
+
+The compute lives in ``libmamba2_ssd.so`` (hand-written CUDA for sm_103a,
+C ABI declared in ``include/mamba2_ssd.h``).  This module only marshals
+arguments: it checks shapes, allocates outputs and workspace with PyTorch's
+device allocator and passes raw pointers and the current CUDA stream to the
+library.  There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["lib", "fwd", "bwd", "Saved", "SsdError", "make_dims", "num_configs", "config_name",
+           "bwd_workspace_size", "fwd_workspace_size", "bwd_num_launches", "bwd_launch_names", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba2_ssd.so")
+
+SSD_F32, SSD_BF16 = 0, 1
+VARIANT_DETERMINISTIC, VARIANT_ATOMIC = 0, 1
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_ARG", 2: "SSD_ERR_UNSUPPORTED", 3: "SSD_ERR_WORKSPACE",
+          4: "SSD_ERR_CUDA", 5: "SSD_ERR_TIMEOUT", 6: "SSD_ERR_HANDLE"}
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s (%s)" % (what, STATUS.get(status, status),
+                                                   lib().mamba2_ssd_status_string(status).decode()))
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
+                ("chunk_size", ctypes.c_int64), ("nseq", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class SavedStruct(ctypes.Structure):
+    _fields_ = [("dims", Dims)] + [(n, ctypes.c_void_p) for n in
+                                   ("x", "dt", "A", "B", "C", "D", "seq_idx", "init_states", "states")] + \
+               [("magic", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it is absent: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmamba2_ssd.so is not built (run __graft_entry__.build()); "
+                               "this package has no CPU or PyTorch fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, ci, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+        pd = ctypes.POINTER(Dims)
+        L.mamba2_ssd_status_string.argtypes = [ci]
+        L.mamba2_ssd_status_string.restype = ctypes.c_char_p
+        L.mamba2_ssd_num_chunks.argtypes = [pd]
+        L.mamba2_ssd_num_chunks.restype = i64
+        L.mamba2_ssd_fwd_workspace_size.argtypes = [pd]
+        L.mamba2_ssd_fwd_workspace_size.restype = sz
+        L.mamba2_ssd_bwd_workspace_size.argtypes = [pd, ci, ci]
+        L.mamba2_ssd_bwd_workspace_size.restype = sz
+        L.mamba2_ssd_num_configs.argtypes = [pd]
+        L.mamba2_ssd_num_configs.restype = ci
+        L.mamba2_ssd_config_name.argtypes = [pd, ci]
+        L.mamba2_ssd_config_name.restype = ctypes.c_char_p
+        L.mamba2_ssd_bwd_num_launches.argtypes = [pd, ci, ci]
+        L.mamba2_ssd_bwd_num_launches.restype = ci
+        L.mamba2_ssd_fwd.argtypes = [pd] + [vp] * 10 + [vp, sz, vp, ctypes.POINTER(SavedStruct)]
+        L.mamba2_ssd_fwd.restype = ci
+        L.mamba2_ssd_bwd.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 9 + [sz, ci, ci, vp]
+        L.mamba2_ssd_bwd.restype = ci
+        L.mamba2_ssd_bwd_traced.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 9 + [sz, ci, ci, vp, vp, ci]
+        L.mamba2_ssd_bwd_traced.restype = ci
+        L.mamba2_ssd_bwd_launch_name.argtypes = [pd, ci, ci, ci]
+        L.mamba2_ssd_bwd_launch_name.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseq=None, dtype=torch.bfloat16):
+    return Dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
+                batch if nseq is None else nseq, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32, 0)
+
+
+def num_configs(dims: Dims) -> int:
+    return lib().mamba2_ssd_num_configs(ctypes.byref(dims))
+
+
+def config_name(dims: Dims, config: int) -> str:
+    return lib().mamba2_ssd_config_name(ctypes.byref(dims), config).decode()
+
+
+def fwd_workspace_size(dims: Dims) -> int:
+    return lib().mamba2_ssd_fwd_workspace_size(ctypes.byref(dims))
+
+
+def bwd_workspace_size(dims: Dims, config: int = 0, variant: int = 0) -> int:
+    return lib().mamba2_ssd_bwd_workspace_size(ctypes.byref(dims), config, variant)
+
+
+def bwd_num_launches(dims: Dims, config: int = 0, variant: int = 0) -> int:
+    return lib().mamba2_ssd_bwd_num_launches(ctypes.byref(dims), config, variant)
+
+
+def bwd_launch_names(dims: Dims, config: int = 0, variant: int = 0):
+    n = bwd_num_launches(dims, config, variant)
+    return [lib().mamba2_ssd_bwd_launch_name(ctypes.byref(dims), config, variant, k).decode() for k in range(n)]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        raise ValueError("%s is required" % name)
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() or t.device != device:
+        raise ValueError("%s: expected contiguous %s %s on %s, got %s %s %s" %
+                         (name, tuple(shape), dtype, device, tuple(t.shape), t.dtype, t.device))
+
+
+class Saved:
+    """What the backward needs: the filled C struct plus references that keep
+    the borrowed tensors (inputs and chunk states) alive."""
+
+    def __init__(self, struct, tensors, dims):
+        self.struct = struct
+        self.tensors = tensors
+        self.dims = dims
+
+    @property
+    def states(self):
+        return self.tensors["states"]
+
+
+def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=None):
+    """Forward.  Returns (y, saved).  x (b,T,H,P) and B, C (b,T,G,N) in
+    bf16 or fp32; dt (b,T,H), A (H), D (H), init_states (nseq,H,P,N) fp32;
+    seq_idx (1,T) int32 with chunk-aligned sequence starts."""
+    b, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    if x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be bf16 or fp32")
+    nseq = init_states.shape[0] if init_states is not None else (
+        int(seq_idx.max().item()) + 1 if seq_idx is not None else b)
+    _check(x, "x", (b, T, H, P), x.dtype, dev)
+    _check(dt, "dt", (b, T, H), torch.float32, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(B, "B", (b, T, G, N), x.dtype, dev)
+    _check(C, "C", (b, T, G, N), x.dtype, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    if seq_idx is not None:
+        _check(seq_idx, "seq_idx", (b, T), torch.int32, dev)
+    if init_states is not None:
+        _check(init_states, "init_states", (nseq, H, P, N), torch.float32, dev)
+    dims = make_dims(b, T, H, P, G, N, chunk_size, nseq, x.dtype)
+    nc = lib().mamba2_ssd_num_chunks(ctypes.byref(dims))
+    if nc < 0:
+        raise ValueError("invalid dims")
+    y = torch.empty_like(x)
+    states = torch.empty((b, nc, H, P, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, fwd_workspace_size(dims)), dtype=torch.uint8, device=dev)
+    sv = SavedStruct()
+    rc = lib().mamba2_ssd_fwd(ctypes.byref(dims), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              _ptr(seq_idx), _ptr(init_states), _ptr(y), _ptr(states), _ptr(ws), ws.numel(),
+                              _stream(stream), ctypes.byref(sv))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_fwd")
+    keep = dict(x=x, dt=dt, A=A, B=B, C=C, D=D, seq_idx=seq_idx, init=init_states, states=states, ws=ws)
+    return y, Saved(sv, keep, dims)
+
+
+def bwd(saved: Saved, dout, config: int = 0, variant: int = VARIANT_DETERMINISTIC, stream=None, out=None,
+        workspace=None, events=None):
+    """Backward of sum(y * dout).  Returns dict of fp32 tensors dx, ddt, dA,
+    dB, dC, dD (and dinit when the forward had initial states).  ``out`` may
+    supply preallocated outputs and ``workspace`` a uint8 buffer."""
+    t = saved.tensors
+    x = t["x"]
+    dev = x.device
+    _check(dout, "dout", tuple(x.shape), x.dtype, dev)
+    if out is None:
+        out = dict(dx=torch.empty(x.shape, dtype=torch.float32, device=dev),
+                   ddt=torch.empty(t["dt"].shape, dtype=torch.float32, device=dev),
+                   dA=torch.empty(t["A"].shape, dtype=torch.float32, device=dev),
+                   dB=torch.empty(t["B"].shape, dtype=torch.float32, device=dev),
+                   dC=torch.empty(t["C"].shape, dtype=torch.float32, device=dev),
+                   dD=torch.empty(t["D"].shape, dtype=torch.float32, device=dev))
+        if t["init"] is not None:
+            out["dinit"] = torch.empty(t["init"].shape, dtype=torch.float32, device=dev)
+    need = bwd_workspace_size(saved.dims, config, variant)
+    if workspace is None:
+        workspace = torch.empty(max(16, need), dtype=torch.uint8, device=dev)
+    args = (ctypes.byref(saved.struct), _ptr(dout), _ptr(out["dx"]), _ptr(out["ddt"]), _ptr(out["dA"]),
+            _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]), _ptr(out.get("dinit")), _ptr(workspace),
+            workspace.numel(), config, variant, _stream(stream))
+    if events is None:
+        rc = lib().mamba2_ssd_bwd(*args)
+    else:
+        # events: recorded torch.cuda.Event objects (enable_timing=True)
+        arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        rc = lib().mamba2_ssd_bwd_traced(*args, arr, len(events))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_bwd")
+    return out

@@ -1,0 +1,186 @@
+// ssd_api.cu -- the C ABI: argument checks, launch-configuration table,
+// workspace sizing and dispatch to the kernel families.  Nothing here
+// allocates device memory or synchronises (except the documented seq_idx
+// check in the forward).
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "mamba2_ssd.h"
+#include "ssd_internal.h"
+
+namespace {
+
+constexpr uint32_t kSavedMagic = 0x53534432u;  // "SSD2"
+
+bool dims_ok(const ssd_dims *d) {
+  if (!d) return false;
+  if (d->batch <= 0 || d->seqlen <= 0 || d->nheads <= 0 || d->headdim <= 0 || d->ngroups <= 0 || d->dstate <= 0 ||
+      d->chunk_size <= 0 || d->nseq <= 0)
+    return false;
+  if (d->nheads % d->ngroups != 0) return false;
+  if (d->dtype != SSD_F32 && d->dtype != SSD_BF16) return false;
+  if (d->reserved != 0) return false;
+  if (d->chunk_size > 1024) return false;
+  const int64_t nc = (d->seqlen + d->chunk_size - 1) / d->chunk_size;
+  if (d->batch * nc * d->nheads > (int64_t(1) << 31) - 1) return false;
+  return true;
+}
+
+ssd::Shape shape_of(const ssd_dims *d) {
+  ssd::Shape s;
+  s.b = d->batch;
+  s.T = d->seqlen;
+  s.H = d->nheads;
+  s.P = d->headdim;
+  s.G = d->ngroups;
+  s.N = d->dstate;
+  s.Q = d->chunk_size;
+  s.nc = (d->seqlen + d->chunk_size - 1) / d->chunk_size;
+  s.hpg = d->nheads / d->ngroups;
+  s.nseq = d->nseq;
+  return s;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch configurations of the general path: block sizes only.  Each output
+// element is computed by one thread in one fixed order, so all of them give
+// the same bits.
+constexpr int kSimtBlocks[] = {256, 128};
+constexpr int kNumSimt = 2;
+
+}  // namespace
+
+extern "C" {
+
+const char *mamba2_ssd_status_string(int status) {
+  switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_ARG: return "invalid argument";
+    case SSD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SSD_ERR_WORKSPACE: return "workspace too small";
+    case SSD_ERR_CUDA: return "CUDA error";
+    case SSD_ERR_TIMEOUT: return "device-side wait timed out";
+    case SSD_ERR_HANDLE: return "invalid saved struct";
+    default: return "unknown status";
+  }
+}
+
+int64_t mamba2_ssd_num_chunks(const ssd_dims *dims) {
+  if (!dims_ok(dims)) return -1;
+  return (dims->seqlen + dims->chunk_size - 1) / dims->chunk_size;
+}
+
+size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
+  if (!dims_ok(dims)) return 0;
+  return ssd::simt_fwd_workspace(shape_of(dims));
+}
+
+int mamba2_ssd_num_configs(const ssd_dims *dims) {
+  if (!dims_ok(dims)) return 0;
+  return kNumSimt;
+}
+
+const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
+  if (!dims_ok(dims) || config < 0 || config >= kNumSimt) return "invalid";
+  return config == 0 ? "simt/block256" : "simt/block128";
+}
+
+size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant) {
+  if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
+  if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC) return 0;
+  return ssd::simt_bwd_workspace(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
+}
+
+int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
+  if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
+  return ssd::simt_bwd_launches(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
+}
+
+const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
+  if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
+  return ssd::simt_bwd_launch_name(variant == SSD_VARIANT_ATOMIC, k);
+}
+
+ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
+                          const void *C, const float *D, const int32_t *seq_idx, const float *init_states, void *y,
+                          float *states, void *workspace, size_t workspace_bytes, void *stream,
+                          ssd_saved *saved_out) {
+  if (!dims_ok(dims) || !saved_out) return SSD_ERR_INVALID_ARG;
+  const void *req[] = {x, dt, A, B, C, D, y, states};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if ((seq_idx && !aligned16(seq_idx)) || (init_states && !aligned16(init_states))) return SSD_ERR_INVALID_ARG;
+  if (!seq_idx && dims->nseq != dims->batch) return SSD_ERR_INVALID_ARG;
+  const ssd::Shape s = shape_of(dims);
+  const size_t need = ssd::simt_fwd_workspace(s);
+  if (workspace_bytes < need) return SSD_ERR_WORKSPACE;
+  if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (seq_idx) {
+    // The chunked kernels reset the state at chunk starts only; check that
+    // every sequence start falls on one.  One synchronous copy, documented.
+    if (dims->batch != 1) return SSD_ERR_UNSUPPORTED;
+    std::vector<int32_t> h(size_t(s.T));
+    if (cudaMemcpyAsync(h.data(), seq_idx, size_t(s.T) * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return SSD_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+    for (int64_t t = 0; t < s.T; ++t) {
+      if (h[t] < 0 || h[t] >= dims->nseq) return SSD_ERR_INVALID_ARG;
+      if (t > 0 && h[t] < h[t - 1]) return SSD_ERR_INVALID_ARG;
+      if (t > 0 && h[t] != h[t - 1] && t % s.Q != 0) return SSD_ERR_UNSUPPORTED;
+    }
+  }
+  ssd::Args a{};
+  a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.D = D;
+  a.init = init_states; a.seq_idx = seq_idx; a.y = y; a.states_out = states;
+  if (ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st) != cudaSuccess) return SSD_ERR_CUDA;
+  saved_out->dims = *dims;
+  saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
+  saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;
+  saved_out->magic = kSavedMagic;
+  saved_out->flags = 0;
+  return SSD_OK;
+}
+
+ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
+                                 float *dB, float *dC, float *dD, float *dinit, void *workspace,
+                                 size_t workspace_bytes, int config, int variant, void *stream,
+                                 void *const *events, int num_events) {
+  if (!saved || saved->magic != kSavedMagic || !dims_ok(&saved->dims)) return SSD_ERR_HANDLE;
+  const ssd_dims *dims = &saved->dims;
+  const void *req[] = {saved->x, saved->dt, saved->A, saved->B, saved->C, saved->D, saved->states,
+                       dout, dx, ddt, dA, dB, dC, dD};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if (dinit && (!aligned16(dinit) || !saved->init_states)) return SSD_ERR_INVALID_ARG;
+  if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC) return SSD_ERR_INVALID_ARG;
+  if (config < 0 || config >= mamba2_ssd_num_configs(dims)) return SSD_ERR_INVALID_ARG;
+  const ssd::Shape s = shape_of(dims);
+  const bool atomic = variant == SSD_VARIANT_ATOMIC;
+  if (workspace_bytes < ssd::simt_bwd_workspace(s, atomic)) return SSD_ERR_WORKSPACE;
+  if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
+  ssd::Args a{};
+  a.x = saved->x; a.B = saved->B; a.C = saved->C; a.dout = dout;
+  a.dt = saved->dt; a.A = saved->A; a.D = saved->D; a.init = saved->init_states; a.states_in = saved->states;
+  a.seq_idx = saved->seq_idx;
+  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dinit = dinit;
+  if (num_events < 0 || (num_events > 0 && !events)) return SSD_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ssd::Trace tr;
+  tr.events = reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events));
+  tr.count = num_events;
+  if (ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], atomic, st, tr) != cudaSuccess)
+    return SSD_ERR_CUDA;
+  return SSD_OK;
+}
+
+ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA, float *dB,
+                          float *dC, float *dD, float *dinit, void *workspace, size_t workspace_bytes, int config,
+                          int variant, void *stream) {
+  return mamba2_ssd_bwd_traced(saved, dout, dx, ddt, dA, dB, dC, dD, dinit, workspace, workspace_bytes, config,
+                               variant, stream, nullptr, 0);
+}
+
+}  // extern "C"

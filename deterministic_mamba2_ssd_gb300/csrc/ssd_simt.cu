@@ -1,0 +1,633 @@
+// ssd_simt.cu -- general CUDA-core path of the Mamba2 SSD forward and
+// backward (any shape, fp32 or bf16 inputs, chunk-aligned sequence starts).
+//
+// Each kernel is one step of the chunked algorithm whose backward "Deterministic
+// bwd kernel for mamba2" (Mamba PR #827) breaks down per kernel:
+// chunk_cumsum, chunk_state, state passing, chunk_scan and their backward
+// counterparts.  Every output element is produced by exactly one thread that
+// sums its terms sequentially in a fixed order, so the result does not depend
+// on the block size (the launch configuration) or on scheduling.  Per-head
+// contributions to the group-shared dB/dC, and per-chunk contributions to dA
+// and dD, are parked in slots and folded in ascending slot order by the
+// reduction kernels at the end (unless the atomic variant is requested).
+//
+// Notation per (batch b, chunk c, head h): local token i in [0, Lc), Lc the
+// chunk's length; Acs_i the in-chunk inclusive prefix sum of dt*A (hi+lo);
+// E = Acs_{Lc-1}; g = dout.  States are (P, N), n fastest.
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+
+namespace ssd {
+
+namespace {
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- cumsum --
+// Acs (b,H,nc,Q) as hi + lo: left-to-right compensated (two-sum) prefix sum
+// of a_i = dt_i * A_h, one thread per (b, c, h), entries past the chunk end
+// padded with the last value.  One fixed order for every launch shape.
+__global__ void cumsum_fwd_kernel(Shape s, const float *__restrict__ dt, const float *__restrict__ A,
+                                  float *__restrict__ acs_hi, float *__restrict__ acs_lo) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.nc * s.H) return;
+  const int64_t h = idx % s.H, c = (idx / s.H) % s.nc, bi = idx / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const float Ah = A[h];
+  float hi = 0.f, lo = 0.f;
+  float *oh = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  float *ol = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  for (int64_t i = 0; i < s.Q; ++i) {
+    if (i < Lc) {
+      const float a = __fmul_rn(dt[(bi * s.T + t0 + i) * s.H + h], Ah);
+      const float sum = __fadd_rn(hi, a);
+      const float bb = __fsub_rn(sum, hi);
+      const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(sum, bb)), __fsub_rn(a, bb));
+      hi = sum;
+      lo = __fadd_rn(lo, err);
+    }
+    oh[i] = hi;
+    ol[i] = lo;
+  }
+}
+
+// ------------------------------------------------------ chunk_state (fwd) --
+// S[b,c,h,p,n] = sum_i exp(E - Acs_i) dt_i x_i[p] B_i[n]; one thread per (p,n).
+template <class TIn>
+__global__ void chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Bm,
+                                       const float *__restrict__ dt, const float *__restrict__ acs_hi,
+                                       const float *__restrict__ acs_lo, float *__restrict__ S) {
+  extern __shared__ float w[];
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x)
+    w[i] = __fmul_rn(expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])), dt[(bi * s.T + t0 + i) * s.H + h]);
+  __syncthreads();
+  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (e >= s.P * s.N) return;
+  const int64_t p = e / s.N, n = e % s.N;
+  float acc = 0.f;
+  for (int64_t i = 0; i < Lc; ++i) {
+    const int64_t t = t0 + i;
+    acc = fmaf(w[i] * ld(x + ((bi * s.T + t) * s.H + h) * s.P + p), ld(Bm + ((bi * s.T + t) * s.G + g) * s.N + n), acc);
+  }
+  S[(((bi * s.nc + c) * s.H + h) * s.P + p) * s.N + n] = acc;
+}
+
+// ------------------------------------------------ state passing (fwd) --
+// states[b,c] = state entering chunk c: init/zero where chunk c starts a
+// sequence, else exp(E_{c-1}) states[b,c-1] + S[b,c-1]. One thread per (b,h,e).
+__global__ void state_passing_fwd_kernel(Shape s, const float *__restrict__ S, const float *__restrict__ acs_hi,
+                                         const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                                         const float *__restrict__ init, float *__restrict__ states) {
+  const int64_t PN = s.P * s.N;
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.H * PN) return;
+  const int64_t e = idx % PN, h = (idx / PN) % s.H, bi = idx / (PN * s.H);
+  float run = 0.f;
+  for (int64_t c = 0; c < s.nc; ++c) {
+    const int64_t t0 = c * s.Q;
+    if (is_seq_start(seq_idx, bi, s.T, t0))
+      run = init ? init[(seq_of(seq_idx, bi, s.T, t0) * s.H + h) * PN + e] : 0.f;
+    const int64_t o = ((bi * s.nc + c) * s.H + h) * PN + e;
+    states[o] = run;
+    const int64_t q = ((bi * s.H + h) * s.nc + c) * s.Q + (s.Q - 1);
+    run = fmaf(expf(__fadd_rn(acs_hi[q], acs_lo[q])), run, S[o]);
+  }
+}
+
+// -------------------------------------------------------------- C . B^T --
+// CB[b,c,g,i,j] = C_i . B_j for j <= i < Lc, else 0.  One thread per (i,j).
+template <class TIn>
+__global__ void cb_kernel(Shape s, const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, float *__restrict__ CB) {
+  const int64_t unit = blockIdx.x;  // (b, c, g)
+  const int64_t g = unit % s.G, c = (unit / s.G) % s.nc, bi = unit / (s.G * s.nc);
+  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (e >= s.Q * s.Q) return;
+  const int64_t i = e / s.Q, j = e % s.Q;
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  float acc = 0.f;
+  if (j <= i && i < Lc) {
+    const TIn *ci = Cm + ((bi * s.T + t0 + i) * s.G + g) * s.N;
+    const TIn *bj = Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N;
+    for (int64_t n = 0; n < s.N; ++n) acc = fmaf(ld(ci + n), ld(bj + n), acc);
+  }
+  CB[((bi * s.nc + c) * s.G + g) * s.Q * s.Q + e] = acc;
+}
+
+// ------------------------------------------------------- chunk_scan (fwd) --
+// y_i[p] = sum_{j<=i} CB[i,j] exp(Acs_i - Acs_j) dt_j x_j[p]
+//        + exp(Acs_i) sum_n states[p,n] C_i[n] + D x_i[p].  One thread per (b,t,h,p).
+template <class TIn>
+__global__ void chunk_scan_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Cm,
+                                      const float *__restrict__ dt, const float *__restrict__ D,
+                                      const float *__restrict__ CB, const float *__restrict__ acs_hi,
+                                      const float *__restrict__ acs_lo, const float *__restrict__ states,
+                                      TIn *__restrict__ y) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.T * s.H * s.P) return;
+  const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
+  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, g = h / s.hpg;
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *cb = CB + (((bi * s.nc + c) * s.G + g) * s.Q + i) * s.Q;
+  float acc = 0.f;
+  for (int64_t j = 0; j <= i; ++j) {
+    const float wgt = cb[j] * expf(acs_diff(ah[i], al[i], ah[j], al[j])) * dt[(bi * s.T + t0 + j) * s.H + h];
+    acc = fmaf(wgt, ld(x + ((bi * s.T + t0 + j) * s.H + h) * s.P + p), acc);
+  }
+  const float *hs = states + (((bi * s.nc + c) * s.H + h) * s.P + p) * s.N;
+  const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
+  float inter = 0.f;
+  for (int64_t n = 0; n < s.N; ++n) inter = fmaf(hs[n], ld(ci + n), inter);
+  const float xv = ld(x + idx);
+  const float out = fmaf(expf(__fadd_rn(ah[i], al[i])), inter, acc) + D[h] * xv;
+  st(y + idx, out);
+}
+
+// ============================================================ backward ====
+
+// Per (b,c,h,i,j) with j <= i < Lc:  L = exp(Acs_i - Acs_j), Gx = g_i . x_j,
+// M = CB[i,j] L, W = L Gx dt_j, MG = M Gx; zero elsewhere.
+template <class TIn>
+__global__ void mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
+                           const float *__restrict__ dt, const float *__restrict__ CB,
+                           const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                           float *__restrict__ Mm, float *__restrict__ Wm, float *__restrict__ MGm) {
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (e >= s.Q * s.Q) return;
+  const int64_t i = e / s.Q, j = e % s.Q;
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  float M = 0.f, W = 0.f, MG = 0.f;
+  if (j <= i && i < Lc) {
+    const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+    const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+    const float L = expf(acs_diff(ah[i], al[i], ah[j], al[j]));
+    const TIn *gi = dout + ((bi * s.T + t0 + i) * s.H + h) * s.P;
+    const TIn *xj = x + ((bi * s.T + t0 + j) * s.H + h) * s.P;
+    float gx = 0.f;
+    for (int64_t p = 0; p < s.P; ++p) gx = fmaf(ld(gi + p), ld(xj + p), gx);
+    const float cbv = CB[(((bi * s.nc + c) * s.G + g) * s.Q + i) * s.Q + j];
+    M = cbv * L;
+    W = L * gx * dt[(bi * s.T + t0 + j) * s.H + h];
+    MG = M * gx;
+  }
+  const int64_t o = unit * s.Q * s.Q + e;
+  Mm[o] = M;
+  Wm[o] = W;
+  MGm[o] = MG;
+}
+
+// dHscan[b,c,h,p,n] = sum_i exp(Acs_i) g_i[p] C_i[n]; one thread per (p,n).
+template <class TIn>
+__global__ void dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Cm,
+                              const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                              float *__restrict__ dH) {
+  extern __shared__ float ea[];
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x) ea[i] = expf(__fadd_rn(ah[i], al[i]));
+  __syncthreads();
+  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
+  if (e >= s.P * s.N) return;
+  const int64_t p = e / s.N, n = e % s.N;
+  float acc = 0.f;
+  for (int64_t i = 0; i < Lc; ++i) {
+    const int64_t t = t0 + i;
+    acc = fmaf(ea[i] * ld(dout + ((bi * s.T + t) * s.H + h) * s.P + p), ld(Cm + ((bi * s.T + t) * s.G + g) * s.N + n), acc);
+  }
+  dH[(((bi * s.nc + c) * s.H + h) * s.P + p) * s.N + n] = acc;
+}
+
+// Fixed-shape block sum: each warp folds by xor-shuffle, then warp sums are
+// added in warp order by thread 0.  Same tree for every call.
+__device__ float block_sum(float v, float *red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float tot = 0.f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) tot += red[w];
+  return tot;  // valid in thread 0
+}
+
+// Reverse state passing, one CTA per (b,h), in place on buf:
+//   in:  buf[c] = dHscan_c;  out: buf[c] = dS_c = gradient reaching the end
+//   state of chunk c (dH_{c+1}, or 0 where chunk c+1 starts a sequence);
+//   dH_c = dHscan_c + exp(E_c) dS_c; dEpass[b,h,c] = exp(E_c) <states_c, dS_c>;
+//   dinit[seq] += dH_c where chunk c starts a sequence.
+__global__ void state_passing_bwd_kernel(Shape s, float *__restrict__ buf, float *__restrict__ carry,
+                                         const float *__restrict__ states, const float *__restrict__ acs_hi,
+                                         const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                                         float *__restrict__ dEpass, float *__restrict__ dinit) {
+  __shared__ float red[32];
+  const int64_t h = blockIdx.x % s.H, bi = blockIdx.x / s.H;
+  const int64_t PN = s.P * s.N;
+  float *cr = carry + (bi * s.H + h) * PN;
+  for (int64_t c = s.nc - 1; c >= 0; --c) {
+    const bool nxt_start = (c + 1 >= s.nc) || is_seq_start(seq_idx, bi, s.T, (c + 1) * s.Q);
+    const bool here_start = is_seq_start(seq_idx, bi, s.T, c * s.Q);
+    const int64_t q = ((bi * s.H + h) * s.nc + c) * s.Q + (s.Q - 1);
+    const float eE = expf(__fadd_rn(acs_hi[q], acs_lo[q]));
+    float *bc = buf + ((bi * s.nc + c) * s.H + h) * PN;
+    const float *hc = states + ((bi * s.nc + c) * s.H + h) * PN;
+    float *di = (here_start && dinit) ? dinit + (seq_of(seq_idx, bi, s.T, c * s.Q) * s.H + h) * PN : nullptr;
+    float part = 0.f;
+    for (int64_t e = threadIdx.x; e < PN; e += blockDim.x) {
+      const float cur = nxt_start ? 0.f : cr[e];
+      const float dh = bc[e];
+      bc[e] = cur;
+      part = fmaf(hc[e], cur, part);
+      const float dHc = fmaf(eE, cur, dh);
+      cr[e] = dHc;
+      if (di) di[e] += dHc;
+    }
+    const float tot = block_sum(part, red);
+    if (threadIdx.x == 0) dEpass[(bi * s.H + h) * s.nc + c] = eE * tot;
+  }
+}
+
+// dx_i[p] = dt_i sum_{j>=i} M[j,i] g_j[p] + w_i sum_n B_i[n] dS[p,n] + D g_i[p],
+// w_i = exp(E - Acs_i) dt_i.  One thread per (b,t,h,p).
+template <class TIn>
+__global__ void dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
+                          const float *__restrict__ dt, const float *__restrict__ D, const float *__restrict__ Mm,
+                          const float *__restrict__ dS, const float *__restrict__ acs_hi,
+                          const float *__restrict__ acs_lo, float *__restrict__ dx) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.T * s.H * s.P) return;
+  const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
+  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const int64_t unit = (bi * s.nc + c) * s.H + h;
+  const float *M = Mm + unit * s.Q * s.Q;
+  float d1 = 0.f;
+  for (int64_t j = i; j < Lc; ++j) d1 = fmaf(M[j * s.Q + i], ld(dout + ((bi * s.T + t0 + j) * s.H + h) * s.P + p), d1);
+  const float *ds = dS + (unit * s.P + p) * s.N;
+  const TIn *bi_ = Bm + ((bi * s.T + t) * s.G + g) * s.N;
+  float y = 0.f;
+  for (int64_t n = 0; n < s.N; ++n) y = fmaf(ld(bi_ + n), ds[n], y);
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float dti = dt[(bi * s.T + t) * s.H + h];
+  const float wi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
+  dx[idx] = fmaf(dti, d1, fmaf(wi, y, D[h] * ld(dout + idx)));
+}
+
+// Per-head dB / dC rows, one thread per (b,t,h,n):
+//   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + exp(Acs_i) sum_p states[p,n] g_i[p]
+//   dB_h[i,n] = sum_{j>=i} W[j,i] C_j[n] + w_i sum_p dS[p,n] x_i[p]
+// Deterministic variant: written to per-head slots (b,T,H,N); atomic
+// variant: added into dB/dC (b,T,G,N) with atomics.
+template <class TIn, bool kAtomic>
+__global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
+                            const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, const float *__restrict__ dt,
+                            const float *__restrict__ Wm, const float *__restrict__ states,
+                            const float *__restrict__ dS, const float *__restrict__ acs_hi,
+                            const float *__restrict__ acs_lo, float *__restrict__ dBo, float *__restrict__ dCo) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.T * s.H * s.N) return;
+  const int64_t n = idx % s.N, h = (idx / s.N) % s.H, t = (idx / (s.N * s.H)) % s.T, bi = idx / (s.N * s.H * s.T);
+  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const int64_t unit = (bi * s.nc + c) * s.H + h;
+  const float *W = Wm + unit * s.Q * s.Q;
+  float dc = 0.f, db = 0.f;
+  for (int64_t j = 0; j <= i; ++j) dc = fmaf(W[i * s.Q + j], ld(Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), dc);
+  for (int64_t j = i; j < Lc; ++j) db = fmaf(W[j * s.Q + i], ld(Cm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), db);
+  const float *hs = states + unit * s.P * s.N + n;
+  const float *ds = dS + unit * s.P * s.N + n;
+  const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
+  const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
+  float hg = 0.f, sx = 0.f;
+  for (int64_t p = 0; p < s.P; ++p) {
+    hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+    sx = fmaf(ds[p * s.N], ld(xi + p), sx);
+  }
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float wi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
+  dc = fmaf(expf(__fadd_rn(ah[i], al[i])), hg, dc);
+  db = fmaf(wi, sx, db);
+  if (kAtomic) {
+    const int64_t o = ((bi * s.T + t) * s.G + g) * s.N + n;
+    atomicAdd(dBo + o, db);
+    atomicAdd(dCo + o, dc);
+  } else {
+    dBo[idx] = db;
+    dCo[idx] = dc;
+  }
+}
+
+// Per token (b,c,h,i): the dt-weight part of ddt and the gradient reaching
+// Acs_i, before the reverse cumsum:
+//   ddt_part = sum_{j>=i} MG[j,i] + exp(E - Acs_i) sx_i
+//   dAcs_i   = sum_{j<i} MG[i,j] dt_j - dt_i sum_{j>i} MG[j,i]
+//            + exp(Acs_i) g_i . (states C_i) - u_i,   u_i = w_i sx_i
+// with sx_i = x_i . (dS B_i).  Also gx_i = g_i . x_i for dD.
+template <class TIn>
+__global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
+                                const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
+                                const float *__restrict__ dt, const float *__restrict__ MGm,
+                                const float *__restrict__ states, const float *__restrict__ dS,
+                                const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                                float *__restrict__ ddt_part, float *__restrict__ dAcs, float *__restrict__ u_buf,
+                                float *__restrict__ gx_buf) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.H * s.nc * s.Q) return;
+  const int64_t i = idx % s.Q, c = (idx / s.Q) % s.nc, h = (idx / (s.Q * s.nc)) % s.H, bi = idx / (s.Q * s.nc * s.H);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg, t = t0 + i;
+  if (i >= Lc) {
+    dAcs[idx] = 0.f;
+    u_buf[idx] = 0.f;
+    gx_buf[idx] = 0.f;
+    return;
+  }
+  const int64_t unit = (bi * s.nc + c) * s.H + h;
+  const float *MG = MGm + unit * s.Q * s.Q;
+  const float *dtc = dt + (bi * s.T + t0) * s.H + h;  // dtc[j * H]
+  float col = 0.f, row = 0.f;
+  const float diag = MG[i * s.Q + i];
+  for (int64_t j = i + 1; j < Lc; ++j) col += MG[j * s.Q + i];
+  for (int64_t j = 0; j < i; ++j) row = fmaf(MG[i * s.Q + j], dtc[j * s.H], row);
+  const float dti = dtc[i * s.H];
+  const float *hs = states + unit * s.P * s.N;
+  const float *ds = dS + unit * s.P * s.N;
+  const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
+  const TIn *b_i = Bm + ((bi * s.T + t) * s.G + g) * s.N;
+  const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
+  const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
+  float inter = 0.f, sx = 0.f, gx = 0.f;
+  for (int64_t p = 0; p < s.P; ++p) {
+    float hc = 0.f, dsb = 0.f;
+    for (int64_t n = 0; n < s.N; ++n) {
+      hc = fmaf(hs[p * s.N + n], ld(ci + n), hc);
+      dsb = fmaf(ds[p * s.N + n], ld(b_i + n), dsb);
+    }
+    const float gp = ld(gi + p), xp = ld(xi + p);
+    inter = fmaf(gp, hc, inter);
+    sx = fmaf(xp, dsb, sx);
+    gx = fmaf(gp, xp, gx);
+  }
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float eEi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i]));
+  const float u = eEi * dti * sx;
+  ddt_part[(bi * s.T + t) * s.H + h] = (col + diag) + eEi * sx;
+  dAcs[idx] = row - dti * col + expf(__fadd_rn(ah[i], al[i])) * inter - u;
+  u_buf[idx] = u;
+  gx_buf[idx] = gx;
+}
+
+// Reverse in-chunk cumsum, one thread per (b,c,h), sequential in one fixed
+// order: dAcs_{Lc-1} += sum_i u_i + dEpass; da_i = sum_{k>=i} dAcs_k;
+// ddt_i = ddt_part_i + A da_i; per-chunk partials dA = sum_i dt_i da_i and
+// dD = sum_i gx_i (slot (b,c,h)), or atomics in the atomic variant.
+template <bool kAtomic>
+__global__ void cumsum_bwd_kernel(Shape s, const float *__restrict__ dt, const float *__restrict__ A,
+                                  const float *__restrict__ dAcs, const float *__restrict__ u_buf,
+                                  const float *__restrict__ gx_buf, const float *__restrict__ dEpass,
+                                  const float *__restrict__ ddt_part, float *__restrict__ ddt,
+                                  float *__restrict__ dA_part, float *__restrict__ dD_part) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.nc * s.H) return;
+  const int64_t h = idx % s.H, c = (idx / s.H) % s.nc, bi = idx / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const int64_t base = ((bi * s.H + h) * s.nc + c) * s.Q;
+  float su = 0.f, sg = 0.f;
+  for (int64_t i = 0; i < Lc; ++i) {
+    su += u_buf[base + i];
+    sg += gx_buf[base + i];
+  }
+  const float Ah = A[h];
+  float da = su + dEpass[(bi * s.H + h) * s.nc + c];
+  float dAp = 0.f;
+  for (int64_t i = Lc - 1; i >= 0; --i) {
+    da += dAcs[base + i];
+    const int64_t o = (bi * s.T + t0 + i) * s.H + h;
+    ddt[o] = fmaf(Ah, da, ddt_part[o]);
+    dAp = fmaf(dt[o], da, dAp);
+  }
+  if (kAtomic) {
+    atomicAdd(dA_part + h, dAp);
+    atomicAdd(dD_part + h, sg);
+  } else {
+    dA_part[idx] = dAp;
+    dD_part[idx] = sg;
+  }
+}
+
+// dB[b,t,g,n] = sum over the group's heads, ascending, of the per-head slots.
+__global__ void reduce_heads_kernel(Shape s, const float *__restrict__ slot_b, const float *__restrict__ slot_c,
+                                    float *__restrict__ dB, float *__restrict__ dC) {
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.T * s.G * s.N) return;
+  const int64_t n = idx % s.N, g = (idx / s.N) % s.G, bt = idx / (s.N * s.G);
+  float sb = 0.f, sc = 0.f;
+  for (int64_t k = 0; k < s.hpg; ++k) {
+    const int64_t o = (bt * s.H + g * s.hpg + k) * s.N + n;
+    sb += slot_b[o];
+    sc += slot_c[o];
+  }
+  dB[idx] = sb;
+  dC[idx] = sc;
+}
+
+// dA[h], dD[h] = sum over (b, c) ascending of the per-chunk partials.
+__global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ dA_part,
+                                            const float *__restrict__ dD_part, float *__restrict__ dA,
+                                            float *__restrict__ dD) {
+  const int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (h >= s.H) return;
+  float a = 0.f, d = 0.f;
+  for (int64_t bc = 0; bc < s.b * s.nc; ++bc) {
+    a += dA_part[bc * s.H + h];
+    d += dD_part[bc * s.H + h];
+  }
+  dA[h] = a;
+  dD[h] = d;
+}
+
+struct BwdWs {
+  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *MGm, *buf, *carry, *dEpass, *dAcs, *u, *gx, *ddt_part, *dA_part,
+      *dD_part, *slot_b, *slot_c;
+};
+
+BwdWs carve_bwd(Carver &cv, const Shape &s, bool atomic) {
+  BwdWs w;
+  const int64_t acs = s.b * s.H * s.nc * s.Q, qq = s.b * s.nc * s.H * s.Q * s.Q;
+  w.acs_hi = cv.take<float>(acs);
+  w.acs_lo = cv.take<float>(acs);
+  w.CB = cv.take<float>(s.b * s.nc * s.G * s.Q * s.Q);
+  w.Mm = cv.take<float>(qq);
+  w.Wm = cv.take<float>(qq);
+  w.MGm = cv.take<float>(qq);
+  w.buf = cv.take<float>(s.b * s.nc * s.H * s.P * s.N);
+  w.carry = cv.take<float>(s.b * s.H * s.P * s.N);
+  w.dEpass = cv.take<float>(s.b * s.H * s.nc);
+  w.dAcs = cv.take<float>(acs);
+  w.u = cv.take<float>(acs);
+  w.gx = cv.take<float>(acs);
+  w.ddt_part = cv.take<float>(s.b * s.T * s.H);
+  w.dA_part = cv.take<float>(s.b * s.nc * s.H);
+  w.dD_part = cv.take<float>(s.b * s.nc * s.H);
+  w.slot_b = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
+  w.slot_c = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
+  return w;
+}
+
+struct FwdWs {
+  float *acs_hi, *acs_lo, *CB, *S;
+};
+
+FwdWs carve_fwd(Carver &cv, const Shape &s) {
+  FwdWs w;
+  const int64_t acs = s.b * s.H * s.nc * s.Q;
+  w.acs_hi = cv.take<float>(acs);
+  w.acs_lo = cv.take<float>(acs);
+  w.CB = cv.take<float>(s.b * s.nc * s.G * s.Q * s.Q);
+  w.S = cv.take<float>(s.b * s.nc * s.H * s.P * s.N);
+  return w;
+}
+
+inline unsigned grid1(int64_t n, int bs) { return unsigned(cdiv(n, bs)); }
+
+template <class TIn>
+cudaError_t fwd_impl(const Shape &s, const Args &a, void *ws, int bs, cudaStream_t st) {
+  Carver cv(ws);
+  FwdWs w = carve_fwd(cv, s);
+  const TIn *x = static_cast<const TIn *>(a.x), *Bm = static_cast<const TIn *>(a.B), *Cm = static_cast<const TIn *>(a.C);
+  cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
+  chunk_state_fwd_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.H), grid1(s.P * s.N, bs)), bs, s.Q * sizeof(float), st>>>(
+      s, x, Bm, a.dt, w.acs_hi, w.acs_lo, w.S);
+  state_passing_fwd_kernel<<<grid1(s.b * s.H * s.P * s.N, bs), bs, 0, st>>>(s, w.S, w.acs_hi, w.acs_lo, a.seq_idx,
+                                                                            a.init, a.states_out);
+  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
+  chunk_scan_fwd_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(
+      s, x, Cm, a.dt, a.D, w.CB, w.acs_hi, w.acs_lo, a.states_out, static_cast<TIn *>(a.y));
+  return cudaGetLastError();
+}
+
+template <class TIn>
+cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomic, cudaStream_t st, Trace &tr) {
+  Carver cv(ws);
+  BwdWs w = carve_bwd(cv, s, atomic);
+  const TIn *x = static_cast<const TIn *>(a.x), *Bm = static_cast<const TIn *>(a.B), *Cm = static_cast<const TIn *>(a.C);
+  const TIn *g = static_cast<const TIn *>(a.dout);
+  const int64_t PN = s.P * s.N;
+  cudaError_t err;
+  if (a.dinit) {
+    err = cudaMemsetAsync(a.dinit, 0, size_t(s.nseq * s.H * PN) * sizeof(float), st);
+    if (err != cudaSuccess) return err;
+  }
+  err = cudaMemsetAsync(w.carry, 0, size_t(s.b * s.H * PN) * sizeof(float), st);
+  if (err != cudaSuccess) return err;
+  if (atomic) {
+    const size_t nbg = size_t(s.b * s.T * s.G * s.N) * sizeof(float);
+    if ((err = cudaMemsetAsync(a.dB, 0, nbg, st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dC, 0, nbg, st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  }
+  const unsigned nbch = unsigned(s.b * s.nc * s.H);
+  tr.mark(st);
+  cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
+  tr.mark(st);
+  tr.mark(st);
+  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
+  tr.mark(st);
+  tr.mark(st);
+  mwg_kernel<TIn><<<dim3(nbch, grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo, w.Mm,
+                                                                    w.Wm, w.MGm);
+  tr.mark(st);
+  tr.mark(st);
+  dhscan_kernel<TIn><<<dim3(nbch, grid1(PN, bs)), bs, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo, w.buf);
+  tr.mark(st);
+  tr.mark(st);
+  state_passing_bwd_kernel<<<unsigned(s.b * s.H), bs, 0, st>>>(s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo,
+                                                                a.seq_idx, w.dEpass, a.dinit);
+  tr.mark(st);
+  tr.mark(st);
+  dx_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(s, g, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi,
+                                                                  w.acs_lo, a.dx);
+  tr.mark(st);
+  if (atomic) {
+    tr.mark(st);
+    dbdc_kernel<TIn, true><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
+        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.dB, a.dC);
+    tr.mark(st);
+  } else {
+    tr.mark(st);
+    dbdc_kernel<TIn, false><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
+        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, w.slot_b, w.slot_c);
+    tr.mark(st);
+  }
+  tr.mark(st);
+  ddt_dacs_kernel<TIn><<<grid1(s.b * s.H * s.nc * s.Q, bs), bs, 0, st>>>(
+      s, x, g, Bm, Cm, a.dt, w.MGm, a.states_in, w.buf, w.acs_hi, w.acs_lo, w.ddt_part, w.dAcs, w.u, w.gx);
+  tr.mark(st);
+  if (atomic) {
+    tr.mark(st);
+    cumsum_bwd_kernel<true><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.dAcs, w.u, w.gx, w.dEpass,
+                                                                        w.ddt_part, a.ddt, a.dA, a.dD);
+    tr.mark(st);
+  } else {
+    tr.mark(st);
+    cumsum_bwd_kernel<false><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(
+        s, a.dt, a.A, w.dAcs, w.u, w.gx, w.dEpass, w.ddt_part, a.ddt, w.dA_part, w.dD_part);
+    tr.mark(st);
+    tr.mark(st);
+    reduce_heads_kernel<<<grid1(s.b * s.T * s.G * s.N, bs), bs, 0, st>>>(s, w.slot_b, w.slot_c, a.dB, a.dC);
+    tr.mark(st);
+    tr.mark(st);
+    reduce_heads_scalars_kernel<<<grid1(s.H, bs), bs, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
+    tr.mark(st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t simt_fwd_workspace(const Shape &s) {
+  Carver cv(nullptr);
+  carve_fwd(cv, s);
+  return cv.bytes();
+}
+
+size_t simt_bwd_workspace(const Shape &s, bool atomic) {
+  Carver cv(nullptr);
+  carve_bwd(cv, s, atomic);
+  return cv.bytes();
+}
+
+int simt_bwd_launches(const Shape &, bool atomic) { return atomic ? 9 : 11; }
+
+const char *simt_bwd_launch_name(bool atomic, int k) {
+  static const char *det[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc",
+                              "ddt_dacs", "cumsum_bwd", "reduce_heads", "reduce_heads_scalars"};
+  static const char *atm[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc_atomic",
+                              "ddt_dacs", "cumsum_bwd_atomic"};
+  if (k < 0) return "invalid";
+  if (atomic) return k < 9 ? atm[k] : "invalid";
+  return k < 11 ? det[k] : "invalid";
+}
+
+cudaError_t simt_fwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, cudaStream_t st) {
+  return bf16 ? fwd_impl<__nv_bfloat16>(s, a, ws, block, st) : fwd_impl<float>(s, a, ws, block, st);
+}
+
+cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, bool atomic, cudaStream_t st,
+                     Trace &tr) {
+  return bf16 ? bwd_impl<__nv_bfloat16>(s, a, ws, block, atomic, st, tr)
+              : bwd_impl<float>(s, a, ws, block, atomic, st, tr);
+}
+
+}  // namespace ssd

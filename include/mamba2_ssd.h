@@ -1,0 +1,161 @@
+/*
+ * mamba2_ssd.h -- C ABI of the deterministic Mamba2 SSD (state-space
+ * duality) chunked scan for GB300 (sm_103a).
+ *
+ * The operation.  "Deterministic bwd kernel for mamba2" (Mamba PR #827)
+ * makes the backward of the mamba2 SSD chunked scan reproducible by taking
+ * the atomics out of it (section "Atomic add non-determinism") and by fixing
+ * the order of every prefix sum (section "Autotuner / kernel-shape
+ * non-determinism"); its per-kernel breakdown table names the steps
+ * (chunk_cumsum, chunk_state_bwd_dx/_db/_ddAcs, chunk_scan_bwd_dC/_dx).  The
+ * recurrence, per batch row b and head h (group g = h / (nheads/ngroups)):
+ *
+ *     state_t = exp(dt_t * A_h) * state_{t-1} + dt_t * x_t B_t^T   (P x N)
+ *     y_t     = state_t C_t + D_h * x_t
+ *
+ * with state_{t-1} replaced by the initial state (or zero) where a sequence
+ * starts.  mamba2_ssd_fwd computes y and the state entering every chunk;
+ * mamba2_ssd_bwd computes dx, ddt, dA, dB, dC, dD (and dinit) of
+ * L = sum(y * dout).
+ *
+ * Determinism.  Every output element has exactly one writer; partial sums
+ * that several CTAs produce are parked in per-unit slots and folded in one
+ * fixed order (the slot pattern of "[PyTorch] Ask cuDNN for a deterministic
+ * dprob when determinism is requested", TransformerEngine PR #3407, and of
+ * the split-slice reduction in xtuner PR #2235).  No atomics are used unless
+ * variant SSD_VARIANT_ATOMIC is requested, which exists only to measure the
+ * cost of determinism.  Results are bitwise identical across runs and across
+ * every `config` index that mamba2_ssd_num_configs reports.
+ *
+ * Memory.  The library allocates no device memory: the caller passes every
+ * input, output and workspace buffer.  All pointers below are DEVICE
+ * pointers unless stated, must be 16-byte aligned and point to densely packed
+ * row-major (C-contiguous) arrays of the stated shapes.  Nothing is
+ * synchronised inside fwd/bwd (one documented exception: seq_idx validation
+ * in fwd); work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) and the call returns.  Buffers must stay alive until that
+ * work has completed.
+ *
+ * Errors.  Every argument is checked on the host before anything is
+ * launched; a failed check returns its status and launches nothing.  No
+ * exception crosses the ABI.  SSD_ERR_CUDA reports a launch failure.
+ *
+ * Shapes: b = batch, T = seqlen, H = nheads, P = headdim, G = ngroups,
+ * N = dstate, Q = chunk_size, nc = ceil(T / Q), nseq = number of sequences.
+ */
+#ifndef MAMBA2_SSD_H_
+#define MAMBA2_SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSD_OK = 0,
+  SSD_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, misalignment, bad saved struct */
+  SSD_ERR_UNSUPPORTED = 2,   /* valid but not supported (e.g. a sequence start inside a chunk) */
+  SSD_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size query */
+  SSD_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  SSD_ERR_TIMEOUT = 5,       /* reserved: a bounded device-side wait ran out */
+  SSD_ERR_HANDLE = 6         /* saved struct not produced by mamba2_ssd_fwd or dims mismatch */
+} ssd_status;
+
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+typedef enum { SSD_VARIANT_DETERMINISTIC = 0, SSD_VARIANT_ATOMIC = 1 } ssd_variant;
+
+typedef struct {
+  int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size;
+  int64_t nseq;       /* rows of init_states / dinit: number of sequences (= batch without seq_idx) */
+  int32_t dtype;      /* ssd_dtype of x, B, C, y and dout; dt, A, D, init and all gradients are fp32 */
+  int32_t reserved;   /* must be 0 */
+} ssd_dims;
+
+/* What the backward needs from the forward.  Filled by mamba2_ssd_fwd; it
+ * borrows the caller's buffers (inputs and `states`), which must stay alive
+ * and unmodified until the backward has run.  Plain data: copy it freely. */
+typedef struct {
+  ssd_dims dims;
+  const void *x;              /* (b,T,H,P) dtype */
+  const float *dt;            /* (b,T,H) fp32, the step after any activation */
+  const float *A;             /* (H) fp32, A < 0 expected */
+  const void *B, *C;          /* (b,T,G,N) dtype; head h uses group h / (H/G) */
+  const float *D;             /* (H) fp32 skip weight */
+  const int32_t *seq_idx;     /* (b,T) int32 or NULL */
+  const float *init_states;   /* (nseq,H,P,N) fp32 or NULL */
+  const float *states;        /* (b,nc,H,P,N) fp32: state entering each chunk */
+  uint32_t magic;
+  uint32_t flags;
+} ssd_saved;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mamba2_ssd_status_string(int status);
+
+/* Number of chunks nc = ceil(seqlen / chunk_size), or -1 for invalid dims. */
+int64_t mamba2_ssd_num_chunks(const ssd_dims *dims);
+
+/* Workspace bytes the forward needs (0 if dims are invalid). */
+size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims);
+
+/* Workspace bytes the backward needs for launch configuration `config`
+ * (0 <= config < mamba2_ssd_num_configs) and `variant` (0 if invalid). */
+size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant);
+
+/* Number of selectable launch configurations for these dims (>= 1, or 0 if
+ * the dims are invalid).  All configurations give bitwise-identical
+ * results; they differ in tile and grid shape only. */
+int mamba2_ssd_num_configs(const ssd_dims *dims);
+
+/* Name of the backward algorithm a configuration selects (static string). */
+const char *mamba2_ssd_config_name(const ssd_dims *dims, int config);
+
+/* Number of kernel launches one mamba2_ssd_bwd call enqueues (this
+ * library's kernels; stream-ordered memsets are not counted). */
+int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant);
+
+/* Name of the k-th kernel launch of mamba2_ssd_bwd (static string;
+ * "invalid" when k is out of range). */
+const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k);
+
+/* Forward.  Inputs x, dt, A, B, C, D as in ssd_saved; seq_idx (b,T) int32
+ * (nullable; requires batch == 1, non-decreasing ids in [0,nseq), every
+ * change of id at a multiple of chunk_size -- checked with one synchronous
+ * device-to-host copy of seq_idx, the only synchronisation in this library);
+ * init_states (nseq,H,P,N) fp32 (nullable: zero initial states).
+ * Outputs: y (b,T,H,P) in dtype; states (b,nc,H,P,N) fp32, the state
+ * entering each chunk (init/zero at a sequence start); *saved_out (host
+ * struct) filled for the backward.  workspace: >= fwd_workspace_size bytes. */
+ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
+                          const void *B, const void *C, const float *D, const int32_t *seq_idx,
+                          const float *init_states, void *y, float *states, void *workspace,
+                          size_t workspace_bytes, void *stream, ssd_saved *saved_out);
+
+/* Backward of L = sum(y * dout).  dout (b,T,H,P) in dtype.  Outputs, all
+ * fp32 and fully overwritten: dx (b,T,H,P), ddt (b,T,H), dA (H), dB, dC
+ * (b,T,G,N), dD (H), dinit (nseq,H,P,N; may be NULL; must be NULL when the
+ * forward had no init_states).  workspace: >= bwd_workspace_size(config,
+ * variant) bytes.  variant: SSD_VARIANT_DETERMINISTIC (the product) or
+ * SSD_VARIANT_ATOMIC (same kernels with atomic accumulation; for measuring
+ * the cost of determinism only, results not reproducible). */
+ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
+                          float *dB, float *dC, float *dD, float *dinit, void *workspace,
+                          size_t workspace_bytes, int config, int variant, void *stream);
+
+/* mamba2_ssd_bwd with a per-launch timing trace, for profiling: `events`
+ * holds num_events caller-created cudaEvent_t handles; events[2k] and
+ * events[2k+1] are recorded on `stream` immediately before and after launch
+ * k (k < num_launches; extra events are left alone, missing ones skipped).
+ * The computation and its result are exactly those of mamba2_ssd_bwd. */
+ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
+                                 float *dB, float *dC, float *dD, float *dinit, void *workspace,
+                                 size_t workspace_bytes, int config, int variant, void *stream,
+                                 void *const *events, int num_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA2_SSD_H_ */

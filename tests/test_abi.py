@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, answers its queries, and rejects bad arguments on the host
+before launching anything (all pointers below are fake and never touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import deterministic_mamba2_ssd_gb300 as ssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba2_ssd.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba2_ssd_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return ssd.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert L.mamba2_ssd_status_string(code).decode() not in ("", "unknown status")
+    assert L.mamba2_ssd_status_string(99).decode() == "unknown status"
+
+
+def test_queries(L):
+    d = ssd.make_dims(1, 16384, 256, 64, 8, 128, 128)
+    assert L.mamba2_ssd_num_chunks(ctypes.byref(d)) == 128
+    n = ssd.num_configs(d)
+    assert n >= 2
+    names = [ssd.config_name(d, c) for c in range(n)]
+    assert len(set(names)) == n and "invalid" not in names
+    assert ssd.config_name(d, n) == "invalid"
+    for c in range(n):
+        assert ssd.bwd_workspace_size(d, c, 0) > 0
+        assert ssd.bwd_num_launches(d, c, 0) > 0
+    assert ssd.fwd_workspace_size(d) > 0
+    ragged = ssd.make_dims(2, 1000, 4, 16, 2, 16, 64)
+    assert L.mamba2_ssd_num_chunks(ctypes.byref(ragged)) == 16
+
+
+@pytest.mark.parametrize("field,value", [("batch", 0), ("seqlen", -1), ("nheads", 0), ("ngroups", 4),
+                                         ("chunk_size", 0), ("chunk_size", 4096), ("dtype", 7),
+                                         ("reserved", 1), ("nseq", 0)])
+def test_invalid_dims_rejected(L, field, value):
+    d = ssd.make_dims(1, 256, 4, 16, 1, 16, 64)
+    if field == "ngroups":
+        d.nheads = 6
+    setattr(d, field, value)
+    assert L.mamba2_ssd_num_chunks(ctypes.byref(d)) == -1
+    assert L.mamba2_ssd_num_configs(ctypes.byref(d)) == 0
+    assert L.mamba2_ssd_fwd_workspace_size(ctypes.byref(d)) == 0
+    assert L.mamba2_ssd_bwd_workspace_size(ctypes.byref(d), 0, 0) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails on the host first
+
+
+def call_fwd(L, d, ptrs=None, ws_bytes=0, saved=True):
+    p = [ctypes.c_void_p(FAKE + 256 * i) for i in range(10)] if ptrs is None else ptrs
+    sv = ssd.SavedStruct()
+    return L.mamba2_ssd_fwd(ctypes.byref(d), *p, ctypes.c_void_p(FAKE), ws_bytes, None,
+                            ctypes.byref(sv) if saved else None)
+
+
+def test_fwd_argument_checks(L):
+    d = ssd.make_dims(1, 256, 4, 16, 1, 16, 64, dtype=torch.float32)
+    need = ssd.fwd_workspace_size(d)
+    no_seq = [ctypes.c_void_p(FAKE + 256 * i) for i in range(10)]
+    no_seq[6] = None      # seq_idx
+    no_seq[7] = None      # init
+    # workspace too small -> SSD_ERR_WORKSPACE, before any launch
+    assert call_fwd(L, d, no_seq, need - 1) == 3
+    # a required pointer missing -> SSD_ERR_INVALID_ARG
+    for k in (0, 1, 2, 3, 4, 5, 8, 9):
+        p = list(no_seq)
+        p[k] = None
+        assert call_fwd(L, d, p, need) == 1, k
+    # misaligned pointer -> SSD_ERR_INVALID_ARG
+    p = list(no_seq)
+    p[0] = ctypes.c_void_p(FAKE + 4)
+    assert call_fwd(L, d, p, need) == 1
+    # missing saved_out
+    assert call_fwd(L, d, no_seq, need, saved=False) == 1
+    # nseq must equal batch without seq_idx
+    d2 = ssd.make_dims(1, 256, 4, 16, 1, 16, 64, nseq=3, dtype=torch.float32)
+    assert call_fwd(L, d2, no_seq, need) == 1
+
+
+def test_bwd_argument_checks(L):
+    d = ssd.make_dims(1, 256, 4, 16, 1, 16, 64, dtype=torch.float32)
+    sv = ssd.SavedStruct()
+    sv.dims = d
+    outs = [ctypes.c_void_p(FAKE + 256 * i) for i in range(7)] + [None]  # dout, dx..dD, dinit
+    args = lambda sv, o, ws, cfg=0, var=0: (ctypes.byref(sv), *o, ctypes.c_void_p(FAKE), ws, cfg, var, None)
+    # not produced by the forward -> SSD_ERR_HANDLE
+    assert L.mamba2_ssd_bwd(*args(sv, outs, 1 << 40)) == 6
+    assert L.mamba2_ssd_bwd(None, *outs, ctypes.c_void_p(FAKE), 0, 0, 0, None) == 6
+    # forge a structurally valid saved struct with fake pointers
+    for n in ("x", "dt", "A", "B", "C", "D", "states"):
+        setattr(sv, n, FAKE + 4096)
+    sv.magic = 0x53534432
+    need = ssd.bwd_workspace_size(d, 0, 0)
+    assert L.mamba2_ssd_bwd(*args(sv, outs, need - 1)) == 3
+    assert L.mamba2_ssd_bwd(*args(sv, outs, need, cfg=99)) == 1
+    assert L.mamba2_ssd_bwd(*args(sv, outs, need, var=5)) == 1
+    o = list(outs)
+    o[1] = None     # dx
+    assert L.mamba2_ssd_bwd(*args(sv, o, need)) == 1
+    o = list(outs)
+    o[7] = ctypes.c_void_p(FAKE)   # dinit without initial states
+    assert L.mamba2_ssd_bwd(*args(sv, o, need)) == 1
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ssd, "_lib", None)
+    monkeypatch.setattr(ssd, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
+        ssd.lib()

@@ -21,6 +21,8 @@ namespace ssd {
 
 namespace {
 
+constexpr int kPassThreads = 256;
+
 __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ---------------------------------------------------------------- cumsum --
@@ -552,7 +554,9 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
   dhscan_kernel<TIn><<<dim3(nbch, grid1(PN, bs)), bs, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo, w.buf);
   tr.mark(st);
   tr.mark(st);
-  state_passing_bwd_kernel<<<unsigned(s.b * s.H), bs, 0, st>>>(s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo,
+  // fixed block: this kernel folds per-thread partial dot products, so its
+  // shape must not follow the launch configuration
+  state_passing_bwd_kernel<<<unsigned(s.b * s.H), kPassThreads, 0, st>>>(s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo,
                                                                 a.seq_idx, w.dEpass, a.dinit);
   tr.mark(st);
   tr.mark(st);

@@ -54,6 +54,15 @@ def grads_digest(grads):
     return digest([grads[k] for k in sorted(grads)])
 
 
+def bits(t):
+    """Integer view of a float tensor: equality of bits, not of values."""
+    return t.detach().contiguous().view(torch.int32 if t.element_size() == 4 else torch.int16)
+
+
+def same_bits(a, b):
+    return all(torch.equal(bits(a[k]), bits(b[k])) for k in a)
+
+
 def head_slice(d, g0, hpg):
     """Sub-problem of one group: heads [g0*hpg, (g0+1)*hpg) with that group's
     B and C (groups never interact, so the oracle can run it alone)."""

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import deterministic_mamba2_ssd_gb300 as ssd
-from _helpers import grads_digest, run_gpu, to_dev
+from _helpers import bits, grads_digest, run_gpu, same_bits, to_dev
 from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS, make_inputs, workload_inputs
 
 pytestmark = pytest.mark.gpu
@@ -19,14 +19,20 @@ REPEATS = 20
 
 
 def repeat_digests(d, chunk, n, config=0, variant=0):
+    """sha256 of the first run's outputs, then, for each further run, that
+    digest again if its bits equal the first run's (compared on the GPU) or
+    a fresh digest if not."""
     g = to_dev(d)
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=chunk,
                        seq_idx=g["seq_idx"], init_states=g["init"])
-    out = []
-    for _ in range(n):
+    first = ssd.bwd(saved, g["dout"], config=config, variant=variant)
+    torch.cuda.synchronize()
+    h0 = grads_digest(first)
+    out = [h0]
+    for _ in range(n - 1):
         grads = ssd.bwd(saved, g["dout"], config=config, variant=variant)
         torch.cuda.synchronize()
-        out.append(grads_digest(grads))
+        out.append(h0 if same_bits(first, grads) else grads_digest(grads))
     return out
 
 

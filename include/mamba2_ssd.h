@@ -154,6 +154,27 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
                                  size_t workspace_bytes, int config, int variant, void *stream,
                                  void *const *events, int num_events);
 
+/* Backward for callers that cannot allocate device memory (no counterpart in
+ * the pages this library follows; it only changes where the scratch lives).
+ * Callers that run inside a fixed, pre-sized memory arena, or inside a host
+ * that forbids allocation after start-up, cannot hand mamba2_ssd_bwd a
+ * workspace.  This entry point takes the same saved struct, dout and outputs
+ * as mamba2_ssd_bwd (deterministic variant) but uses a fixed array of
+ * mamba2_ssd_static_scratch_bytes() bytes in device global memory, built
+ * into the library, as its workspace; it calls no allocating routine.
+ * - Shapes whose workspace (mamba2_ssd_bwd_workspace_size) exceeds that size
+ *   are rejected with SSD_ERR_WORKSPACE before anything is launched.
+ * - The first call on a device (with that device current) looks the array's
+ *   address up once; make that first call before any stream capture.
+ * - Every call on a device shares the one array: calls whose work may
+ *   overlap on the GPU (unordered streams) race and must not be made.
+ * - Every GPU that loads the library holds the array until the process exits.
+ * Results are bitwise identical to mamba2_ssd_bwd with the same config. */
+size_t mamba2_ssd_static_scratch_bytes(void);
+ssd_status mamba2_ssd_bwd_static_scratch(const ssd_saved *saved, const void *dout, float *dx, float *ddt,
+                                         float *dA, float *dB, float *dC, float *dD, float *dinit, int config,
+                                         void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,6 +80,12 @@ def lib():
         L.mamba2_ssd_bwd_traced.restype = ci
         L.mamba2_ssd_bwd_launch_name.argtypes = [pd, ci, ci, ci]
         L.mamba2_ssd_bwd_launch_name.restype = ctypes.c_char_p
+        L.mamba2_ssd_selftest_umma.argtypes = [vp] * 3 + [ci] * 6 + [vp]
+        L.mamba2_ssd_selftest_umma.restype = ci
+        L.mamba2_ssd_static_scratch_bytes.argtypes = []
+        L.mamba2_ssd_static_scratch_bytes.restype = sz
+        L.mamba2_ssd_bwd_static_scratch.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 8 + [ci, vp]
+        L.mamba2_ssd_bwd_static_scratch.restype = ci
         _lib = L
     return _lib
 

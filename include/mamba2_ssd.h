@@ -154,6 +154,16 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
                                  size_t workspace_bytes, int config, int variant, void *stream,
                                  void *const *events, int num_events);
 
+/* Diagnostic: one 128 x N x K bf16 product on the tensor cores through the
+ * same shared-memory descriptors, TMEM accumulator and (optionally) TMA
+ * loads that the fused backward uses.  A and B are device bf16 arrays in
+ * storage order: A is [M][K] (a_mn = 0, K-major) or [K][M] (a_mn = 1,
+ * MN-major); B is [N][K] (b_mn = 0) or [K][N] (b_mn = 1).  D (device fp32,
+ * [M][N]) receives A*B.  M must be 128, N 64 or 128, K 64 or 128.  Enqueued
+ * on `stream`; a NaN in D[0] reports a bounded wait that ran out. */
+ssd_status mamba2_ssd_selftest_umma(const void *A, const void *B, float *D, int M, int N, int K, int a_mn,
+                                    int b_mn, int use_tma, void *stream);
+
 /* Backward for callers that cannot allocate device memory (no counterpart in
  * the pages this library follows; it only changes where the scratch lives).
  * Callers that run inside a fixed, pre-sized memory arena, or inside a host

@@ -134,3 +134,11 @@ def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ssd, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
         ssd.lib()
+
+
+def test_selftest_and_static_entry_reject_bad_arguments_on_host(L):
+    # exercises the ctypes signatures without touching a GPU
+    assert L.mamba2_ssd_selftest_umma(None, None, None, 128, 64, 64, 0, 0, 0, None) == 1
+    assert L.mamba2_ssd_selftest_umma(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, None) == 1
+    assert L.mamba2_ssd_static_scratch_bytes() == 32 << 20
+    assert L.mamba2_ssd_bwd_static_scratch(None, None, None, None, None, None, None, None, None, 0, None) == 6

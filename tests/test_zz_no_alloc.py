@@ -23,11 +23,7 @@ GRADS = ("dx", "ddt", "dA", "dB", "dC", "dD", "dinit")
 
 def _fn():
     L = ssd.lib()
-    f = L.mamba2_ssd_bwd_static_scratch
-    f.argtypes = [ctypes.POINTER(ssd.SavedStruct)] + [ctypes.c_void_p] * 8 + [ctypes.c_int, ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    L.mamba2_ssd_static_scratch_bytes.restype = ctypes.c_size_t
-    return f, L.mamba2_ssd_static_scratch_bytes()
+    return L.mamba2_ssd_bwd_static_scratch, L.mamba2_ssd_static_scratch_bytes()
 
 
 def _empty_like_grads(ref):

@@ -36,7 +36,7 @@ class Dims(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
                 ("headdim", ctypes.c_int64), ("ngroups", ctypes.c_int64), ("dstate", ctypes.c_int64),
                 ("chunk_size", ctypes.c_int64), ("nseq", ctypes.c_int64), ("dtype", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
 
 
 class SavedStruct(ctypes.Structure):
@@ -80,6 +80,11 @@ def lib():
         L.mamba2_ssd_bwd_traced.restype = ci
         L.mamba2_ssd_bwd_launch_name.argtypes = [pd, ci, ci, ci]
         L.mamba2_ssd_bwd_launch_name.restype = ctypes.c_char_p
+        L.mamba2_ssd_bwd_check.argtypes = [pd, ci, vp, vp]
+        L.mamba2_ssd_bwd_check.restype = ci
+        L.mamba2_ssd_bwd_fault_test.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 9 + [sz, i64, ctypes.c_uint32,
+                                                                                           vp]
+        L.mamba2_ssd_bwd_fault_test.restype = ci
         L.mamba2_ssd_selftest_umma.argtypes = [vp] * 3 + [ci] * 6 + [vp]
         L.mamba2_ssd_selftest_umma.restype = ci
         L.mamba2_ssd_static_scratch_bytes.argtypes = []
@@ -90,9 +95,14 @@ def lib():
     return _lib
 
 
-def make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseq=None, dtype=torch.bfloat16):
+DIMS_SEQ_IDX = 1
+
+
+def make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseq=None, dtype=torch.bfloat16,
+              seq_idx=False):
     return Dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
-                batch if nseq is None else nseq, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32, 0)
+                batch if nseq is None else nseq, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32,
+                DIMS_SEQ_IDX if seq_idx else 0)
 
 
 def num_configs(dims: Dims) -> int:
@@ -118,6 +128,11 @@ def bwd_num_launches(dims: Dims, config: int = 0, variant: int = 0) -> int:
 def bwd_launch_names(dims: Dims, config: int = 0, variant: int = 0):
     n = bwd_num_launches(dims, config, variant)
     return [lib().mamba2_ssd_bwd_launch_name(ctypes.byref(dims), config, variant, k).decode() for k in range(n)]
+
+
+def bwd_check(saved: "Saved", workspace, config: int = 0, stream=None) -> int:
+    """Status word the device left in ``workspace`` after a backward."""
+    return lib().mamba2_ssd_bwd_check(ctypes.byref(saved.dims), config, _ptr(workspace), _stream(stream))
 
 
 def _ptr(t):
@@ -172,7 +187,7 @@ def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=No
         _check(seq_idx, "seq_idx", (b, T), torch.int32, dev)
     if init_states is not None:
         _check(init_states, "init_states", (nseq, H, P, N), torch.float32, dev)
-    dims = make_dims(b, T, H, P, G, N, chunk_size, nseq, x.dtype)
+    dims = make_dims(b, T, H, P, G, N, chunk_size, nseq, x.dtype, seq_idx=seq_idx is not None)
     nc = lib().mamba2_ssd_num_chunks(ctypes.byref(dims))
     if nc < 0:
         raise ValueError("invalid dims")

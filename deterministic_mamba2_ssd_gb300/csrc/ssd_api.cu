@@ -20,7 +20,7 @@ bool dims_ok(const ssd_dims *d) {
     return false;
   if (d->nheads % d->ngroups != 0) return false;
   if (d->dtype != SSD_F32 && d->dtype != SSD_BF16) return false;
-  if (d->reserved != 0) return false;
+  if ((d->flags & ~SSD_DIMS_SEQ_IDX) != 0) return false;
   if (d->chunk_size > 1024) return false;
   const int64_t nc = (d->seqlen + d->chunk_size - 1) / d->chunk_size;
   if (d->batch * nc * d->nheads > (int64_t(1) << 31) - 1) return false;
@@ -44,11 +44,26 @@ ssd::Shape shape_of(const ssd_dims *d) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launch configurations of the general path: block sizes only.  Each output
-// element is computed by one thread in one fixed order, so all of them give
-// the same bits.
+// Launch configurations.  General path: block sizes only (each output
+// element is computed by one thread in one fixed order).  Fused path: depth
+// of the state-gradient ring (scheduling slack only; the arithmetic and its
+// order are the same).  Within a shape every configuration gives the same
+// bits; the two paths are never both selectable for one shape.
 constexpr int kSimtBlocks[] = {256, 128};
 constexpr int kNumSimt = 2;
+constexpr int kFusedRings[] = {4, 2};
+constexpr int kNumFused = 2;
+
+bool use_fused(const ssd_dims *d) { return ssd::fused_bwd_supported(shape_of(d), d->dtype == SSD_BF16); }
+
+ssd::FusedOptions fused_options(const ssd_dims *d, int config, int variant) {
+  ssd::FusedOptions o;
+  // with sequence starts the chain can be cut, so every chunk gets its own slot
+  o.ring_depth = (d->flags & SSD_DIMS_SEQ_IDX) ? int((d->seqlen + d->chunk_size - 1) / d->chunk_size)
+                                                : kFusedRings[config];
+  o.atomic = variant == SSD_VARIANT_ATOMIC;
+  return o;
+}
 
 }  // namespace
 
@@ -79,28 +94,46 @@ size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
 
 int mamba2_ssd_num_configs(const ssd_dims *dims) {
   if (!dims_ok(dims)) return 0;
-  return kNumSimt;
+  return use_fused(dims) ? kNumFused : kNumSimt;
 }
 
 const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
-  if (!dims_ok(dims) || config < 0 || config >= kNumSimt) return "invalid";
+  if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
+  if (use_fused(dims)) return config == 0 ? "fused/ring4" : "fused/ring2";
   return config == 0 ? "simt/block256" : "simt/block128";
 }
 
 size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC) return 0;
+  if (use_fused(dims)) return ssd::fused_bwd_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
   return ssd::simt_bwd_workspace(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
 }
 
 int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
+  if (use_fused(dims)) return variant == SSD_VARIANT_ATOMIC ? 1 : 2;
   return ssd::simt_bwd_launches(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
 }
 
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
+  if (use_fused(dims)) {
+    if (variant == SSD_VARIANT_ATOMIC) return k == 0 ? "fused_bwd_atomic" : "invalid";
+    return k == 0 ? "fused_bwd" : (k == 1 ? "fold_scalars" : "invalid");
+  }
   return ssd::simt_bwd_launch_name(variant == SSD_VARIANT_ATOMIC, k);
+}
+
+ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream) {
+  if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims) || !workspace)
+    return SSD_ERR_INVALID_ARG;
+  if (!use_fused(dims)) return SSD_OK;
+  int word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  return word ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 
 ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
@@ -113,6 +146,7 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
     if (!p || !aligned16(p)) return SSD_ERR_INVALID_ARG;
   if ((seq_idx && !aligned16(seq_idx)) || (init_states && !aligned16(init_states))) return SSD_ERR_INVALID_ARG;
   if (!seq_idx && dims->nseq != dims->batch) return SSD_ERR_INVALID_ARG;
+  if ((seq_idx != nullptr) != ((dims->flags & SSD_DIMS_SEQ_IDX) != 0)) return SSD_ERR_INVALID_ARG;
   const ssd::Shape s = shape_of(dims);
   const size_t need = ssd::simt_fwd_workspace(s);
   if (workspace_bytes < need) return SSD_ERR_WORKSPACE;
@@ -159,7 +193,7 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   if (config < 0 || config >= mamba2_ssd_num_configs(dims)) return SSD_ERR_INVALID_ARG;
   const ssd::Shape s = shape_of(dims);
   const bool atomic = variant == SSD_VARIANT_ATOMIC;
-  if (workspace_bytes < ssd::simt_bwd_workspace(s, atomic)) return SSD_ERR_WORKSPACE;
+  if (workspace_bytes < mamba2_ssd_bwd_workspace_size(dims, config, variant)) return SSD_ERR_WORKSPACE;
   if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
   ssd::Args a{};
   a.x = saved->x; a.B = saved->B; a.C = saved->C; a.dout = dout;
@@ -171,9 +205,39 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   ssd::Trace tr;
   tr.events = reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events));
   tr.count = num_events;
-  if (ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], atomic, st, tr) != cudaSuccess)
-    return SSD_ERR_CUDA;
-  return SSD_OK;
+  cudaError_t err;
+  if (use_fused(dims))
+    err = ssd::fused_bwd(s, a, workspace, fused_options(dims, config, variant), st, tr);
+  else
+    err = ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], atomic, st, tr);
+  return err == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status mamba2_ssd_bwd_fault_test(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
+                                     float *dB, float *dC, float *dD, float *dinit, void *workspace,
+                                     size_t workspace_bytes, int64_t silent_chunk, uint32_t spin_limit,
+                                     void *stream) {
+  if (!saved || saved->magic != kSavedMagic || !dims_ok(&saved->dims)) return SSD_ERR_HANDLE;
+  const ssd_dims *dims = &saved->dims;
+  if (!use_fused(dims)) return SSD_ERR_UNSUPPORTED;
+  const void *req[] = {saved->x, saved->dt, saved->A, saved->B, saved->C, saved->D, saved->states,
+                       dout, dx, ddt, dA, dB, dC, dD};
+  for (const void *p : req)
+    if (!p || !aligned16(p)) return SSD_ERR_INVALID_ARG;
+  if (workspace_bytes < mamba2_ssd_bwd_workspace_size(dims, 0, 0)) return SSD_ERR_WORKSPACE;
+  if (!workspace || !aligned16(workspace) || spin_limit == 0) return SSD_ERR_INVALID_ARG;
+  ssd::Args a{};
+  a.x = saved->x; a.B = saved->B; a.C = saved->C; a.dout = dout;
+  a.dt = saved->dt; a.A = saved->A; a.D = saved->D; a.init = saved->init_states; a.states_in = saved->states;
+  a.seq_idx = saved->seq_idx;
+  a.dx = dx; a.ddt = ddt; a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dinit = dinit;
+  ssd::FusedOptions o = fused_options(dims, 0, 0);
+  o.silent_chunk = silent_chunk;
+  o.spin_limit = spin_limit;
+  ssd::Trace tr;
+  return ssd::fused_bwd(shape_of(dims), a, workspace, o, static_cast<cudaStream_t>(stream), tr) == cudaSuccess
+             ? SSD_OK
+             : SSD_ERR_CUDA;
 }
 
 ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA, float *dB,

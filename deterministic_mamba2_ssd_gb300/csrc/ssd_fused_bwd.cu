@@ -1,0 +1,998 @@
+// ssd_fused_bwd.cu -- fused tensor-core backward of the Mamba2 SSD for the
+// shape family chunk 128, dstate 128, headdim 64, bf16 inputs.
+//
+// One CTA owns one (batch row b, chunk c, group g) unit and walks the
+// group's heads in ascending order.  For each head it computes, on the
+// tcgen05 tensor cores with TMEM accumulators, every product of the chunked
+// backward that "Deterministic bwd kernel for mamba2" (Mamba PR #827) splits
+// into chunk_scan_bwd_dC/_dx, chunk_state_bwd_dx/_db/_ddAcs and the
+// combined dx kernel; the cumsum backward and the reverse state recurrence
+// run in its CUDA-core epilogue.  Determinism comes from ownership instead
+// of atomics:
+//   * dB and dC of the unit's (chunk, group) are accumulated over the heads
+//     inside the CTA (TMEM accumulators, head order fixed), so no cross-CTA
+//     fold of them exists at all;
+//   * every dx/ddt element has exactly one writer;
+//   * the reverse state recurrence dH_c = dHscan_c + exp(E_c) dH_{c+1} is
+//     chained between chunk CTAs: the unit of chunk c waits for the unit of
+//     chunk c+1 to publish dH_{c+1} (an L2-resident ring plus a flag), so
+//     each dH_c has one formula whatever the schedule;
+//   * per-(chunk, head) partials of dA and dD are folded in ascending chunk
+//     order by a second small kernel.
+// Units are handed out in descending chunk order through an atomic ticket,
+// so a unit only ever waits for a unit that is already running: no deadlock
+// whatever the number of resident CTAs.
+//
+// Roles (320 threads): warps 0-7 epilogue (thread = one row of a 128-row
+// tile and one half of its columns), warp 8 TMA producer, warp 9 TMEM owner
+// and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
+// the one product whose rounding dominates the error (dx_intra = M^T g with
+// M = CB o L) runs in fp16 with exact power-of-two scaling of both operands,
+// and the head-summed intra-chunk matrix for dB/dC is split into a bf16
+// hi + lo pair.
+#include <cuda_fp16.h>
+
+#include <cstring>
+
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+#include "tmap.h"
+#include "umma.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kQ = 128, kN = 128, kP = 64;
+constexpr int kEpiThreads = 256;
+constexpr int kThreads = 320;
+
+// shared memory map (offsets from the 1024-byte aligned base)
+constexpr uint32_t OFF_B = 0;          // B chunk  [t][n] bf16, 2 panels x 16 KB
+constexpr uint32_t OFF_C = 32768;      // C chunk  [t][n] bf16, 2 panels
+constexpr uint32_t OFF_X0 = 65536;     // stage 0: x [t][p] 16 KB, g 16 KB (bf16 from TMA, then scaled fp16 in place)
+constexpr uint32_t OFF_X1 = 98304;     // stage 1
+constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [p][n] bf16, 2 panels x 8 KB each; later dS (hi half)
+constexpr uint32_t OFF_GW = 163840;    // exp(Acs) o g hi | lo: [t][p] bf16; later w o x (hi half) + scratch (lo half)
+constexpr uint32_t OFF_M16 = 196608;   // scaled M: [t][s] fp16, 2 panels x 16 KB
+constexpr uint32_t OFF_SMALL = 229376;
+constexpr uint32_t SMALL_BYTES = 2048;
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;  // + slack for aligning the base to 1 KB
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// scratch that lives in the idle lo half of GW between the dC/dHscan products and the next head
+constexpr uint32_t OFF_XBUF = OFF_GW + 16384;
+// at the end of a unit the head-summed matrix W (hi, lo) reuses the x/g stages
+constexpr uint32_t OFF_WHI = OFF_X0, OFF_WLO = OFF_X1;
+
+// TMEM columns
+// RA holds, in turn: C B^T (unit start), g x^T, then C H (cols 0-63) and
+// dHscan^T (64-127), then D1 (0-63) and Y (64-127).  WS accumulates W.
+constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
+constexpr uint32_t T_CH = T_RA, T_DH = T_RA + 64;
+
+enum Bar {
+  B_BC, B_CB, E_CBREAD, B_XG0, B_XG1, E_XG0, E_XG1, E_X16, B_G1, B_G2, E_M16, E_DS, B_G4, E_RA, E_WSUM, B_FIN,
+  NBARS
+};
+
+struct Small {
+  float acs_hi[kQ], acs_lo[kQ], dtv[kQ];
+  float red[32];
+  uint64_t bars[NBARS];
+  uint32_t tmem_base;
+  int unit;
+  volatile int abort;  // set when a bounded wait ran out: later waits give up at once
+};
+static_assert(sizeof(Small) <= SMALL_BYTES, "small region");
+
+// exchange scratch between the two column halves of a row, and the
+// per-quadrant partial column sums (strict lower part of M o Gx)
+struct XBuf {
+  float xch[5][kQ];
+  float colpart[4][kQ];
+};
+static_assert(sizeof(XBuf) <= 16384, "scratch");
+
+struct Params {
+  Shape s;
+  const __nv_bfloat16 *x, *dout;
+  const float *dt, *A, *D, *states;
+  const int32_t *seq_idx;
+  float *dx, *ddt, *dB, *dC, *dinit;
+  float *ring;
+  int ring_depth;
+  int *flags, *ticket, *err;
+  float *dA_part, *dD_part;
+  float *dA, *dD;         // atomic variant: accumulated directly
+  uint32_t spin_limit;
+  int atomic;
+  int64_t silent_chunk;   // fault injection: this chunk's units never publish (-1: none)
+};
+
+// ------------------------------------------------------------- helpers --
+__device__ __forceinline__ void ep_sync() { umma::named_bar(1, kEpiThreads); }
+__device__ __forceinline__ void lo_sync() { umma::named_bar(2, 128); }  // warps 0-3
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// 32 consecutive bf16 of row r (columns c0..c0+31, c0 % 32 == 0) of a 64-col panel
+__device__ __forceinline__ void ld_row32_bf16(const uint8_t *panel, int r, int c0, float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    uint4 u = *reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16);
+    bf16x8_to_f32(u, &v[8 * j]);
+  }
+}
+
+__device__ __forceinline__ void st_row32_bf16(uint8_t *panel, int r, int c0, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
+  }
+}
+
+__device__ __forceinline__ void st_row32_f16(uint8_t *panel, int r, int c0, const float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 u;
+    __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
+  }
+}
+
+__device__ __forceinline__ void ld_row16_bf16(const uint8_t *panel, int r, int c0, float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    uint4 u = *reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16);
+    bf16x8_to_f32(u, &v[8 * j]);
+  }
+}
+
+__device__ __forceinline__ void st_row16_bf16(uint8_t *panel, int r, int c0, const float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
+  }
+}
+
+__device__ __forceinline__ void st_row16_f16(uint8_t *panel, int r, int c0, const float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint4 u;
+    __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
+  }
+}
+
+__device__ __forceinline__ void f16x8_to_f32(uint4 u, float *f) {
+  const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ void ld_row32_f16(const uint8_t *panel, int r, int c0, float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16), &v[8 * j]);
+  }
+}
+
+__device__ __forceinline__ void ld_row16_f16(const uint8_t *panel, int r, int c0, float (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
+    f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16), &v[8 * j]);
+  }
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t *panel, int r, int c, float v) {
+  *reinterpret_cast<__nv_bfloat16 *>(panel + umma::sw128_offset_bf16(uint32_t(r), uint32_t(c))) =
+      __float2bfloat16_rn(v);
+}
+
+// exponent k with max * 2^k in [2^14, 2^15) (0 for max == 0)
+__device__ __forceinline__ int fp16_scale_exp(float mx) {
+  if (!(mx > 0.f)) return 0;
+  int e;
+  frexpf(mx, &e);
+  int k = 15 - e;
+  return max(-120, min(120, k));
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// (h1,l1) + (h2,l2): left operand is the earlier part of the sequence
+__device__ __forceinline__ void comp_add(float h1, float l1, float h2, float l2, float &h, float &l) {
+  float s, e;
+  two_sum(h1, h2, s, e);
+  h = s;
+  l = __fadd_rn(__fadd_rn(l1, l2), e);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+constexpr long long kWaitCycles = 2000000000LL;  // about one second
+
+// Bounded mbarrier wait: gives up after kWaitCycles (or at once once any
+// wait of this CTA gave up), recording error bit 2.  The kernel then runs to
+// its end with invalid results instead of hanging.
+__device__ __forceinline__ void wait_bar_impl(uint64_t *b, uint32_t parity, int *err, volatile int *abort) {
+  if (*abort) return;
+  const long long t0 = clock64();
+  while (!umma::mbar_try_wait(b, parity)) {
+    if (*abort) return;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      atomicOr(err, 2);
+      return;
+    }
+  }
+}
+// single-lane roles (TMA, MMA issuer)
+#define wait_bar(b, parity, err) wait_bar_impl((b), (parity), (err), &sm->abort)
+// full epilogue warps: lane 0 waits, the warp reconverges before any
+// warp-collective TMEM access
+#define ewait(b, parity, err)                                  \
+  do {                                                         \
+    if (lane == 0) wait_bar_impl((b), (parity), (err), &sm->abort); \
+    __syncwarp();                                              \
+  } while (0)
+
+// Column sums of a 32 x 16 block held one row per lane (v[c], c < 16): a
+// fixed butterfly (16 shuffles) leaves the total of column col16(lane) in
+// lanes 2k and 2k+1.  Same tree on every call.
+__device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ int col16_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+// Deterministic sum over the 256 epilogue threads (fixed tree); result in all.
+__device__ __forceinline__ float ep_sum(float v, Small *sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5;
+  ep_sync();
+  if ((threadIdx.x & 31) == 0) sm->red[warp] = v;
+  ep_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += sm->red[w];
+  return t;
+}
+__device__ __forceinline__ float ep_max(float v, Small *sm) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5;
+  ep_sync();
+  if ((threadIdx.x & 31) == 0) sm->red[warp] = v;
+  ep_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t = fmaxf(t, sm->red[w]);
+  return t;
+}
+// Sum over the 128 threads of warps 0-3 (fixed tree); result in all of them.
+__device__ __forceinline__ float lo_sum(float v, Small *sm, int slot) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) sm->red[8 + 4 * slot + warp] = v;
+  lo_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) t += sm->red[8 + 4 * slot + w];
+  return t;
+}
+
+// ============================================================== kernel ===
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_bwd_kernel(const Params p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_g,
+                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *sm_base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Small *sm = reinterpret_cast<Small *>(sm_base + OFF_SMALL);
+  uint64_t *bars = sm->bars;
+  const Shape &s = p.s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 9) {
+    umma::tmem_alloc(&sm->tmem_base, 512);
+    umma::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], 1);
+    umma::fence_mbar_init();
+    sm->unit = atomicAdd(p.ticket, 1);
+    sm->abort = 0;
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = sm->tmem_base;
+
+  // unit from the ticket: chunks in descending order, then batch row, then group
+  const int64_t unit = sm->unit;
+  const int64_t per_row = s.b * s.G;
+  const int64_t c = s.nc - 1 - unit / per_row;
+  const int64_t bi = (unit % per_row) / s.G;
+  const int64_t g = unit % s.G;
+  const int64_t t0 = c * kQ;
+  const int64_t row0 = bi * s.T + t0;  // first global token row of the chunk
+  const int hpg = int(s.hpg);
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      umma::tma_prefetch_desc(&tm_x);
+      umma::tma_prefetch_desc(&tm_g);
+      umma::tma_prefetch_desc(&tm_b);
+      umma::tma_prefetch_desc(&tm_c);
+      umma::mbar_expect_tx(&bars[B_BC], 65536);
+      for (int j = 0; j < 2; ++j) {
+        umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int(g * kN + j * 64), int(row0), &bars[B_BC]);
+        umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int(g * kN + j * 64), int(row0), &bars[B_BC]);
+      }
+      for (int k = 0; k < hpg; ++k) {
+        const int st = k & 1;
+        if (k >= 2) wait_bar(&bars[E_XG0 + st], uint32_t(((k >> 1) - 1) & 1), p.err);
+        const int64_t h = g * hpg + k;
+        uint8_t *dst = sm_base + (st ? OFF_X1 : OFF_X0);
+        umma::mbar_expect_tx(&bars[B_XG0 + st], 32768);
+        umma::tma_load_2d(dst, &tm_x, int(h * kP), int(row0), &bars[B_XG0 + st]);
+        umma::tma_load_2d(dst + 16384, &tm_g, int(h * kP), int(row0), &bars[B_XG0 + st]);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      const uint32_t aB = umma::smem_u32(sm_base + OFF_B), aC = umma::smem_u32(sm_base + OFF_C);
+      const uint32_t aHh = umma::smem_u32(sm_base + OFF_HD), aHl = aHh + 16384;
+      const uint32_t aGh = umma::smem_u32(sm_base + OFF_GW), aGl = aGh + 16384;
+      const uint32_t aM16 = umma::smem_u32(sm_base + OFF_M16);
+      constexpr uint32_t id_kk128 = umma::idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t id_kk64 = umma::idesc_bf16_f32(128, 64, 0, 0);
+      constexpr uint32_t id_mm64 = umma::idesc_bf16_f32(128, 64, 1, 1);
+      constexpr uint32_t id_km128 = umma::idesc_bf16_f32(128, 128, 0, 1);
+      constexpr uint32_t id_mm128 = umma::idesc_bf16_f32(128, 128, 1, 1);
+      // fp16 A/B (formats 0): g x^T K-major/K-major N = 128; D1 MN-major/MN-major N = 64
+      constexpr uint32_t id_f16_kk128 = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+      constexpr uint32_t id_f16_mm64 = (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+      auto kdesc = [](uint32_t base, uint32_t panel_bytes, int kk) {  // K-major operand, K step kk
+        return umma::smem_desc_sw128(base + uint32_t(kk / 64) * panel_bytes + uint32_t(kk % 64) * 2, 16, 1024);
+      };
+      auto mdesc = [](uint32_t base, uint32_t panel_bytes, int kk) {  // MN-major operand, K step kk
+        return umma::smem_desc_sw128(base + uint32_t(kk) * 128, panel_bytes, 1024);
+      };
+      wait_bar(&bars[B_BC], 0, p.err);
+      umma::fence_after_sync();
+      // CB = C B^T  (M = t, N = s, K = n)
+      for (int kk = 0; kk < kN; kk += 16)
+        umma::mma_bf16(tmem + T_RA, kdesc(aC, 16384, kk), kdesc(aB, 16384, kk), id_kk128, kk > 0);
+      umma::mma_commit(&bars[B_CB]);
+      wait_bar(&bars[E_CBREAD], 0, p.err);
+      for (int k = 0; k < hpg; ++k) {
+        const int st = k & 1;
+        const uint32_t par = uint32_t(k & 1);
+        const uint32_t aX = umma::smem_u32(sm_base + (st ? OFF_X1 : OFF_X0)), aG = aX + 16384;
+        if (k > 0) wait_bar(&bars[E_RA], par ^ 1u, p.err);
+        wait_bar(&bars[E_X16], par, p.err);  // x, g scaled to fp16 in place
+        umma::fence_after_sync();
+        // Gx = g x^T (M = t, N = s, K = p), fp16 operands
+        for (int kk = 0; kk < kP; kk += 16)
+          umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_f16_kk128, kk > 0);
+        umma::mma_commit(&bars[B_G1]);
+        wait_bar(&bars[E_M16], par, p.err);  // g x^T consumed; G~ and H (hi, lo) and M16 in smem
+        umma::fence_after_sync();
+        // CH = C (H_hi + H_lo)  (M = t, N = p, K = n)
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < kN; kk += 16)
+            umma::mma_bf16(tmem + T_CH, kdesc(aC, 16384, kk), kdesc(part ? aHl : aHh, 8192, kk), id_kk64,
+                           (part > 0) || (kk > 0));
+        // dHscan^T = C^T (G~_hi + G~_lo)  (M = n, N = p, K = t)
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < kQ; kk += 16)
+            umma::mma_bf16(tmem + T_DH, mdesc(aC, 16384, kk), mdesc(part ? aGl : aGh, 16384, kk), id_mm64,
+                           (part > 0) || (kk > 0));
+        // dC += G~ H^T  (M = t, N = n, K = p): hi*hi + hi*lo + lo*hi
+        for (int part = 0; part < 3; ++part) {
+          const uint32_t aA = part == 2 ? aGl : aGh, aBb = part == 1 ? aHl : aHh;
+          for (int kk = 0; kk < kP; kk += 16)
+            umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), mdesc(aBb, 8192, kk), id_km128,
+                           (k > 0) || (part > 0) || (kk > 0));
+        }
+        umma::mma_commit(&bars[B_G2]);
+        wait_bar(&bars[E_DS], par, p.err);  // CH, dHscan read; dS and w o x in smem
+        umma::fence_after_sync();
+        // D1 = M^T g  (fp16 scaled operands; M = s, N = p, K = t)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + T_RA, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
+        // Y = B dS^T  (M = t, N = p, K = n)
+        for (int kk = 0; kk < kN; kk += 16)
+          umma::mma_bf16(tmem + T_RA + 64, kdesc(aB, 16384, kk), kdesc(aHh, 8192, kk), id_kk64, kk > 0);
+        // dB += (w o x) dS  (M = t, N = n, K = p)
+        for (int kk = 0; kk < kP; kk += 16)
+          umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), mdesc(aHh, 8192, kk), id_km128, (k > 0) || (kk > 0));
+        umma::mma_commit(&bars[B_G4]);
+      }
+      wait_bar(&bars[E_WSUM], 0, p.err);
+      umma::fence_after_sync();
+      const uint32_t aWh = umma::smem_u32(sm_base + OFF_WHI), aWl = umma::smem_u32(sm_base + OFF_WLO);
+      for (int part = 0; part < 2; ++part) {
+        const uint32_t aW = part ? aWl : aWh;
+        // dC += W B  (M = t, N = n, K = s)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + T_DC, kdesc(aW, 16384, kk), mdesc(aB, 16384, kk), id_km128, 1);
+        // dB += W^T C  (M = s, N = n, K = t)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + T_DB, mdesc(aW, 16384, kk), mdesc(aC, 16384, kk), id_mm128, 1);
+      }
+      umma::mma_commit(&bars[B_FIN]);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = warp & 3, hf = warp >> 2;
+    const int r = 32 * q + lane;                       // row (token / state index) of this thread
+    const uint32_t lane_off = uint32_t(32 * q) << 16;  // TMEM lane field of this warp's quadrant
+    const float *dtg = p.dt + row0 * s.H;
+    XBuf *xb = reinterpret_cast<XBuf *>(sm_base + OFF_XBUF);
+
+    // CB rows (this thread's row, its 64 columns) into registers, and the
+    // power of two that scales M into the fp16 range
+    float cb[64];
+    ewait(&bars[B_CB], 0, p.err);
+    umma::fence_after_sync();
+    float cbmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v[16];
+      umma::tmem_ld16(tmem + lane_off + T_RA + 64 * hf + 16 * j, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        cb[16 * j + i] = v[i];
+        cbmax = fmaxf(cbmax, fabsf(v[i]));
+      }
+    }
+    {
+      float z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) umma::tmem_st16(tmem + lane_off + T_WS + 64 * hf + 16 * j, z);
+      umma::tmem_wait_st();
+    }
+    umma::fence_before_sync();
+    cbmax = ep_max(cbmax, sm);
+    if (tid == 0) umma::mbar_arrive(&bars[E_CBREAD]);
+    const int kM = fp16_scale_exp(cbmax);
+    const float sM = ldexpf(1.f, kM);
+
+    const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
+    const bool here_start = is_seq_start(p.seq_idx, bi, s.T, t0);
+    const int64_t seq = seq_of(p.seq_idx, bi, s.T, t0);
+    const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
+
+    for (int k = 0; k < hpg; ++k) {
+      const int st = k & 1;
+      const uint32_t par = uint32_t(k & 1);
+      const int64_t h = g * hpg + k;
+      uint8_t *sX = sm_base + (st ? OFF_X1 : OFF_X0);
+      uint8_t *sG = sX + 16384;
+      const float Ah = p.A[h], Dh = p.D[h];
+
+      // ---- P0: step sizes and in-chunk cumulative decay (compensated scan, fixed tree)
+      if (hf == 0) {
+        const float dtr = dtg[int64_t(r) * s.H + h];
+        float hi = __fmul_rn(dtr, Ah), lo = 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float h2 = __shfl_up_sync(0xffffffffu, hi, o), l2 = __shfl_up_sync(0xffffffffu, lo, o);
+          if (lane >= o) comp_add(h2, l2, hi, lo, hi, lo);
+        }
+        if (lane == 31) {
+          sm->red[24 + q] = hi;
+          sm->red[28 + q] = lo;
+        }
+        lo_sync();
+        float ph = 0.f, pl = 0.f;
+        for (int w = 0; w < q; ++w) comp_add(ph, pl, sm->red[24 + w], sm->red[28 + w], ph, pl);
+        comp_add(ph, pl, hi, lo, hi, lo);
+        sm->acs_hi[r] = hi;
+        sm->acs_lo[r] = lo;
+        sm->dtv[r] = dtr;
+      }
+      ewait(&bars[B_XG0 + st], uint32_t((k >> 1) & 1), p.err);
+      ep_sync();
+      const float ahr = sm->acs_hi[r], alr = sm->acs_lo[r], dtr = sm->dtv[r];
+      const float eh = sm->acs_hi[kQ - 1], el = sm->acs_lo[kQ - 1];
+      const float eacs = expf(__fadd_rn(ahr, alr));
+      const float eEA = expf(acs_diff(eh, el, ahr, alr));
+      const float wr = eEA * dtr;
+      const float eE = expf(__fadd_rn(eh, el));
+
+      // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |x|, |g| for the fp16 scaling
+      float gmax = 0.f, xmax = 0.f, gx = 0.f;
+      {
+        float gv[32], xv[32], hi[32], lo[32];
+        ld_row32_bf16(sG, r, 32 * hf, gv);
+        ld_row32_bf16(sX, r, 32 * hf, xv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float t = eacs * gv[i];
+          hi[i] = __bfloat162float(__float2bfloat16_rn(t));
+          lo[i] = t - hi[i];
+          gmax = fmaxf(gmax, fabsf(gv[i]));
+          xmax = fmaxf(xmax, fabsf(xv[i]));
+          gx = fmaf(gv[i], xv[i], gx);
+        }
+        st_row32_bf16(sm_base + OFF_GW, r, 32 * hf, hi);
+        st_row32_bf16(sm_base + OFF_GW + 16384, r, 32 * hf, lo);
+      }
+      // H (fp32 state entering the chunk) -> bf16 hi + lo, [p][n]
+      {
+        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e4 = tid + kEpiThreads * j;
+          const float4 v = __ldg(hs + e4);
+          const int pp = (4 * e4) / kN, nn = (4 * e4) % kN;
+          const int col = nn % 64;
+          const uint32_t off = (nn / 64) * 8192 + pp * 128 + (((col >> 3) ^ (pp & 7)) << 4) + (col & 7) * 2;
+          const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+          const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+          uint2 uh, ul;
+          reinterpret_cast<__nv_bfloat162 *>(&uh)[0] = h01;
+          reinterpret_cast<__nv_bfloat162 *>(&uh)[1] = h23;
+          reinterpret_cast<__nv_bfloat162 *>(&ul)[0] = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+          reinterpret_cast<__nv_bfloat162 *>(&ul)[1] = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+          *reinterpret_cast<uint2 *>(sm_base + OFF_HD + off) = uh;
+          *reinterpret_cast<uint2 *>(sm_base + OFF_HD + 16384 + off) = ul;
+        }
+      }
+      // x and g -> fp16 scaled by exact powers of two, in place
+      gmax = ep_max(gmax, sm);
+      xmax = ep_max(xmax, sm);
+      const int kg = fp16_scale_exp(gmax), kx = fp16_scale_exp(xmax);
+      const float ug = ldexpf(1.f, -kg), ux = ldexpf(1.f, -kx);
+      {
+        float v[32];
+        ld_row32_bf16(sG, r, 32 * hf, v);
+        const float sg = ldexpf(1.f, kg);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= sg;
+        st_row32_f16(sG, r, 32 * hf, v);
+        ld_row32_bf16(sX, r, 32 * hf, v);
+        const float sx = ldexpf(1.f, kx);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= sx;
+        st_row32_f16(sX, r, 32 * hf, v);
+      }
+      umma::fence_proxy_async_smem();
+      ep_sync();
+      if (tid == 0) umma::mbar_arrive(&bars[E_X16]);
+
+      // ---- E1: intra-chunk matrices from g x^T (TMEM) and C B^T (registers)
+      ewait(&bars[B_G1], par, p.err);
+      umma::fence_after_sync();
+      const float ugx = ug * ux;
+      float rowp = 0.f, diag = 0.f;
+      float csum[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = 64 * hf + 16 * j;
+        float m16[16];
+        csum[j] = 0.f;
+        if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
+          float gxv[16], ws[16], mgs[16];
+          umma::tmem_ld16(tmem + lane_off + T_RA + c0, gxv);
+          umma::tmem_ld16(tmem + lane_off + T_WS + c0, ws);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int sidx = c0 + i;
+            float mval = 0.f;
+            mgs[i] = 0.f;
+            if (sidx <= r) {
+              const float L = expf(acs_diff(ahr, alr, sm->acs_hi[sidx], sm->acs_lo[sidx]));
+              const float dts = sm->dtv[sidx];
+              const float gxs = gxv[i] * ugx;
+              mval = cb[16 * j + i] * L;
+              ws[i] = fmaf(L * gxs, dts, ws[i]);
+              const float mg = mval * gxs;
+              if (sidx < r) {
+                rowp = fmaf(mg, dts, rowp);
+                mgs[i] = mg;
+              } else {
+                diag = mg;
+              }
+            }
+            m16[i] = mval * sM;
+          }
+          umma::tmem_st16(tmem + lane_off + T_WS + c0, ws);
+          csum[j] = warp_colsum16(mgs, lane);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) m16[i] = 0.f;
+        }
+        st_row16_f16(sm_base + OFF_M16 + hf * 16384, r, 16 * j, m16);
+      }
+      umma::tmem_wait_st();
+      umma::fence_before_sync();
+      umma::fence_proxy_async_smem();
+      ep_sync();
+      if (tid == 0) umma::mbar_arrive(&bars[E_M16]);
+
+      // ---- E2: carried-in state term of the decay gradient; E3: chain step
+      ewait(&bars[B_G2], par, p.err);
+      umma::fence_after_sync();
+      // the lo half of GW is idle from here to the next head: exchange scratch
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((lane & 1) == 0) xb->colpart[q][64 * hf + 16 * j + col16_of_lane(lane)] = csum[j];
+      if (hf == 1) {
+        xb->xch[0][r] = rowp;
+        xb->xch[1][r] = diag;
+        xb->xch[3][r] = gx;
+      }
+      float inter_part = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float ch[16], gv[16];
+        umma::tmem_ld16(tmem + lane_off + T_CH + 32 * hf + 16 * u, ch);
+        ld_row16_f16(sG, r, 32 * hf + 16 * u, gv);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) inter_part = fmaf(gv[i], ch[i], inter_part);
+      }
+      inter_part *= ug;
+      if (has_next) {
+        const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
+        if (tid == 0) {
+          uint32_t it = 0;
+          while (!sm->abort && ld_acquire_gpu(flag) == 0) {
+            if (++it > p.spin_limit) {
+              atomicOr(p.err, 1);
+              break;
+            }
+            __nanosleep(100);
+          }
+        }
+        ep_sync();
+        (void)ld_acquire_gpu(flag);
+      }
+      float hdot = 0.f;
+      {
+        const float *src = p.ring + ((((c + 1) % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
+        const float *hs = p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN;
+        float *dst = nullptr;
+        if (here_start) {
+          if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
+        } else {
+          dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
+        }
+        uint8_t *panel = sm_base + OFF_HD + (n / 64) * 8192;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float dh[16];
+          umma::tmem_ld16(tmem + lane_off + T_DH + 32 * hf + 16 * u, dh);  // lane = n, columns p
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int pp = 32 * hf + 16 * u + i;
+            float ds = 0.f;
+            if (has_next) {
+              ds = __ldcg(src + pp * kN + n);
+              hdot = fmaf(__ldg(hs + pp * kN + n), ds, hdot);
+            }
+            if (dst) __stcg(dst + pp * kN + n, fmaf(eE, ds, dh[i]));
+            st_bf16(panel, pp, n % 64, ds);  // dS -> bf16 [p][n]
+          }
+        }
+      }
+      umma::fence_before_sync();
+      __threadfence();
+      const float dEpass = eE * ep_sum(hdot, sm);  // its barriers also order the ring stores before the flag
+      if (tid == 0 && !here_start && c != p.silent_chunk)
+        st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h), 1);
+      // w o x -> GW hi half (bf16)
+      {
+        float xv[32];
+        ld_row32_f16(sX, r, 32 * hf, xv);
+        const float f = wr * ux;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xv[i] *= f;
+        st_row32_bf16(sm_base + OFF_GW, r, 32 * hf, xv);
+      }
+      umma::fence_proxy_async_smem();
+      if (hf == 1) xb->xch[2][r] = inter_part;
+      ep_sync();
+      if (tid == 0) umma::mbar_arrive(&bars[E_DS]);
+
+      // ---- E4: dx and the row dot product x . Y
+      ewait(&bars[B_G4], par, p.err);
+      umma::fence_after_sync();
+      const float unscale = ldexpf(1.f, -(kM + kg));
+      float sxy = 0.f;
+      {
+        float *dxr = p.dx + ((row0 + r) * s.H + h) * kP + 32 * hf;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float d1[16], y[16], xv[16], gv[16];
+          umma::tmem_ld16(tmem + lane_off + T_RA + 32 * hf + 16 * u, d1);
+          umma::tmem_ld16(tmem + lane_off + T_RA + 64 + 32 * hf + 16 * u, y);
+          ld_row16_f16(sX, r, 32 * hf + 16 * u, xv);
+          ld_row16_f16(sG, r, 32 * hf + 16 * u, gv);
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 4 * i4 + e;
+              sxy = fmaf(xv[i], y[i], sxy);
+              o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], (Dh * ug) * gv[i]));
+            }
+            *reinterpret_cast<float4 *>(dxr + 16 * u + 4 * i4) = make_float4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      sxy *= ux;
+      umma::fence_before_sync();
+      if (hf == 1) xb->xch[4][r] = sxy;
+      ep_sync();
+      if (tid == 0) {
+        umma::mbar_arrive(&bars[E_RA]);
+        umma::mbar_arrive(&bars[E_XG0 + st]);
+      }
+
+      // ---- E5: decay gradient, reverse cumsum, ddt, dA/dD partials (rows, warps 0-3)
+      if (hf == 0) {
+        rowp += xb->xch[0][r];
+        diag += xb->xch[1][r];
+        sxy += xb->xch[4][r];
+        gx += xb->xch[3][r];
+        const float inter = eacs * (inter_part + xb->xch[2][r]);
+        // strict column sum of M o Gx for column r, quadrants in fixed order
+        const float cstrict =
+            ((xb->colpart[0][r] + xb->colpart[1][r]) + xb->colpart[2][r]) + xb->colpart[3][r];
+        const float dintra = cstrict + diag;
+        const float colp = dtr * cstrict;
+        const float u = wr * sxy;
+        const float dacs = rowp - colp + inter - u;
+        const float su = lo_sum(u, sm, 0);
+        float sfx = dacs;  // suffix sum over rows: fixed tree in the warp, fixed order across warps
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float v = __shfl_down_sync(0xffffffffu, sfx, o);
+          if (lane + o < 32) sfx += v;
+        }
+        if (lane == 0) sm->red[20 + q] = sfx;
+        lo_sync();
+        float off = 0.f;
+        for (int w = 3; w > q; --w) off += sm->red[20 + w];
+        const float da = (sfx + off) + (su + dEpass);
+        p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA * sxy);
+        const float dap = lo_sum(dtr * da, sm, 1);
+        const float ddp = lo_sum(gx, sm, 2);
+        if (tid == 0) {
+          if (p.atomic) {
+            atomicAdd(p.dA + h, dap);
+            atomicAdd(p.dD + h, ddp);
+          } else {
+            p.dA_part[(bi * s.nc + c) * s.H + h] = dap;
+            p.dD_part[(bi * s.nc + c) * s.H + h] = ddp;
+          }
+        }
+      }
+      ep_sync();
+    }
+
+    // ---- unit end: head-summed W (hi + lo) for the intra-chunk dB/dC products
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float w[16], hi[16], lo[16];
+      umma::tmem_ld16(tmem + lane_off + T_WS + 64 * hf + 16 * j, w);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        hi[i] = __bfloat162float(__float2bfloat16_rn(w[i]));
+        lo[i] = w[i] - hi[i];
+      }
+      st_row16_bf16(sm_base + OFF_WHI + hf * 16384, r, 16 * j, hi);
+      st_row16_bf16(sm_base + OFF_WLO + hf * 16384, r, 16 * j, lo);
+    }
+    umma::fence_before_sync();
+    umma::fence_proxy_async_smem();
+    ep_sync();
+    if (tid == 0) umma::mbar_arrive(&bars[E_WSUM]);
+    ewait(&bars[B_FIN], 0, p.err);
+    umma::fence_after_sync();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n0 = 64 * hf + 16 * j;
+      float v[16];
+      umma::tmem_ld16(tmem + lane_off + T_DB + n0, v);
+      float *o = p.dB + ((row0 + r) * s.G + g) * kN + n0;
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4)
+        *reinterpret_cast<float4 *>(o + 4 * i4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+      umma::tmem_ld16(tmem + lane_off + T_DC + n0, v);
+      o = p.dC + ((row0 + r) * s.G + g) * kN + n0;
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4)
+        *reinterpret_cast<float4 *>(o + 4 * i4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+    }
+    umma::fence_before_sync();
+  }
+  __syncthreads();
+  if (warp == 9) {
+    // after a give-up, let the tensor cores drain (bounded) before freeing TMEM
+    if (sm->abort && lane == 0) {
+      const long long t0 = clock64();
+      while (!umma::mbar_try_wait(&bars[B_FIN], 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+    __syncwarp();
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dA[h], dD[h]: per-(batch, chunk) partials summed in ascending order.
+__global__ void fold_scalars_kernel(Shape s, const float *__restrict__ dA_part, const float *__restrict__ dD_part,
+                                    float *__restrict__ dA, float *__restrict__ dD) {
+  const int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (h >= s.H) return;
+  float a = 0.f, d = 0.f;
+  for (int64_t bc = 0; bc < s.b * s.nc; ++bc) {
+    a += dA_part[bc * s.H + h];
+    d += dD_part[bc * s.H + h];
+  }
+  dA[h] = a;
+  dD[h] = d;
+}
+
+struct FusedWs {
+  int *status;   // [0] error bits, [1] ticket
+  int *flags;
+  float *ring, *dA_part, *dD_part;
+};
+
+FusedWs carve_fused(Carver &cv, const Shape &s, int ring_depth) {
+  FusedWs w;
+  w.status = cv.take<int>(64);
+  w.flags = cv.take<int>(s.b * s.nc * s.H);
+  w.dA_part = cv.take<float>(s.b * s.nc * s.H);
+  w.dD_part = cv.take<float>(s.b * s.nc * s.H);
+  w.ring = cv.take<float>(int64_t(ring_depth) * s.b * s.H * kP * kN);
+  return w;
+}
+
+}  // namespace
+
+bool fused_bwd_supported(const Shape &s, bool bf16) {
+  return bf16 && s.Q == kQ && s.N == kN && s.P == kP && s.T % kQ == 0 && s.hpg >= 1 &&
+         s.b * s.nc * s.G <= (int64_t(1) << 30) && s.b * s.T <= (int64_t(1) << 30);
+}
+
+size_t fused_bwd_workspace(const Shape &s, int ring_depth) {
+  Carver cv(nullptr);
+  carve_fused(cv, s, ring_depth);
+  return cv.bytes();
+}
+
+cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
+                      Trace &tr) {
+  Carver cv(ws);
+  FusedWs w = carve_fused(cv, s, opt.ring_depth);
+  CUtensorMap tm_x, tm_g, tm_b, tm_c;
+  const uint64_t rows = uint64_t(s.b * s.T);
+  if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
+                    128, true) ||
+      !make_tmap_2d(&tm_g, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP),
+                    64, 128, true) ||
+      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+                    128, true) ||
+      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+                    128, true))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaMemsetAsync(w.status, 0, 64 * sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(w.flags, 0, size_t(s.b * s.nc * s.H) * sizeof(int), st)) != cudaSuccess) return err;
+  if (a.dinit && (err = cudaMemsetAsync(a.dinit, 0, size_t(s.nseq * s.H * kP * kN) * sizeof(float), st)) !=
+                     cudaSuccess)
+    return err;
+  if (opt.atomic) {
+    if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  }
+  if ((err = cudaFuncSetAttribute(fused_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
+      cudaSuccess)
+    return err;
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.s = s;
+  p.x = static_cast<const __nv_bfloat16 *>(a.x);
+  p.dout = static_cast<const __nv_bfloat16 *>(a.dout);
+  p.dt = a.dt;
+  p.A = a.A;
+  p.D = a.D;
+  p.states = a.states_in;
+  p.seq_idx = a.seq_idx;
+  p.dx = a.dx;
+  p.ddt = a.ddt;
+  p.dB = a.dB;
+  p.dC = a.dC;
+  p.dinit = a.dinit;
+  p.ring = w.ring;
+  p.ring_depth = opt.ring_depth;
+  p.flags = w.flags;
+  p.err = w.status;
+  p.ticket = w.status + 1;
+  p.dA_part = w.dA_part;
+  p.dD_part = w.dD_part;
+  p.dA = a.dA;
+  p.dD = a.dD;
+  p.spin_limit = opt.spin_limit;
+  p.atomic = opt.atomic ? 1 : 0;
+  p.silent_chunk = opt.silent_chunk;
+  const unsigned units = unsigned(s.b * s.nc * s.G);
+  tr.mark(st);
+  fused_bwd_kernel<<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c);
+  tr.mark(st);
+  if (!opt.atomic) {
+    tr.mark(st);
+    fold_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
+    tr.mark(st);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

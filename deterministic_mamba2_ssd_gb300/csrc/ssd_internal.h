@@ -17,4 +17,15 @@ cudaError_t simt_fwd(const Shape &s, bool bf16, const Args &a, void *ws, int blo
 cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, bool atomic, cudaStream_t st,
                      Trace &tr);
 
+// Fused tensor-core backward (bf16, chunk 128, dstate 128, headdim 64).
+struct FusedOptions {
+  int ring_depth = 4;              // chunk slots of the state-gradient ring
+  uint32_t spin_limit = 1u << 22;  // polls before a chain wait gives up (error bit 1)
+  bool atomic = false;             // dA/dD by atomics instead of ordered partials
+  int64_t silent_chunk = -1;       // fault injection: units of this chunk never publish
+};
+bool fused_bwd_supported(const Shape &s, bool bf16);
+size_t fused_bwd_workspace(const Shape &s, int ring_depth);
+cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
+
 }  // namespace ssd

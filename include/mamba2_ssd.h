@@ -59,7 +59,7 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 2,   /* valid but not supported (e.g. a sequence start inside a chunk) */
   SSD_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size query */
   SSD_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
-  SSD_ERR_TIMEOUT = 5,       /* reserved: a bounded device-side wait ran out */
+  SSD_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out (see mamba2_ssd_bwd_check) */
   SSD_ERR_HANDLE = 6         /* saved struct not produced by mamba2_ssd_fwd or dims mismatch */
 } ssd_status;
 
@@ -71,8 +71,11 @@ typedef struct {
   int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size;
   int64_t nseq;       /* rows of init_states / dinit: number of sequences (= batch without seq_idx) */
   int32_t dtype;      /* ssd_dtype of x, B, C, y and dout; dt, A, D, init and all gradients are fp32 */
-  int32_t reserved;   /* must be 0 */
+  int32_t flags;      /* SSD_DIMS_* bits; all others must be 0 */
 } ssd_dims;
+
+/* ssd_dims.flags: seq_idx will be passed (packed variable-length batch). */
+#define SSD_DIMS_SEQ_IDX 1
 
 /* What the backward needs from the forward.  Filled by mamba2_ssd_fwd; it
  * borrows the caller's buffers (inputs and `states`), which must stay alive
@@ -106,7 +109,10 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
 
 /* Number of selectable launch configurations for these dims (>= 1, or 0 if
  * the dims are invalid).  All configurations give bitwise-identical
- * results; they differ in tile and grid shape only. */
+ * results; they differ in launch shape and scheduling only.  bf16 problems
+ * with chunk 128, dstate 128, headdim 64 and seqlen a multiple of 128 run
+ * the fused tensor-core backward; every other shape runs the general
+ * CUDA-core backward. */
 int mamba2_ssd_num_configs(const ssd_dims *dims);
 
 /* Name of the backward algorithm a configuration selects (static string). */
@@ -121,7 +127,8 @@ int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant);
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k);
 
 /* Forward.  Inputs x, dt, A, B, C, D as in ssd_saved; seq_idx (b,T) int32
- * (nullable; requires batch == 1, non-decreasing ids in [0,nseq), every
+ * (nullable, and given exactly when dims->flags has SSD_DIMS_SEQ_IDX;
+ * requires batch == 1, non-decreasing ids in [0,nseq), every
  * change of id at a multiple of chunk_size -- checked with one synchronous
  * device-to-host copy of seq_idx, the only synchronisation in this library);
  * init_states (nseq,H,P,N) fp32 (nullable: zero initial states).
@@ -143,6 +150,23 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
 ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
                           float *dB, float *dC, float *dD, float *dinit, void *workspace,
                           size_t workspace_bytes, int config, int variant, void *stream);
+
+/* Status of the last backward that used this workspace: reads one word
+ * written by the device (synchronises `stream`).  SSD_ERR_TIMEOUT when a
+ * bounded device-side wait of the fused backward ran out (its outputs are
+ * then invalid), SSD_OK otherwise. */
+ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream);
+
+/* Fault-injection diagnostic of the fused backward (fused shapes only): the
+ * units of chunk `silent_chunk` never publish their state gradient, and
+ * every wait for it gives up after `spin_limit` polls, so the consumer of
+ * that chunk times out.  Nothing hangs or faults; the call returns SSD_OK
+ * and mamba2_ssd_bwd_check then reports SSD_ERR_TIMEOUT.  Same arguments as
+ * mamba2_ssd_bwd otherwise (config and variant 0). */
+ssd_status mamba2_ssd_bwd_fault_test(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
+                                     float *dB, float *dC, float *dD, float *dinit, void *workspace,
+                                     size_t workspace_bytes, int64_t silent_chunk, uint32_t spin_limit,
+                                     void *stream);
 
 /* mamba2_ssd_bwd with a per-launch timing trace, for profiling: `events`
  * holds num_events caller-created cudaEvent_t handles; events[2k] and

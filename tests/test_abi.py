@@ -58,7 +58,7 @@ def test_queries(L):
 
 @pytest.mark.parametrize("field,value", [("batch", 0), ("seqlen", -1), ("nheads", 0), ("ngroups", 4),
                                          ("chunk_size", 0), ("chunk_size", 4096), ("dtype", 7),
-                                         ("reserved", 1), ("nseq", 0)])
+                                         ("flags", 2), ("nseq", 0)])
 def test_invalid_dims_rejected(L, field, value):
     d = ssd.make_dims(1, 256, 4, 16, 1, 16, 64)
     if field == "ngroups":

@@ -309,8 +309,8 @@ def main():
     (jdom, ndom), tdom = max(tot.items(), key=lambda kv: kv[1])
     dom_ms = tdom / args.steps
     peak, peak_kind = load_peaks()
-    if nl == 1:
-        alg = api_bytes(w, es)
+    if ndom.startswith("fused_bwd"):
+        alg = api_bytes(w, es)      # the fused kernel moves the whole backward's API I/O
     else:
         alg = kernel_bytes(ndom, w, es)
     achieved = alg / (dom_ms / 1e3) / 1e9 if alg else None

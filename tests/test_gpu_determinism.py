@@ -60,12 +60,17 @@ def test_bitwise_across_every_config():
         assert len(flat) == 1, digests
 
 
-def test_atomic_variant_shows_the_test_has_teeth():
+@pytest.mark.parametrize("name", ["bf16_T16384", "simt_bf16"])
+def test_atomic_variant_shows_the_test_has_teeth(name):
     """The same kernels with atomic accumulation: expected to differ between
-    runs at this shape.  If they happen not to, the repeat test above is not
-    proof of anything and this test says so."""
-    w = WORKLOADS["bf16_T2048"]
-    hs = repeat_digests(workload_inputs("bf16_T2048"), w.chunk, REPEATS, variant=1)
+    runs at these shapes (fused path: dA/dD; general path: dB/dC/dA/dD).  If
+    they happen not to, the repeat test above is not proof of anything and
+    this test says so."""
+    if name == "simt_bf16":
+        d, Q = make_inputs(1, 2000, 64, 64, 2, 128, dtype=torch.bfloat16, seed=8, dt_shift=4.0), 128
+    else:
+        d, Q = workload_inputs(name), WORKLOADS[name].chunk
+    hs = repeat_digests(d, Q, REPEATS, variant=1)
     if len(set(hs)) == 1:
         pytest.skip("atomic variant was reproducible in %d runs: repeat test non-probative here" % REPEATS)
     assert len(set(hs)) > 1

@@ -76,7 +76,9 @@ enum Bar {
 };
 
 struct Small {
-  float acs_hi[kQ], acs_lo[kQ], dtv[kQ];
+  float a2[kQ];    // in-chunk cumulative decay of the current head, log2 units: A log2(e) cumsum(dt)
+  float dtv[kQ];   // step sizes of the current head
+  float dtu[kQ];   // step sizes times the scale that undoes the fp16 scaling of g x^T
   float red[32];
   uint64_t bars[NBARS];
   uint32_t tmem_base;
@@ -88,7 +90,7 @@ static_assert(sizeof(Small) <= SMALL_BYTES, "small region");
 // exchange scratch between the two column halves of a row, and the
 // per-quadrant partial column sums (strict lower part of M o Gx)
 struct XBuf {
-  float xch[5][kQ];
+  float v[5][2][kQ];     // per column half: rowp, diag, inter, g.x, x.Y
   float colpart[4][kQ];
 };
 static_assert(sizeof(XBuf) <= 16384, "scratch");
@@ -216,6 +218,30 @@ __device__ __forceinline__ void ld_row16_f16(const uint8_t *panel, int r, int c0
   }
 }
 
+__device__ __forceinline__ void st_row8_f16(uint8_t *panel, int r, int c0, const float (&v)[8]) {
+  uint4 u;
+  __half2 *h = reinterpret_cast<__half2 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+  const int chunk = (c0 >> 3) ^ (r & 7);
+  *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
+}
+
+// 8 consecutive elements (one 16-byte chunk) of row r, columns c0..c0+7 (c0 % 8 == 0)
+__device__ __forceinline__ void ld8_bf16(const uint8_t *panel, int r, int c0, float (&v)[8]) {
+  bf16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
+}
+__device__ __forceinline__ void ld8_f16(const uint8_t *panel, int r, int c0, float (&v)[8]) {
+  f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
+}
+__device__ __forceinline__ void st8_bf16(uint8_t *panel, int r, int c0, const float (&v)[8]) {
+  uint4 u;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)) = u;
+}
+
 __device__ __forceinline__ void st_bf16(uint8_t *panel, int r, int c, float v) {
   *reinterpret_cast<__nv_bfloat16 *>(panel + umma::sw128_offset_bf16(uint32_t(r), uint32_t(c))) =
       __float2bfloat16_rn(v);
@@ -259,8 +285,10 @@ constexpr long long kWaitCycles = 2000000000LL;  // about one second
 // its end with invalid results instead of hanging.
 __device__ __forceinline__ void wait_bar_impl(uint64_t *b, uint32_t parity, int *err, volatile int *abort) {
   if (*abort) return;
+  if (umma::mbar_try_wait(b, parity)) return;
   const long long t0 = clock64();
-  while (!umma::mbar_try_wait(b, parity)) {
+  // sleep in the barrier (woken when the phase completes) rather than spin
+  while (!umma::mbar_try_wait_sleep(b, parity, 20000u)) {
     if (*abort) return;
     if (clock64() - t0 > kWaitCycles) {
       *abort = 1;
@@ -295,6 +323,24 @@ __device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
   }
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
+// Same for a 32 x 8 block: column total lands in the 4 lanes with equal bits 4..2.
+__device__ __forceinline__ float warp_colsum8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int half = 4, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+    }
+  }
+  float t = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return t + __shfl_xor_sync(0xffffffffu, t, 1);
+}
+__device__ __forceinline__ int col8_of_lane(int lane) {
+  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+}
 __device__ __forceinline__ int col16_of_lane(int lane) {
   return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
 }
@@ -312,35 +358,39 @@ __device__ __forceinline__ float ep_sum(float v, Small *sm) {
   for (int w = 0; w < 8; ++w) t += sm->red[w];
   return t;
 }
-__device__ __forceinline__ float ep_max(float v, Small *sm) {
+// Maxima of two values over the 256 epilogue threads in one round.
+__device__ __forceinline__ void ep_max2(float &a, float &b, Small *sm) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
   const int warp = threadIdx.x >> 5;
   ep_sync();
-  if ((threadIdx.x & 31) == 0) sm->red[warp] = v;
+  if ((threadIdx.x & 31) == 0) {
+    sm->red[warp] = a;
+    sm->red[8 + warp] = b;
+  }
   ep_sync();
-  float t = 0.f;
+  a = 0.f;
+  b = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) t = fmaxf(t, sm->red[w]);
-  return t;
+  for (int w = 0; w < 8; ++w) {
+    a = fmaxf(a, sm->red[w]);
+    b = fmaxf(b, sm->red[8 + w]);
+  }
 }
-// Sum over the 128 threads of warps 0-3 (fixed tree); result in all of them.
-__device__ __forceinline__ float lo_sum(float v, Small *sm, int slot) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) sm->red[8 + 4 * slot + warp] = v;
-  lo_sync();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) t += sm->red[8 + 4 * slot + w];
-  return t;
+  return v;
 }
 
 // ============================================================== kernel ===
 __global__ void __launch_bounds__(kThreads, 1)
     fused_bwd_kernel(const Params p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_g,
-                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c) {
+                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
+                     const __grid_constant__ CUtensorMap tm_dx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm_base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Small *sm = reinterpret_cast<Small *>(sm_base + OFF_SMALL);
@@ -488,10 +538,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(32 * q) << 16;  // TMEM lane field of this warp's quadrant
     const float *dtg = p.dt + row0 * s.H;
     XBuf *xb = reinterpret_cast<XBuf *>(sm_base + OFF_XBUF);
+    constexpr float kLog2e = 1.4426950408889634f;
 
-    // CB rows (this thread's row, its 64 columns) into registers, and the
-    // power of two that scales M into the fp16 range
-    float cb[64];
+    // C B^T rows (this thread's row, its 64 columns) into registers, pre-scaled
+    // by the power of two that brings M = CB o L into the fp16 range
+    float cbs[64];
     ewait(&bars[B_CB], 0, p.err);
     umma::fence_after_sync();
     float cbmax = 0.f;
@@ -501,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::tmem_ld16(tmem + lane_off + T_RA + 64 * hf + 16 * j, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        cb[16 * j + i] = v[i];
+        cbs[16 * j + i] = v[i];
         cbmax = fmaxf(cbmax, fabsf(v[i]));
       }
     }
@@ -514,16 +565,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::tmem_wait_st();
     }
     umma::fence_before_sync();
-    cbmax = ep_max(cbmax, sm);
+    {
+      float dummy = 0.f;
+      ep_max2(cbmax, dummy, sm);
+    }
     if (tid == 0) umma::mbar_arrive(&bars[E_CBREAD]);
     const int kM = fp16_scale_exp(cbmax);
     const float sM = ldexpf(1.f, kM);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) cbs[i] *= sM;
 
     const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
     const bool here_start = is_seq_start(p.seq_idx, bi, s.T, t0);
     const int64_t seq = seq_of(p.seq_idx, bi, s.T, t0);
     const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
 
+    float dt_next = (hf == 0) ? dtg[int64_t(r) * s.H + g * hpg] : 0.f;  // step size of the first head
     for (int k = 0; k < hpg; ++k) {
       const int st = k & 1;
       const uint32_t par = uint32_t(k & 1);
@@ -532,44 +589,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *sG = sX + 16384;
       const float Ah = p.A[h], Dh = p.D[h];
 
-      // ---- P0: step sizes and in-chunk cumulative decay (compensated scan, fixed tree)
+      // the state tile entering the chunk (fp32, L2-warm): loads in flight during the scan
+      float4 hv[8];
+      {
+        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = __ldg(hs + tid + kEpiThreads * j);
+      }
+      // ---- P0: cumulative step sizes (fixed-tree scan), decay in log2 units
+      float cumdt = 0.f;
       if (hf == 0) {
-        const float dtr = dtg[int64_t(r) * s.H + h];
-        float hi = __fmul_rn(dtr, Ah), lo = 0.f;
+        cumdt = dt_next;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const float h2 = __shfl_up_sync(0xffffffffu, hi, o), l2 = __shfl_up_sync(0xffffffffu, lo, o);
-          if (lane >= o) comp_add(h2, l2, hi, lo, hi, lo);
+          const float v = __shfl_up_sync(0xffffffffu, cumdt, o);
+          if (lane >= o) cumdt += v;
         }
-        if (lane == 31) {
-          sm->red[24 + q] = hi;
-          sm->red[28 + q] = lo;
-        }
+        if (lane == 31) sm->red[24 + q] = cumdt;
         lo_sync();
-        float ph = 0.f, pl = 0.f;
-        for (int w = 0; w < q; ++w) comp_add(ph, pl, sm->red[24 + w], sm->red[28 + w], ph, pl);
-        comp_add(ph, pl, hi, lo, hi, lo);
-        sm->acs_hi[r] = hi;
-        sm->acs_lo[r] = lo;
-        sm->dtv[r] = dtr;
+        float pre = 0.f;
+        for (int w = 0; w < q; ++w) pre += sm->red[24 + w];
+        cumdt += pre;
+        sm->a2[r] = cumdt * (Ah * kLog2e);
+        sm->dtv[r] = dt_next;
+        if (r == kQ - 1) sm->red[31] = cumdt;  // sum of the chunk's step sizes
       }
       ewait(&bars[B_XG0 + st], uint32_t((k >> 1) & 1), p.err);
       ep_sync();
-      const float ahr = sm->acs_hi[r], alr = sm->acs_lo[r], dtr = sm->dtv[r];
-      const float eh = sm->acs_hi[kQ - 1], el = sm->acs_lo[kQ - 1];
-      const float eacs = expf(__fadd_rn(ahr, alr));
-      const float eEA = expf(acs_diff(eh, el, ahr, alr));
-      const float wr = eEA * dtr;
-      const float eE = expf(__fadd_rn(eh, el));
+      const float a2r = sm->a2[r], dtr = sm->dtv[r], a2E = sm->a2[kQ - 1];
 
-      // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |x|, |g| for the fp16 scaling
-      float gmax = 0.f, xmax = 0.f, gx = 0.f;
-      {
-        float gv[32], xv[32], hi[32], lo[32];
-        ld_row32_bf16(sG, r, 32 * hf, gv);
-        ld_row32_bf16(sX, r, 32 * hf, xv);
+      const float eacs = umma::ex2_approx(a2r);        // exp(Acs_r)
+      const float eEA = umma::ex2_approx(a2E - a2r);   // exp(E - Acs_r)
+      const float wr = eEA * dtr;
+      const float eE = umma::ex2_approx(a2E);
+
+      // H (fp32 state entering the chunk) -> bf16 hi + lo, [p][n]
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+      for (int j = 0; j < 8; ++j) {
+        const int e4 = tid + kEpiThreads * j;
+        const float4 v = hv[j];
+        const int pp = (4 * e4) / kN, nn = (4 * e4) % kN;
+        const int col = nn % 64;
+        const uint32_t off = (nn / 64) * 8192 + pp * 128 + (((col >> 3) ^ (pp & 7)) << 4) + (col & 7) * 2;
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        uint2 uh, ul;
+        reinterpret_cast<__nv_bfloat162 *>(&uh)[0] = h01;
+        reinterpret_cast<__nv_bfloat162 *>(&uh)[1] = h23;
+        reinterpret_cast<__nv_bfloat162 *>(&ul)[0] = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+        reinterpret_cast<__nv_bfloat162 *>(&ul)[1] = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+        *reinterpret_cast<uint2 *>(sm_base + OFF_HD + off) = uh;
+        *reinterpret_cast<uint2 *>(sm_base + OFF_HD + 16384 + off) = ul;
+      }
+      // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |x|, |g| for the fp16 scaling; g . x
+      float gmax = 0.f, xmax = 0.f, gx = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const int c0 = 32 * hf + 8 * c8;
+        float gv[8], xv[8], hi[8], lo[8];
+        ld8_bf16(sG, r, c0, gv);
+        ld8_bf16(sX, r, c0, xv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
           const float t = eacs * gv[i];
           hi[i] = __bfloat162float(__float2bfloat16_rn(t));
           lo[i] = t - hi[i];
@@ -577,95 +658,82 @@ __global__ void __launch_bounds__(kThreads, 1)
           xmax = fmaxf(xmax, fabsf(xv[i]));
           gx = fmaf(gv[i], xv[i], gx);
         }
-        st_row32_bf16(sm_base + OFF_GW, r, 32 * hf, hi);
-        st_row32_bf16(sm_base + OFF_GW + 16384, r, 32 * hf, lo);
+        st8_bf16(sm_base + OFF_GW, r, c0, hi);
+        st8_bf16(sm_base + OFF_GW + 16384, r, c0, lo);
       }
-      // H (fp32 state entering the chunk) -> bf16 hi + lo, [p][n]
-      {
-        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int e4 = tid + kEpiThreads * j;
-          const float4 v = __ldg(hs + e4);
-          const int pp = (4 * e4) / kN, nn = (4 * e4) % kN;
-          const int col = nn % 64;
-          const uint32_t off = (nn / 64) * 8192 + pp * 128 + (((col >> 3) ^ (pp & 7)) << 4) + (col & 7) * 2;
-          const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
-          const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-          uint2 uh, ul;
-          reinterpret_cast<__nv_bfloat162 *>(&uh)[0] = h01;
-          reinterpret_cast<__nv_bfloat162 *>(&uh)[1] = h23;
-          reinterpret_cast<__nv_bfloat162 *>(&ul)[0] = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-          reinterpret_cast<__nv_bfloat162 *>(&ul)[1] = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-          *reinterpret_cast<uint2 *>(sm_base + OFF_HD + off) = uh;
-          *reinterpret_cast<uint2 *>(sm_base + OFF_HD + 16384 + off) = ul;
-        }
-      }
+      // warm L2 with the next head's state tile (32 KB) while this head runs
+      if (tid == 0 && k + 1 < hpg)
+        umma::prefetch_l2(p.states + (((bi * s.nc + c) * s.H + h + 1) * kP) * kN, kP * kN * 4);
       // x and g -> fp16 scaled by exact powers of two, in place
-      gmax = ep_max(gmax, sm);
-      xmax = ep_max(xmax, sm);
+      ep_max2(gmax, xmax, sm);
       const int kg = fp16_scale_exp(gmax), kx = fp16_scale_exp(xmax);
       const float ug = ldexpf(1.f, -kg), ux = ldexpf(1.f, -kx);
+      const float ugx = ug * ux;
+      if (hf == 0) sm->dtu[r] = dtr * ugx;
       {
-        float v[32];
-        ld_row32_bf16(sG, r, 32 * hf, v);
-        const float sg = ldexpf(1.f, kg);
+        const float sg = ldexpf(1.f, kg), sx = ldexpf(1.f, kx);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= sg;
-        st_row32_f16(sG, r, 32 * hf, v);
-        ld_row32_bf16(sX, r, 32 * hf, v);
-        const float sx = ldexpf(1.f, kx);
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const int c0 = 32 * hf + 8 * c8;
+          float v[8];
+          ld8_bf16(sG, r, c0, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= sx;
-        st_row32_f16(sX, r, 32 * hf, v);
+          for (int i = 0; i < 8; ++i) v[i] *= sg;
+          st_row8_f16(sG, r, c0, v);
+          ld8_bf16(sX, r, c0, v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] *= sx;
+          st_row8_f16(sX, r, c0, v);
+        }
       }
       umma::fence_proxy_async_smem();
+      if (tid == 128) umma::tma_store_wait_read();  // dx staging (the M16 buffer) has been read out
       ep_sync();
       if (tid == 0) umma::mbar_arrive(&bars[E_X16]);
 
-      // ---- E1: intra-chunk matrices from g x^T (TMEM) and C B^T (registers)
+      // ---- E1: intra-chunk matrices from g x^T (TMEM, raw fp16 scale) and C B^T (registers)
       ewait(&bars[B_G1], par, p.err);
       umma::fence_after_sync();
-      const float ugx = ug * ux;
-      float rowp = 0.f, diag = 0.f;
-      float csum[4];
+      float rowp = 0.f, diag = 0.f;   // raw units: times sM 2^(kg+kx)
+      float csum[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c0 = 64 * hf + 16 * j;
-        float m16[16];
+      for (int j = 0; j < 8; ++j) {
+        const int c0 = 64 * hf + 8 * j;
+        float m16[8];
         csum[j] = 0.f;
         if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
-          float gxv[16], ws[16], mgs[16];
-          umma::tmem_ld16(tmem + lane_off + T_RA + c0, gxv);
-          umma::tmem_ld16(tmem + lane_off + T_WS + c0, ws);
+          float gxv[8], ws[8], mgs[8];
+          umma::tmem_ld8(tmem + lane_off + T_RA + c0, gxv);
+          umma::tmem_ld8(tmem + lane_off + T_WS + c0, ws);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int sidx = c0 + i;
-            float mval = 0.f;
-            mgs[i] = 0.f;
-            if (sidx <= r) {
-              const float L = expf(acs_diff(ahr, alr, sm->acs_hi[sidx], sm->acs_lo[sidx]));
-              const float dts = sm->dtv[sidx];
-              const float gxs = gxv[i] * ugx;
-              mval = cb[16 * j + i] * L;
-              ws[i] = fmaf(L * gxs, dts, ws[i]);
-              const float mg = mval * gxs;
-              if (sidx < r) {
-                rowp = fmaf(mg, dts, rowp);
-                mgs[i] = mg;
-              } else {
-                diag = mg;
-              }
+          for (int e4 = 0; e4 < 2; ++e4) {
+            const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[c0 + 4 * e4]);
+            const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtu[c0 + 4 * e4]);
+            const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
+            const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
+#pragma unroll
+            for (int e1 = 0; e1 < 4; ++e1) {
+              const int e = 4 * e4 + e1;
+              const int sidx = c0 + e;
+              const float L = umma::ex2_approx(a2r - a2s[e1]);
+              const float lg = L * gxv[e];
+              const float cbv = cbs[8 * j + e];
+              const float mgr = cbv * lg;
+              const bool causal = sidx <= r, strict = sidx < r;
+              ws[e] = causal ? fmaf(lg, dus[e1], ws[e]) : ws[e];
+              m16[e] = causal ? cbv * L : 0.f;
+              mgs[e] = strict ? mgr : 0.f;
+              rowp = strict ? fmaf(mgr, dus[e1], rowp) : rowp;   // dt_s ugx: undone with the other scales
+              diag = (sidx == r) ? mgr : diag;
             }
-            m16[i] = mval * sM;
           }
-          umma::tmem_st16(tmem + lane_off + T_WS + c0, ws);
-          csum[j] = warp_colsum16(mgs, lane);
+          umma::tmem_st8(tmem + lane_off + T_WS + c0, ws);
+          csum[j] = warp_colsum8(mgs, lane);
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m16[i] = 0.f;
+          for (int e = 0; e < 8; ++e) m16[e] = 0.f;
         }
-        st_row16_f16(sm_base + OFF_M16 + hf * 16384, r, 16 * j, m16);
+        st_row8_f16(sm_base + OFF_M16 + hf * 16384, r, 8 * j, m16);
       }
       umma::tmem_wait_st();
       umma::fence_before_sync();
@@ -678,23 +746,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_after_sync();
       // the lo half of GW is idle from here to the next head: exchange scratch
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((lane & 1) == 0) xb->colpart[q][64 * hf + 16 * j + col16_of_lane(lane)] = csum[j];
-      if (hf == 1) {
-        xb->xch[0][r] = rowp;
-        xb->xch[1][r] = diag;
-        xb->xch[3][r] = gx;
-      }
+      for (int j = 0; j < 8; ++j)
+        if ((lane & 3) == 0) xb->colpart[q][64 * hf + 8 * j + col8_of_lane(lane)] = csum[j];
+      xb->v[0][hf][r] = rowp;
+      xb->v[1][hf][r] = diag;
+      xb->v[3][hf][r] = gx;
+      if (hf == 0) sm->dtu[r] = cumdt;   // dtu is no longer needed this head: keep the cumulative step there
       float inter_part = 0.f;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        float ch[16], gv[16];
-        umma::tmem_ld16(tmem + lane_off + T_CH + 32 * hf + 16 * u, ch);
-        ld_row16_f16(sG, r, 32 * hf + 16 * u, gv);
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float ch[8], gv[8];
+        umma::tmem_ld8(tmem + lane_off + T_CH + 32 * hf + 8 * c8, ch);
+        ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) inter_part = fmaf(gv[i], ch[i], inter_part);
+        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch[i], inter_part);
       }
-      inter_part *= ug;
+      xb->v[2][hf][r] = inter_part;
       if (has_next) {
         const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
         if (tid == 0) {
@@ -704,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               atomicOr(p.err, 1);
               break;
             }
-            __nanosleep(100);
+            __nanosleep(64);
           }
         }
         ep_sync();
@@ -713,7 +780,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       float hdot = 0.f;
       {
         const float *src = p.ring + ((((c + 1) % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
-        const float *hs = p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN;
         float *dst = nullptr;
         if (here_start) {
           if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
@@ -722,113 +788,158 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t *panel = sm_base + OFF_HD + (n / 64) * 8192;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float dh[16];
-          umma::tmem_ld16(tmem + lane_off + T_DH + 32 * hf + 16 * u, dh);  // lane = n, columns p
+        for (int u = 0; u < 4; ++u) {
+          const int p0 = 32 * hf + 8 * u;
+          float ds[8], hv[8], dh[8];
+          if (has_next) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int pp = 32 * hf + 16 * u + i;
-            float ds = 0.f;
-            if (has_next) {
-              ds = __ldcg(src + pp * kN + n);
-              hdot = fmaf(__ldg(hs + pp * kN + n), ds, hdot);
-            }
-            if (dst) __stcg(dst + pp * kN + n, fmaf(eE, ds, dh[i]));
-            st_bf16(panel, pp, n % 64, ds);  // dS -> bf16 [p][n]
+            for (int i = 0; i < 8; ++i) ds[i] = __ldcg(src + (p0 + i) * kN + n);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ds[i] = 0.f;
+          }
+          // H = hi + lo from shared memory, read before dS overwrites the hi half
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t o = umma::sw128_offset_bf16(uint32_t(p0 + i), uint32_t(n % 64));
+            hv[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(panel + o)) +
+                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(panel + 16384 + o));
+          }
+          umma::tmem_ld8(tmem + lane_off + T_DH + p0, dh);  // lane = n, columns p
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            hdot = fmaf(hv[i], ds[i], hdot);
+            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, ds[i], dh[i]));
+            st_bf16(panel, p0 + i, n % 64, ds[i]);  // dS -> bf16 [p][n]
           }
         }
       }
       umma::fence_before_sync();
-      __threadfence();
-      const float dEpass = eE * ep_sum(hdot, sm);  // its barriers also order the ring stores before the flag
+      // the barriers of this sum order every thread's ring stores before thread 0's release of the flag
+      const float dEpass = eE * ep_sum(hdot, sm);
+      if (tid == 0) sm->red[30] = dEpass;
       if (tid == 0 && !here_start && c != p.silent_chunk)
         st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h), 1);
       // w o x -> GW hi half (bf16)
       {
-        float xv[32];
-        ld_row32_f16(sX, r, 32 * hf, xv);
         const float f = wr * ux;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] *= f;
-        st_row32_bf16(sm_base + OFF_GW, r, 32 * hf, xv);
+        for (int c8 = 0; c8 < 4; ++c8) {
+          float xv[8];
+          ld8_f16(sX, r, 32 * hf + 8 * c8, xv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xv[i] *= f;
+          st8_bf16(sm_base + OFF_GW, r, 32 * hf + 8 * c8, xv);
+        }
       }
       umma::fence_proxy_async_smem();
-      if (hf == 1) xb->xch[2][r] = inter_part;
       ep_sync();
       if (tid == 0) umma::mbar_arrive(&bars[E_DS]);
 
       // ---- E4: dx and the row dot product x . Y
+      if (hf == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
       const float unscale = ldexpf(1.f, -(kM + kg));
       float sxy = 0.f;
       {
-        float *dxr = p.dx + ((row0 + r) * s.H + h) * kP + 32 * hf;
+        // dx rows staged in the (now idle) M16 buffer, 128-byte swizzled fp32, then TMA-stored
+        uint8_t *stage = sm_base + OFF_M16 + hf * 16384;
+        const float dg = Dh * ug;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float d1[16], y[16], xv[16], gv[16];
-          umma::tmem_ld16(tmem + lane_off + T_RA + 32 * hf + 16 * u, d1);
-          umma::tmem_ld16(tmem + lane_off + T_RA + 64 + 32 * hf + 16 * u, y);
-          ld_row16_f16(sX, r, 32 * hf + 16 * u, xv);
-          ld_row16_f16(sG, r, 32 * hf + 16 * u, gv);
+        for (int c8 = 0; c8 < 4; ++c8) {
+          float d1[8], y[8], xv[8], gv[8];
+          umma::tmem_ld8(tmem + lane_off + T_RA + 32 * hf + 8 * c8, d1);
+          umma::tmem_ld8(tmem + lane_off + T_RA + 64 + 32 * hf + 8 * c8, y);
+          ld8_f16(sX, r, 32 * hf + 8 * c8, xv);
+          ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
 #pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4) {
+          for (int i4 = 0; i4 < 2; ++i4) {
             float o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int i = 4 * i4 + e;
               sxy = fmaf(xv[i], y[i], sxy);
-              o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], (Dh * ug) * gv[i]));
+              o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], dg * gv[i]));
             }
-            *reinterpret_cast<float4 *>(dxr + 16 * u + 4 * i4) = make_float4(o[0], o[1], o[2], o[3]);
+            const int chunk = (2 * c8 + i4) ^ (r & 7);
+            *reinterpret_cast<float4 *>(stage + r * 128 + chunk * 16) = make_float4(o[0], o[1], o[2], o[3]);
           }
         }
       }
       sxy *= ux;
       umma::fence_before_sync();
-      if (hf == 1) xb->xch[4][r] = sxy;
+      umma::fence_proxy_async_smem();
+      xb->v[4][hf][r] = sxy;
       ep_sync();
-      if (tid == 0) {
+      // a thread of the upper column half issues the hand-offs: warps 0-3 go straight on to E5
+      if (tid == 128) {
         umma::mbar_arrive(&bars[E_RA]);
         umma::mbar_arrive(&bars[E_XG0 + st]);
+        umma::tma_store_2d(&tm_dx, sm_base + OFF_M16, int(h * kP), int(row0));
+        umma::tma_store_2d(&tm_dx, sm_base + OFF_M16 + 16384, int(h * kP + 32), int(row0));
+        umma::tma_store_commit();
       }
 
-      // ---- E5: decay gradient, reverse cumsum, ddt, dA/dD partials (rows, warps 0-3)
-      if (hf == 0) {
-        rowp += xb->xch[0][r];
-        diag += xb->xch[1][r];
-        sxy += xb->xch[4][r];
-        gx += xb->xch[3][r];
-        const float inter = eacs * (inter_part + xb->xch[2][r]);
+      // ---- E5: decay gradient, reverse cumsum, ddt, dA/dD partials
+      // Both column halves form the same per-row values (from shared memory);
+      // the lower half runs the suffix scan while the upper half runs the row
+      // sums, in parallel, then the lower half finishes the rows.
+      {
+        const float a2r5 = sm->a2[r], a2E5 = sm->a2[kQ - 1], dt5 = sm->dtv[r];
+        const float eEA5 = umma::ex2_approx(a2E5 - a2r5), wr5 = eEA5 * dt5;
+        const float ug5 = ldexpf(1.f, -kg), ugx5 = ldexpf(1.f, -(kg + kx));
+        const float raw = ugx5 / sM;   // raw E1 units -> true units
+        const float rowp5 = (xb->v[0][0][r] + xb->v[0][1][r]) * (raw / ugx5);   // rowp also carries dt_s ugx
+        const float diag5 = (xb->v[1][0][r] + xb->v[1][1][r]) * raw;
+        const float inter = umma::ex2_approx(a2r5) * ug5 * (xb->v[2][0][r] + xb->v[2][1][r]);
+        const float gx5 = xb->v[3][0][r] + xb->v[3][1][r];
+        const float sxy5 = xb->v[4][0][r] + xb->v[4][1][r];
+        const float cumdt5 = sm->dtu[r];
         // strict column sum of M o Gx for column r, quadrants in fixed order
         const float cstrict =
-            ((xb->colpart[0][r] + xb->colpart[1][r]) + xb->colpart[2][r]) + xb->colpart[3][r];
-        const float dintra = cstrict + diag;
-        const float colp = dtr * cstrict;
-        const float u = wr * sxy;
-        const float dacs = rowp - colp + inter - u;
-        const float su = lo_sum(u, sm, 0);
-        float sfx = dacs;  // suffix sum over rows: fixed tree in the warp, fixed order across warps
+            (((xb->colpart[0][r] + xb->colpart[1][r]) + xb->colpart[2][r]) + xb->colpart[3][r]) * raw;
+        const float dintra = cstrict + diag5;
+        const float colp = dt5 * cstrict;
+        const float u = wr5 * sxy5;
+        const float dacs = rowp5 - colp + inter - u;
+        float sfx = dacs;
+        if (hf == 0) {
+          // suffix sum over rows: fixed tree in the warp, fixed order across warps
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_down_sync(0xffffffffu, sfx, o);
-          if (lane + o < 32) sfx += v;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_down_sync(0xffffffffu, sfx, o);
+            if (lane + o < 32) sfx += v;
+          }
+          if (lane == 0) sm->red[q] = sfx;
+        } else {
+          // warp totals of u, g.x and dacs * cumdt
+          const float wu = warp_sum(u), wg = warp_sum(gx5), wc = warp_sum(dacs * cumdt5);
+          if (lane == 0) {
+            sm->red[4 + q] = wu;
+            sm->red[8 + q] = wg;
+            sm->red[12 + q] = wc;
+          }
         }
-        if (lane == 0) sm->red[20 + q] = sfx;
-        lo_sync();
-        float off = 0.f;
-        for (int w = 3; w > q; --w) off += sm->red[20 + w];
-        const float da = (sfx + off) + (su + dEpass);
-        p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA * sxy);
-        const float dap = lo_sum(dtr * da, sm, 1);
-        const float ddp = lo_sum(gx, sm, 2);
-        if (tid == 0) {
-          if (p.atomic) {
-            atomicAdd(p.dA + h, dap);
-            atomicAdd(p.dD + h, ddp);
-          } else {
-            p.dA_part[(bi * s.nc + c) * s.H + h] = dap;
-            p.dD_part[(bi * s.nc + c) * s.H + h] = ddp;
+        ep_sync();
+        if (hf == 0) {
+          float off = 0.f;
+          for (int w = 3; w > q; --w) off += sm->red[w];
+          const float su = ((sm->red[4] + sm->red[5]) + sm->red[6]) + sm->red[7];
+          const float K = su + sm->red[30];
+          const float da = (sfx + off) + K;
+          p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA5 * sxy5);
+          if (tid == 0) {
+            const float sg = ((sm->red[8] + sm->red[9]) + sm->red[10]) + sm->red[11];
+            const float sc = ((sm->red[12] + sm->red[13]) + sm->red[14]) + sm->red[15];
+            const float dap = fmaf(K, sm->red[31], sc);
+            if (p.atomic) {
+              atomicAdd(p.dA + h, dap);
+              atomicAdd(p.dD + h, sg);
+            } else {
+              p.dA_part[(bi * s.nc + c) * s.H + h] = dap;
+              p.dD_part[(bi * s.nc + c) * s.H + h] = sg;
+            }
           }
         }
       }
@@ -870,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4 *>(o + 4 * i4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
     }
     umma::fence_before_sync();
+    if (tid == 128) umma::tma_store_wait_all();
   }
   __syncthreads();
   if (warp == 9) {
@@ -932,7 +1044,7 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
                       Trace &tr) {
   Carver cv(ws);
   FusedWs w = carve_fused(cv, s, opt.ring_depth);
-  CUtensorMap tm_x, tm_g, tm_b, tm_c;
+  CUtensorMap tm_x, tm_g, tm_b, tm_c, tm_dx;
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
                     128, true) ||
@@ -941,6 +1053,8 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
       !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
                     128, true) ||
       !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+                    128, true) ||
+      !make_tmap_2d(&tm_dx, a.dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 32,
                     128, true))
     return cudaErrorInvalidValue;
   cudaError_t err = cudaMemsetAsync(w.status, 0, 64 * sizeof(int), st);
@@ -985,7 +1099,7 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
   p.silent_chunk = opt.silent_chunk;
   const unsigned units = unsigned(s.b * s.nc * s.G);
   tr.mark(st);
-  fused_bwd_kernel<<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c);
+  fused_bwd_kernel<<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   tr.mark(st);
   if (!opt.atomic) {
     tr.mark(st);

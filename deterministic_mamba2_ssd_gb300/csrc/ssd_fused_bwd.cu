@@ -71,7 +71,7 @@ constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
 constexpr uint32_t T_CH = T_RA, T_DH = T_RA + 64;
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG0, B_XG1, E_XG0, E_XG1, E_X16, B_G1, B_G2, E_M16, E_DS, B_G4, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG0, B_XG1, E_XG0, E_XG1, E_X16, B_G1, B_G2, E_M16, E_CHR, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -90,8 +90,7 @@ static_assert(sizeof(Small) <= SMALL_BYTES, "small region");
 // exchange scratch between the two column halves of a row, and the
 // per-quadrant partial column sums (strict lower part of M o Gx)
 struct XBuf {
-  float v[5][2][kQ];     // per column half: rowp, diag, inter, g.x, x.Y
-  float colpart[4][kQ];
+  float v[5][2][kQ];     // per column half: row sum of M o Gx o dt, x.D1, inter, g.x, x.Y
 };
 static_assert(sizeof(XBuf) <= 16384, "scratch");
 
@@ -125,49 +124,6 @@ __device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
   }
 }
 
-// 32 consecutive bf16 of row r (columns c0..c0+31, c0 % 32 == 0) of a 64-col panel
-__device__ __forceinline__ void ld_row32_bf16(const uint8_t *panel, int r, int c0, float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    uint4 u = *reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16);
-    bf16x8_to_f32(u, &v[8 * j]);
-  }
-}
-
-__device__ __forceinline__ void st_row32_bf16(uint8_t *panel, int r, int c0, const float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 u;
-    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
-  }
-}
-
-__device__ __forceinline__ void st_row32_f16(uint8_t *panel, int r, int c0, const float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint4 u;
-    __half2 *h = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
-  }
-}
-
-__device__ __forceinline__ void ld_row16_bf16(const uint8_t *panel, int r, int c0, float (&v)[16]) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    uint4 u = *reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16);
-    bf16x8_to_f32(u, &v[8 * j]);
-  }
-}
-
 __device__ __forceinline__ void st_row16_bf16(uint8_t *panel, int r, int c0, const float (&v)[16]) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
@@ -180,18 +136,6 @@ __device__ __forceinline__ void st_row16_bf16(uint8_t *panel, int r, int c0, con
   }
 }
 
-__device__ __forceinline__ void st_row16_f16(uint8_t *panel, int r, int c0, const float (&v)[16]) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    uint4 u;
-    __half2 *h = reinterpret_cast<__half2 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
-  }
-}
-
 __device__ __forceinline__ void f16x8_to_f32(uint4 u, float *f) {
   const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
@@ -199,22 +143,6 @@ __device__ __forceinline__ void f16x8_to_f32(uint4 u, float *f) {
     float2 t = __half22float2(h[i]);
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
-  }
-}
-
-__device__ __forceinline__ void ld_row32_f16(const uint8_t *panel, int r, int c0, float (&v)[32]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16), &v[8 * j]);
-  }
-}
-
-__device__ __forceinline__ void ld_row16_f16(const uint8_t *panel, int r, int c0, float (&v)[16]) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int chunk = ((c0 >> 3) + j) ^ (r & 7);
-    f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + chunk * 16), &v[8 * j]);
   }
 }
 
@@ -256,19 +184,6 @@ __device__ __forceinline__ int fp16_scale_exp(float mx) {
   return max(-120, min(120, k));
 }
 
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-  s = __fadd_rn(a, b);
-  const float bb = __fsub_rn(s, a);
-  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-// (h1,l1) + (h2,l2): left operand is the earlier part of the sequence
-__device__ __forceinline__ void comp_add(float h1, float l1, float h2, float l2, float &h, float &l) {
-  float s, e;
-  two_sum(h1, h2, s, e);
-  h = s;
-  l = __fadd_rn(__fadd_rn(l1, l2), e);
-}
-
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -307,57 +222,6 @@ __device__ __forceinline__ void wait_bar_impl(uint64_t *b, uint32_t parity, int 
     __syncwarp();                                              \
   } while (0)
 
-// Column sums of a 32 x 16 block held one row per lane (v[c], c < 16): a
-// fixed butterfly (16 shuffles) leaves the total of column col16(lane) in
-// lanes 2k and 2k+1.  Same tree on every call.
-__device__ __forceinline__ float warp_colsum16(float (&v)[16], int lane) {
-#pragma unroll
-  for (int half = 8, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
-    const bool upper = (lane & bit) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-    }
-  }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-// Same for a 32 x 8 block: column total lands in the 4 lanes with equal bits 4..2.
-__device__ __forceinline__ float warp_colsum8(float (&v)[8], int lane) {
-#pragma unroll
-  for (int half = 4, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
-    const bool upper = (lane & bit) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-    }
-  }
-  float t = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
-  return t + __shfl_xor_sync(0xffffffffu, t, 1);
-}
-__device__ __forceinline__ int col8_of_lane(int lane) {
-  return ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-}
-__device__ __forceinline__ int col16_of_lane(int lane) {
-  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-}
-
-// Deterministic sum over the 256 epilogue threads (fixed tree); result in all.
-__device__ __forceinline__ float ep_sum(float v, Small *sm) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5;
-  ep_sync();
-  if ((threadIdx.x & 31) == 0) sm->red[warp] = v;
-  ep_sync();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) t += sm->red[w];
-  return t;
-}
 // Maxima of two values over the 256 epilogue threads in one round.
 __device__ __forceinline__ void ep_max2(float &a, float &b, Small *sm) {
 #pragma unroll
@@ -403,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], 1);
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], i == E_CHR ? 8 : 1);  // E_CHR: one arrival per epilogue warp
     umma::fence_mbar_init();
     sm->unit = atomicAdd(p.ticket, 1);
     sm->abort = 0;
@@ -435,14 +299,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int(g * kN + j * 64), int(row0), &bars[B_BC]);
         umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int(g * kN + j * 64), int(row0), &bars[B_BC]);
       }
-      for (int k = 0; k < hpg; ++k) {
+      auto load_xg = [&](int k) {
         const int st = k & 1;
-        if (k >= 2) wait_bar(&bars[E_XG0 + st], uint32_t(((k >> 1) - 1) & 1), p.err);
         const int64_t h = g * hpg + k;
         uint8_t *dst = sm_base + (st ? OFF_X1 : OFF_X0);
         umma::mbar_expect_tx(&bars[B_XG0 + st], 32768);
         umma::tma_load_2d(dst, &tm_x, int(h * kP), int(row0), &bars[B_XG0 + st]);
         umma::tma_load_2d(dst + 16384, &tm_g, int(h * kP), int(row0), &bars[B_XG0 + st]);
+      };
+      load_xg(0);
+      if (hpg > 1) load_xg(1);
+      // This thread also publishes each head's state gradient to the chunk
+      // before: the release waits for the epilogue's ring stores to reach L2,
+      // which would otherwise stall an epilogue warp.
+      const bool publish = !is_seq_start(p.seq_idx, bi, s.T, t0) && c != p.silent_chunk;
+      for (int k = 0; k < hpg; ++k) {
+        // ring stores of head k done (epilogue barrier + arrive); one barrier per head parity, so
+        // the epilogue can never be a full phase ahead of this wait
+        wait_bar(&bars[E_DS0 + (k & 1)], uint32_t((k >> 1) & 1), p.err);
+        if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + g * hpg + k), 1);
+        if (k + 2 < hpg) {
+          wait_bar(&bars[E_XG0 + (k & 1)], uint32_t((k >> 1) & 1), p.err);
+          load_xg(k + 2);
+        }
       }
     }
   } else if (warp == 9) {
@@ -484,7 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kP; kk += 16)
           umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_f16_kk128, kk > 0);
         umma::mma_commit(&bars[B_G1]);
-        wait_bar(&bars[E_M16], par, p.err);  // g x^T consumed; G~ and H (hi, lo) and M16 in smem
+        // dC += G~ H^T  (M = t, N = n, K = p): hi*hi + hi*lo + lo*hi; runs while the epilogue reads g x^T
+        for (int part = 0; part < 3; ++part) {
+          const uint32_t aA = part == 2 ? aGl : aGh, aBb = part == 1 ? aHl : aHh;
+          for (int kk = 0; kk < kP; kk += 16)
+            umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), mdesc(aBb, 8192, kk), id_km128,
+                           (k > 0) || (part > 0) || (kk > 0));
+        }
+        wait_bar(&bars[E_M16], par, p.err);  // g x^T consumed; M16 in smem
         umma::fence_after_sync();
         // CH = C (H_hi + H_lo)  (M = t, N = p, K = n)
         for (int part = 0; part < 2; ++part)
@@ -496,19 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kQ; kk += 16)
             umma::mma_bf16(tmem + T_DH, mdesc(aC, 16384, kk), mdesc(part ? aGl : aGh, 16384, kk), id_mm64,
                            (part > 0) || (kk > 0));
-        // dC += G~ H^T  (M = t, N = n, K = p): hi*hi + hi*lo + lo*hi
-        for (int part = 0; part < 3; ++part) {
-          const uint32_t aA = part == 2 ? aGl : aGh, aBb = part == 1 ? aHl : aHh;
-          for (int kk = 0; kk < kP; kk += 16)
-            umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), mdesc(aBb, 8192, kk), id_km128,
-                           (k > 0) || (part > 0) || (kk > 0));
-        }
         umma::mma_commit(&bars[B_G2]);
-        wait_bar(&bars[E_DS], par, p.err);  // CH, dHscan read; dS and w o x in smem
+        wait_bar(&bars[E_CHR], par, p.err);  // CH read: its columns take D1 while the chain step runs
         umma::fence_after_sync();
         // D1 = M^T g  (fp16 scaled operands; M = s, N = p, K = t)
         for (int kk = 0; kk < kQ; kk += 16)
           umma::mma_bf16(tmem + T_RA, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
+        wait_bar(&bars[E_DS0 + st], uint32_t((k >> 1) & 1), p.err);  // dHscan read; dS and w o x in smem
+        umma::fence_after_sync();
         // Y = B dS^T  (M = t, N = p, K = n)
         for (int kk = 0; kk < kN; kk += 16)
           umma::mma_bf16(tmem + T_RA + 64, kdesc(aB, 16384, kk), kdesc(aHh, 8192, kk), id_kk64, kk > 0);
@@ -691,49 +572,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       ep_sync();
       if (tid == 0) umma::mbar_arrive(&bars[E_X16]);
 
-      // ---- E1: intra-chunk matrices from g x^T (TMEM, raw fp16 scale) and C B^T (registers)
+      // ---- E1: intra-chunk matrices from g x^T (TMEM, raw fp16 scale) and C B^T (registers).
+      // The decay gradient needs the row and the column sums of M o Gx o dt;
+      // both are taken from the same fp16-rounded M that the dx product
+      // uses (the column sums come out of that product in E4), so their
+      // difference keeps its cancellation exact up to fp32 accumulation.
       ewait(&bars[B_G1], par, p.err);
       umma::fence_after_sync();
-      float rowp = 0.f, diag = 0.f;   // raw units: times sM 2^(kg+kx)
-      float csum[8];
+      float rowp = 0.f;   // sum_s M16_rs Gx_rs dt_s, times sM
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int c0 = 64 * hf + 8 * j;
-        float m16[8];
-        csum[j] = 0.f;
+        uint32_t m16[4];
         if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
-          float gxv[8], ws[8], mgs[8];
-          umma::tmem_ld8(tmem + lane_off + T_RA + c0, gxv);
-          umma::tmem_ld8(tmem + lane_off + T_WS + c0, ws);
+          float gxv[8], ws[8];
+          umma::tmem_ld8x2(tmem + lane_off + T_RA + c0, tmem + lane_off + T_WS + c0, gxv, ws);
+          const bool diag_blk = c0 + 8 > 32 * q;   // may cross the diagonal for some lane
 #pragma unroll
           for (int e4 = 0; e4 < 2; ++e4) {
             const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[c0 + 4 * e4]);
             const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtu[c0 + 4 * e4]);
             const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
             const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
+            float mv[4];
 #pragma unroll
             for (int e1 = 0; e1 < 4; ++e1) {
               const int e = 4 * e4 + e1;
-              const int sidx = c0 + e;
-              const float L = umma::ex2_approx(a2r - a2s[e1]);
-              const float lg = L * gxv[e];
-              const float cbv = cbs[8 * j + e];
-              const float mgr = cbv * lg;
-              const bool causal = sidx <= r, strict = sidx < r;
-              ws[e] = causal ? fmaf(lg, dus[e1], ws[e]) : ws[e];
-              m16[e] = causal ? cbv * L : 0.f;
-              mgs[e] = strict ? mgr : 0.f;
-              rowp = strict ? fmaf(mgr, dus[e1], rowp) : rowp;   // dt_s ugx: undone with the other scales
-              diag = (sidx == r) ? mgr : diag;
+              const bool causal = !diag_blk || (c0 + e <= r);
+              const float L = causal ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
+              const float gd = gxv[e] * dus[e1];       // Gx dt (true units)
+              ws[e] = fmaf(L, gd, ws[e]);
+              mv[e1] = cbs[8 * j + e] * L;
             }
+            const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            rowp = fmaf(f01.x, gxv[4 * e4 + 0] * dus[0], rowp);
+            rowp = fmaf(f01.y, gxv[4 * e4 + 1] * dus[1], rowp);
+            rowp = fmaf(f23.x, gxv[4 * e4 + 2] * dus[2], rowp);
+            rowp = fmaf(f23.y, gxv[4 * e4 + 3] * dus[3], rowp);
+            m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
+            m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
           }
           umma::tmem_st8(tmem + lane_off + T_WS + c0, ws);
-          csum[j] = warp_colsum8(mgs, lane);
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) m16[e] = 0.f;
+          for (int e = 0; e < 4; ++e) m16[e] = 0u;
         }
-        st_row8_f16(sm_base + OFF_M16 + hf * 16384, r, 8 * j, m16);
+        *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + hf * 16384 + r * 128 + ((j ^ (r & 7)) << 4)) =
+            make_uint4(m16[0], m16[1], m16[2], m16[3]);
       }
       umma::tmem_wait_st();
       umma::fence_before_sync();
@@ -745,34 +631,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       ewait(&bars[B_G2], par, p.err);
       umma::fence_after_sync();
       // the lo half of GW is idle from here to the next head: exchange scratch
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if ((lane & 3) == 0) xb->colpart[q][64 * hf + 8 * j + col8_of_lane(lane)] = csum[j];
       xb->v[0][hf][r] = rowp;
-      xb->v[1][hf][r] = diag;
       xb->v[3][hf][r] = gx;
       if (hf == 0) sm->dtu[r] = cumdt;   // dtu is no longer needed this head: keep the cumulative step there
       float inter_part = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        float ch[8], gv[8];
-        umma::tmem_ld8(tmem + lane_off + T_CH + 32 * hf + 8 * c8, ch);
+      for (int c8 = 0; c8 < 4; c8 += 2) {
+        float ch0[8], ch1[8], gv[8];
+        umma::tmem_ld8x2(tmem + lane_off + T_CH + 32 * hf + 8 * c8, tmem + lane_off + T_CH + 32 * hf + 8 * c8 + 8, ch0,
+                         ch1);
         ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch[i], inter_part);
+        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch0[i], inter_part);
+        ld8_f16(sG, r, 32 * hf + 8 * c8 + 8, gv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch1[i], inter_part);
       }
       xb->v[2][hf][r] = inter_part;
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&bars[E_CHR]);
       if (has_next) {
         const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
-        if (tid == 0) {
+        if (warp == 0) {   // the whole warp polls (one address), so it reaches the barrier converged
           uint32_t it = 0;
-          while (!sm->abort && ld_acquire_gpu(flag) == 0) {
+          while (!sm->abort && !__all_sync(0xffffffffu, ld_acquire_gpu(flag) != 0)) {
             if (++it > p.spin_limit) {
-              atomicOr(p.err, 1);
+              if (lane == 0) atomicOr(p.err, 1);
               break;
             }
             __nanosleep(64);
           }
+          __syncwarp();
         }
         ep_sync();
         (void)ld_acquire_gpu(flag);
@@ -787,17 +677,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
         }
         uint8_t *panel = sm_base + OFF_HD + (n / 64) * 8192;
+        // all 32 dS values of this thread in flight at once (one L2 round trip)
+        float ds[32];
+        if (has_next) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ds[i] = __ldcg(src + (32 * hf + i) * kN + n);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ds[i] = 0.f;
+        }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int p0 = 32 * hf + 8 * u;
-          float ds[8], hv[8], dh[8];
-          if (has_next) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ds[i] = __ldcg(src + (p0 + i) * kN + n);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ds[i] = 0.f;
-          }
+          float hv[8], dh[8];
           // H = hi + lo from shared memory, read before dS overwrites the hi half
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -808,18 +700,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma::tmem_ld8(tmem + lane_off + T_DH + p0, dh);  // lane = n, columns p
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            hdot = fmaf(hv[i], ds[i], hdot);
-            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, ds[i], dh[i]));
-            st_bf16(panel, p0 + i, n % 64, ds[i]);  // dS -> bf16 [p][n]
+            hdot = fmaf(hv[i], ds[8 * u + i], hdot);
+            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, ds[8 * u + i], dh[i]));
+            st_bf16(panel, p0 + i, n % 64, ds[8 * u + i]);  // dS -> bf16 [p][n]
           }
         }
       }
-      umma::fence_before_sync();
-      // the barriers of this sum order every thread's ring stores before thread 0's release of the flag
-      const float dEpass = eE * ep_sum(hdot, sm);
-      if (tid == 0) sm->red[30] = dEpass;
-      if (tid == 0 && !here_start && c != p.silent_chunk)
-        st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h), 1);
+      // per-warp partials of <H, dS>, folded in fixed order in E5
+      hdot = warp_sum(hdot);
+      if (lane == 0) sm->red[16 + warp] = hdot;
       // w o x -> GW hi half (bf16)
       {
         const float f = wr * ux;
@@ -832,16 +721,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           st8_bf16(sm_base + OFF_GW, r, 32 * hf + 8 * c8, xv);
         }
       }
+      umma::fence_before_sync();
       umma::fence_proxy_async_smem();
       ep_sync();
-      if (tid == 0) umma::mbar_arrive(&bars[E_DS]);
+      // the barrier above orders every thread's ring stores before this arrival, and the
+      // producer thread releases the chunk's flag only after waiting for it
+      if (tid == 0) umma::mbar_arrive(&bars[E_DS0 + st]);
 
       // ---- E4: dx and the row dot product x . Y
       if (hf == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
       const float unscale = ldexpf(1.f, -(kM + kg));
-      float sxy = 0.f;
+      float sxy = 0.f, xd1 = 0.f;   // x . Y and x . D1 (raw units) of this row
       {
         // dx rows staged in the (now idle) M16 buffer, 128-byte swizzled fp32, then TMA-stored
         uint8_t *stage = sm_base + OFF_M16 + hf * 16384;
@@ -849,8 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           float d1[8], y[8], xv[8], gv[8];
-          umma::tmem_ld8(tmem + lane_off + T_RA + 32 * hf + 8 * c8, d1);
-          umma::tmem_ld8(tmem + lane_off + T_RA + 64 + 32 * hf + 8 * c8, y);
+          umma::tmem_ld8x2(tmem + lane_off + T_RA + 32 * hf + 8 * c8, tmem + lane_off + T_RA + 64 + 32 * hf + 8 * c8, d1,
+                           y);
           ld8_f16(sX, r, 32 * hf + 8 * c8, xv);
           ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
 #pragma unroll
@@ -860,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) {
               const int i = 4 * i4 + e;
               sxy = fmaf(xv[i], y[i], sxy);
+              xd1 = fmaf(xv[i], d1[i], xd1);
               o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], dg * gv[i]));
             }
             const int chunk = (2 * c8 + i4) ^ (r & 7);
@@ -871,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_before_sync();
       umma::fence_proxy_async_smem();
       xb->v[4][hf][r] = sxy;
+      xb->v[1][hf][r] = xd1;
       ep_sync();
       // a thread of the upper column half issues the hand-offs: warps 0-3 go straight on to E5
       if (tid == 128) {
@@ -890,17 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float eEA5 = umma::ex2_approx(a2E5 - a2r5), wr5 = eEA5 * dt5;
         const float ug5 = ldexpf(1.f, -kg), ugx5 = ldexpf(1.f, -(kg + kx));
         const float raw = ugx5 / sM;   // raw E1 units -> true units
-        const float rowp5 = (xb->v[0][0][r] + xb->v[0][1][r]) * (raw / ugx5);   // rowp also carries dt_s ugx
-        const float diag5 = (xb->v[1][0][r] + xb->v[1][1][r]) * raw;
+        // inclusive row and column sums of M o Gx o dt: the diagonal cancels in their difference
+        const float rowp5 = (xb->v[0][0][r] + xb->v[0][1][r]) * (raw / ugx5);
+        const float dintra = (xb->v[1][0][r] + xb->v[1][1][r]) * raw;   // sum_t M_tr Gx_tr (x . D1)
         const float inter = umma::ex2_approx(a2r5) * ug5 * (xb->v[2][0][r] + xb->v[2][1][r]);
         const float gx5 = xb->v[3][0][r] + xb->v[3][1][r];
         const float sxy5 = xb->v[4][0][r] + xb->v[4][1][r];
         const float cumdt5 = sm->dtu[r];
-        // strict column sum of M o Gx for column r, quadrants in fixed order
-        const float cstrict =
-            (((xb->colpart[0][r] + xb->colpart[1][r]) + xb->colpart[2][r]) + xb->colpart[3][r]) * raw;
-        const float dintra = cstrict + diag5;
-        const float colp = dt5 * cstrict;
+        const float colp = dt5 * dintra;
         const float u = wr5 * sxy5;
         const float dacs = rowp5 - colp + inter - u;
         float sfx = dacs;
@@ -926,7 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           float off = 0.f;
           for (int w = 3; w > q; --w) off += sm->red[w];
           const float su = ((sm->red[4] + sm->red[5]) + sm->red[6]) + sm->red[7];
-          const float K = su + sm->red[30];
+          const float hsum = (((sm->red[16] + sm->red[17]) + (sm->red[18] + sm->red[19])) +
+                              ((sm->red[20] + sm->red[21]) + (sm->red[22] + sm->red[23])));
+          const float K = su + umma::ex2_approx(a2E5) * hsum;   // + dEpass = exp(E) <H, dS>
           const float da = (sfx + off) + K;
           p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA5 * sxy5);
           if (tid == 0) {

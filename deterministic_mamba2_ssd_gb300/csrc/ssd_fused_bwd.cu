@@ -23,9 +23,9 @@
 // so a unit only ever waits for a unit that is already running: no deadlock
 // whatever the number of resident CTAs.
 //
-// Roles (320 threads): warps 0-7 epilogue (thread = one row of a 128-row
-// tile and one half of its columns), warp 8 TMA producer, warp 9 TMEM owner
-// and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
+// Roles (576 threads): warps 0-15 epilogue (thread = one row of a 128-row
+// tile and one quarter of its columns; the TMEM lane quadrant of a warp is
+// its index mod 4), warp 16 TMA producer, warp 17 TMEM owner and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
 // the one product whose rounding dominates the error (dx_intra = M^T g with
 // M = CB o L) runs in fp16 with exact power-of-two scaling of both operands,
 // and the head-summed intra-chunk matrix for dB/dC is split into a bf16
@@ -44,15 +44,17 @@ namespace ssd {
 namespace {
 
 constexpr int kQ = 128, kN = 128, kP = 64;
-constexpr int kEpiThreads = 256;
-constexpr int kThreads = 320;
+constexpr int kEpiWarps = 16;                // 4 TMEM lane quadrants x 4 column quarters
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kTmaWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+constexpr int kThreads = kEpiThreads + 64;
 
 // shared memory map (offsets from the 1024-byte aligned base)
 constexpr uint32_t OFF_B = 0;          // B chunk  [t][n] bf16, 2 panels x 16 KB
 constexpr uint32_t OFF_C = 32768;      // C chunk  [t][n] bf16, 2 panels
-constexpr uint32_t OFF_X0 = 65536;     // stage 0: x [t][p] 16 KB, g 16 KB (bf16 from TMA, then scaled fp16 in place)
-constexpr uint32_t OFF_X1 = 98304;     // stage 1
-constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [p][n] bf16, 2 panels x 8 KB each; later dS (hi half)
+constexpr uint32_t OFF_XG = 65536;     // x [t][p] 16 KB, g 16 KB (bf16 from TMA, then scaled fp16 in place)
+constexpr uint32_t OFF_STG = 98304;    // fp32 [p][n] 32 KB: the state tile entering the chunk, then dS (bulk copies)
+constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [n][p] bf16, 16 KB each; later dS [n][p] (hi half)
 constexpr uint32_t OFF_GW = 163840;    // exp(Acs) o g hi | lo: [t][p] bf16; later w o x (hi half) + scratch (lo half)
 constexpr uint32_t OFF_M16 = 196608;   // scaled M: [t][s] fp16, 2 panels x 16 KB
 constexpr uint32_t OFF_SMALL = 229376;
@@ -62,7 +64,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // scratch that lives in the idle lo half of GW between the dC/dHscan products and the next head
 constexpr uint32_t OFF_XBUF = OFF_GW + 16384;
 // at the end of a unit the head-summed matrix W (hi, lo) reuses the x/g stages
-constexpr uint32_t OFF_WHI = OFF_X0, OFF_WLO = OFF_X1;
+constexpr uint32_t OFF_WHI = OFF_XG, OFF_WLO = OFF_STG;
 
 // TMEM columns
 // RA holds, in turn: C B^T (unit start), g x^T, then C H (cols 0-63) and
@@ -71,7 +73,7 @@ constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
 constexpr uint32_t T_CH = T_RA, T_DH = T_RA + 64;
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG0, B_XG1, E_XG0, E_XG1, E_X16, B_G1, B_G2, E_M16, E_CHR, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, E_HCONV, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_CH, B_G2, E_M16, E_CHR, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -79,7 +81,7 @@ struct Small {
   float a2[kQ];    // in-chunk cumulative decay of the current head, log2 units: A log2(e) cumsum(dt)
   float dtv[kQ];   // step sizes of the current head
   float dtu[kQ];   // step sizes times the scale that undoes the fp16 scaling of g x^T
-  float red[32];
+  float red[64];
   uint64_t bars[NBARS];
   uint32_t tmem_base;
   int unit;
@@ -90,7 +92,7 @@ static_assert(sizeof(Small) <= SMALL_BYTES, "small region");
 // exchange scratch between the two column halves of a row, and the
 // per-quadrant partial column sums (strict lower part of M o Gx)
 struct XBuf {
-  float v[5][2][kQ];     // per column half: row sum of M o Gx o dt, x.D1, inter, g.x, x.Y
+  float v[5][4][kQ];     // per column quarter: row sum of M o Gx o dt, x.D1, inter, g.x, x.Y
 };
 static_assert(sizeof(XBuf) <= 16384, "scratch");
 
@@ -170,11 +172,6 @@ __device__ __forceinline__ void st8_bf16(uint8_t *panel, int r, int c0, const fl
   *reinterpret_cast<uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)) = u;
 }
 
-__device__ __forceinline__ void st_bf16(uint8_t *panel, int r, int c, float v) {
-  *reinterpret_cast<__nv_bfloat16 *>(panel + umma::sw128_offset_bf16(uint32_t(r), uint32_t(c))) =
-      __float2bfloat16_rn(v);
-}
-
 // exponent k with max * 2^k in [2^14, 2^15) (0 for max == 0)
 __device__ __forceinline__ int fp16_scale_exp(float mx) {
   if (!(mx > 0.f)) return 0;
@@ -222,7 +219,7 @@ __device__ __forceinline__ void wait_bar_impl(uint64_t *b, uint32_t parity, int 
     __syncwarp();                                              \
   } while (0)
 
-// Maxima of two values over the 256 epilogue threads in one round.
+// Maxima of two values over all epilogue threads in one round.
 __device__ __forceinline__ void ep_max2(float &a, float &b, Small *sm) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -230,18 +227,18 @@ __device__ __forceinline__ void ep_max2(float &a, float &b, Small *sm) {
     b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
   }
   const int warp = threadIdx.x >> 5;
-  ep_sync();
+  // red[0 .. 2 kEpiWarps) is free here: every earlier reader passed a barrier since
   if ((threadIdx.x & 31) == 0) {
     sm->red[warp] = a;
-    sm->red[8 + warp] = b;
+    sm->red[kEpiWarps + warp] = b;
   }
   ep_sync();
   a = 0.f;
   b = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < kEpiWarps; ++w) {
     a = fmaxf(a, sm->red[w]);
-    b = fmaxf(b, sm->red[8 + w]);
+    b = fmaxf(b, sm->red[kEpiWarps + w]);
   }
 }
 __device__ __forceinline__ float warp_sum(float v) {
@@ -262,12 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Shape &s = p.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     umma::tmem_alloc(&sm->tmem_base, 512);
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], i == E_CHR ? 8 : 1);  // E_CHR: one arrival per epilogue warp
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_HCONV || i == E_GXL) ? kEpiWarps : 1);  // per-warp arrivals
     umma::fence_mbar_init();
     sm->unit = atomicAdd(p.ticket, 1);
     sm->abort = 0;
@@ -287,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t row0 = bi * s.T + t0;  // first global token row of the chunk
   const int hpg = int(s.hpg);
 
-  if (warp == 8) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       umma::tma_prefetch_desc(&tm_x);
@@ -299,32 +296,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int(g * kN + j * 64), int(row0), &bars[B_BC]);
         umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int(g * kN + j * 64), int(row0), &bars[B_BC]);
       }
-      auto load_xg = [&](int k) {
-        const int st = k & 1;
-        const int64_t h = g * hpg + k;
-        uint8_t *dst = sm_base + (st ? OFF_X1 : OFF_X0);
-        umma::mbar_expect_tx(&bars[B_XG0 + st], 32768);
-        umma::tma_load_2d(dst, &tm_x, int(h * kP), int(row0), &bars[B_XG0 + st]);
-        umma::tma_load_2d(dst + 16384, &tm_g, int(h * kP), int(row0), &bars[B_XG0 + st]);
-      };
-      load_xg(0);
-      if (hpg > 1) load_xg(1);
-      // This thread also publishes each head's state gradient to the chunk
-      // before: the release waits for the epilogue's ring stores to reach L2,
-      // which would otherwise stall an epilogue warp.
+      const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
+      // this thread also publishes each head's state gradient to the chunk before
       const bool publish = !is_seq_start(p.seq_idx, bi, s.T, t0) && c != p.silent_chunk;
+      const float *states = p.states + (bi * s.nc + c) * s.H * kP * kN;
+      int n_h = 0, n_xg = 0, n_ds = 0;   // copies issued per barrier (drained before exit)
       for (int k = 0; k < hpg; ++k) {
-        // ring stores of head k done (epilogue barrier + arrive); one barrier per head parity, so
-        // the epilogue can never be a full phase ahead of this wait
-        wait_bar(&bars[E_DS0 + (k & 1)], uint32_t((k >> 1) & 1), p.err);
-        if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + g * hpg + k), 1);
-        if (k + 2 < hpg) {
-          wait_bar(&bars[E_XG0 + (k & 1)], uint32_t((k >> 1) & 1), p.err);
-          load_xg(k + 2);
+        const int64_t h = g * hpg + k;
+        const uint32_t par = uint32_t(k & 1);
+        if (k > 0) {
+          // ring stores of head k-1 done (epilogue barrier + arrive), and the staging buffer is free again
+          wait_bar(&bars[E_DS0 + ((k - 1) & 1)], uint32_t(((k - 1) >> 1) & 1), p.err);
+          if (sm->abort) break;
+          if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h - 1), 1);
+        }
+        // the state tile entering the chunk, fp32, into the staging buffer
+        umma::mbar_expect_tx(&bars[B_H], kP * kN * 4);
+        umma::bulk_load(sm_base + OFF_STG, states + h * kP * kN, kP * kN * 4, &bars[B_H]);
+        ++n_h;
+        if (k + 1 < hpg) umma::prefetch_l2(states + (h + 1) * kP * kN, kP * kN * 4);
+        // x and g of this head once the previous head's are consumed
+        if (k > 0) {
+          wait_bar(&bars[E_XG], par ^ 1u, p.err);
+          if (sm->abort) break;
+        }
+        umma::mbar_expect_tx(&bars[B_XG], 32768);
+        umma::tma_load_2d(sm_base + OFF_XG, &tm_x, int(h * kP), int(row0), &bars[B_XG]);
+        umma::tma_load_2d(sm_base + OFF_XG + 16384, &tm_g, int(h * kP), int(row0), &bars[B_XG]);
+        ++n_xg;
+        if (k + 1 < hpg) {
+          umma::tma_prefetch_2d(&tm_x, int((h + 1) * kP), int(row0));
+          umma::tma_prefetch_2d(&tm_g, int((h + 1) * kP), int(row0));
+        }
+        if (has_next) {
+          // dS = dH of the chunk after, once its unit has published it and the
+          // state tile has been converted out of the staging buffer
+          wait_bar(&bars[E_HCONV], par, p.err);
+          const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
+          uint32_t it = 0;
+          while (!sm->abort && ld_acquire_gpu(flag) == 0) {
+            if (++it > p.spin_limit) {
+              atomicOr(p.err, 1);
+              sm->abort = 1;   // every later wait of this CTA gives up at once
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (sm->abort) break;
+          umma::fence_proxy_async_global();   // the bulk copy reads what the acquire made visible
+          umma::mbar_expect_tx(&bars[B_DSL], kP * kN * 4);
+          umma::bulk_load(sm_base + OFF_STG, p.ring + ((((c + 1) % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN),
+                          kP * kN * 4, &bars[B_DSL]);
+          ++n_ds;
         }
       }
+      if (!sm->abort) {
+        wait_bar(&bars[E_DS0 + ((hpg - 1) & 1)], uint32_t(((hpg - 1) >> 1) & 1), p.err);
+        if (!sm->abort && publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + g * hpg + hpg - 1), 1);
+      }
+      // every issued copy has landed before the CTA may exit (bounded; after a
+      // give-up nobody else waited for them)
+      auto drain = [&](uint64_t *b, int n) {
+        if (n == 0) return;
+        const long long w0 = clock64();
+        while (!umma::mbar_try_wait(b, uint32_t((n - 1) & 1)) && clock64() - w0 < kWaitCycles) {
+        }
+      };
+      drain(&bars[B_H], n_h);
+      drain(&bars[B_XG], n_xg);
+      drain(&bars[B_DSL], n_ds);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       const uint32_t aB = umma::smem_u32(sm_base + OFF_B), aC = umma::smem_u32(sm_base + OFF_C);
@@ -332,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aGh = umma::smem_u32(sm_base + OFF_GW), aGl = aGh + 16384;
       const uint32_t aM16 = umma::smem_u32(sm_base + OFF_M16);
       constexpr uint32_t id_kk128 = umma::idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t id_kk64 = umma::idesc_bf16_f32(128, 64, 0, 0);
+      constexpr uint32_t id_km64 = umma::idesc_bf16_f32(128, 64, 0, 1);
       constexpr uint32_t id_mm64 = umma::idesc_bf16_f32(128, 64, 1, 1);
       constexpr uint32_t id_km128 = umma::idesc_bf16_f32(128, 128, 0, 1);
       constexpr uint32_t id_mm128 = umma::idesc_bf16_f32(128, 128, 1, 1);
-      // fp16 A/B (formats 0): g x^T K-major/K-major N = 128; D1 MN-major/MN-major N = 64
-      constexpr uint32_t id_f16_kk128 = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+      // fp16 A/B (formats 0): D1 MN-major/MN-major N = 64
+      constexpr uint32_t id_kk64 = umma::idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t id_f16_mm64 = (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
       auto kdesc = [](uint32_t base, uint32_t panel_bytes, int kk) {  // K-major operand, K step kk
         return umma::smem_desc_sw128(base + uint32_t(kk / 64) * panel_bytes + uint32_t(kk % 64) * 2, 16, 1024);
@@ -355,28 +397,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < hpg; ++k) {
         const int st = k & 1;
         const uint32_t par = uint32_t(k & 1);
-        const uint32_t aX = umma::smem_u32(sm_base + (st ? OFF_X1 : OFF_X0)), aG = aX + 16384;
+        const uint32_t aX = umma::smem_u32(sm_base + OFF_XG), aG = aX + 16384;
         if (k > 0) wait_bar(&bars[E_RA], par ^ 1u, p.err);
-        wait_bar(&bars[E_X16], par, p.err);  // x, g scaled to fp16 in place
+        wait_bar(&bars[B_XG], par, p.err);   // x, g landed (bf16)
         umma::fence_after_sync();
-        // Gx = g x^T (M = t, N = s, K = p), fp16 operands
+        // Gx = g x^T (M = t, N = s, K = p), bf16 operands, in two column halves so
+        // that the epilogue can hand the left half back early
         for (int kk = 0; kk < kP; kk += 16)
-          umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_f16_kk128, kk > 0);
+          umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_kk64, kk > 0);
         umma::mma_commit(&bars[B_G1]);
+        for (int kk = 0; kk < kP; kk += 16)
+          umma::mma_bf16(tmem + T_RA + 64, kdesc(aG, 16384, kk), kdesc(aX + 8192, 16384, kk), id_kk64, kk > 0);
+        umma::mma_commit(&bars[B_G1R]);
+        wait_bar(&bars[E_X16], par, p.err);  // G~ and H (hi, lo) in smem
+        umma::fence_after_sync();
         // dC += G~ H^T  (M = t, N = n, K = p): hi*hi + hi*lo + lo*hi; runs while the epilogue reads g x^T
         for (int part = 0; part < 3; ++part) {
           const uint32_t aA = part == 2 ? aGl : aGh, aBb = part == 1 ? aHl : aHh;
           for (int kk = 0; kk < kP; kk += 16)
-            umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), mdesc(aBb, 8192, kk), id_km128,
+            umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), kdesc(aBb, 16384, kk), id_kk128,
                            (k > 0) || (part > 0) || (kk > 0));
         }
-        wait_bar(&bars[E_M16], par, p.err);  // g x^T consumed; M16 in smem
+        wait_bar(&bars[E_GXL], par, p.err);  // left half of g x^T read: C H goes there
         umma::fence_after_sync();
         // CH = C (H_hi + H_lo)  (M = t, N = p, K = n)
         for (int part = 0; part < 2; ++part)
           for (int kk = 0; kk < kN; kk += 16)
-            umma::mma_bf16(tmem + T_CH, kdesc(aC, 16384, kk), kdesc(part ? aHl : aHh, 8192, kk), id_kk64,
+            umma::mma_bf16(tmem + T_CH, kdesc(aC, 16384, kk), mdesc(part ? aHl : aHh, 16384, kk), id_km64,
                            (part > 0) || (kk > 0));
+        umma::mma_commit(&bars[B_CH]);
+        wait_bar(&bars[E_M16], par, p.err);  // right half read too; M16 in smem
+        umma::fence_after_sync();
         // dHscan^T = C^T (G~_hi + G~_lo)  (M = n, N = p, K = t)
         for (int part = 0; part < 2; ++part)
           for (int kk = 0; kk < kQ; kk += 16)
@@ -390,12 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma::mma_bf16(tmem + T_RA, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
         wait_bar(&bars[E_DS0 + st], uint32_t((k >> 1) & 1), p.err);  // dHscan read; dS and w o x in smem
         umma::fence_after_sync();
-        // Y = B dS^T  (M = t, N = p, K = n)
+        // Y = B dS^T  (M = t, N = p, K = n); dS stored [n][p]
         for (int kk = 0; kk < kN; kk += 16)
-          umma::mma_bf16(tmem + T_RA + 64, kdesc(aB, 16384, kk), kdesc(aHh, 8192, kk), id_kk64, kk > 0);
+          umma::mma_bf16(tmem + T_RA + 64, kdesc(aB, 16384, kk), mdesc(aHh, 16384, kk), id_km64, kk > 0);
         // dB += (w o x) dS  (M = t, N = n, K = p)
         for (int kk = 0; kk < kP; kk += 16)
-          umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), mdesc(aHh, 8192, kk), id_km128, (k > 0) || (kk > 0));
+          umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), kdesc(aHh, 16384, kk), id_kk128, (k > 0) || (kk > 0));
         umma::mma_commit(&bars[B_G4]);
       }
       wait_bar(&bars[E_WSUM], 0, p.err);
@@ -412,25 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma::mma_commit(&bars[B_FIN]);
     }
-  } else {
+  } else if (warp < kEpiWarps) {
     // ---------------------------------------------------------- epilogue --
-    const int q = warp & 3, hf = warp >> 2;
+    const int q = warp & 3, cq = warp >> 2;            // TMEM lane quadrant, column quarter
     const int r = 32 * q + lane;                       // row (token / state index) of this thread
     const uint32_t lane_off = uint32_t(32 * q) << 16;  // TMEM lane field of this warp's quadrant
     const float *dtg = p.dt + row0 * s.H;
     XBuf *xb = reinterpret_cast<XBuf *>(sm_base + OFF_XBUF);
     constexpr float kLog2e = 1.4426950408889634f;
 
-    // C B^T rows (this thread's row, its 64 columns) into registers, pre-scaled
-    // by the power of two that brings M = CB o L into the fp16 range
-    float cbs[64];
+    // C B^T rows (this thread's row, its 32 columns: 16 in each column half)
+    // into registers, pre-scaled by the power of two that brings M = CB o L
+    // into the fp16 range
+    float cbs[32];
     ewait(&bars[B_CB], 0, p.err);
     umma::fence_after_sync();
     float cbmax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 2; ++j) {
       float v[16];
-      umma::tmem_ld16(tmem + lane_off + T_RA + 64 * hf + 16 * j, v);
+      umma::tmem_ld16(tmem + lane_off + T_RA + 64 * j + 16 * cq, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         cbs[16 * j + i] = v[i];
@@ -442,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) umma::tmem_st16(tmem + lane_off + T_WS + 64 * hf + 16 * j, z);
+      for (int j = 0; j < 2; ++j) umma::tmem_st16(tmem + lane_off + T_WS + 64 * j + 16 * cq, z);
       umma::tmem_wait_st();
     }
     umma::fence_before_sync();
@@ -454,48 +506,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kM = fp16_scale_exp(cbmax);
     const float sM = ldexpf(1.f, kM);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) cbs[i] *= sM;
+    for (int i = 0; i < 32; ++i) cbs[i] *= sM;
 
     const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
     const bool here_start = is_seq_start(p.seq_idx, bi, s.T, t0);
     const int64_t seq = seq_of(p.seq_idx, bi, s.T, t0);
     const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
 
-    float dt_next = (hf == 0) ? dtg[int64_t(r) * s.H + g * hpg] : 0.f;  // step size of the first head
+    float dt_next = (cq == 0) ? dtg[int64_t(r) * s.H + g * hpg] : 0.f;  // step size of the first head
     for (int k = 0; k < hpg; ++k) {
       const int st = k & 1;
       const uint32_t par = uint32_t(k & 1);
       const int64_t h = g * hpg + k;
-      uint8_t *sX = sm_base + (st ? OFF_X1 : OFF_X0);
+      uint8_t *sX = sm_base + OFF_XG;
       uint8_t *sG = sX + 16384;
       const float Ah = p.A[h], Dh = p.D[h];
 
-      // the state tile entering the chunk (fp32, L2-warm): loads in flight during the scan
-      float4 hv[8];
-      {
-        const float4 *hs = reinterpret_cast<const float4 *>(p.states + (((bi * s.nc + c) * s.H + h) * kP) * kN);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hv[j] = __ldg(hs + tid + kEpiThreads * j);
-      }
       // ---- P0: cumulative step sizes (fixed-tree scan), decay in log2 units
       float cumdt = 0.f;
-      if (hf == 0) {
+      if (cq == 0) {
         cumdt = dt_next;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float v = __shfl_up_sync(0xffffffffu, cumdt, o);
           if (lane >= o) cumdt += v;
         }
-        if (lane == 31) sm->red[24 + q] = cumdt;
+        if (lane == 31) sm->red[32 + q] = cumdt;
         lo_sync();
         float pre = 0.f;
-        for (int w = 0; w < q; ++w) pre += sm->red[24 + w];
+        for (int w = 0; w < q; ++w) pre += sm->red[32 + w];
         cumdt += pre;
         sm->a2[r] = cumdt * (Ah * kLog2e);
         sm->dtv[r] = dt_next;
-        if (r == kQ - 1) sm->red[31] = cumdt;  // sum of the chunk's step sizes
+        if (r == kQ - 1) sm->red[36] = cumdt;  // sum of the chunk's step sizes
       }
-      ewait(&bars[B_XG0 + st], uint32_t((k >> 1) & 1), p.err);
+      ewait(&bars[B_XG], par, p.err);
+      ewait(&bars[B_H], par, p.err);
       ep_sync();
       const float a2r = sm->a2[r], dtr = sm->dtv[r], a2E = sm->a2[kQ - 1];
 
@@ -504,29 +550,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float wr = eEA * dtr;
       const float eE = umma::ex2_approx(a2E);
 
-      // H (fp32 state entering the chunk) -> bf16 hi + lo, [p][n]
+      // H (fp32 [p][n] state entering the chunk, staging buffer) -> bf16 hi + lo,
+      // stored [n][p]: this thread takes state index n and its 16 p values
+      {
+        const float *hs = reinterpret_cast<const float *>(sm_base + OFF_STG);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e4 = tid + kEpiThreads * j;
-        const float4 v = hv[j];
-        const int pp = (4 * e4) / kN, nn = (4 * e4) % kN;
-        const int col = nn % 64;
-        const uint32_t off = (nn / 64) * 8192 + pp * 128 + (((col >> 3) ^ (pp & 7)) << 4) + (col & 7) * 2;
-        const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
-        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-        uint2 uh, ul;
-        reinterpret_cast<__nv_bfloat162 *>(&uh)[0] = h01;
-        reinterpret_cast<__nv_bfloat162 *>(&uh)[1] = h23;
-        reinterpret_cast<__nv_bfloat162 *>(&ul)[0] = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-        reinterpret_cast<__nv_bfloat162 *>(&ul)[1] = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-        *reinterpret_cast<uint2 *>(sm_base + OFF_HD + off) = uh;
-        *reinterpret_cast<uint2 *>(sm_base + OFF_HD + 16384 + off) = ul;
+        for (int u = 0; u < 2; ++u) {
+          const int pg = 2 * cq + u;   // group of 8 p values
+          float hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float v = hs[(8 * pg + i) * kN + n];
+            hi[i] = __bfloat162float(__float2bfloat16_rn(v));
+            lo[i] = v - hi[i];
+          }
+          st8_bf16(sm_base + OFF_HD, n, 8 * pg, hi);
+          st8_bf16(sm_base + OFF_HD + 16384, n, 8 * pg, lo);
+        }
       }
-      // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |x|, |g| for the fp16 scaling; g . x
-      float gmax = 0.f, xmax = 0.f, gx = 0.f;
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&bars[E_HCONV]);   // the staging buffer may take dS now
+      // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |g| for the fp16 scaling of g; g . x
+      float gmax = 0.f, gx = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const int c0 = 32 * hf + 8 * c8;
+      for (int c8 = 0; c8 < 2; ++c8) {
+        const int c0 = 16 * cq + 8 * c8;
         float gv[8], xv[8], hi[8], lo[8];
         ld8_bf16(sG, r, c0, gv);
         ld8_bf16(sX, r, c0, xv);
@@ -536,90 +584,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi[i] = __bfloat162float(__float2bfloat16_rn(t));
           lo[i] = t - hi[i];
           gmax = fmaxf(gmax, fabsf(gv[i]));
-          xmax = fmaxf(xmax, fabsf(xv[i]));
           gx = fmaf(gv[i], xv[i], gx);
         }
         st8_bf16(sm_base + OFF_GW, r, c0, hi);
         st8_bf16(sm_base + OFF_GW + 16384, r, c0, lo);
       }
-      // warm L2 with the next head's state tile (32 KB) while this head runs
-      if (tid == 0 && k + 1 < hpg)
-        umma::prefetch_l2(p.states + (((bi * s.nc + c) * s.H + h + 1) * kP) * kN, kP * kN * 4);
-      // x and g -> fp16 scaled by exact powers of two, in place
-      ep_max2(gmax, xmax, sm);
-      const int kg = fp16_scale_exp(gmax), kx = fp16_scale_exp(xmax);
-      const float ug = ldexpf(1.f, -kg), ux = ldexpf(1.f, -kx);
-      const float ugx = ug * ux;
-      if (hf == 0) sm->dtu[r] = dtr * ugx;
-      {
-        const float sg = ldexpf(1.f, kg), sx = ldexpf(1.f, kx);
+      // per-warp maxima of |g|; read after the barrier that ends E1
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const int c0 = 32 * hf + 8 * c8;
-          float v[8];
-          ld8_bf16(sG, r, c0, v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] *= sg;
-          st_row8_f16(sG, r, c0, v);
-          ld8_bf16(sX, r, c0, v);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] *= sx;
-          st_row8_f16(sX, r, c0, v);
-        }
-      }
+      for (int o = 16; o > 0; o >>= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+      if (lane == 0) sm->red[warp] = gmax;
       umma::fence_proxy_async_smem();
       if (tid == 128) umma::tma_store_wait_read();  // dx staging (the M16 buffer) has been read out
       ep_sync();
       if (tid == 0) umma::mbar_arrive(&bars[E_X16]);
 
-      // ---- E1: intra-chunk matrices from g x^T (TMEM, raw fp16 scale) and C B^T (registers).
+      // ---- E1: intra-chunk matrices from g x^T (TMEM, bf16 products) and C B^T (registers).
       // The decay gradient needs the row and the column sums of M o Gx o dt;
       // both are taken from the same fp16-rounded M that the dx product
       // uses (the column sums come out of that product in E4), so their
       // difference keeps its cancellation exact up to fp32 accumulation.
-      ewait(&bars[B_G1], par, p.err);
-      umma::fence_after_sync();
+      // Two passes over the column halves of g x^T; after the left one every
+      // warp hands its columns back so that C H can be computed there while
+      // the right half is processed.
       float rowp = 0.f;   // sum_s M16_rs Gx_rs dt_s, times sM
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c0 = 64 * hf + 8 * j;
-        uint32_t m16[4];
-        if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
-          float gxv[8], ws[8];
-          umma::tmem_ld8x2(tmem + lane_off + T_RA + c0, tmem + lane_off + T_WS + c0, gxv, ws);
-          const bool diag_blk = c0 + 8 > 32 * q;   // may cross the diagonal for some lane
+      for (int half = 0; half < 2; ++half) {
+        ewait(&bars[half ? B_G1R : B_G1], par, p.err);
+        umma::fence_after_sync();
 #pragma unroll
-          for (int e4 = 0; e4 < 2; ++e4) {
-            const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[c0 + 4 * e4]);
-            const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtu[c0 + 4 * e4]);
-            const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
-            const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
-            float mv[4];
+        for (int jj = 0; jj < 2; ++jj) {
+          const int c0 = 64 * half + 16 * cq + 8 * jj;   // this thread's 8 columns
+          const int j = 2 * half + jj;                   // their slot in cbs
+          uint32_t m16[4];
+          if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
+            float gxv[8], ws[8];
+            umma::tmem_ld8x2(tmem + lane_off + T_RA + c0, tmem + lane_off + T_WS + c0, gxv, ws);
+            const bool diag_blk = c0 + 8 > 32 * q;   // may cross the diagonal for some lane
 #pragma unroll
-            for (int e1 = 0; e1 < 4; ++e1) {
-              const int e = 4 * e4 + e1;
-              const bool causal = !diag_blk || (c0 + e <= r);
-              const float L = causal ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
-              const float gd = gxv[e] * dus[e1];       // Gx dt (true units)
-              ws[e] = fmaf(L, gd, ws[e]);
-              mv[e1] = cbs[8 * j + e] * L;
+            for (int e4 = 0; e4 < 2; ++e4) {
+              const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[c0 + 4 * e4]);
+              const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtv[c0 + 4 * e4]);
+              const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
+              const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
+              float mv[4];
+#pragma unroll
+              for (int e1 = 0; e1 < 4; ++e1) {
+                const int e = 4 * e4 + e1;
+                const bool causal = !diag_blk || (c0 + e <= r);
+                const float L = causal ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
+                const float gd = gxv[e] * dus[e1];       // Gx dt (true units)
+                ws[e] = fmaf(L, gd, ws[e]);
+                mv[e1] = cbs[8 * j + e] * L;
+              }
+              const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
+              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+              rowp = fmaf(f01.x, gxv[4 * e4 + 0] * dus[0], rowp);
+              rowp = fmaf(f01.y, gxv[4 * e4 + 1] * dus[1], rowp);
+              rowp = fmaf(f23.x, gxv[4 * e4 + 2] * dus[2], rowp);
+              rowp = fmaf(f23.y, gxv[4 * e4 + 3] * dus[3], rowp);
+              m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
+              m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
             }
-            const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            rowp = fmaf(f01.x, gxv[4 * e4 + 0] * dus[0], rowp);
-            rowp = fmaf(f01.y, gxv[4 * e4 + 1] * dus[1], rowp);
-            rowp = fmaf(f23.x, gxv[4 * e4 + 2] * dus[2], rowp);
-            rowp = fmaf(f23.y, gxv[4 * e4 + 3] * dus[3], rowp);
-            m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
-            m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-          }
-          umma::tmem_st8(tmem + lane_off + T_WS + c0, ws);
-        } else {
+            umma::tmem_st8(tmem + lane_off + T_WS + c0, ws);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) m16[e] = 0u;
+            for (int e = 0; e < 4; ++e) m16[e] = 0u;
+          }
+          *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
+              make_uint4(m16[0], m16[1], m16[2], m16[3]);
         }
-        *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + hf * 16384 + r * 128 + ((j ^ (r & 7)) << 4)) =
-            make_uint4(m16[0], m16[1], m16[2], m16[3]);
+        if (half == 0) {
+          umma::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) umma::mbar_arrive(&bars[E_GXL]);
+        }
       }
       umma::tmem_wait_st();
       umma::fence_before_sync();
@@ -628,97 +666,94 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) umma::mbar_arrive(&bars[E_M16]);
 
       // ---- E2: carried-in state term of the decay gradient; E3: chain step
-      ewait(&bars[B_G2], par, p.err);
+      ewait(&bars[B_CH], par, p.err);
       umma::fence_after_sync();
-      // the lo half of GW is idle from here to the next head: exchange scratch
-      xb->v[0][hf][r] = rowp;
-      xb->v[3][hf][r] = gx;
-      if (hf == 0) sm->dtu[r] = cumdt;   // dtu is no longer needed this head: keep the cumulative step there
+      if (cq == 0) sm->dtu[r] = cumdt;   // keep the cumulative step for E5
+      // g -> fp16 scaled by an exact power of two, in place (the dx product
+      // pairs it with the fp16 M); g x^T has been computed from the bf16 g
+      float gm = 0.f;
+#pragma unroll
+      for (int w = 0; w < kEpiWarps; ++w) gm = fmaxf(gm, sm->red[w]);
+      const int kg = fp16_scale_exp(gm);
       float inter_part = 0.f;
-#pragma unroll
-      for (int c8 = 0; c8 < 4; c8 += 2) {
+      {
+        const float sg = ldexpf(1.f, kg);
         float ch0[8], ch1[8], gv[8];
-        umma::tmem_ld8x2(tmem + lane_off + T_CH + 32 * hf + 8 * c8, tmem + lane_off + T_CH + 32 * hf + 8 * c8 + 8, ch0,
-                         ch1);
-        ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
+        umma::tmem_ld8x2(tmem + lane_off + T_CH + 16 * cq, tmem + lane_off + T_CH + 16 * cq + 8, ch0, ch1);
+        ld8_bf16(sG, r, 16 * cq, gv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch0[i], inter_part);
-        ld8_f16(sG, r, 32 * hf + 8 * c8 + 8, gv);
+        for (int i = 0; i < 8; ++i) {
+          inter_part = fmaf(gv[i], ch0[i], inter_part);
+          gv[i] *= sg;
+        }
+        st_row8_f16(sG, r, 16 * cq, gv);
+        ld8_bf16(sG, r, 16 * cq + 8, gv);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) inter_part = fmaf(gv[i], ch1[i], inter_part);
+        for (int i = 0; i < 8; ++i) {
+          inter_part = fmaf(gv[i], ch1[i], inter_part);
+          gv[i] *= sg;
+        }
+        st_row8_f16(sG, r, 16 * cq + 8, gv);
       }
-      xb->v[2][hf][r] = inter_part;
+      umma::fence_proxy_async_smem();   // g16 is read by the dx product issued after E_CHR
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&bars[E_CHR]);
-      if (has_next) {
-        const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
-        if (warp == 0) {   // the whole warp polls (one address), so it reaches the barrier converged
-          uint32_t it = 0;
-          while (!sm->abort && !__all_sync(0xffffffffu, ld_acquire_gpu(flag) != 0)) {
-            if (++it > p.spin_limit) {
-              if (lane == 0) atomicOr(p.err, 1);
-              break;
-            }
-            __nanosleep(64);
-          }
-          __syncwarp();
-        }
-        ep_sync();
-        (void)ld_acquire_gpu(flag);
-      }
+      ewait(&bars[B_G2], par, p.err);                   // dHscan^T in TMEM; G~ (lo half of GW) read
+      umma::fence_after_sync();
+      // the lo half of GW is idle from here to the next head: exchange scratch
+      xb->v[0][cq][r] = rowp;
+      xb->v[3][cq][r] = gx;
+      xb->v[2][cq][r] = inter_part;
+      if (has_next) ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
       float hdot = 0.f;
       {
-        const float *src = p.ring + ((((c + 1) % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
+        const float *src = reinterpret_cast<const float *>(sm_base + OFF_STG);
         float *dst = nullptr;
         if (here_start) {
           if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
         } else {
           dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
         }
-        uint8_t *panel = sm_base + OFF_HD + (n / 64) * 8192;
-        // all 32 dS values of this thread in flight at once (one L2 round trip)
-        float ds[32];
+        float ds[16];
         if (has_next) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ds[i] = __ldcg(src + (32 * hf + i) * kN + n);
+          for (int i = 0; i < 16; ++i) ds[i] = src[(16 * cq + i) * kN + n];
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ds[i] = 0.f;
+          for (int i = 0; i < 16; ++i) ds[i] = 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int p0 = 32 * hf + 8 * u;
-          float hv[8], dh[8];
-          // H = hi + lo from shared memory, read before dS overwrites the hi half
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t o = umma::sw128_offset_bf16(uint32_t(p0 + i), uint32_t(n % 64));
-            hv[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(panel + o)) +
-                    __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(panel + 16384 + o));
-          }
+        for (int u = 0; u < 2; ++u) {
+          const int p0 = 16 * cq + 8 * u;
+          float hh[8], hl[8], dh[8];
+          // H = hi + lo (row n of the [n][p] tiles), read before dS overwrites the hi tile
+          ld8_bf16(sm_base + OFF_HD, n, p0, hh);
+          ld8_bf16(sm_base + OFF_HD + 16384, n, p0, hl);
           umma::tmem_ld8(tmem + lane_off + T_DH + p0, dh);  // lane = n, columns p
+          float d8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            hdot = fmaf(hv[i], ds[8 * u + i], hdot);
-            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, ds[8 * u + i], dh[i]));
-            st_bf16(panel, p0 + i, n % 64, ds[8 * u + i]);  // dS -> bf16 [p][n]
+            d8[i] = ds[8 * u + i];
+            hdot = fmaf(hh[i] + hl[i], d8[i], hdot);
+            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, d8[i], dh[i]));
           }
+          st8_bf16(sm_base + OFF_HD, n, p0, d8);  // dS -> bf16 [n][p]
         }
       }
       // per-warp partials of <H, dS>, folded in fixed order in E5
       hdot = warp_sum(hdot);
-      if (lane == 0) sm->red[16 + warp] = hdot;
+      if (lane == 0) sm->red[40 + warp] = hdot;
       // w o x -> GW hi half (bf16)
       {
-        const float f = wr * ux;
+        const float f = wr;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
+        for (int c8 = 0; c8 < 2; ++c8) {
           float xv[8];
-          ld8_f16(sX, r, 32 * hf + 8 * c8, xv);
+          ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
 #pragma unroll
           for (int i = 0; i < 8; ++i) xv[i] *= f;
-          st8_bf16(sm_base + OFF_GW, r, 32 * hf + 8 * c8, xv);
+          st8_bf16(sm_base + OFF_GW, r, 16 * cq + 8 * c8, xv);
         }
       }
       umma::fence_before_sync();
@@ -729,22 +764,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) umma::mbar_arrive(&bars[E_DS0 + st]);
 
       // ---- E4: dx and the row dot product x . Y
-      if (hf == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
+      if (cq == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
       const float unscale = ldexpf(1.f, -(kM + kg));
       float sxy = 0.f, xd1 = 0.f;   // x . Y and x . D1 (raw units) of this row
       {
         // dx rows staged in the (now idle) M16 buffer, 128-byte swizzled fp32, then TMA-stored
-        uint8_t *stage = sm_base + OFF_M16 + hf * 16384;
-        const float dg = Dh * ug;
+        uint8_t *stage = sm_base + OFF_M16 + (cq >> 1) * 16384;
+        const float dg = Dh * ldexpf(1.f, -kg);
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
+        for (int c8 = 0; c8 < 2; ++c8) {
           float d1[8], y[8], xv[8], gv[8];
-          umma::tmem_ld8x2(tmem + lane_off + T_RA + 32 * hf + 8 * c8, tmem + lane_off + T_RA + 64 + 32 * hf + 8 * c8, d1,
+          umma::tmem_ld8x2(tmem + lane_off + T_RA + 16 * cq + 8 * c8, tmem + lane_off + T_RA + 64 + 16 * cq + 8 * c8, d1,
                            y);
-          ld8_f16(sX, r, 32 * hf + 8 * c8, xv);
-          ld8_f16(sG, r, 32 * hf + 8 * c8, gv);
+          ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
+          ld8_f16(sG, r, 16 * cq + 8 * c8, gv);
 #pragma unroll
           for (int i4 = 0; i4 < 2; ++i4) {
             float o[4];
@@ -755,47 +790,48 @@ __global__ void __launch_bounds__(kThreads, 1)
               xd1 = fmaf(xv[i], d1[i], xd1);
               o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], dg * gv[i]));
             }
-            const int chunk = (2 * c8 + i4) ^ (r & 7);
+            const int chunk = (4 * (cq & 1) + 2 * c8 + i4) ^ (r & 7);
             *reinterpret_cast<float4 *>(stage + r * 128 + chunk * 16) = make_float4(o[0], o[1], o[2], o[3]);
           }
         }
       }
-      sxy *= ux;
       umma::fence_before_sync();
       umma::fence_proxy_async_smem();
-      xb->v[4][hf][r] = sxy;
-      xb->v[1][hf][r] = xd1;
+      xb->v[4][cq][r] = sxy;
+      xb->v[1][cq][r] = xd1;
       ep_sync();
       // a thread of the upper column half issues the hand-offs: warps 0-3 go straight on to E5
       if (tid == 128) {
         umma::mbar_arrive(&bars[E_RA]);
-        umma::mbar_arrive(&bars[E_XG0 + st]);
+        umma::mbar_arrive(&bars[E_XG]);
         umma::tma_store_2d(&tm_dx, sm_base + OFF_M16, int(h * kP), int(row0));
         umma::tma_store_2d(&tm_dx, sm_base + OFF_M16 + 16384, int(h * kP + 32), int(row0));
         umma::tma_store_commit();
       }
 
       // ---- E5: decay gradient, reverse cumsum, ddt, dA/dD partials
-      // Both column halves form the same per-row values (from shared memory);
-      // the lower half runs the suffix scan while the upper half runs the row
-      // sums, in parallel, then the lower half finishes the rows.
+      // Every column quarter forms the same per-row values (from shared
+      // memory); quarter 0 runs the suffix scan while quarter 1 runs the row
+      // sums, in parallel, then quarter 0 finishes the rows.
       {
         const float a2r5 = sm->a2[r], a2E5 = sm->a2[kQ - 1], dt5 = sm->dtv[r];
         const float eEA5 = umma::ex2_approx(a2E5 - a2r5), wr5 = eEA5 * dt5;
-        const float ug5 = ldexpf(1.f, -kg), ugx5 = ldexpf(1.f, -(kg + kx));
-        const float raw = ugx5 / sM;   // raw E1 units -> true units
+        const float raw = ldexpf(1.f, -(kM + kg));   // x . D1 in true units
         // inclusive row and column sums of M o Gx o dt: the diagonal cancels in their difference
-        const float rowp5 = (xb->v[0][0][r] + xb->v[0][1][r]) * (raw / ugx5);
-        const float dintra = (xb->v[1][0][r] + xb->v[1][1][r]) * raw;   // sum_t M_tr Gx_tr (x . D1)
-        const float inter = umma::ex2_approx(a2r5) * ug5 * (xb->v[2][0][r] + xb->v[2][1][r]);
-        const float gx5 = xb->v[3][0][r] + xb->v[3][1][r];
-        const float sxy5 = xb->v[4][0][r] + xb->v[4][1][r];
+        auto qsum = [&](int i) {   // the four column quarters, fixed order
+          return (xb->v[i][0][r] + xb->v[i][1][r]) + (xb->v[i][2][r] + xb->v[i][3][r]);
+        };
+        const float rowp5 = qsum(0) / sM;
+        const float dintra = qsum(1) * raw;   // sum_t M_tr Gx_tr (x . D1)
+        const float inter = umma::ex2_approx(a2r5) * qsum(2);
+        const float gx5 = qsum(3);
+        const float sxy5 = qsum(4);
         const float cumdt5 = sm->dtu[r];
         const float colp = dt5 * dintra;
         const float u = wr5 * sxy5;
         const float dacs = rowp5 - colp + inter - u;
         float sfx = dacs;
-        if (hf == 0) {
+        if (cq == 0) {
           // suffix sum over rows: fixed tree in the warp, fixed order across warps
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
@@ -803,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane + o < 32) sfx += v;
           }
           if (lane == 0) sm->red[q] = sfx;
-        } else {
+        } else if (cq == 1) {
           // warp totals of u, g.x and dacs * cumdt
           const float wu = warp_sum(u), wg = warp_sum(gx5), wc = warp_sum(dacs * cumdt5);
           if (lane == 0) {
@@ -813,19 +849,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ep_sync();
-        if (hf == 0) {
+        if (cq == 0) {
           float off = 0.f;
           for (int w = 3; w > q; --w) off += sm->red[w];
           const float su = ((sm->red[4] + sm->red[5]) + sm->red[6]) + sm->red[7];
-          const float hsum = (((sm->red[16] + sm->red[17]) + (sm->red[18] + sm->red[19])) +
-                              ((sm->red[20] + sm->red[21]) + (sm->red[22] + sm->red[23])));
+          float hsum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kEpiWarps; ++w) hsum += sm->red[40 + w];
           const float K = su + umma::ex2_approx(a2E5) * hsum;   // + dEpass = exp(E) <H, dS>
           const float da = (sfx + off) + K;
           p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA5 * sxy5);
           if (tid == 0) {
             const float sg = ((sm->red[8] + sm->red[9]) + sm->red[10]) + sm->red[11];
             const float sc = ((sm->red[12] + sm->red[13]) + sm->red[14]) + sm->red[15];
-            const float dap = fmaf(K, sm->red[31], sc);
+            const float dap = fmaf(K, sm->red[36], sc);
             if (p.atomic) {
               atomicAdd(p.dA + h, dap);
               atomicAdd(p.dD + h, sg);
@@ -841,16 +878,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- unit end: head-summed W (hi + lo) for the intra-chunk dB/dC products
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 2; ++j) {
       float w[16], hi[16], lo[16];
-      umma::tmem_ld16(tmem + lane_off + T_WS + 64 * hf + 16 * j, w);
+      umma::tmem_ld16(tmem + lane_off + T_WS + 64 * j + 16 * cq, w);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         hi[i] = __bfloat162float(__float2bfloat16_rn(w[i]));
         lo[i] = w[i] - hi[i];
       }
-      st_row16_bf16(sm_base + OFF_WHI + hf * 16384, r, 16 * j, hi);
-      st_row16_bf16(sm_base + OFF_WLO + hf * 16384, r, 16 * j, lo);
+      st_row16_bf16(sm_base + OFF_WHI + j * 16384, r, 16 * cq, hi);
+      st_row16_bf16(sm_base + OFF_WLO + j * 16384, r, 16 * cq, lo);
     }
     umma::fence_before_sync();
     umma::fence_proxy_async_smem();
@@ -859,8 +896,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ewait(&bars[B_FIN], 0, p.err);
     umma::fence_after_sync();
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n0 = 64 * hf + 16 * j;
+    for (int j = 0; j < 2; ++j) {
+      const int n0 = 32 * cq + 16 * j;
       float v[16];
       umma::tmem_ld16(tmem + lane_off + T_DB + n0, v);
       float *o = p.dB + ((row0 + r) * s.G + g) * kN + n0;
@@ -877,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 128) umma::tma_store_wait_all();
   }
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     // after a give-up, let the tensor cores drain (bounded) before freeing TMEM
     if (sm->abort && lane == 0) {
       const long long t0 = clock64();

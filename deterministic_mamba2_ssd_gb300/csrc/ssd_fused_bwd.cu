@@ -67,13 +67,13 @@ constexpr uint32_t OFF_XBUF = OFF_GW + 16384;
 constexpr uint32_t OFF_WHI = OFF_XG, OFF_WLO = OFF_STG;
 
 // TMEM columns
-// RA holds, in turn: C B^T (unit start), g x^T, then C H (cols 0-63) and
-// dHscan^T (64-127), then D1 (0-63) and Y (64-127).  WS accumulates W.
+// RA holds, in turn: C B^T (unit start), g x^T, then dHscan^T (cols 0-63)
+// and C H (64-127), then Y (0-63) and D1 (64-127).  WS accumulates W.
 constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
-constexpr uint32_t T_CH = T_RA, T_DH = T_RA + 64;
+constexpr uint32_t T_DH = T_RA, T_CH = T_RA + 64, T_Y = T_RA, T_D1 = T_RA + 64;
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, E_HCONV, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_CH, B_G2, E_M16, E_CHR, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, E_HCONV, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_HCONV || i == E_GXL) ? kEpiWarps : 1);  // per-warp arrivals
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_HCONV || i == E_GXL || i == E_RING || i == E_DS0 || i == E_DS1) ? kEpiWarps : 1);  // per-warp arrivals
     umma::fence_mbar_init();
     sm->unit = atomicAdd(p.ticket, 1);
     sm->abort = 0;
@@ -305,8 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t h = g * hpg + k;
         const uint32_t par = uint32_t(k & 1);
         if (k > 0) {
-          // ring stores of head k-1 done (epilogue barrier + arrive), and the staging buffer is free again
-          wait_bar(&bars[E_DS0 + ((k - 1) & 1)], uint32_t(((k - 1) >> 1) & 1), p.err);
+          // every epilogue warp stored its part of head k-1's dH (warp barrier + arrive), and
+          // the staging buffer is free again
+          wait_bar(&bars[E_RING], uint32_t((k - 1) & 1), p.err);
           if (sm->abort) break;
           if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h - 1), 1);
         }
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!sm->abort) {
-        wait_bar(&bars[E_DS0 + ((hpg - 1) & 1)], uint32_t(((hpg - 1) >> 1) & 1), p.err);
+        wait_bar(&bars[E_RING], uint32_t((hpg - 1) & 1), p.err);
         if (!sm->abort && publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + g * hpg + hpg - 1), 1);
       }
       // every issued copy has landed before the CTA may exit (bounded; after a
@@ -418,7 +419,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), kdesc(aBb, 16384, kk), id_kk128,
                            (k > 0) || (part > 0) || (kk > 0));
         }
-        wait_bar(&bars[E_GXL], par, p.err);  // left half of g x^T read: C H goes there
+        wait_bar(&bars[E_GXL], par, p.err);  // left half of g x^T read: dHscan^T goes there
+        umma::fence_after_sync();
+        // dHscan^T = C^T (G~_hi + G~_lo)  (M = n, N = p, K = t)
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < kQ; kk += 16)
+            umma::mma_bf16(tmem + T_DH, mdesc(aC, 16384, kk), mdesc(part ? aGl : aGh, 16384, kk), id_mm64,
+                           (part > 0) || (kk > 0));
+        umma::mma_commit(&bars[B_DHS]);
+        wait_bar(&bars[E_M16], par, p.err);  // right half read too; M16 in smem
         umma::fence_after_sync();
         // CH = C (H_hi + H_lo)  (M = t, N = p, K = n)
         for (int part = 0; part < 2; ++part)
@@ -426,27 +435,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mma_bf16(tmem + T_CH, kdesc(aC, 16384, kk), mdesc(part ? aHl : aHh, 16384, kk), id_km64,
                            (part > 0) || (kk > 0));
         umma::mma_commit(&bars[B_CH]);
-        wait_bar(&bars[E_M16], par, p.err);  // right half read too; M16 in smem
-        umma::fence_after_sync();
-        // dHscan^T = C^T (G~_hi + G~_lo)  (M = n, N = p, K = t)
-        for (int part = 0; part < 2; ++part)
-          for (int kk = 0; kk < kQ; kk += 16)
-            umma::mma_bf16(tmem + T_DH, mdesc(aC, 16384, kk), mdesc(part ? aGl : aGh, 16384, kk), id_mm64,
-                           (part > 0) || (kk > 0));
-        umma::mma_commit(&bars[B_G2]);
-        wait_bar(&bars[E_CHR], par, p.err);  // CH read: its columns take D1 while the chain step runs
-        umma::fence_after_sync();
-        // D1 = M^T g  (fp16 scaled operands; M = s, N = p, K = t)
-        for (int kk = 0; kk < kQ; kk += 16)
-          umma::mma_bf16(tmem + T_RA, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
         wait_bar(&bars[E_DS0 + st], uint32_t((k >> 1) & 1), p.err);  // dHscan read; dS and w o x in smem
         umma::fence_after_sync();
         // Y = B dS^T  (M = t, N = p, K = n); dS stored [n][p]
         for (int kk = 0; kk < kN; kk += 16)
-          umma::mma_bf16(tmem + T_RA + 64, kdesc(aB, 16384, kk), mdesc(aHh, 16384, kk), id_km64, kk > 0);
+          umma::mma_bf16(tmem + T_Y, kdesc(aB, 16384, kk), mdesc(aHh, 16384, kk), id_km64, kk > 0);
         // dB += (w o x) dS  (M = t, N = n, K = p)
         for (int kk = 0; kk < kP; kk += 16)
           umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), kdesc(aHh, 16384, kk), id_kk128, (k > 0) || (kk > 0));
+        wait_bar(&bars[E_CHR], par, p.err);  // CH read and g in fp16: D1 into CH's columns
+        umma::fence_after_sync();
+        // D1 = M^T g  (fp16 scaled operands; M = s, N = p, K = t)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + T_D1, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
         umma::mma_commit(&bars[B_G4]);
       }
       wait_bar(&bars[E_WSUM], 0, p.err);
@@ -665,10 +666,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       ep_sync();
       if (tid == 0) umma::mbar_arrive(&bars[E_M16]);
 
-      // ---- E2: carried-in state term of the decay gradient; E3: chain step
-      ewait(&bars[B_CH], par, p.err);
+      // ---- E3: chain step (dH to the chunk before), then E2: carried-in state term
+      ewait(&bars[B_DHS], par, p.err);   // dHscan^T in TMEM; dC and dHscan have read G~ (GW)
       umma::fence_after_sync();
+      // GW is idle from here to the next head: exchange scratch (lo half) and w o x (hi half)
+      xb->v[0][cq][r] = rowp;
+      xb->v[3][cq][r] = gx;
       if (cq == 0) sm->dtu[r] = cumdt;   // keep the cumulative step for E5
+      {
+#pragma unroll
+        for (int c8 = 0; c8 < 2; ++c8) {
+          float xv[8];
+          ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xv[i] *= wr;
+          st8_bf16(sm_base + OFF_GW, r, 16 * cq + 8 * c8, xv);
+        }
+      }
+      if (has_next) ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
+      float hdot = 0.f;
+      float ds[16];   // this thread's dS values (state index n, 16 p values)
+      {
+        const float *src = reinterpret_cast<const float *>(sm_base + OFF_STG);
+        float *dst = nullptr;
+        if (here_start) {
+          if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
+        } else {
+          dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
+        }
+        if (has_next) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ds[i] = src[(16 * cq + i) * kN + n];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ds[i] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int p0 = 16 * cq + 8 * u;
+          float hh[8], hl[8], dh[8];
+          // H = hi + lo (row n of the [n][p] tiles), read before dS overwrites the hi tile
+          ld8_bf16(sm_base + OFF_HD, n, p0, hh);
+          ld8_bf16(sm_base + OFF_HD + 16384, n, p0, hl);
+          umma::tmem_ld8(tmem + lane_off + T_DH + p0, dh);  // lane = n, columns p
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            hdot = fmaf(hh[i] + hl[i], ds[8 * u + i], hdot);
+            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, ds[8 * u + i], dh[i]));
+          }
+        }
+      }
+      // Per-warp hand-off of the chain step: the producer thread waits for
+      // every warp before it releases the chunk's flag (the warp barrier
+      // orders all lanes' ring stores before lane 0's arrival).
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&bars[E_RING]);
+      // per-warp partials of <H, dS>, folded in fixed order in E5
+      hdot = warp_sum(hdot);
+      if (lane == 0) sm->red[40 + warp] = hdot;
+
+      ewait(&bars[B_CH], par, p.err);   // C H done: H (hi tile) may now give way to dS
+      umma::fence_after_sync();
+      {
+        float d8[8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) d8[i] = ds[8 * u + i];
+          st8_bf16(sm_base + OFF_HD, n, 16 * cq + 8 * u, d8);  // dS -> bf16 [n][p]
+        }
+      }
+      umma::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&bars[E_DS0 + st]);   // Y and dB may start
       // g -> fp16 scaled by an exact power of two, in place (the dx product
       // pairs it with the fp16 M); g x^T has been computed from the bf16 g
       float gm = 0.f;
@@ -695,73 +766,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         st_row8_f16(sG, r, 16 * cq + 8, gv);
       }
+      xb->v[2][cq][r] = inter_part;
       umma::fence_proxy_async_smem();   // g16 is read by the dx product issued after E_CHR
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&bars[E_CHR]);
-      ewait(&bars[B_G2], par, p.err);                   // dHscan^T in TMEM; G~ (lo half of GW) read
-      umma::fence_after_sync();
-      // the lo half of GW is idle from here to the next head: exchange scratch
-      xb->v[0][cq][r] = rowp;
-      xb->v[3][cq][r] = gx;
-      xb->v[2][cq][r] = inter_part;
-      if (has_next) ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
-      float hdot = 0.f;
-      {
-        const float *src = reinterpret_cast<const float *>(sm_base + OFF_STG);
-        float *dst = nullptr;
-        if (here_start) {
-          if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
-        } else {
-          dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
-        }
-        float ds[16];
-        if (has_next) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ds[i] = src[(16 * cq + i) * kN + n];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ds[i] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int p0 = 16 * cq + 8 * u;
-          float hh[8], hl[8], dh[8];
-          // H = hi + lo (row n of the [n][p] tiles), read before dS overwrites the hi tile
-          ld8_bf16(sm_base + OFF_HD, n, p0, hh);
-          ld8_bf16(sm_base + OFF_HD + 16384, n, p0, hl);
-          umma::tmem_ld8(tmem + lane_off + T_DH + p0, dh);  // lane = n, columns p
-          float d8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            d8[i] = ds[8 * u + i];
-            hdot = fmaf(hh[i] + hl[i], d8[i], hdot);
-            if (dst) __stcg(dst + (p0 + i) * kN + n, fmaf(eE, d8[i], dh[i]));
-          }
-          st8_bf16(sm_base + OFF_HD, n, p0, d8);  // dS -> bf16 [n][p]
-        }
-      }
-      // per-warp partials of <H, dS>, folded in fixed order in E5
-      hdot = warp_sum(hdot);
-      if (lane == 0) sm->red[40 + warp] = hdot;
-      // w o x -> GW hi half (bf16)
-      {
-        const float f = wr;
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          float xv[8];
-          ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) xv[i] *= f;
-          st8_bf16(sm_base + OFF_GW, r, 16 * cq + 8 * c8, xv);
-        }
-      }
-      umma::fence_before_sync();
-      umma::fence_proxy_async_smem();
-      ep_sync();
-      // the barrier above orders every thread's ring stores before this arrival, and the
-      // producer thread releases the chunk's flag only after waiting for it
-      if (tid == 0) umma::mbar_arrive(&bars[E_DS0 + st]);
 
       // ---- E4: dx and the row dot product x . Y
       if (cq == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
@@ -776,8 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
           float d1[8], y[8], xv[8], gv[8];
-          umma::tmem_ld8x2(tmem + lane_off + T_RA + 16 * cq + 8 * c8, tmem + lane_off + T_RA + 64 + 16 * cq + 8 * c8, d1,
-                           y);
+          umma::tmem_ld8x2(tmem + lane_off + T_D1 + 16 * cq + 8 * c8, tmem + lane_off + T_Y + 16 * cq + 8 * c8, d1, y);
           ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
           ld8_f16(sG, r, 16 * cq + 8 * c8, gv);
 #pragma unroll

@@ -85,6 +85,10 @@ struct Small {
   uint64_t bars[NBARS];
   uint32_t tmem_base;
   int unit;
+  int has_next;          // the chunk after this one belongs to the same sequence
+  float *dst0;           // where head g*hpg's dH goes: ring slot or initial-state gradient (or null)
+  int64_t dst_stride;    // elements between consecutive heads' dH tiles
+  float ad[2];           // A and D of the head about to start
   volatile int abort;  // set when a bounded wait ran out: later waits give up at once
 };
 static_assert(sizeof(Small) <= SMALL_BYTES, "small region");
@@ -275,13 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm->tmem_base;
 
   // unit from the ticket: chunks in descending order, then batch row, then group
-  const int64_t unit = sm->unit;
-  const int64_t per_row = s.b * s.G;
-  const int64_t c = s.nc - 1 - unit / per_row;
-  const int64_t bi = (unit % per_row) / s.G;
-  const int64_t g = unit % s.G;
-  const int64_t t0 = c * kQ;
-  const int64_t row0 = bi * s.T + t0;  // first global token row of the chunk
+  // (32-bit: the supported shapes keep units and token rows below 2^30; every
+  // index that can grow past that is formed with the 64-bit shape fields)
+  const int unit = sm->unit;
+  const int per_row = int(s.b * s.G);
+  const int c = int(s.nc) - 1 - unit / per_row;
+  const int bi = (unit % per_row) / int(s.G);
+  const int g = unit % int(s.G);
+  const int t0 = c * kQ;
+  const int row0 = bi * int(s.T) + t0;  // first global token row of the chunk
   const int hpg = int(s.hpg);
 
   if (warp == kTmaWarp) {
@@ -509,19 +515,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; ++i) cbs[i] *= sM;
 
-    const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
-    const bool here_start = is_seq_start(p.seq_idx, bi, s.T, t0);
-    const int64_t seq = seq_of(p.seq_idx, bi, s.T, t0);
+    if (tid == 0) {
+      sm->has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
+      const int64_t h0 = g * hpg;
+      if (is_seq_start(p.seq_idx, bi, s.T, t0)) {
+        sm->dst0 = p.dinit ? p.dinit + ((seq_of(p.seq_idx, bi, s.T, t0) * s.H + h0) * kP) * kN : nullptr;
+      } else {
+        sm->dst0 = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h0) * (kP * kN);
+      }
+      sm->dst_stride = kP * kN;
+      sm->ad[0] = p.A[g * hpg];
+      sm->ad[1] = p.D[g * hpg];
+    }
+    ep_sync();
     const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
 
     float dt_next = (cq == 0) ? dtg[int64_t(r) * s.H + g * hpg] : 0.f;  // step size of the first head
     for (int k = 0; k < hpg; ++k) {
       const int st = k & 1;
       const uint32_t par = uint32_t(k & 1);
-      const int64_t h = g * hpg + k;
+      const int h = g * hpg + k;
       uint8_t *sX = sm_base + OFF_XG;
       uint8_t *sG = sX + 16384;
-      const float Ah = p.A[h], Dh = p.D[h];
+      const float Ah = sm->ad[0], Dh = sm->ad[1];
 
       // ---- P0: cumulative step sizes (fixed-tree scan), decay in log2 units
       float cumdt = 0.f;
@@ -683,17 +699,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           st8_bf16(sm_base + OFF_GW, r, 16 * cq + 8 * c8, xv);
         }
       }
+      const bool has_next = sm->has_next != 0;
       if (has_next) ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
       float hdot = 0.f;
       float ds[16];   // this thread's dS values (state index n, 16 p values)
       {
         const float *src = reinterpret_cast<const float *>(sm_base + OFF_STG);
-        float *dst = nullptr;
-        if (here_start) {
-          if (p.dinit) dst = p.dinit + ((seq * s.H + h) * kP) * kN;
-        } else {
-          dst = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN);
-        }
+        float *dst = sm->dst0 ? sm->dst0 + k * sm->dst_stride : nullptr;
         if (has_next) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) ds[i] = src[(16 * cq + i) * kN + n];
@@ -774,6 +786,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- E4: dx and the row dot product x . Y
       if (cq == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
+      float a_next = 0.f, d_next = 0.f;
+      if (tid == 0 && k + 1 < hpg) {
+        a_next = p.A[h + 1];
+        d_next = p.D[h + 1];
+      }
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
       const float unscale = ldexpf(1.f, -(kM + kg));
@@ -807,6 +824,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::fence_proxy_async_smem();
       xb->v[4][cq][r] = sxy;
       xb->v[1][cq][r] = xd1;
+      if (tid == 0 && k + 1 < hpg) {   // every thread read this head's A, D at the top of the head
+        sm->ad[0] = a_next;
+        sm->ad[1] = d_next;
+      }
       ep_sync();
       // a thread of the upper column half issues the hand-offs: warps 0-3 go straight on to E5
       if (tid == 128) {

@@ -566,6 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float eEA = umma::ex2_approx(a2E - a2r);   // exp(E - Acs_r)
       const float wr = eEA * dtr;
       const float eE = umma::ex2_approx(a2E);
+      // Column factors of the decay below the diagonal blocks: within each
+      // 16-column block, exp(Acs_ref - Acs_s) with ref the block's last
+      // column, so that exp(Acs_r - Acs_s) = exp(Acs_r - Acs_ref) exp(Acs_ref - Acs_s)
+      // with both factors at most one (kept in dtu until E3 reuses it).
+      if (cq == 0) sm->dtu[r] = umma::ex2_approx(sm->a2[r | 15] - a2r);
 
       // H (fp32 [p][n] state entering the chunk, staging buffer) -> bf16 hi + lo,
       // stored [n][p]: this thread takes state index n and its 16 p values
@@ -628,47 +633,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int half = 0; half < 2; ++half) {
         ewait(&bars[half ? B_G1R : B_G1], par, p.err);
         umma::fence_after_sync();
+        const int c0 = 64 * half + 16 * cq;   // this thread's 16 columns in this half
+        if (c0 < 32 * (q + 1)) {               // the block touches the causal triangle (warp-uniform)
+          const bool diag = c0 + 16 > 32 * q;  // the block may cross the diagonal for some lane
+          const float er = diag ? 0.f : umma::ex2_approx(a2r - sm->a2[c0 + 15]);
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int c0 = 64 * half + 16 * cq + 8 * jj;   // this thread's 8 columns
-          const int j = 2 * half + jj;                   // their slot in cbs
-          uint32_t m16[4];
-          if (c0 < 32 * (q + 1)) {  // sub-block touches the causal triangle (warp-uniform)
+          for (int jj = 0; jj < 2; ++jj) {
             float gxv[8], ws[8];
-            umma::tmem_ld8x2(tmem + lane_off + T_RA + c0, tmem + lane_off + T_WS + c0, gxv, ws);
-            const bool diag_blk = c0 + 8 > 32 * q;   // may cross the diagonal for some lane
+            uint32_t m16[4];
+            umma::tmem_ld8x2(tmem + lane_off + T_RA + c0 + 8 * jj, tmem + lane_off + T_WS + c0 + 8 * jj, gxv, ws);
 #pragma unroll
             for (int e4 = 0; e4 < 2; ++e4) {
-              const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[c0 + 4 * e4]);
-              const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtv[c0 + 4 * e4]);
-              const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
+              const int cb = c0 + 8 * jj + 4 * e4;   // first of these 4 columns
+              const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtv[cb]);
               const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
-              float mv[4];
+              float Lv[4];
+              if (diag) {
+                const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[cb]);
+                const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
+#pragma unroll
+                for (int e1 = 0; e1 < 4; ++e1) Lv[e1] = (cb + e1 <= r) ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
+              } else {
+                const float4 ecv = *reinterpret_cast<const float4 *>(&sm->dtu[cb]);
+                Lv[0] = er * ecv.x;
+                Lv[1] = er * ecv.y;
+                Lv[2] = er * ecv.z;
+                Lv[3] = er * ecv.w;
+              }
+              float mv[4], gd[4];
 #pragma unroll
               for (int e1 = 0; e1 < 4; ++e1) {
                 const int e = 4 * e4 + e1;
-                const bool causal = !diag_blk || (c0 + e <= r);
-                const float L = causal ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
-                const float gd = gxv[e] * dus[e1];       // Gx dt (true units)
-                ws[e] = fmaf(L, gd, ws[e]);
-                mv[e1] = cbs[8 * j + e] * L;
+                gd[e1] = gxv[e] * dus[e1];       // Gx dt (true units)
+                ws[e] = fmaf(Lv[e1], gd[e1], ws[e]);
+                mv[e1] = cbs[16 * half + 8 * jj + e] * Lv[e1];
               }
               const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
               const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-              rowp = fmaf(f01.x, gxv[4 * e4 + 0] * dus[0], rowp);
-              rowp = fmaf(f01.y, gxv[4 * e4 + 1] * dus[1], rowp);
-              rowp = fmaf(f23.x, gxv[4 * e4 + 2] * dus[2], rowp);
-              rowp = fmaf(f23.y, gxv[4 * e4 + 3] * dus[3], rowp);
+              rowp = fmaf(f01.x, gd[0], rowp);
+              rowp = fmaf(f01.y, gd[1], rowp);
+              rowp = fmaf(f23.x, gd[2], rowp);
+              rowp = fmaf(f23.y, gd[3], rowp);
               m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
               m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
             }
-            umma::tmem_st8(tmem + lane_off + T_WS + c0, ws);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) m16[e] = 0u;
+            umma::tmem_st8(tmem + lane_off + T_WS + c0 + 8 * jj, ws);
+            *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
+                make_uint4(m16[0], m16[1], m16[2], m16[3]);
           }
-          *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
-              make_uint4(m16[0], m16[1], m16[2], m16[3]);
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj)
+            *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
         if (half == 0) {
           umma::fence_before_sync();

@@ -150,6 +150,36 @@ __device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float (&va)
     vb[i] = __uint_as_float(r[8 + i]);
   }
 }
+// Four x8 loads behind a single wait.
+__device__ __forceinline__ void tmem_ld8x4(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t td, float (&va)[8],
+                                           float (&vb)[8], float (&vc)[8], float (&vd)[8]) {
+  uint32_t r[32];
+#define SSD_TMEM_LD8(base, addr)                                                                                \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"                        \
+               : "=r"(r[base]), "=r"(r[base + 1]), "=r"(r[base + 2]), "=r"(r[base + 3]), "=r"(r[base + 4]),     \
+                 "=r"(r[base + 5]), "=r"(r[base + 6]), "=r"(r[base + 7])                                        \
+               : "r"(addr))
+  SSD_TMEM_LD8(0, ta);
+  SSD_TMEM_LD8(8, tb);
+  SSD_TMEM_LD8(16, tc);
+  SSD_TMEM_LD8(24, td);
+#undef SSD_TMEM_LD8
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[8 + i]);
+    vc[i] = __uint_as_float(r[16 + i]);
+    vd[i] = __uint_as_float(r[24 + i]);
+  }
+}
 // Warp-collective store of 8 consecutive fp32 columns of this warp's quadrant.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),

@@ -178,6 +178,29 @@ def kernel_bytes(name, w, es):
     return tab.get(name)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the fused
+# backward kernel per token, measured with ncu on the revision of its source
+# whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
+# no entry, and the bench then reports traffic as null until it is measured.
+FUSED_TRAFFIC_PER_TOKEN = {
+    "463badf57fa287eadc47dea7699cc500a176d69624760b893c61fafd4153724f": {
+        "bytes_per_token": 1.476270e12 * 612.064e-6 / 4096,
+        "capture": "bf16_T4096, one launch, dram__bytes.sum.per_second x gpu__time_duration.sum",
+    },
+}
+
+
+def fused_traffic(tokens):
+    import hashlib
+    path = os.path.join(ROOT, "deterministic_mamba2_ssd_gb300", "csrc", "ssd_fused_bwd.cu")
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    rec = FUSED_TRAFFIC_PER_TOKEN.get(digest)
+    return None if rec is None else rec["bytes_per_token"] * tokens
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -386,7 +409,8 @@ def main():
                        "l2": "flushed between steps (256 MB write) and inputs larger than L2"},
             "roofline": {"bound": "hbm", "kernel": ndom, "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "frac": (achieved / peak) if achieved else None,
+                         "traffic": fused_traffic(w.batch * w.seqlen) if ndom == "fused_bwd" else None,
                          "algorithmic_bytes_per_launch": alg, "launch_ms": dom_ms},
             "bwd_roofline_8TBps_frac": (api_bytes(w, es) / 8e12) / (ms_max / 1e3),
             "kernel_share": shares,

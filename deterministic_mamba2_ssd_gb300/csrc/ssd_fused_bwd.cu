@@ -176,14 +176,17 @@ __device__ __forceinline__ void st8_bf16(uint8_t *panel, int r, int c0, const fl
   *reinterpret_cast<uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)) = u;
 }
 
-// exponent k with max * 2^k in [2^14, 2^15) (0 for max == 0)
+// exponent k with max * 2^k in [2^14, 2^15) (0 for max == 0 or not finite);
+// read from the float's exponent field (max is normal: the fp16 path only
+// sees bf16 data and products of it)
 __device__ __forceinline__ int fp16_scale_exp(float mx) {
-  if (!(mx > 0.f)) return 0;
-  int e;
-  frexpf(mx, &e);
-  int k = 15 - e;
+  if (!(mx > 0.f) || !(mx < 3.0e38f)) return 0;
+  const int e = int((__float_as_uint(mx) >> 23) & 0xffu) - 126;   // mx in [2^(e-1), 2^e)
+  const int k = 15 - e;
   return max(-120, min(120, k));
 }
+// 2^k for |k| <= 126, exact (callers keep k within +-120)
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float(uint32_t(127 + k) << 23); }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
   int v;
@@ -388,11 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // fp16 A/B (formats 0): D1 MN-major/MN-major N = 64
       constexpr uint32_t id_kk64 = umma::idesc_bf16_f32(128, 64, 0, 0);
       constexpr uint32_t id_f16_mm64 = (1u << 4) | (1u << 15) | (1u << 16) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+      // Descriptors of a K step kk: the start-address field (address >> 4, 14 bits) of the
+      // operand's base descriptor plus the step's byte offset >> 4.  Every operand lies below
+      // 256 KB, so the field never wraps and the base descriptor is loop-invariant.
       auto kdesc = [](uint32_t base, uint32_t panel_bytes, int kk) {  // K-major operand, K step kk
-        return umma::smem_desc_sw128(base + uint32_t(kk / 64) * panel_bytes + uint32_t(kk % 64) * 2, 16, 1024);
+        return umma::smem_desc_sw128(base, 16, 1024) +
+               uint64_t((uint32_t(kk / 64) * panel_bytes + uint32_t(kk % 64) * 2) >> 4);
       };
       auto mdesc = [](uint32_t base, uint32_t panel_bytes, int kk) {  // MN-major operand, K step kk
-        return umma::smem_desc_sw128(base + uint32_t(kk) * 128, panel_bytes, 1024);
+        return umma::smem_desc_sw128(base, panel_bytes, 1024) + uint64_t((uint32_t(kk) * 128) >> 4);
       };
       wait_bar(&bars[B_BC], 0, p.err);
       umma::fence_after_sync();
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid == 0) umma::mbar_arrive(&bars[E_CBREAD]);
     const int kM = fp16_scale_exp(cbmax);
-    const float sM = ldexpf(1.f, kM);
+    const float sM = exp2i(kM), sMinv = exp2i(-kM);
 #pragma unroll
     for (int i = 0; i < 32; ++i) cbs[i] *= sM;
 
@@ -771,13 +778,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) umma::mbar_arrive(&bars[E_DS0 + st]);   // Y and dB may start
       // g -> fp16 scaled by an exact power of two, in place (the dx product
       // pairs it with the fp16 M); g x^T has been computed from the bf16 g
-      float gm = 0.f;
+      float gmw[kEpiWarps];
 #pragma unroll
-      for (int w = 0; w < kEpiWarps; ++w) gm = fmaxf(gm, sm->red[w]);
+      for (int w = 0; w < kEpiWarps; ++w) gmw[w] = sm->red[w];
+#pragma unroll
+      for (int st2 = kEpiWarps / 2; st2 > 0; st2 >>= 1)
+#pragma unroll
+        for (int w = 0; w < st2; ++w) gmw[w] = fmaxf(gmw[w], gmw[w + st2]);
+      const float gm = gmw[0];
       const int kg = fp16_scale_exp(gm);
       float inter_part = 0.f;
       {
-        const float sg = ldexpf(1.f, kg);
+        const float sg = exp2i(kg);
         float ch0[8], ch1[8], gv[8];
         umma::tmem_ld8x2(tmem + lane_off + T_CH + 16 * cq, tmem + lane_off + T_CH + 16 * cq + 8, ch0, ch1);
         ld8_bf16(sG, r, 16 * cq, gv);
@@ -810,12 +822,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
-      const float unscale = ldexpf(1.f, -(kM + kg));
+      const float unscale = exp2i(-kM) * exp2i(-kg);
       float sxy = 0.f, xd1 = 0.f;   // x . Y and x . D1 (raw units) of this row
       {
         // dx rows staged in the (now idle) M16 buffer, 128-byte swizzled fp32, then TMA-stored
         uint8_t *stage = sm_base + OFF_M16 + (cq >> 1) * 16384;
-        const float dg = Dh * ldexpf(1.f, -kg);
+        const float dg = Dh * exp2i(-kg);
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
           float d1[8], y[8], xv[8], gv[8];
@@ -862,12 +874,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float a2r5 = sm->a2[r], a2E5 = sm->a2[kQ - 1], dt5 = sm->dtv[r];
         const float eEA5 = umma::ex2_approx(a2E5 - a2r5), wr5 = eEA5 * dt5;
-        const float raw = ldexpf(1.f, -(kM + kg));   // x . D1 in true units
+        const float raw = exp2i(-kM) * exp2i(-kg);   // x . D1 in true units
         // inclusive row and column sums of M o Gx o dt: the diagonal cancels in their difference
         auto qsum = [&](int i) {   // the four column quarters, fixed order
           return (xb->v[i][0][r] + xb->v[i][1][r]) + (xb->v[i][2][r] + xb->v[i][3][r]);
         };
-        const float rowp5 = qsum(0) / sM;
+        const float rowp5 = qsum(0) * sMinv;
         const float dintra = qsum(1) * raw;   // sum_t M_tr Gx_tr (x . D1)
         const float inter = umma::ex2_approx(a2r5) * qsum(2);
         const float gx5 = qsum(3);

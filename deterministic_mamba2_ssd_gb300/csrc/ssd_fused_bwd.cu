@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cumdt += pre;
         sm->a2[r] = cumdt * (Ah * kLog2e);
         sm->dtv[r] = dt_next;
-        if (r == kQ - 1) sm->red[36] = cumdt;  // sum of the chunk's step sizes
+        if (r == kQ - 1) sm->red[36 + (k & 1)] = cumdt;  // sum of the chunk's step sizes (by head parity)
       }
       ewait(&bars[B_XG], par, p.err);
       ewait(&bars[B_H], par, p.err);
@@ -920,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tid == 0) {
             const float sg = ((sm->red[8] + sm->red[9]) + sm->red[10]) + sm->red[11];
             const float sc = ((sm->red[12] + sm->red[13]) + sm->red[14]) + sm->red[15];
-            const float dap = fmaf(K, sm->red[36], sc);
+            const float dap = fmaf(K, sm->red[36 + (k & 1)], sc);
             if (p.atomic) {
               atomicAdd(p.dA + h, dap);
               atomicAdd(p.dD + h, sg);
@@ -931,8 +931,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      ep_sync();
+      // No barrier here: only quarter-0 warps go on using this head's shared
+      // values, and everything the next head overwrites is read before E5's
+      // barrier above (or, for the step-size total, kept per head parity).
     }
+    ep_sync();
 
     // ---- unit end: head-summed W (hi + lo) for the intra-chunk dB/dC products
 #pragma unroll

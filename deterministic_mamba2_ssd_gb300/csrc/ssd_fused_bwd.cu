@@ -152,6 +152,25 @@ __device__ __forceinline__ void f16x8_to_f32(uint4 u, float *f) {
   }
 }
 
+// v -> bf16 hi + lo (hi = round(v), lo = round(v - hi)) as packed pairs, and
+// both stored as 8 consecutive elements of row r of two 64-column panels
+__device__ __forceinline__ void st8_bf16_hilo(uint8_t *panel_hi, uint8_t *panel_lo, int r, int c0,
+                                              const float (&v)[8]) {
+  uint4 uh, ul;
+  uint32_t *ph = reinterpret_cast<uint32_t *>(&uh), *pl = reinterpret_cast<uint32_t *>(&ul);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+    pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+  }
+  const uint32_t off = r * 128 + (((c0 >> 3) ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4 *>(panel_hi + off) = uh;
+  *reinterpret_cast<uint4 *>(panel_lo + off) = ul;
+}
+
 __device__ __forceinline__ void st_row8_f16(uint8_t *panel, int r, int c0, const float (&v)[8]) {
   uint4 u;
   __half2 *h = reinterpret_cast<__half2 *>(&u);
@@ -586,15 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int pg = 2 * cq + u;   // group of 8 p values
-          float hi[8], lo[8];
+          float v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float v = hs[(8 * pg + i) * kN + n];
-            hi[i] = __bfloat162float(__float2bfloat16_rn(v));
-            lo[i] = v - hi[i];
-          }
-          st8_bf16(sm_base + OFF_HD, n, 8 * pg, hi);
-          st8_bf16(sm_base + OFF_HD + 16384, n, 8 * pg, lo);
+          for (int i = 0; i < 8; ++i) v[i] = hs[(8 * pg + i) * kN + n];
+          st8_bf16_hilo(sm_base + OFF_HD, sm_base + OFF_HD + 16384, n, 8 * pg, v);
         }
       }
       __syncwarp();
@@ -604,19 +618,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c8 = 0; c8 < 2; ++c8) {
         const int c0 = 16 * cq + 8 * c8;
-        float gv[8], xv[8], hi[8], lo[8];
+        float gv[8], xv[8], t[8];
         ld8_bf16(sG, r, c0, gv);
         ld8_bf16(sX, r, c0, xv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float t = eacs * gv[i];
-          hi[i] = __bfloat162float(__float2bfloat16_rn(t));
-          lo[i] = t - hi[i];
+          t[i] = eacs * gv[i];
           gmax = fmaxf(gmax, fabsf(gv[i]));
           gx = fmaf(gv[i], xv[i], gx);
         }
-        st8_bf16(sm_base + OFF_GW, r, c0, hi);
-        st8_bf16(sm_base + OFF_GW + 16384, r, c0, lo);
+        st8_bf16_hilo(sm_base + OFF_GW, sm_base + OFF_GW + 16384, r, c0, t);
       }
       // per-warp maxima of |g|; read after the barrier that ends E1
 #pragma unroll

@@ -550,13 +550,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->dst0 = p.ring + (((c % p.ring_depth) * s.b + bi) * s.H + h0) * (kP * kN);
       }
       sm->dst_stride = kP * kN;
-      sm->ad[0] = p.A[g * hpg];
-      sm->ad[1] = p.D[g * hpg];
+      sm->ad[0] = __ldcg(p.A + g * hpg);
+      sm->ad[1] = __ldcg(p.D + g * hpg);
     }
     ep_sync();
     const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
 
-    float dt_next = (cq == 0) ? dtg[int64_t(r) * s.H + g * hpg] : 0.f;  // step size of the first head
+    // (scalar loads and stores below bypass L1: its few KB beside the shared
+    // memory carve-out are left to the register spill slots)
+    float dt_next = (cq == 0) ? __ldcg(dtg + int64_t(r) * s.H + g * hpg) : 0.f;  // step size of the first head
     for (int k = 0; k < hpg; ++k) {
       const int st = k & 1;
       const uint32_t par = uint32_t(k & 1);
@@ -825,11 +827,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) umma::mbar_arrive(&bars[E_CHR]);
 
       // ---- E4: dx and the row dot product x . Y
-      if (cq == 0 && k + 1 < hpg) dt_next = dtg[int64_t(r) * s.H + h + 1];  // next head's step size
+      if (cq == 0 && k + 1 < hpg) dt_next = __ldcg(dtg + int64_t(r) * s.H + h + 1);  // next head's step size
       float a_next = 0.f, d_next = 0.f;
       if (tid == 0 && k + 1 < hpg) {
-        a_next = p.A[h + 1];
-        d_next = p.D[h + 1];
+        a_next = __ldcg(p.A + h + 1);
+        d_next = __ldcg(p.D + h + 1);
       }
       ewait(&bars[B_G4], par, p.err);
       umma::fence_after_sync();
@@ -927,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int w = 0; w < kEpiWarps; ++w) hsum += sm->red[40 + w];
           const float K = su + umma::ex2_approx(a2E5) * hsum;   // + dEpass = exp(E) <H, dS>
           const float da = (sfx + off) + K;
-          p.ddt[(row0 + r) * s.H + h] = fmaf(Ah, da, dintra + eEA5 * sxy5);
+          __stcg(p.ddt + (row0 + r) * s.H + h, fmaf(Ah, da, dintra + eEA5 * sxy5));
           if (tid == 0) {
             const float sg = ((sm->red[8] + sm->red[9]) + sm->red[10]) + sm->red[11];
             const float sc = ((sm->red[12] + sm->red[13]) + sm->red[14]) + sm->red[15];
@@ -936,8 +938,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               atomicAdd(p.dA + h, dap);
               atomicAdd(p.dD + h, sg);
             } else {
-              p.dA_part[(bi * s.nc + c) * s.H + h] = dap;
-              p.dD_part[(bi * s.nc + c) * s.H + h] = sg;
+              __stcg(p.dA_part + (bi * s.nc + c) * s.H + h, dap);
+              __stcg(p.dD_part + (bi * s.nc + c) * s.H + h, sg);
             }
           }
         }
@@ -975,12 +977,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *o = p.dB + ((row0 + r) * s.G + g) * kN + n0;
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
-        *reinterpret_cast<float4 *>(o + 4 * i4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+        __stcg(reinterpret_cast<float4 *>(o + 4 * i4), make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]));
       umma::tmem_ld16(tmem + lane_off + T_DC + n0, v);
       o = p.dC + ((row0 + r) * s.G + g) * kN + n0;
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
-        *reinterpret_cast<float4 *>(o + 4 * i4) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+        __stcg(reinterpret_cast<float4 *>(o + 4 * i4), make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]));
     }
     umma::fence_before_sync();
     if (tid == 128) umma::tma_store_wait_all();

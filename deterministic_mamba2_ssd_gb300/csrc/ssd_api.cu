@@ -133,6 +133,7 @@ ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *wo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (word & 4) return SSD_ERR_UNSUPPORTED;   // the fused kernel found its shared memory misaligned
   return word ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 

@@ -58,8 +58,8 @@ constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [n][p] bf16, 16 KB each; 
 constexpr uint32_t OFF_GW = 163840;    // exp(Acs) o g hi | lo: [t][p] bf16; later w o x (hi half) + scratch (lo half)
 constexpr uint32_t OFF_M16 = 196608;   // scaled M: [t][s] fp16, 2 panels x 16 KB
 constexpr uint32_t OFF_SMALL = 229376;
-constexpr uint32_t SMALL_BYTES = 2048;
-constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;  // + slack for aligning the base to 1 KB
+constexpr uint32_t SMALL_BYTES = 3072;
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // scratch that lives in the idle lo half of GW between the dC/dHscan products and the next head
 constexpr uint32_t OFF_XBUF = OFF_GW + 16384;
@@ -278,8 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     fused_bwd_kernel(const Params p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
                      const __grid_constant__ CUtensorMap tm_dx) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *sm_base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // The 128-byte swizzled tiles need a 1 KB aligned base, which is where the
+  // dynamic shared memory of this kernel starts (no static shared memory).
+  // Checked rather than assumed: a misaligned base reports and exits.  With a
+  // fixed base every shared-memory address is a constant offset, so no base
+  // pointer has to stay in a register.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *const sm_base = smem_raw;
+  if (umma::smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, 4);
+    return;
+  }
   Small *sm = reinterpret_cast<Small *>(sm_base + OFF_SMALL);
   uint64_t *bars = sm->bars;
   const Shape &s = p.s;
@@ -588,17 +597,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ewait(&bars[B_XG], par, p.err);
       ewait(&bars[B_H], par, p.err);
       ep_sync();
-      const float a2r = sm->a2[r], dtr = sm->dtv[r], a2E = sm->a2[kQ - 1];
-
-      const float eacs = umma::ex2_approx(a2r);        // exp(Acs_r)
-      const float eEA = umma::ex2_approx(a2E - a2r);   // exp(E - Acs_r)
-      const float wr = eEA * dtr;
-      const float eE = umma::ex2_approx(a2E);
+      // per-row values are re-read from shared memory in each phase that uses
+      // them rather than kept in registers across phases (fewer spills)
+      const float eacs = umma::ex2_approx(sm->a2[r]);   // exp(Acs_r)
       // Column factors of the decay below the diagonal blocks: within each
       // 16-column block, exp(Acs_ref - Acs_s) with ref the block's last
       // column, so that exp(Acs_r - Acs_s) = exp(Acs_r - Acs_ref) exp(Acs_ref - Acs_s)
       // with both factors at most one (kept in dtu until E3 reuses it).
-      if (cq == 0) sm->dtu[r] = umma::ex2_approx(sm->a2[r | 15] - a2r);
+      if (cq == 0) sm->dtu[r] = umma::ex2_approx(sm->a2[r | 15] - sm->a2[r]);
 
       // H (fp32 [p][n] state entering the chunk, staging buffer) -> bf16 hi + lo,
       // stored [n][p]: this thread takes state index n and its 16 p values
@@ -649,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp hands its columns back so that C H can be computed there while
       // the right half is processed.
       float rowp = 0.f;   // sum_s M16_rs Gx_rs dt_s, times sM
+      const float a2r = sm->a2[r];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         ewait(&bars[half ? B_G1R : B_G1], par, p.err);
@@ -722,6 +729,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- E3: chain step (dH to the chunk before), then E2: carried-in state term
       ewait(&bars[B_DHS], par, p.err);   // dHscan^T in TMEM; dC and dHscan have read G~ (GW)
       umma::fence_after_sync();
+      const float a2E3 = sm->a2[kQ - 1], dtr = sm->dtv[r];
+      const float wr3 = umma::ex2_approx(a2E3 - sm->a2[r]) * dtr;   // w = exp(E - Acs_r) dt_r
+      const float eE = umma::ex2_approx(a2E3);                        // exp(E)
       // GW is idle from here to the next head: exchange scratch (lo half) and w o x (hi half)
       xb->v[0][cq][r] = rowp;
       xb->v[3][cq][r] = gx;
@@ -732,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float xv[8];
           ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xv[i] *= wr;
+          for (int i = 0; i < 8; ++i) xv[i] *= wr3;
           st8_bf16(sm_base + OFF_GW, r, 16 * cq + 8 * c8, xv);
         }
       }
@@ -855,7 +865,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int i = 4 * i4 + e;
               sxy = fmaf(xv[i], y[i], sxy);
               xd1 = fmaf(xv[i], d1[i], xd1);
-              o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr, y[i], dg * gv[i]));
+              o[e] = fmaf(dtr, d1[i] * unscale, fmaf(wr3, y[i], dg * gv[i]));
             }
             const int chunk = (4 * (cq & 1) + 2 * c8 + i4) ^ (r & 7);
             *reinterpret_cast<float4 *>(stage + r * 128 + chunk * 16) = make_float4(o[0], o[1], o[2], o[3]);

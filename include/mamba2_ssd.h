@@ -153,8 +153,9 @@ ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, f
 
 /* Status of the last backward that used this workspace: reads one word
  * written by the device (synchronises `stream`).  SSD_ERR_TIMEOUT when a
- * bounded device-side wait of the fused backward ran out (its outputs are
- * then invalid), SSD_OK otherwise. */
+ * bounded device-side wait of the fused backward ran out, SSD_ERR_UNSUPPORTED
+ * when the fused kernel found its dynamic shared memory not 1 KB aligned and
+ * did no work (outputs invalid in both cases), SSD_OK otherwise. */
 ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream);
 
 /* Fault-injection diagnostic of the fused backward (fused shapes only): the

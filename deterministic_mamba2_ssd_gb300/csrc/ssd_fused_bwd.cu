@@ -80,7 +80,8 @@ enum Bar {
 struct Small {
   float a2[kQ];    // in-chunk cumulative decay of the current head, log2 units: A log2(e) cumsum(dt)
   float dtv[kQ];   // step sizes of the current head
-  float dtu[kQ];   // step sizes times the scale that undoes the fp16 scaling of g x^T
+  float dtu[kQ];   // column decay factors of E1 (per 16-column block)
+  float cdt[kQ];   // cumulative step sizes of the head about to run (E5 reads them)
   float red[64];
   uint64_t bars[NBARS];
   uint32_t tmem_base;
@@ -118,7 +119,7 @@ struct Params {
 
 // ------------------------------------------------------------- helpers --
 __device__ __forceinline__ void ep_sync() { umma::named_bar(1, kEpiThreads); }
-__device__ __forceinline__ void lo_sync() { umma::named_bar(2, 128); }  // warps 0-3
+__device__ __forceinline__ void scan_sync() { umma::named_bar(2, 128); }  // warps 8-11 (column quarter 2)
 
 __device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
   const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -567,7 +568,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // (scalar loads and stores below bypass L1: its few KB beside the shared
     // memory carve-out are left to the register spill slots)
-    float dt_next = (cq == 0) ? __ldcg(dtg + int64_t(r) * s.H + g * hpg) : 0.f;  // step size of the first head
+    // Step-size scan of a head (fixed tree: warp shuffles, then the four row
+    // quadrants in order), run by the column-quarter-2 warps one head ahead:
+    // Acs in log2 units into a2, dt into dtv, the cumulative step into cdt,
+    // the chunk's total into red[36 + head parity].
+    auto scan_head = [&](int kk, float dtr_in, float Ak) {
+      float cum = dtr_in;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, cum, o);
+        if (lane >= o) cum += v;
+      }
+      if (lane == 31) sm->red[32 + q] = cum;
+      scan_sync();
+      float pre = 0.f;
+      for (int w = 0; w < q; ++w) pre += sm->red[32 + w];
+      cum += pre;
+      sm->a2[r] = cum * (Ak * kLog2e);
+      sm->dtv[r] = dtr_in;
+      sm->cdt[r] = cum;
+      if (r == kQ - 1) sm->red[36 + (kk & 1)] = cum;
+    };
+    float dt_next = (cq == 2) ? __ldcg(dtg + int64_t(r) * s.H + g * hpg) : 0.f;  // step size of the first head
+    if (cq == 2) scan_head(0, dt_next, sm->ad[0]);
     for (int k = 0; k < hpg; ++k) {
       const int st = k & 1;
       const uint32_t par = uint32_t(k & 1);
@@ -576,24 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *sG = sX + 16384;
       const float Ah = sm->ad[0], Dh = sm->ad[1];
 
-      // ---- P0: cumulative step sizes (fixed-tree scan), decay in log2 units
-      float cumdt = 0.f;
-      if (cq == 0) {
-        cumdt = dt_next;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float v = __shfl_up_sync(0xffffffffu, cumdt, o);
-          if (lane >= o) cumdt += v;
-        }
-        if (lane == 31) sm->red[32 + q] = cumdt;
-        lo_sync();
-        float pre = 0.f;
-        for (int w = 0; w < q; ++w) pre += sm->red[32 + w];
-        cumdt += pre;
-        sm->a2[r] = cumdt * (Ah * kLog2e);
-        sm->dtv[r] = dt_next;
-        if (r == kQ - 1) sm->red[36 + (k & 1)] = cumdt;  // sum of the chunk's step sizes (by head parity)
-      }
+      // ---- P0 (the step-size scan of this head ran at the end of the previous one)
       ewait(&bars[B_XG], par, p.err);
       ewait(&bars[B_H], par, p.err);
       ep_sync();
@@ -735,7 +741,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // GW is idle from here to the next head: exchange scratch (lo half) and w o x (hi half)
       xb->v[0][cq][r] = rowp;
       xb->v[3][cq][r] = gx;
-      if (cq == 0) sm->dtu[r] = cumdt;   // keep the cumulative step for E5
       {
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
@@ -837,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) umma::mbar_arrive(&bars[E_CHR]);
 
       // ---- E4: dx and the row dot product x . Y
-      if (cq == 0 && k + 1 < hpg) dt_next = __ldcg(dtg + int64_t(r) * s.H + h + 1);  // next head's step size
+      if (cq == 2 && k + 1 < hpg) dt_next = __ldcg(dtg + int64_t(r) * s.H + h + 1);  // next head's step size
       float a_next = 0.f, d_next = 0.f;
       if (tid == 0 && k + 1 < hpg) {
         a_next = __ldcg(p.A + h + 1);
@@ -907,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inter = umma::ex2_approx(a2r5) * qsum(2);
         const float gx5 = qsum(3);
         const float sxy5 = qsum(4);
-        const float cumdt5 = sm->dtu[r];
+        const float cumdt5 = sm->cdt[r];
         const float colp = dt5 * dintra;
         const float u = wr5 * sxy5;
         const float dacs = rowp5 - colp + inter - u;
@@ -930,6 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         ep_sync();
+        // every E5 read of a2, dtv and cdt is done: the next head's scan may overwrite them
+        if (cq == 2 && k + 1 < hpg) scan_head(k + 1, dt_next, sm->ad[0]);
         if (cq == 0) {
           float off = 0.f;
           for (int w = 3; w > q; --w) off += sm->red[w];

@@ -183,9 +183,9 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "463badf57fa287eadc47dea7699cc500a176d69624760b893c61fafd4153724f": {
-        "bytes_per_token": 1.476270e12 * 612.064e-6 / 4096,
-        "capture": "bf16_T4096, one launch, dram__bytes.sum.per_second x gpu__time_duration.sum",
+    "8ccfe17fe2797996e2802c7724d11264af42dc7faf61877190d137c3b530b85c": {
+        "bytes_per_token": (2.28e9 + 1.58e9) / 16384,
+        "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }
 

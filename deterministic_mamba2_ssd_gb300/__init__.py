@@ -96,13 +96,14 @@ def lib():
 
 
 DIMS_SEQ_IDX = 1
+DIMS_SEQ_ANY_START = 2
 
 
 def make_dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size, nseq=None, dtype=torch.bfloat16,
-              seq_idx=False):
+              seq_idx=False, any_start=False):
     return Dims(batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size,
                 batch if nseq is None else nseq, SSD_BF16 if dtype == torch.bfloat16 else SSD_F32,
-                DIMS_SEQ_IDX if seq_idx else 0)
+                (DIMS_SEQ_IDX if seq_idx else 0) | (DIMS_SEQ_ANY_START if any_start else 0))
 
 
 def num_configs(dims: Dims) -> int:
@@ -166,10 +167,11 @@ class Saved:
         return self.tensors["states"]
 
 
-def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=None):
+def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=None, any_start=False):
     """Forward.  Returns (y, saved).  x (b,T,H,P) and B, C (b,T,G,N) in
     bf16 or fp32; dt (b,T,H), A (H), D (H), init_states (nseq,H,P,N) fp32;
-    seq_idx (1,T) int32 with chunk-aligned sequence starts."""
+    seq_idx (1,T) int32, non-decreasing, with sequence starts at multiples of
+    chunk_size unless ``any_start`` (which selects the general backward)."""
     b, T, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     dev = x.device
@@ -187,7 +189,10 @@ def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=No
         _check(seq_idx, "seq_idx", (b, T), torch.int32, dev)
     if init_states is not None:
         _check(init_states, "init_states", (nseq, H, P, N), torch.float32, dev)
-    dims = make_dims(b, T, H, P, G, N, chunk_size, nseq, x.dtype, seq_idx=seq_idx is not None)
+    if any_start and seq_idx is None:
+        raise ValueError("any_start needs seq_idx")
+    dims = make_dims(b, T, H, P, G, N, chunk_size, nseq, x.dtype, seq_idx=seq_idx is not None,
+                     any_start=any_start)
     nc = lib().mamba2_ssd_num_chunks(ctypes.byref(dims))
     if nc < 0:
         raise ValueError("invalid dims")

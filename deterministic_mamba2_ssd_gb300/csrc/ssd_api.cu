@@ -20,7 +20,10 @@ bool dims_ok(const ssd_dims *d) {
     return false;
   if (d->nheads % d->ngroups != 0) return false;
   if (d->dtype != SSD_F32 && d->dtype != SSD_BF16) return false;
-  if ((d->flags & ~SSD_DIMS_SEQ_IDX) != 0) return false;
+  if ((d->flags & ~(SSD_DIMS_SEQ_IDX | SSD_DIMS_SEQ_ANY_START)) != 0) return false;
+  if ((d->flags & SSD_DIMS_SEQ_ANY_START) && !(d->flags & SSD_DIMS_SEQ_IDX)) return false;
+  // with seq_idx the kernels keep token positions and sequence ids in int32
+  if ((d->flags & SSD_DIMS_SEQ_IDX) && (d->seqlen > INT32_MAX || d->nseq > INT32_MAX)) return false;
   if (d->chunk_size > 1024) return false;
   const int64_t nc = (d->seqlen + d->chunk_size - 1) / d->chunk_size;
   if (d->batch * nc * d->nheads > (int64_t(1) << 31) - 1) return false;
@@ -54,7 +57,13 @@ constexpr int kNumSimt = 2;
 constexpr int kFusedRings[] = {4, 2};
 constexpr int kNumFused = 2;
 
-bool use_fused(const ssd_dims *d) { return ssd::fused_bwd_supported(shape_of(d), d->dtype == SSD_BF16); }
+// The fused kernel resets the state at chunk boundaries only, so sequence
+// starts inside a chunk always take the general path.
+bool use_fused(const ssd_dims *d) {
+  return !(d->flags & SSD_DIMS_SEQ_ANY_START) && ssd::fused_bwd_supported(shape_of(d), d->dtype == SSD_BF16);
+}
+
+bool has_seq(const ssd_dims *d) { return (d->flags & SSD_DIMS_SEQ_IDX) != 0; }
 
 ssd::FusedOptions fused_options(const ssd_dims *d, int config, int variant) {
   ssd::FusedOptions o;
@@ -113,7 +122,7 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
 int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (use_fused(dims)) return variant == SSD_VARIANT_ATOMIC ? 1 : 2;
-  return ssd::simt_bwd_launches(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
+  return ssd::simt_bwd_launches(shape_of(dims), variant == SSD_VARIANT_ATOMIC, has_seq(dims));
 }
 
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
@@ -122,7 +131,7 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
     if (variant == SSD_VARIANT_ATOMIC) return k == 0 ? "fused_bwd_atomic" : "invalid";
     return k == 0 ? "fused_bwd" : (k == 1 ? "fold_scalars" : "invalid");
   }
-  return ssd::simt_bwd_launch_name(variant == SSD_VARIANT_ATOMIC, k);
+  return ssd::simt_bwd_launch_name(variant == SSD_VARIANT_ATOMIC, has_seq(dims), k);
 }
 
 ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream) {
@@ -154,8 +163,9 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (seq_idx) {
-    // The chunked kernels reset the state at chunk starts only; check that
-    // every sequence start falls on one.  One synchronous copy, documented.
+    // Ids must be valid and non-decreasing; without SSD_DIMS_SEQ_ANY_START
+    // every sequence start must also fall on a chunk start (the fused
+    // backward resets the state there only).  One synchronous copy, documented.
     if (dims->batch != 1) return SSD_ERR_UNSUPPORTED;
     std::vector<int32_t> h(size_t(s.T));
     if (cudaMemcpyAsync(h.data(), seq_idx, size_t(s.T) * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -164,7 +174,8 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
     for (int64_t t = 0; t < s.T; ++t) {
       if (h[t] < 0 || h[t] >= dims->nseq) return SSD_ERR_INVALID_ARG;
       if (t > 0 && h[t] < h[t - 1]) return SSD_ERR_INVALID_ARG;
-      if (t > 0 && h[t] != h[t - 1] && t % s.Q != 0) return SSD_ERR_UNSUPPORTED;
+      if (t > 0 && h[t] != h[t - 1] && t % s.Q != 0 && !(dims->flags & SSD_DIMS_SEQ_ANY_START))
+        return SSD_ERR_UNSUPPORTED;
     }
   }
   ssd::Args a{};

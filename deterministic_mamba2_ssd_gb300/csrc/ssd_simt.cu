@@ -1,5 +1,5 @@
 // ssd_simt.cu -- general CUDA-core path of the Mamba2 SSD forward and
-// backward (any shape, fp32 or bf16 inputs, chunk-aligned sequence starts).
+// backward (any shape, fp32 or bf16 inputs, sequence starts anywhere).
 //
 // Each kernel is one step of the chunked algorithm whose backward "Deterministic
 // bwd kernel for mamba2" (Mamba PR #827) breaks down per kernel:
@@ -14,6 +14,16 @@
 // Notation per (batch b, chunk c, head h): local token i in [0, Lc), Lc the
 // chunk's length; Acs_i the in-chunk inclusive prefix sum of dt*A (hi+lo);
 // E = Acs_{Lc-1}; g = dout.  States are (P, N), n fastest.
+//
+// Packed variable-length batches (seq_idx, batch row 0 only) may start a
+// sequence inside a chunk.  A token then sees the state entering the chunk
+// only if its sequence entered the chunk from the previous one (or starts at
+// the chunk's first token, where that state is the initial one); a sequence
+// that starts at local position f >= 1 begins from its own initial state (or
+// zero), decayed from just before f, i.e. by exp(Acs_i - Acs_{f-1}).  Decay
+// terms between tokens of different sequences are zero, and only the
+// sequence holding the chunk's last token reaches the chunk-end state.  With
+// chunk-aligned starts every mask below is a no-op.
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
 
@@ -24,6 +34,25 @@ namespace {
 constexpr int kPassThreads = 256;
 
 __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// first[s] = first token of sequence s (batch row 0); one writer per entry
+// (the token where the id changes); entries of ids with no token keep the
+// -1 of the preceding memset.
+__global__ void seq_first_kernel(int64_t T, const int32_t *__restrict__ seq_idx, int32_t *__restrict__ first) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  if (t == 0 || seq_idx[t] != seq_idx[t - 1]) first[seq_idx[t]] = int32_t(t);
+}
+
+// Local position at which the sequence holding token t started inside the
+// chunk beginning at t0, or 0 when it entered the chunk from the previous one
+// or starts at t0 (it then sees the state entering the chunk).
+__device__ __forceinline__ int64_t local_start(const int32_t *seq_idx, const int32_t *first, int64_t bi,
+                                               int64_t T, int64_t t, int64_t t0) {
+  if (seq_idx == nullptr) return 0;
+  const int64_t f = int64_t(first[seq_idx[bi * T + t]]) - t0;
+  return f > 0 ? f : 0;
+}
 
 // ---------------------------------------------------------------- cumsum --
 // Acs (b,H,nc,Q) as hi + lo: left-to-right compensated (two-sum) prefix sum
@@ -54,19 +83,23 @@ __global__ void cumsum_fwd_kernel(Shape s, const float *__restrict__ dt, const f
 }
 
 // ------------------------------------------------------ chunk_state (fwd) --
-// S[b,c,h,p,n] = sum_i exp(E - Acs_i) dt_i x_i[p] B_i[n]; one thread per (p,n).
+// S[b,c,h,p,n] = sum_i exp(E - Acs_i) dt_i x_i[p] B_i[n] over the tokens of
+// the sequence holding the chunk's last token (i >= fe); one thread per (p,n).
 template <class TIn>
 __global__ void chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Bm,
                                        const float *__restrict__ dt, const float *__restrict__ acs_hi,
-                                       const float *__restrict__ acs_lo, float *__restrict__ S) {
+                                       const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                                       const int32_t *__restrict__ first, float *__restrict__ S) {
   extern __shared__ float w[];
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x)
-    w[i] = __fmul_rn(expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])), dt[(bi * s.T + t0 + i) * s.H + h]);
+    w[i] = i < fe ? 0.f
+                  : __fmul_rn(expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])), dt[(bi * s.T + t0 + i) * s.H + h]);
   __syncthreads();
   const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
   if (e >= s.P * s.N) return;
@@ -81,23 +114,33 @@ __global__ void chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const
 
 // ------------------------------------------------ state passing (fwd) --
 // states[b,c] = state entering chunk c: init/zero where chunk c starts a
-// sequence, else exp(E_{c-1}) states[b,c-1] + S[b,c-1]. One thread per (b,h,e).
+// sequence, else (carried part) + S[b,c-1], the carried part being
+// exp(E_{c-1}) states[b,c-1], or exp(E_{c-1} - Acs_{fe-1}) init[seq] when the
+// sequence holding chunk c-1's last token started inside it at fe >= 1.
+// One thread per (b,h,e).
 __global__ void state_passing_fwd_kernel(Shape s, const float *__restrict__ S, const float *__restrict__ acs_hi,
                                          const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                                         const float *__restrict__ init, float *__restrict__ states) {
+                                         const int32_t *__restrict__ first, const float *__restrict__ init,
+                                         float *__restrict__ states) {
   const int64_t PN = s.P * s.N;
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.H * PN) return;
   const int64_t e = idx % PN, h = (idx / PN) % s.H, bi = idx / (PN * s.H);
   float run = 0.f;
   for (int64_t c = 0; c < s.nc; ++c) {
-    const int64_t t0 = c * s.Q;
+    const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
     if (is_seq_start(seq_idx, bi, s.T, t0))
       run = init ? init[(seq_of(seq_idx, bi, s.T, t0) * s.H + h) * PN + e] : 0.f;
     const int64_t o = ((bi * s.nc + c) * s.H + h) * PN + e;
     states[o] = run;
-    const int64_t q = ((bi * s.H + h) * s.nc + c) * s.Q + (s.Q - 1);
-    run = fmaf(expf(__fadd_rn(acs_hi[q], acs_lo[q])), run, S[o]);
+    const int64_t q0 = ((bi * s.H + h) * s.nc + c) * s.Q, q = q0 + (s.Q - 1);
+    const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+    if (fe == 0) {
+      run = fmaf(expf(__fadd_rn(acs_hi[q], acs_lo[q])), run, S[o]);
+    } else {
+      const float in = init ? init[(seq_of(seq_idx, bi, s.T, t0 + Lc - 1) * s.H + h) * PN + e] : 0.f;
+      run = fmaf(expf(acs_diff(acs_hi[q], acs_lo[q], acs_hi[q0 + fe - 1], acs_lo[q0 + fe - 1])), in, S[o]);
+    }
   }
 }
 
@@ -121,43 +164,52 @@ __global__ void cb_kernel(Shape s, const TIn *__restrict__ Bm, const TIn *__rest
 }
 
 // ------------------------------------------------------- chunk_scan (fwd) --
-// y_i[p] = sum_{j<=i} CB[i,j] exp(Acs_i - Acs_j) dt_j x_j[p]
-//        + exp(Acs_i) sum_n states[p,n] C_i[n] + D x_i[p].  One thread per (b,t,h,p).
+// y_i[p] = sum_{f<=j<=i} CB[i,j] exp(Acs_i - Acs_j) dt_j x_j[p]
+//        + din_i sum_n Hin[p,n] C_i[n] + D x_i[p], f = local_start(i): Hin = states
+// and din_i = exp(Acs_i) when f = 0, else Hin = init[seq] (or 0) and
+// din_i = exp(Acs_i - Acs_{f-1}).  One thread per (b,t,h,p).
 template <class TIn>
 __global__ void chunk_scan_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Cm,
                                       const float *__restrict__ dt, const float *__restrict__ D,
                                       const float *__restrict__ CB, const float *__restrict__ acs_hi,
                                       const float *__restrict__ acs_lo, const float *__restrict__ states,
-                                      TIn *__restrict__ y) {
+                                      const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                                      const float *__restrict__ init, TIn *__restrict__ y) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.T * s.H * s.P) return;
   const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
   const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, g = h / s.hpg;
+  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *cb = CB + (((bi * s.nc + c) * s.G + g) * s.Q + i) * s.Q;
   float acc = 0.f;
-  for (int64_t j = 0; j <= i; ++j) {
+  for (int64_t j = f; j <= i; ++j) {
     const float wgt = cb[j] * expf(acs_diff(ah[i], al[i], ah[j], al[j])) * dt[(bi * s.T + t0 + j) * s.H + h];
     acc = fmaf(wgt, ld(x + ((bi * s.T + t0 + j) * s.H + h) * s.P + p), acc);
   }
-  const float *hs = states + (((bi * s.nc + c) * s.H + h) * s.P + p) * s.N;
+  const float *hs = f == 0 ? states + (((bi * s.nc + c) * s.H + h) * s.P + p) * s.N
+                           : (init ? init + ((seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P + p) * s.N : nullptr);
   const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
   float inter = 0.f;
-  for (int64_t n = 0; n < s.N; ++n) inter = fmaf(hs[n], ld(ci + n), inter);
+  if (hs)
+    for (int64_t n = 0; n < s.N; ++n) inter = fmaf(hs[n], ld(ci + n), inter);
+  const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
   const float xv = ld(x + idx);
-  const float out = fmaf(expf(__fadd_rn(ah[i], al[i])), inter, acc) + D[h] * xv;
+  const float out = fmaf(din, inter, acc) + D[h] * xv;
   st(y + idx, out);
 }
 
 // ============================================================ backward ====
 
-// Per (b,c,h,i,j) with j <= i < Lc:  L = exp(Acs_i - Acs_j), Gx = g_i . x_j,
-// M = CB[i,j] L, W = L Gx dt_j, MG = M Gx; zero elsewhere.
+// Per (b,c,h,i,j) with local_start(i) <= j <= i < Lc (same sequence):
+// L = exp(Acs_i - Acs_j), Gx = g_i . x_j, M = CB[i,j] L, W = L Gx dt_j,
+// MG = M Gx; zero elsewhere.
 template <class TIn>
 __global__ void mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
                            const float *__restrict__ dt, const float *__restrict__ CB,
                            const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                           const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
                            float *__restrict__ Mm, float *__restrict__ Wm, float *__restrict__ MGm) {
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
@@ -166,7 +218,7 @@ __global__ void mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__rest
   const int64_t i = e / s.Q, j = e % s.Q;
   const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
   float M = 0.f, W = 0.f, MG = 0.f;
-  if (j <= i && i < Lc) {
+  if (j <= i && i < Lc && j >= local_start(seq_idx, first, bi, s.T, t0 + i, t0)) {
     const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
     const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
     const float L = expf(acs_diff(ah[i], al[i], ah[j], al[j]));
@@ -185,10 +237,12 @@ __global__ void mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__rest
   MGm[o] = MG;
 }
 
-// dHscan[b,c,h,p,n] = sum_i exp(Acs_i) g_i[p] C_i[n]; one thread per (p,n).
+// dHscan[b,c,h,p,n] = sum_i exp(Acs_i) g_i[p] C_i[n] over the tokens that see
+// the state entering the chunk (local_start(i) == 0); one thread per (p,n).
 template <class TIn>
 __global__ void dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Cm,
                               const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                              const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
                               float *__restrict__ dH) {
   extern __shared__ float ea[];
   const int64_t unit = blockIdx.x;  // (b, c, h)
@@ -196,7 +250,8 @@ __global__ void dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *
   const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x) ea[i] = expf(__fadd_rn(ah[i], al[i]));
+  for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x)
+    ea[i] = local_start(seq_idx, first, bi, s.T, t0 + i, t0) == 0 ? expf(__fadd_rn(ah[i], al[i])) : 0.f;
   __syncthreads();
   const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
   if (e >= s.P * s.N) return;
@@ -226,46 +281,89 @@ __device__ float block_sum(float v, float *red) {
 // Reverse state passing, one CTA per (b,h), in place on buf:
 //   in:  buf[c] = dHscan_c;  out: buf[c] = dS_c = gradient reaching the end
 //   state of chunk c (dH_{c+1}, or 0 where chunk c+1 starts a sequence);
-//   dH_c = dHscan_c + exp(E_c) dS_c; dEpass[b,h,c] = exp(E_c) <states_c, dS_c>;
-//   dinit[seq] += dH_c where chunk c starts a sequence.
+//   dH_c = dHscan_c + exp(E_c) dS_c when the sequence holding the chunk's
+//   last token entered the chunk (fe = 0), else dH_c = dHscan_c;
+//   dEpass[b,h,c] = exp(E_c) <states_c, dS_c> (fe = 0), or
+//   exp(E_c - Acs_{fe-1}) <init[seq], dS_c> (fe >= 1: the carried part of the
+//   chunk-end state then starts from that sequence's initial state);
+//   dinit[seq] += dH_c where chunk c starts a sequence at its first token.
 __global__ void state_passing_bwd_kernel(Shape s, float *__restrict__ buf, float *__restrict__ carry,
                                          const float *__restrict__ states, const float *__restrict__ acs_hi,
                                          const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                                         const int32_t *__restrict__ first, const float *__restrict__ init,
                                          float *__restrict__ dEpass, float *__restrict__ dinit) {
   __shared__ float red[32];
   const int64_t h = blockIdx.x % s.H, bi = blockIdx.x / s.H;
   const int64_t PN = s.P * s.N;
   float *cr = carry + (bi * s.H + h) * PN;
   for (int64_t c = s.nc - 1; c >= 0; --c) {
+    const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
     const bool nxt_start = (c + 1 >= s.nc) || is_seq_start(seq_idx, bi, s.T, (c + 1) * s.Q);
-    const bool here_start = is_seq_start(seq_idx, bi, s.T, c * s.Q);
-    const int64_t q = ((bi * s.H + h) * s.nc + c) * s.Q + (s.Q - 1);
+    const bool here_start = is_seq_start(seq_idx, bi, s.T, t0);
+    const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+    const int64_t q0 = ((bi * s.H + h) * s.nc + c) * s.Q, q = q0 + (s.Q - 1);
     const float eE = expf(__fadd_rn(acs_hi[q], acs_lo[q]));
+    const float eIn = fe == 0 ? eE : expf(acs_diff(acs_hi[q], acs_lo[q], acs_hi[q0 + fe - 1], acs_lo[q0 + fe - 1]));
+    const float eCarry = fe == 0 ? eE : 0.f;
     float *bc = buf + ((bi * s.nc + c) * s.H + h) * PN;
-    const float *hc = states + ((bi * s.nc + c) * s.H + h) * PN;
-    float *di = (here_start && dinit) ? dinit + (seq_of(seq_idx, bi, s.T, c * s.Q) * s.H + h) * PN : nullptr;
+    const float *hin = fe == 0 ? states + ((bi * s.nc + c) * s.H + h) * PN
+                               : (init ? init + (seq_of(seq_idx, bi, s.T, t0 + Lc - 1) * s.H + h) * PN : nullptr);
+    float *di = (here_start && dinit) ? dinit + (seq_of(seq_idx, bi, s.T, t0) * s.H + h) * PN : nullptr;
     float part = 0.f;
     for (int64_t e = threadIdx.x; e < PN; e += blockDim.x) {
       const float cur = nxt_start ? 0.f : cr[e];
       const float dh = bc[e];
       bc[e] = cur;
-      part = fmaf(hc[e], cur, part);
-      const float dHc = fmaf(eE, cur, dh);
+      if (hin) part = fmaf(hin[e], cur, part);
+      const float dHc = fmaf(eCarry, cur, dh);
       cr[e] = dHc;
       if (di) di[e] += dHc;
     }
     const float tot = block_sum(part, red);
-    if (threadIdx.x == 0) dEpass[(bi * s.H + h) * s.nc + c] = eE * tot;
+    if (threadIdx.x == 0) dEpass[(bi * s.H + h) * s.nc + c] = eIn * tot;
   }
 }
 
+// Gradient of the initial state of a sequence that starts inside a chunk, at
+// local position f >= 1 of chunk c (one thread per (seq, h, p, n)):
+//   dinit[seq] = sum_{i of seq in chunk c} exp(Acs_i - Acs_{f-1}) g_i C_i^T
+//              + exp(E_c - Acs_{f-1}) dS_c   when seq holds the chunk's last token.
+// Sequences that start at a chunk's first token get theirs from the reverse
+// state passing; ids with no token keep the zeros of the preceding memset.
+template <class TIn>
+__global__ void dinit_mid_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Cm,
+                                 const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                                 const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                                 const float *__restrict__ dS, float *__restrict__ dinit) {
+  const int64_t PN = s.P * s.N;
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (dinit == nullptr || idx >= s.nseq * s.H * PN) return;
+  const int64_t e = idx % PN, h = (idx / PN) % s.H, sq = idx / (PN * s.H);
+  const int64_t p = e / s.N, n = e % s.N, g = h / s.hpg;
+  const int64_t ts = first[sq];
+  if (ts < 0 || ts % s.Q == 0) return;
+  const int64_t c = ts / s.Q, t0 = c * s.Q, Lc = min(s.Q, s.T - t0), f = ts - t0;
+  const float *ah = acs_hi + (h * s.nc + c) * s.Q;   // batch row 0
+  const float *al = acs_lo + (h * s.nc + c) * s.Q;
+  float acc = 0.f;
+  for (int64_t i = f; i < Lc && seq_idx[t0 + i] == sq; ++i) {
+    const float w = expf(acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+    acc = fmaf(w * ld(dout + ((t0 + i) * s.H + h) * s.P + p), ld(Cm + ((t0 + i) * s.G + g) * s.N + n), acc);
+  }
+  if (seq_idx[t0 + Lc - 1] == sq)
+    acc = fmaf(expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[f - 1], al[f - 1])), dS[(c * s.H + h) * PN + e], acc);
+  dinit[idx] = acc;
+}
+
 // dx_i[p] = dt_i sum_{j>=i} M[j,i] g_j[p] + w_i sum_n B_i[n] dS[p,n] + D g_i[p],
-// w_i = exp(E - Acs_i) dt_i.  One thread per (b,t,h,p).
+// w_i = exp(E - Acs_i) dt_i for the tokens of the sequence holding the
+// chunk's last token (i >= fe), else 0.  One thread per (b,t,h,p).
 template <class TIn>
 __global__ void dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
                           const float *__restrict__ dt, const float *__restrict__ D, const float *__restrict__ Mm,
                           const float *__restrict__ dS, const float *__restrict__ acs_hi,
-                          const float *__restrict__ acs_lo, float *__restrict__ dx) {
+                          const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                          const int32_t *__restrict__ first, float *__restrict__ dx) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.T * s.H * s.P) return;
   const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
@@ -281,21 +379,25 @@ __global__ void dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__re
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float dti = dt[(bi * s.T + t) * s.H + h];
-  const float wi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
   dx[idx] = fmaf(dti, d1, fmaf(wi, y, D[h] * ld(dout + idx)));
 }
 
 // Per-head dB / dC rows, one thread per (b,t,h,n):
-//   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + exp(Acs_i) sum_p states[p,n] g_i[p]
+//   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + din_i sum_p Hin[p,n] g_i[p]
 //   dB_h[i,n] = sum_{j>=i} W[j,i] C_j[n] + w_i sum_p dS[p,n] x_i[p]
-// Deterministic variant: written to per-head slots (b,T,H,N); atomic
-// variant: added into dB/dC (b,T,G,N) with atomics.
+// (din_i, Hin as in chunk_scan_fwd; w_i as in dx_kernel).  Deterministic
+// variant: written to per-head slots (b,T,H,N); atomic variant: added into
+// dB/dC (b,T,G,N) with atomics.
 template <class TIn, bool kAtomic>
 __global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
                             const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, const float *__restrict__ dt,
                             const float *__restrict__ Wm, const float *__restrict__ states,
                             const float *__restrict__ dS, const float *__restrict__ acs_hi,
-                            const float *__restrict__ acs_lo, float *__restrict__ dBo, float *__restrict__ dCo) {
+                            const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                            const int32_t *__restrict__ first, const float *__restrict__ init,
+                            float *__restrict__ dBo, float *__restrict__ dCo) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.T * s.H * s.N) return;
   const int64_t n = idx % s.N, h = (idx / s.N) % s.H, t = (idx / (s.N * s.H)) % s.T, bi = idx / (s.N * s.H * s.T);
@@ -305,19 +407,23 @@ __global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__res
   float dc = 0.f, db = 0.f;
   for (int64_t j = 0; j <= i; ++j) dc = fmaf(W[i * s.Q + j], ld(Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), dc);
   for (int64_t j = i; j < Lc; ++j) db = fmaf(W[j * s.Q + i], ld(Cm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), db);
-  const float *hs = states + unit * s.P * s.N + n;
+  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  const float *hs = f == 0 ? states + unit * s.P * s.N + n
+                           : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N + n : nullptr);
   const float *ds = dS + unit * s.P * s.N + n;
   const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
   const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
   float hg = 0.f, sx = 0.f;
   for (int64_t p = 0; p < s.P; ++p) {
-    hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+    if (hs) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
     sx = fmaf(ds[p * s.N], ld(xi + p), sx);
   }
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float wi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
-  dc = fmaf(expf(__fadd_rn(ah[i], al[i])), hg, dc);
+  const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
+  const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+  dc = fmaf(din, hg, dc);
   db = fmaf(wi, sx, db);
   if (kAtomic) {
     const int64_t o = ((bi * s.T + t) * s.G + g) * s.N + n;
@@ -333,16 +439,21 @@ __global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__res
 // Acs_i, before the reverse cumsum:
 //   ddt_part = sum_{j>=i} MG[j,i] + exp(E - Acs_i) sx_i
 //   dAcs_i   = sum_{j<i} MG[i,j] dt_j - dt_i sum_{j>i} MG[j,i]
-//            + exp(Acs_i) g_i . (states C_i) - u_i,   u_i = w_i sx_i
-// with sx_i = x_i . (dS B_i).  Also gx_i = g_i . x_i for dD.
+//            + v_i - u_i,   v_i = din_i g_i . (Hin C_i),   u_i = w_i sx_i
+// with sx_i = x_i . (dS B_i) (din_i, Hin as in chunk_scan_fwd; w_i and the
+// exp(E - Acs_i) factor zero before fe).  Also gx_i = g_i . x_i for dD, and
+// vin_i = v_i for tokens of a sequence that started inside the chunk (their
+// decay exp(Acs_i - Acs_{f-1}) also depends on Acs_{f-1}), else 0.
 template <class TIn>
 __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
                                 const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
                                 const float *__restrict__ dt, const float *__restrict__ MGm,
                                 const float *__restrict__ states, const float *__restrict__ dS,
                                 const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
-                                float *__restrict__ ddt_part, float *__restrict__ dAcs, float *__restrict__ u_buf,
-                                float *__restrict__ gx_buf) {
+                                const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                                const float *__restrict__ init, float *__restrict__ ddt_part,
+                                float *__restrict__ dAcs, float *__restrict__ u_buf, float *__restrict__ gx_buf,
+                                float *__restrict__ vin_buf) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.H * s.nc * s.Q) return;
   const int64_t i = idx % s.Q, c = (idx / s.Q) % s.nc, h = (idx / (s.Q * s.nc)) % s.H, bi = idx / (s.Q * s.nc * s.H);
@@ -351,6 +462,7 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
     dAcs[idx] = 0.f;
     u_buf[idx] = 0.f;
     gx_buf[idx] = 0.f;
+    vin_buf[idx] = 0.f;
     return;
   }
   const int64_t unit = (bi * s.nc + c) * s.H + h;
@@ -361,7 +473,10 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
   for (int64_t j = i + 1; j < Lc; ++j) col += MG[j * s.Q + i];
   for (int64_t j = 0; j < i; ++j) row = fmaf(MG[i * s.Q + j], dtc[j * s.H], row);
   const float dti = dtc[i * s.H];
-  const float *hs = states + unit * s.P * s.N;
+  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  const float *hs = f == 0 ? states + unit * s.P * s.N
+                           : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N : nullptr);
   const float *ds = dS + unit * s.P * s.N;
   const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
   const TIn *b_i = Bm + ((bi * s.T + t) * s.G + g) * s.N;
@@ -371,7 +486,7 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
   for (int64_t p = 0; p < s.P; ++p) {
     float hc = 0.f, dsb = 0.f;
     for (int64_t n = 0; n < s.N; ++n) {
-      hc = fmaf(hs[p * s.N + n], ld(ci + n), hc);
+      if (hs) hc = fmaf(hs[p * s.N + n], ld(ci + n), hc);
       dsb = fmaf(ds[p * s.N + n], ld(b_i + n), dsb);
     }
     const float gp = ld(gi + p), xp = ld(xi + p);
@@ -381,24 +496,31 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
   }
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float eEi = expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i]));
+  const float eEi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i]));
+  const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
   const float u = eEi * dti * sx;
+  const float v = din * inter;
   ddt_part[(bi * s.T + t) * s.H + h] = (col + diag) + eEi * sx;
-  dAcs[idx] = row - dti * col + expf(__fadd_rn(ah[i], al[i])) * inter - u;
+  dAcs[idx] = row - dti * col + v - u;
   u_buf[idx] = u;
   gx_buf[idx] = gx;
+  vin_buf[idx] = f == 0 ? 0.f : v;
 }
 
 // Reverse in-chunk cumsum, one thread per (b,c,h), sequential in one fixed
 // order: dAcs_{Lc-1} += sum_i u_i + dEpass; da_i = sum_{k>=i} dAcs_k;
 // ddt_i = ddt_part_i + A da_i; per-chunk partials dA = sum_i dt_i da_i and
-// dD = sum_i gx_i (slot (b,c,h)), or atomics in the atomic variant.
+// dD = sum_i gx_i (slot (b,c,h)), or atomics in the atomic variant.  Where a
+// sequence starts inside the chunk at f >= 1, the decays measured from
+// Acs_{f-1} give dAcs_{f-1} -= sum of that sequence's vin (plus dEpass when
+// it holds the chunk's last token).
 template <bool kAtomic>
 __global__ void cumsum_bwd_kernel(Shape s, const float *__restrict__ dt, const float *__restrict__ A,
                                   const float *__restrict__ dAcs, const float *__restrict__ u_buf,
-                                  const float *__restrict__ gx_buf, const float *__restrict__ dEpass,
-                                  const float *__restrict__ ddt_part, float *__restrict__ ddt,
-                                  float *__restrict__ dA_part, float *__restrict__ dD_part) {
+                                  const float *__restrict__ gx_buf, const float *__restrict__ vin_buf,
+                                  const float *__restrict__ dEpass, const int32_t *__restrict__ seq_idx,
+                                  const int32_t *__restrict__ first, const float *__restrict__ ddt_part,
+                                  float *__restrict__ ddt, float *__restrict__ dA_part, float *__restrict__ dD_part) {
   const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= s.b * s.nc * s.H) return;
   const int64_t h = idx % s.H, c = (idx / s.H) % s.nc, bi = idx / (s.H * s.nc);
@@ -410,10 +532,19 @@ __global__ void cumsum_bwd_kernel(Shape s, const float *__restrict__ dt, const f
     sg += gx_buf[base + i];
   }
   const float Ah = A[h];
-  float da = su + dEpass[(bi * s.H + h) * s.nc + c];
+  const float dEp = dEpass[(bi * s.H + h) * s.nc + c];
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  float da = su + dEp;
+  float pend = fe > 0 ? dEp : 0.f;  // owed by Acs_{f-1} of the sequence being walked
   float dAp = 0.f;
   for (int64_t i = Lc - 1; i >= 0; --i) {
-    da += dAcs[base + i];
+    float d = dAcs[base + i];
+    if (seq_idx && i + 1 < Lc && seq_idx[bi * s.T + t0 + i] != seq_idx[bi * s.T + t0 + i + 1]) {
+      d -= pend;  // token i + 1 starts a sequence inside the chunk
+      pend = 0.f;
+    }
+    da += d;
+    pend += vin_buf[base + i];
     const int64_t o = (bi * s.T + t0 + i) * s.H + h;
     ddt[o] = fmaf(Ah, da, ddt_part[o]);
     dAp = fmaf(dt[o], da, dAp);
@@ -459,8 +590,9 @@ __global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ d
 }
 
 struct BwdWs {
-  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *MGm, *buf, *carry, *dEpass, *dAcs, *u, *gx, *ddt_part, *dA_part,
+  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *MGm, *buf, *carry, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
       *dD_part, *slot_b, *slot_c;
+  int32_t *first;
 };
 
 BwdWs carve_bwd(Carver &cv, const Shape &s, bool atomic) {
@@ -478,16 +610,19 @@ BwdWs carve_bwd(Carver &cv, const Shape &s, bool atomic) {
   w.dAcs = cv.take<float>(acs);
   w.u = cv.take<float>(acs);
   w.gx = cv.take<float>(acs);
+  w.vin = cv.take<float>(acs);
   w.ddt_part = cv.take<float>(s.b * s.T * s.H);
   w.dA_part = cv.take<float>(s.b * s.nc * s.H);
   w.dD_part = cv.take<float>(s.b * s.nc * s.H);
   w.slot_b = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
   w.slot_c = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
+  w.first = cv.take<int32_t>(s.nseq);
   return w;
 }
 
 struct FwdWs {
   float *acs_hi, *acs_lo, *CB, *S;
+  int32_t *first;
 };
 
 FwdWs carve_fwd(Carver &cv, const Shape &s) {
@@ -497,7 +632,16 @@ FwdWs carve_fwd(Carver &cv, const Shape &s) {
   w.acs_lo = cv.take<float>(acs);
   w.CB = cv.take<float>(s.b * s.nc * s.G * s.Q * s.Q);
   w.S = cv.take<float>(s.b * s.nc * s.H * s.P * s.N);
+  w.first = cv.take<int32_t>(s.nseq);
   return w;
+}
+
+// Table of sequence first tokens (only with seq_idx; batch row 0).
+cudaError_t build_first(const Shape &s, const int32_t *seq_idx, int32_t *first, int bs, cudaStream_t st) {
+  const cudaError_t err = cudaMemsetAsync(first, 0xff, size_t(s.nseq) * sizeof(int32_t), st);
+  if (err != cudaSuccess) return err;
+  seq_first_kernel<<<unsigned(cdiv(s.T, bs)), bs, 0, st>>>(s.T, seq_idx, first);
+  return cudaSuccess;
 }
 
 inline unsigned grid1(int64_t n, int bs) { return unsigned(cdiv(n, bs)); }
@@ -507,14 +651,20 @@ cudaError_t fwd_impl(const Shape &s, const Args &a, void *ws, int bs, cudaStream
   Carver cv(ws);
   FwdWs w = carve_fwd(cv, s);
   const TIn *x = static_cast<const TIn *>(a.x), *Bm = static_cast<const TIn *>(a.B), *Cm = static_cast<const TIn *>(a.C);
+  const int32_t *first = a.seq_idx ? w.first : nullptr;
+  if (a.seq_idx) {
+    const cudaError_t err = build_first(s, a.seq_idx, w.first, bs, st);
+    if (err != cudaSuccess) return err;
+  }
   cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
   chunk_state_fwd_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.H), grid1(s.P * s.N, bs)), bs, s.Q * sizeof(float), st>>>(
-      s, x, Bm, a.dt, w.acs_hi, w.acs_lo, w.S);
+      s, x, Bm, a.dt, w.acs_hi, w.acs_lo, a.seq_idx, first, w.S);
   state_passing_fwd_kernel<<<grid1(s.b * s.H * s.P * s.N, bs), bs, 0, st>>>(s, w.S, w.acs_hi, w.acs_lo, a.seq_idx,
-                                                                            a.init, a.states_out);
+                                                                            first, a.init, a.states_out);
   cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
   chunk_scan_fwd_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(
-      s, x, Cm, a.dt, a.D, w.CB, w.acs_hi, w.acs_lo, a.states_out, static_cast<TIn *>(a.y));
+      s, x, Cm, a.dt, a.D, w.CB, w.acs_hi, w.acs_lo, a.states_out, a.seq_idx, first, a.init,
+      static_cast<TIn *>(a.y));
   return cudaGetLastError();
 }
 
@@ -540,6 +690,12 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
     if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
   }
   const unsigned nbch = unsigned(s.b * s.nc * s.H);
+  const int32_t *first = a.seq_idx ? w.first : nullptr;
+  if (a.seq_idx) {
+    tr.mark(st);
+    if ((err = build_first(s, a.seq_idx, w.first, bs, st)) != cudaSuccess) return err;
+    tr.mark(st);
+  }
   tr.mark(st);
   cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
   tr.mark(st);
@@ -547,46 +703,55 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
   cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
   tr.mark(st);
   tr.mark(st);
-  mwg_kernel<TIn><<<dim3(nbch, grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo, w.Mm,
-                                                                    w.Wm, w.MGm);
+  mwg_kernel<TIn><<<dim3(nbch, grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo,
+                                                                    a.seq_idx, first, w.Mm, w.Wm, w.MGm);
   tr.mark(st);
   tr.mark(st);
-  dhscan_kernel<TIn><<<dim3(nbch, grid1(PN, bs)), bs, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo, w.buf);
+  dhscan_kernel<TIn><<<dim3(nbch, grid1(PN, bs)), bs, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo,
+                                                                                 a.seq_idx, first, w.buf);
   tr.mark(st);
   tr.mark(st);
   // fixed block: this kernel folds per-thread partial dot products, so its
   // shape must not follow the launch configuration
-  state_passing_bwd_kernel<<<unsigned(s.b * s.H), kPassThreads, 0, st>>>(s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo,
-                                                                a.seq_idx, w.dEpass, a.dinit);
+  state_passing_bwd_kernel<<<unsigned(s.b * s.H), kPassThreads, 0, st>>>(
+      s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.dEpass, a.dinit);
   tr.mark(st);
+  if (a.seq_idx) {
+    tr.mark(st);
+    dinit_mid_kernel<TIn><<<grid1(s.nseq * s.H * PN, bs), bs, 0, st>>>(s, g, Cm, w.acs_hi, w.acs_lo, a.seq_idx,
+                                                                       first, w.buf, a.dinit);
+    tr.mark(st);
+  }
   tr.mark(st);
   dx_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(s, g, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi,
-                                                                  w.acs_lo, a.dx);
+                                                                  w.acs_lo, a.seq_idx, first, a.dx);
   tr.mark(st);
   if (atomic) {
     tr.mark(st);
     dbdc_kernel<TIn, true><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
-        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.dB, a.dC);
+        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, a.dB, a.dC);
     tr.mark(st);
   } else {
     tr.mark(st);
     dbdc_kernel<TIn, false><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
-        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, w.slot_b, w.slot_c);
+        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.slot_b,
+        w.slot_c);
     tr.mark(st);
   }
   tr.mark(st);
   ddt_dacs_kernel<TIn><<<grid1(s.b * s.H * s.nc * s.Q, bs), bs, 0, st>>>(
-      s, x, g, Bm, Cm, a.dt, w.MGm, a.states_in, w.buf, w.acs_hi, w.acs_lo, w.ddt_part, w.dAcs, w.u, w.gx);
+      s, x, g, Bm, Cm, a.dt, w.MGm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.ddt_part,
+      w.dAcs, w.u, w.gx, w.vin);
   tr.mark(st);
   if (atomic) {
     tr.mark(st);
-    cumsum_bwd_kernel<true><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.dAcs, w.u, w.gx, w.dEpass,
-                                                                        w.ddt_part, a.ddt, a.dA, a.dD);
+    cumsum_bwd_kernel<true><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(
+        s, a.dt, a.A, w.dAcs, w.u, w.gx, w.vin, w.dEpass, a.seq_idx, first, w.ddt_part, a.ddt, a.dA, a.dD);
     tr.mark(st);
   } else {
     tr.mark(st);
     cumsum_bwd_kernel<false><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(
-        s, a.dt, a.A, w.dAcs, w.u, w.gx, w.dEpass, w.ddt_part, a.ddt, w.dA_part, w.dD_part);
+        s, a.dt, a.A, w.dAcs, w.u, w.gx, w.vin, w.dEpass, a.seq_idx, first, w.ddt_part, a.ddt, w.dA_part, w.dD_part);
     tr.mark(st);
     tr.mark(st);
     reduce_heads_kernel<<<grid1(s.b * s.T * s.G * s.N, bs), bs, 0, st>>>(s, w.slot_b, w.slot_c, a.dB, a.dC);
@@ -612,16 +777,22 @@ size_t simt_bwd_workspace(const Shape &s, bool atomic) {
   return cv.bytes();
 }
 
-int simt_bwd_launches(const Shape &, bool atomic) { return atomic ? 9 : 11; }
+int simt_bwd_launches(const Shape &, bool atomic, bool seq) { return (atomic ? 9 : 11) + (seq ? 2 : 0); }
 
-const char *simt_bwd_launch_name(bool atomic, int k) {
+const char *simt_bwd_launch_name(bool atomic, bool seq, int k) {
   static const char *det[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc",
                               "ddt_dacs", "cumsum_bwd", "reduce_heads", "reduce_heads_scalars"};
   static const char *atm[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc_atomic",
                               "ddt_dacs", "cumsum_bwd_atomic"};
-  if (k < 0) return "invalid";
-  if (atomic) return k < 9 ? atm[k] : "invalid";
-  return k < 11 ? det[k] : "invalid";
+  const int n = atomic ? 9 : 11;
+  if (k < 0 || k >= n + (seq ? 2 : 0)) return "invalid";
+  if (seq) {
+    // seq_first runs first, dinit_mid right after the reverse state passing
+    if (k == 0) return "seq_first";
+    if (k == 6) return "dinit_mid";
+    k = k < 6 ? k - 1 : k - 2;
+  }
+  return atomic ? atm[k] : det[k];
 }
 
 cudaError_t simt_fwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, cudaStream_t st) {

@@ -76,6 +76,13 @@ typedef struct {
 
 /* ssd_dims.flags: seq_idx will be passed (packed variable-length batch). */
 #define SSD_DIMS_SEQ_IDX 1
+/* ssd_dims.flags (with SSD_DIMS_SEQ_IDX): sequences may start anywhere, not
+ * only at multiples of chunk_size.  A sequence that starts inside a chunk
+ * begins from its own initial state (or zero) exactly as the recurrence
+ * says; decay terms never cross a sequence start.  These dims always run the
+ * general CUDA-core backward (the fused one resets states at chunk starts
+ * only). */
+#define SSD_DIMS_SEQ_ANY_START 2
 
 /* What the backward needs from the forward.  Filled by mamba2_ssd_fwd; it
  * borrows the caller's buffers (inputs and `states`), which must stay alive
@@ -111,8 +118,8 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
  * the dims are invalid).  All configurations give bitwise-identical
  * results; they differ in launch shape and scheduling only.  bf16 problems
  * with chunk 128, dstate 128, headdim 64 and seqlen a multiple of 128 run
- * the fused tensor-core backward; every other shape runs the general
- * CUDA-core backward. */
+ * the fused tensor-core backward (unless SSD_DIMS_SEQ_ANY_START is set);
+ * every other shape runs the general CUDA-core backward. */
 int mamba2_ssd_num_configs(const ssd_dims *dims);
 
 /* Name of the backward algorithm a configuration selects (static string). */
@@ -128,9 +135,11 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
 
 /* Forward.  Inputs x, dt, A, B, C, D as in ssd_saved; seq_idx (b,T) int32
  * (nullable, and given exactly when dims->flags has SSD_DIMS_SEQ_IDX;
- * requires batch == 1, non-decreasing ids in [0,nseq), every
- * change of id at a multiple of chunk_size -- checked with one synchronous
- * device-to-host copy of seq_idx, the only synchronisation in this library);
+ * requires batch == 1, seqlen and nseq below 2^31, non-decreasing ids in
+ * [0,nseq) -- else SSD_ERR_INVALID_ARG -- and, unless dims->flags has
+ * SSD_DIMS_SEQ_ANY_START, every change of id at a multiple of chunk_size --
+ * else SSD_ERR_UNSUPPORTED; checked with one synchronous device-to-host copy
+ * of seq_idx, the only synchronisation in this library);
  * init_states (nseq,H,P,N) fp32 (nullable: zero initial states).
  * Outputs: y (b,T,H,P) in dtype; states (b,nc,H,P,N) fp32, the state
  * entering each chunk (init/zero at a sequence start); *saved_out (host

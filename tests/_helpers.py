@@ -24,10 +24,10 @@ def to_dev(d, dev="cuda"):
     return {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
 
 
-def run_gpu(d, chunk, config=0, variant=0, g=None):
+def run_gpu(d, chunk, config=0, variant=0, g=None, any_start=False):
     g = to_dev(d) if g is None else g
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=chunk,
-                       seq_idx=g["seq_idx"], init_states=g["init"])
+                       seq_idx=g["seq_idx"], init_states=g["init"], any_start=any_start)
     grads = ssd.bwd(saved, g["dout"], config=config, variant=variant)
     torch.cuda.synchronize()
     return y, saved, grads

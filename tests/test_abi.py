@@ -58,7 +58,7 @@ def test_queries(L):
 
 @pytest.mark.parametrize("field,value", [("batch", 0), ("seqlen", -1), ("nheads", 0), ("ngroups", 4),
                                          ("chunk_size", 0), ("chunk_size", 4096), ("dtype", 7),
-                                         ("flags", 2), ("nseq", 0)])
+                                         ("flags", 2), ("flags", 4), ("nseq", 0)])
 def test_invalid_dims_rejected(L, field, value):
     d = ssd.make_dims(1, 256, 4, 16, 1, 16, 64)
     if field == "ngroups":
@@ -127,6 +127,20 @@ def test_bwd_argument_checks(L):
     o = list(outs)
     o[7] = ctypes.c_void_p(FAKE)   # dinit without initial states
     assert L.mamba2_ssd_bwd(*args(sv, o, need)) == 1
+
+
+def test_any_start_dims_take_the_general_path(L):
+    fused = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, seq_idx=True)
+    anyst = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, seq_idx=True, any_start=True)
+    assert ssd.config_name(fused, 0).startswith("fused")
+    assert ssd.config_name(anyst, 0).startswith("simt")
+    for var in (0, 1):
+        names = ssd.bwd_launch_names(anyst, 0, var)
+        assert names[0] == "seq_first" and names[6] == "dinit_mid" and names[5] == "state_passing_bwd"
+        assert "invalid" not in names and len(names) == ssd.bwd_num_launches(anyst, 0, var)
+    plain = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, dtype=torch.float32)
+    assert ssd.bwd_launch_names(plain, 0, 0)[0] == "cumsum_fwd"
+    assert ssd.bwd_num_launches(anyst, 0, 0) == ssd.bwd_num_launches(plain, 0, 0) + 2
 
 
 def test_binding_refuses_without_library(monkeypatch, tmp_path):

@@ -1,0 +1,101 @@
+"""Packed variable-length batches whose sequences start inside a chunk
+(SSD_DIMS_SEQ_ANY_START), against the fp64 oracle, which resets the state
+token by token wherever the sequence id changes.
+
+Cases cover a start at the second and at the last token of a chunk, a
+sequence wholly inside one chunk, a one-token sequence, a sequence that
+starts inside a chunk and runs through several, a ragged tail, ids with a
+gap (a sequence with no token keeps a zero initial-state gradient), runs
+with and without initial states, and bf16 inputs on the shape the fused
+backward would take (these dims always run the general path).
+"""
+import numpy as np
+import pytest
+import torch
+
+import deterministic_mamba2_ssd_gb300 as ssd
+from _helpers import GRADS, relerr, run_gpu, run_oracle, same_bits, to_dev
+from deterministic_mamba2_ssd_gb300.inputs import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def check(d, chunk, tol, config=0):
+    y, saved, g = run_gpu(d, chunk, config=config, any_start=True)
+    ref = run_oracle(d, chunk=chunk)
+    errs = {"y": relerr(y, ref["y"]), "states": relerr(saved.states, ref["states"])}
+    for k in GRADS:
+        errs[k] = relerr(g[k], ref[k])
+    if d["init"] is not None:
+        errs["dinit"] = relerr(g["dinit"], ref["dinit"])
+    bad = {k: v for k, v in errs.items() if not v < tol}
+    assert not bad, (bad, errs)
+    return g
+
+
+@pytest.mark.parametrize("lens,Q,init", [
+    ((1, 63, 64), 64, True),                 # start at local 1, then aligned
+    ((63, 1, 64, 2), 64, True),              # start at the last token of a chunk; one-token sequence
+    ((50, 17, 100, 133), 64, True),          # a sequence wholly inside chunk 0; ragged tail
+    ((50, 17, 100, 133), 64, False),
+    ((5, 3, 7, 1, 9, 2, 13), 16, True),      # many starts per chunk, small chunk
+    ((200,), 64, True),                      # one sequence: same as no boundaries
+    ((37, 91, 9, 30), 32, False),
+])
+def test_fp32_mid_chunk_starts(lens, Q, init):
+    T = sum(lens)
+    d = make_inputs(1, T, 4, 16, 2, 16, dtype=torch.float32, seed=T + Q + len(lens), dt_shift=2.0,
+                    d_mode="normal", seq_lens=lens, with_init=init)
+    check(d, Q, 1e-5)
+
+
+def test_fp32_mid_chunk_ids_with_gap():
+    lens = (40, 30, 58)
+    d = make_inputs(1, sum(lens), 4, 16, 1, 16, dtype=torch.float32, seed=77, dt_shift=2.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    # ids 0, 2, 3: id 1 has no token
+    d["seq_idx"] = torch.where(d["seq_idx"] >= 1, d["seq_idx"] + 1, d["seq_idx"]).contiguous()
+    d["init"] = torch.cat([d["init"][:1], torch.randn_like(d["init"][:1]), d["init"][1:]]).contiguous()
+    g = check(d, 32, 1e-5)
+    assert torch.count_nonzero(g["dinit"][1]) == 0
+
+
+def test_bf16_mid_chunk_on_fused_shape():
+    lens = (100, 300, 1, 111)
+    d = make_inputs(1, sum(lens), 4, 64, 1, 128, dtype=torch.bfloat16, seed=11, dt_shift=4.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    dims = ssd.make_dims(1, sum(lens), 4, 64, 1, 128, 128, nseq=len(lens), dtype=torch.bfloat16, seq_idx=True,
+                         any_start=True)
+    assert ssd.config_name(dims, 0).startswith("simt")
+    check(d, 128, 2e-3)
+
+
+def test_mid_chunk_start_without_flag_is_unsupported():
+    lens = (100, 156)
+    d = to_dev(make_inputs(1, 256, 4, 64, 1, 128, dtype=torch.bfloat16, seed=2, dt_shift=4.0, d_mode="normal",
+                           seq_lens=lens))
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], chunk_size=128, seq_idx=d["seq_idx"])
+    assert e.value.status == 2
+
+
+def test_mid_chunk_bitwise_repeat_and_configs():
+    lens = (50, 17, 100, 133)
+    d = make_inputs(1, sum(lens), 4, 16, 2, 16, dtype=torch.float32, seed=5, dt_shift=2.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    g = to_dev(d)
+    runs = [run_gpu(d, 64, config=c, g=g, any_start=True)[2] for c in (0, 0, 1, 1)]
+    for r in runs[1:]:
+        assert same_bits(runs[0], r)
+
+
+def test_aligned_starts_same_with_and_without_flag():
+    # with chunk-aligned starts every mask is a no-op: the general path must
+    # give the same bits with or without the flag (fp32: general path both ways)
+    lens = (64, 32, 128, 32)
+    d = make_inputs(1, 256, 4, 16, 1, 16, dtype=torch.float32, seed=5, dt_shift=2.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    g = to_dev(d)
+    a = run_gpu(d, 32, g=g)[2]
+    b = run_gpu(d, 32, g=g, any_start=True)[2]
+    assert same_bits(a, b)

@@ -11,6 +11,8 @@ specification.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
 oracle instead (on the host cores, bounded samples of the same workload).
+``--op dt_bwd`` / ``--op gate_bwd`` time the steps either side of the scan
+(step-size preprocessing, z-gate) on the same workload's tensors instead.
 Under torchrun each rank runs an independent replica (the backward does not
 shard across GPUs here): value = all ranks' tokens / max-over-ranks time.
 """
@@ -48,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd"],
+                    help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()
 
 
@@ -260,11 +264,102 @@ def run_reference(args):
     return 0
 
 
+# -------------------------------------------------- adjacent steps ----
+def run_adjacent(args):
+    """Times the backward of a step either side of the scan on the workload's
+    tensors: dt_bwd (step-size preprocessing; (b*T, H) fp32) or gate_bwd
+    (z-gate; (b, T, H, P) in the workload dtype).  Inputs seeded, synthetic,
+    resident in HBM; L2 flushed between steps."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import deterministic_mamba2_ssd_gb300 as ssd
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    rows = w.batch * w.seqlen
+    gen = torch.Generator().manual_seed(4321)
+    if args.op == "dt_bwd":
+        raw = (torch.randn((rows, w.nheads), generator=gen) - 4.0).to(dev)
+        bias = torch.randn((w.nheads,), generator=gen).to(dev)
+        ddt = torch.randn((rows, w.nheads), generator=gen).to(dev)
+        ddt_raw = torch.empty_like(raw)
+        ddt_bias = torch.empty_like(bias)
+        wsb = ssd.lib().mamba2_ssd_dt_bwd_workspace_size(rows, w.nheads)
+        ws = torch.empty(max(16, wsb), dtype=torch.uint8, device=dev)
+        import ctypes
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+
+        def step():
+            rc = ssd.lib().mamba2_ssd_dt_bwd(rows, w.nheads, ptr(raw), ptr(bias), 1, 0.0, float("inf"), ptr(ddt),
+                                             ptr(ddt_raw), ptr(ddt_bias), ptr(ws), ws.numel(), st)
+            if rc:
+                raise ssd.SsdError(rc, "mamba2_ssd_dt_bwd")
+        alg = 3 * rows * w.nheads * 4 + 2 * w.nheads * 4
+        launches = 2
+        kernel = "dt_bwd"
+        dtype = "f32"
+    else:
+        shape = (w.batch, w.seqlen, w.nheads, w.headdim)
+        y = torch.randn(shape, generator=gen).to(w.dtype).to(dev)
+        z = torch.randn(shape, generator=gen).to(w.dtype).to(dev)
+        gout = torch.randn(shape, generator=gen).to(w.dtype).to(dev)
+        n = y.numel()
+
+        def step():
+            ssd.gate_bwd(y, z, gout)
+        alg = 4 * n * es + n * 4
+        launches = 1
+        kernel = "gate_bwd"
+        dtype = "bf16" if es == 2 else "f32"
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    barrier(world, dev)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.fill_(1.0)
+        evs[k][0].record(stream)
+        step()
+        evs[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world, dev)
+    clocks = clk.stop()
+    ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), world, dev)
+    peak, peak_kind = load_peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "%s tokens/s @ seqlen %d" % (kernel, w.seqlen), "value": world * rows / (ms / 1e3),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": w.name, "op": kernel, "seq_len": w.seqlen, "nheads": w.nheads,
+                       "headdim": w.headdim, "l2": "flushed between steps (256 MB write)"},
+            "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "algorithmic_bytes_per_launch": alg},
+            "gpu_launches": launches * args.steps, "clocks": clocks, "e2e": None, "cpu_baseline": None}))
+    return 0
+
+
 # ------------------------------------------------------------- ours ----
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.op != "ssd_bwd":
+        return run_adjacent(args)
     import __graft_entry__
     __graft_entry__.build()
     import deterministic_mamba2_ssd_gb300 as ssd

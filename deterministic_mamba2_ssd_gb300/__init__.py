@@ -15,7 +15,8 @@ import os
 import torch
 
 __all__ = ["lib", "fwd", "bwd", "Saved", "SsdError", "make_dims", "num_configs", "config_name",
-           "bwd_workspace_size", "fwd_workspace_size", "bwd_num_launches", "bwd_launch_names", "LIB_PATH"]
+           "bwd_workspace_size", "fwd_workspace_size", "bwd_num_launches", "bwd_launch_names", "LIB_PATH",
+           "dt_fwd", "dt_bwd", "gate_fwd", "gate_bwd"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba2_ssd.so")
 
@@ -91,6 +92,17 @@ def lib():
         L.mamba2_ssd_static_scratch_bytes.restype = sz
         L.mamba2_ssd_bwd_static_scratch.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 8 + [ci, vp]
         L.mamba2_ssd_bwd_static_scratch.restype = ci
+        f32 = ctypes.c_float
+        L.mamba2_ssd_dt_fwd.argtypes = [i64, i64, vp, vp, ci, f32, f32, vp, vp]
+        L.mamba2_ssd_dt_fwd.restype = ci
+        L.mamba2_ssd_dt_bwd_workspace_size.argtypes = [i64, i64]
+        L.mamba2_ssd_dt_bwd_workspace_size.restype = sz
+        L.mamba2_ssd_dt_bwd.argtypes = [i64, i64, vp, vp, ci, f32, f32, vp, vp, vp, vp, sz, vp]
+        L.mamba2_ssd_dt_bwd.restype = ci
+        L.mamba2_ssd_gate_fwd.argtypes = [i64, ctypes.c_int32, vp, vp, vp, vp]
+        L.mamba2_ssd_gate_fwd.restype = ci
+        L.mamba2_ssd_gate_bwd.argtypes = [i64, ctypes.c_int32, vp, vp, vp, vp, vp, vp]
+        L.mamba2_ssd_gate_bwd.restype = ci
         _lib = L
     return _lib
 
@@ -242,3 +254,74 @@ def bwd(saved: Saved, dout, config: int = 0, variant: int = VARIANT_DETERMINISTI
     if rc:
         raise SsdError(rc, "mamba2_ssd_bwd")
     return out
+
+
+# ---- steps either side of the scan ------------------------------------------
+
+def _dt_check(dt_raw, dt_bias):
+    if dt_raw.dim() < 2:
+        raise ValueError("dt_raw must be (..., nheads)")
+    H = dt_raw.shape[-1]
+    _check(dt_raw, "dt_raw", tuple(dt_raw.shape), torch.float32, dt_raw.device)
+    if dt_bias is not None:
+        _check(dt_bias, "dt_bias", (H,), torch.float32, dt_raw.device)
+    return dt_raw.numel() // H, H
+
+
+def dt_fwd(dt_raw, dt_bias=None, softplus=True, dt_min=0.0, dt_max=float("inf"), stream=None):
+    """dt = clamp(softplus(dt_raw + dt_bias), dt_min, dt_max) (softplus optional);
+    dt_raw (..., nheads) fp32, dt_bias (nheads,) fp32 or None."""
+    rows, H = _dt_check(dt_raw, dt_bias)
+    dt = torch.empty_like(dt_raw)
+    rc = lib().mamba2_ssd_dt_fwd(rows, H, _ptr(dt_raw), _ptr(dt_bias), int(bool(softplus)), dt_min, dt_max,
+                                 _ptr(dt), _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_dt_fwd")
+    return dt
+
+
+def dt_bwd(dt_raw, ddt, dt_bias=None, softplus=True, dt_min=0.0, dt_max=float("inf"), stream=None,
+           want_bias_grad=True):
+    """(ddt_raw, ddt_bias or None) from ddt, the gradient w.r.t. dt_fwd's output."""
+    rows, H = _dt_check(dt_raw, dt_bias)
+    _check(ddt, "ddt", tuple(dt_raw.shape), torch.float32, dt_raw.device)
+    ddt_raw = torch.empty_like(dt_raw)
+    ddt_bias = torch.empty((H,), dtype=torch.float32, device=dt_raw.device) if want_bias_grad else None
+    need = lib().mamba2_ssd_dt_bwd_workspace_size(rows, H)
+    ws = torch.empty(max(16, need), dtype=torch.uint8, device=dt_raw.device)
+    rc = lib().mamba2_ssd_dt_bwd(rows, H, _ptr(dt_raw), _ptr(dt_bias), int(bool(softplus)), dt_min, dt_max,
+                                 _ptr(ddt), _ptr(ddt_raw), _ptr(ddt_bias), _ptr(ws), ws.numel(), _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_dt_bwd")
+    return ddt_raw, ddt_bias
+
+
+def _gate_dtype(y, z):
+    if y.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("y must be bf16 or fp32")
+    _check(y, "y", tuple(y.shape), y.dtype, y.device)
+    _check(z, "z", tuple(y.shape), y.dtype, y.device)
+    return SSD_BF16 if y.dtype == torch.bfloat16 else SSD_F32
+
+
+def gate_fwd(y, z, stream=None):
+    """out = y * silu(z), same shape and dtype as y."""
+    dt = _gate_dtype(y, z)
+    out = torch.empty_like(y)
+    rc = lib().mamba2_ssd_gate_fwd(y.numel(), dt, _ptr(y), _ptr(z), _ptr(out), _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_gate_fwd")
+    return out
+
+
+def gate_bwd(y, z, dout, stream=None):
+    """(dy in y's dtype, dz fp32) of out = y * silu(z)."""
+    dt = _gate_dtype(y, z)
+    _check(dout, "dout", tuple(y.shape), y.dtype, y.device)
+    dy = torch.empty_like(y)
+    dz = torch.empty(y.shape, dtype=torch.float32, device=y.device)
+    rc = lib().mamba2_ssd_gate_bwd(y.numel(), dt, _ptr(y), _ptr(z), _ptr(dout), _ptr(dy), _ptr(dz),
+                                   _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_gate_bwd")
+    return dy, dz

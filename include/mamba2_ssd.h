@@ -219,6 +219,44 @@ ssd_status mamba2_ssd_bwd_static_scratch(const ssd_saved *saved, const void *dou
                                          float *dA, float *dB, float *dC, float *dD, float *dinit, int config,
                                          void *stream);
 
+/* ---- Steps either side of the scan ------------------------------------
+ * The step-size preprocessing that Mamba2 folds into its chunk_cumsum (whose
+ * backward "Deterministic bwd kernel for mamba2" lists as chunk_cumsum_bwd)
+ * and the z-gate on the scan's output.  Elementwise; all pointers are device
+ * pointers, 16-byte aligned, densely packed; enqueued on `stream`; nothing is
+ * synchronised.  A count of 0 launches nothing and returns SSD_OK. */
+
+/* dt[r,h] = clamp(sp(dt_raw[r,h] + dt_bias[h]), dt_min, dt_max) for r < rows
+ * (rows = batch * seqlen, layout (rows, nheads) fp32), sp(v) = log(1 + e^v)
+ * when use_softplus != 0, else sp(v) = v.  dt_bias (nheads) may be NULL
+ * (zero).  dt_min <= dt_max, neither NaN (pass 0 and INFINITY, or -INFINITY
+ * and INFINITY, for no clamp); rows < 2^36. */
+ssd_status mamba2_ssd_dt_fwd(int64_t rows, int64_t nheads, const float *dt_raw, const float *dt_bias,
+                             int use_softplus, float dt_min, float dt_max, float *dt, void *stream);
+
+/* Workspace bytes of mamba2_ssd_dt_bwd (0 for invalid sizes). */
+size_t mamba2_ssd_dt_bwd_workspace_size(int64_t rows, int64_t nheads);
+
+/* Backward of mamba2_ssd_dt_fwd given ddt = dL/d dt (rows, nheads) fp32:
+ * ddt_raw = ddt * sp'(v) where dt_min <= sp(v) <= dt_max, else 0
+ * (v = dt_raw + dt_bias, sp' the logistic function or 1); ddt_bias[h] (may
+ * be NULL) = sum over rows of ddt_raw[., h], computed over 32 fixed slabs of
+ * rows folded in ascending order, so bitwise reproducible.  workspace (only
+ * needed with ddt_bias) >= mamba2_ssd_dt_bwd_workspace_size bytes. */
+ssd_status mamba2_ssd_dt_bwd(int64_t rows, int64_t nheads, const float *dt_raw, const float *dt_bias,
+                             int use_softplus, float dt_min, float dt_max, const float *ddt, float *ddt_raw,
+                             float *ddt_bias, void *workspace, size_t workspace_bytes, void *stream);
+
+/* out = y * silu(z), silu(z) = z / (1 + e^-z); y, z, out: n elements of
+ * `dtype` (ssd_dtype; fp32 arithmetic, out rounded once). */
+ssd_status mamba2_ssd_gate_fwd(int64_t n, int32_t dtype, const void *y, const void *z, void *out, void *stream);
+
+/* Backward of the gate given dout (n elements of `dtype`): dy = dout *
+ * silu(z) in `dtype` (ready as the scan's dout), dz = dout * y * silu'(z) in
+ * fp32, silu'(z) = s (1 + z (1 - s)), s = 1 / (1 + e^-z). */
+ssd_status mamba2_ssd_gate_bwd(int64_t n, int32_t dtype, const void *y, const void *z, const void *dout, void *dy,
+                               float *dz, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

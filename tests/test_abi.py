@@ -156,3 +156,31 @@ def test_selftest_and_static_entry_reject_bad_arguments_on_host(L):
     assert L.mamba2_ssd_selftest_umma(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, None) == 1
     assert L.mamba2_ssd_static_scratch_bytes() == 32 << 20
     assert L.mamba2_ssd_bwd_static_scratch(None, None, None, None, None, None, None, None, None, 0, None) == 6
+
+
+def test_adjacent_steps_reject_bad_arguments_on_host(L):
+    f32 = ctypes.c_float
+    p = lambda k: ctypes.c_void_p(FAKE + 256 * k)
+    inf = float("inf")
+    # clamp bounds out of order or NaN; zero heads
+    assert L.mamba2_ssd_dt_fwd(4, 8, p(0), None, 1, f32(1.0), f32(0.5), p(1), None) == 1
+    assert L.mamba2_ssd_dt_fwd(4, 8, p(0), None, 1, f32(float("nan")), f32(inf), p(1), None) == 1
+    assert L.mamba2_ssd_dt_fwd(4, 0, p(0), None, 1, f32(0.0), f32(inf), p(1), None) == 1
+    # misaligned or missing pointers
+    assert L.mamba2_ssd_dt_fwd(4, 8, ctypes.c_void_p(FAKE + 4), None, 1, f32(0.0), f32(inf), p(1), None) == 1
+    assert L.mamba2_ssd_dt_fwd(4, 8, None, None, 1, f32(0.0), f32(inf), p(1), None) == 1
+    # empty input: nothing to do, nothing launched
+    assert L.mamba2_ssd_dt_fwd(0, 8, None, None, 1, f32(0.0), f32(inf), None, None) == 0
+    need = L.mamba2_ssd_dt_bwd_workspace_size(1000, 8)
+    assert need == 32 * 8 * 4      # 32 row slabs, one partial per head each
+    assert L.mamba2_ssd_dt_bwd_workspace_size(-1, 8) == 0
+    assert L.mamba2_ssd_dt_bwd(1000, 8, p(0), None, 1, f32(0.0), f32(inf), p(1), p(2), p(3), p(4), need - 1,
+                               None) == 3
+    assert L.mamba2_ssd_dt_bwd(1000, 8, p(0), None, 1, f32(0.0), f32(inf), None, p(2), p(3), p(4), need,
+                               None) == 1
+    # gate: bad dtype, misaligned, missing output; empty is a no-op
+    assert L.mamba2_ssd_gate_fwd(16, 7, p(0), p(1), p(2), None) == 1
+    assert L.mamba2_ssd_gate_fwd(16, 1, p(0), ctypes.c_void_p(FAKE + 2), p(2), None) == 1
+    assert L.mamba2_ssd_gate_bwd(16, 0, p(0), p(1), p(2), p(3), None, None) == 1
+    assert L.mamba2_ssd_gate_fwd(0, 1, None, None, None, None) == 0
+    assert L.mamba2_ssd_gate_bwd(-1, 1, p(0), p(1), p(2), p(3), p(4), None) == 1

@@ -173,6 +173,7 @@ def kernel_bytes(name, w, es):
         "dx": x + bc + dt + qq + st + acs + b * T * H * P * f4,
         "dbdc": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * slots,
         "dbdc_atomic": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * b * T * G * N * f4,
+        "dbdc_ordered": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * b * T * G * N * f4,
         "ddt_dacs": 2 * x + 2 * bc + dt + qq + 2 * st + acs + dt + 3 * b * H * nc * Q * f4,
         "cumsum_bwd": 2 * dt + 4 * b * H * nc * Q * f4,
         "cumsum_bwd_atomic": 2 * dt + 4 * b * H * nc * Q * f4,

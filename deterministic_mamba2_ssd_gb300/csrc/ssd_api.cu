@@ -65,6 +65,20 @@ bool use_fused(const ssd_dims *d) {
 
 bool has_seq(const ssd_dims *d) { return (d->flags & SSD_DIMS_SEQ_IDX) != 0; }
 
+// Which variants a shape supports: the fused path folds dB/dC over heads
+// inside one CTA, so the ordered-semaphore fold exists for the general path
+// only (and needs its tile of 2 x 32 x dstate fp32 in shared memory and a
+// unit count that fits a 1-D grid).
+bool variant_ok(const ssd_dims *d, int variant) {
+  if (variant == SSD_VARIANT_DETERMINISTIC || variant == SSD_VARIANT_ATOMIC) return true;
+  if (variant != SSD_VARIANT_ORDERED || use_fused(d)) return false;
+  const int64_t nc = (d->seqlen + d->chunk_size - 1) / d->chunk_size;
+  const int64_t units = d->batch * nc * d->nheads * ((d->chunk_size + 31) / 32);
+  return d->dstate <= 512 && units < (int64_t(1) << 31);
+}
+
+constexpr uint32_t kOrderedSpinLimit = 1u << 24;   // polls before an ordered-fold wait gives up
+
 ssd::FusedOptions fused_options(const ssd_dims *d, int config, int variant) {
   ssd::FusedOptions o;
   // with sequence starts the chain can be cut, so every chunk gets its own slot
@@ -114,30 +128,32 @@ const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
 
 size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
-  if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC) return 0;
+  if (!variant_ok(dims, variant)) return 0;
   if (use_fused(dims)) return ssd::fused_bwd_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
-  return ssd::simt_bwd_workspace(shape_of(dims), variant == SSD_VARIANT_ATOMIC);
+  return ssd::simt_bwd_workspace(shape_of(dims), variant);
 }
 
 int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
+  if (!variant_ok(dims, variant)) return 0;
   if (use_fused(dims)) return variant == SSD_VARIANT_ATOMIC ? 1 : 2;
-  return ssd::simt_bwd_launches(shape_of(dims), variant == SSD_VARIANT_ATOMIC, has_seq(dims));
+  return ssd::simt_bwd_launches(shape_of(dims), variant, has_seq(dims));
 }
 
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
+  if (!variant_ok(dims, variant)) return "invalid";
   if (use_fused(dims)) {
     if (variant == SSD_VARIANT_ATOMIC) return k == 0 ? "fused_bwd_atomic" : "invalid";
     return k == 0 ? "fused_bwd" : (k == 1 ? "fold_scalars" : "invalid");
   }
-  return ssd::simt_bwd_launch_name(variant == SSD_VARIANT_ATOMIC, has_seq(dims), k);
+  return ssd::simt_bwd_launch_name(variant, has_seq(dims), k);
 }
 
 ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims) || !workspace)
     return SSD_ERR_INVALID_ARG;
-  if (!use_fused(dims)) return SSD_OK;
+  // both paths keep their status word at the start of the workspace
   int word = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
@@ -201,10 +217,11 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   for (const void *p : req)
     if (!p || !aligned16(p)) return SSD_ERR_INVALID_ARG;
   if (dinit && (!aligned16(dinit) || !saved->init_states)) return SSD_ERR_INVALID_ARG;
-  if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC) return SSD_ERR_INVALID_ARG;
+  if (variant != SSD_VARIANT_DETERMINISTIC && variant != SSD_VARIANT_ATOMIC && variant != SSD_VARIANT_ORDERED)
+    return SSD_ERR_INVALID_ARG;
   if (config < 0 || config >= mamba2_ssd_num_configs(dims)) return SSD_ERR_INVALID_ARG;
+  if (!variant_ok(dims, variant)) return SSD_ERR_UNSUPPORTED;
   const ssd::Shape s = shape_of(dims);
-  const bool atomic = variant == SSD_VARIANT_ATOMIC;
   if (workspace_bytes < mamba2_ssd_bwd_workspace_size(dims, config, variant)) return SSD_ERR_WORKSPACE;
   if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
   ssd::Args a{};
@@ -221,7 +238,8 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   if (use_fused(dims))
     err = ssd::fused_bwd(s, a, workspace, fused_options(dims, config, variant), st, tr);
   else
-    err = ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], atomic, st, tr);
+    err = ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], variant, kOrderedSpinLimit, st,
+                        tr);
   return err == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 

@@ -10,12 +10,13 @@ namespace ssd {
 
 // General CUDA-core path (any shape; fp32 or bf16 inputs).
 size_t simt_fwd_workspace(const Shape &s);
-size_t simt_bwd_workspace(const Shape &s, bool atomic);
-int simt_bwd_launches(const Shape &s, bool atomic, bool seq);
-const char *simt_bwd_launch_name(bool atomic, bool seq, int k);
+// variant: 0 per-head slots folded in order, 1 atomics, 2 ordered semaphore fold
+size_t simt_bwd_workspace(const Shape &s, int variant);
+int simt_bwd_launches(const Shape &s, int variant, bool seq);
+const char *simt_bwd_launch_name(int variant, bool seq, int k);
 cudaError_t simt_fwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, cudaStream_t st);
-cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, bool atomic, cudaStream_t st,
-                     Trace &tr);
+cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, int variant, uint32_t spin_limit,
+                     cudaStream_t st, Trace &tr);
 
 // Fused tensor-core backward (bf16, chunk 128, dstate 128, headdim 64).
 struct FusedOptions {

@@ -10,6 +10,12 @@
 // contributions to the group-shared dB/dC, and per-chunk contributions to dA
 // and dD, are parked in slots and folded in ascending slot order by the
 // reduction kernels at the end (unless the atomic variant is requested).
+// The ordered variant folds dB/dC without slots instead: the CTA of head k
+// adds its tile into dB/dC only after the CTA of head k-1 of the same group
+// has published its own (a semaphore per tile, as in the ordered dQ
+// accumulation of "FlashAttention 2 deterministic backward"), so each
+// element is summed over heads in the same ascending order as the slot fold
+// and the bits are identical.
 //
 // Notation per (batch b, chunk c, head h): local token i in [0, Lc), Lc the
 // chunk's length; Acs_i the in-chunk inclusive prefix sum of dt*A (hi+lo);
@@ -435,6 +441,103 @@ __global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__res
   }
 }
 
+constexpr int kOrdTile = 32;   // tokens per tile of the ordered dB/dC fold
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Ordered dB/dC fold.  Work unit = (b, c, g, token tile tt, head k of the
+// group), k fastest, handed out in that order by an atomic ticket, so a CTA
+// only ever waits for units with smaller tickets, which are already running.
+// The CTA computes its tile's per-head dB/dC rows exactly as dbdc_kernel does
+// (same terms, same order) into shared memory, waits until the tile's
+// semaphore reads k (a bounded spin: past spin_limit polls it sets status
+// bit 1 and skips its add), then stores (k = 0) or adds its rows into dB/dC,
+// and releases the semaphore to k + 1.
+template <class TIn>
+__global__ void dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
+                                    const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
+                                    const float *__restrict__ dt, const float *__restrict__ Wm,
+                                    const float *__restrict__ states, const float *__restrict__ dS,
+                                    const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                                    const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                                    const float *__restrict__ init, int *__restrict__ status, int *__restrict__ sem,
+                                    uint32_t spin_limit, float *__restrict__ dBo, float *__restrict__ dCo) {
+  extern __shared__ float tile[];   // [2][kOrdTile][N]: dB rows then dC rows
+  __shared__ int s_unit, s_go;
+  if (threadIdx.x == 0) s_unit = atomicAdd(status + 1, 1);
+  __syncthreads();
+  const int64_t ntt = cdiv(s.Q, kOrdTile);
+  const int64_t unit = s_unit;
+  const int64_t k = unit % s.hpg, tileid = unit / s.hpg;
+  const int64_t tt = tileid % ntt, g = (tileid / ntt) % s.G, c = (tileid / (ntt * s.G)) % s.nc;
+  const int64_t bi = tileid / (ntt * s.G * s.nc);
+  const int64_t h = g * s.hpg + k, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const int64_t i0 = tt * kOrdTile, i1 = min(Lc, i0 + kOrdTile);
+  const int64_t hunit = (bi * s.nc + c) * s.H + h;
+  const float *W = Wm + hunit * s.Q * s.Q;
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  for (int64_t e = threadIdx.x; e < (i1 - i0) * s.N; e += blockDim.x) {
+    const int64_t i = i0 + e / s.N, n = e % s.N, t = t0 + i;
+    float dc = 0.f, db = 0.f;
+    for (int64_t j = 0; j <= i; ++j) dc = fmaf(W[i * s.Q + j], ld(Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), dc);
+    for (int64_t j = i; j < Lc; ++j) db = fmaf(W[j * s.Q + i], ld(Cm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), db);
+    const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
+    const float *hs = f == 0 ? states + hunit * s.P * s.N + n
+                             : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N + n : nullptr);
+    const float *ds = dS + hunit * s.P * s.N + n;
+    const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
+    const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
+    float hg = 0.f, sx = 0.f;
+    for (int64_t p = 0; p < s.P; ++p) {
+      if (hs) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+      sx = fmaf(ds[p * s.N], ld(xi + p), sx);
+    }
+    const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
+    const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+    tile[e] = fmaf(wi, sx, db);
+    tile[kOrdTile * s.N + e] = fmaf(din, hg, dc);
+  }
+  __syncthreads();
+  int *sm_flag = sem + tileid;
+  if (threadIdx.x == 0) {
+    int go = 1;
+    if (k > 0) {
+      uint32_t it = 0;
+      while (ld_acquire_gpu(sm_flag) != int(k)) {
+        if (++it > spin_limit) {   // predecessor never published: report, skip the add
+          atomicOr(status, 1);
+          go = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    s_go = go;
+  }
+  __syncthreads();
+  if (!s_go) return;
+  for (int64_t e = threadIdx.x; e < (i1 - i0) * s.N; e += blockDim.x) {
+    const int64_t i = i0 + e / s.N, n = e % s.N;
+    const int64_t o = ((bi * s.T + t0 + i) * s.G + g) * s.N + n;
+    const float db = tile[e], dc = tile[kOrdTile * s.N + e];
+    dBo[o] = (k == 0 ? 0.f : dBo[o]) + db;   // 0 + s0 + s1 + ..., as the slot fold adds
+    dCo[o] = (k == 0 ? 0.f : dCo[o]) + dc;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) st_release_gpu(sm_flag, int(k) + 1);
+}
+
 // Per token (b,c,h,i): the dt-weight part of ddt and the gradient reaching
 // Acs_i, before the reverse cumsum:
 //   ddt_part = sum_{j>=i} MG[j,i] + exp(E - Acs_i) sx_i
@@ -590,13 +693,19 @@ __global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ d
 }
 
 struct BwdWs {
+  int *status;   // [0] error bits (bit 1: an ordered-fold wait gave up), [1] ticket; first in the workspace
   float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *MGm, *buf, *carry, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
       *dD_part, *slot_b, *slot_c;
   int32_t *first;
+  int *sem;
 };
 
-BwdWs carve_bwd(Carver &cv, const Shape &s, bool atomic) {
+int64_t ordered_tiles(const Shape &s) { return s.b * s.nc * s.G * cdiv(s.Q, kOrdTile); }
+
+BwdWs carve_bwd(Carver &cv, const Shape &s, int variant) {
+  const bool atomic = variant == 1, ordered = variant == 2;
   BwdWs w;
+  w.status = cv.take<int>(2);
   const int64_t acs = s.b * s.H * s.nc * s.Q, qq = s.b * s.nc * s.H * s.Q * s.Q;
   w.acs_hi = cv.take<float>(acs);
   w.acs_lo = cv.take<float>(acs);
@@ -614,9 +723,10 @@ BwdWs carve_bwd(Carver &cv, const Shape &s, bool atomic) {
   w.ddt_part = cv.take<float>(s.b * s.T * s.H);
   w.dA_part = cv.take<float>(s.b * s.nc * s.H);
   w.dD_part = cv.take<float>(s.b * s.nc * s.H);
-  w.slot_b = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
-  w.slot_c = atomic ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
+  w.slot_b = (atomic || ordered) ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
+  w.slot_c = (atomic || ordered) ? nullptr : cv.take<float>(s.b * s.T * s.H * s.N);
   w.first = cv.take<int32_t>(s.nseq);
+  w.sem = ordered ? cv.take<int>(ordered_tiles(s)) : nullptr;
   return w;
 }
 
@@ -669,9 +779,11 @@ cudaError_t fwd_impl(const Shape &s, const Args &a, void *ws, int bs, cudaStream
 }
 
 template <class TIn>
-cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomic, cudaStream_t st, Trace &tr) {
+cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int variant, uint32_t spin_limit, cudaStream_t st,
+                     Trace &tr) {
+  const bool atomic = variant == 1, ordered = variant == 2;
   Carver cv(ws);
-  BwdWs w = carve_bwd(cv, s, atomic);
+  BwdWs w = carve_bwd(cv, s, variant);
   const TIn *x = static_cast<const TIn *>(a.x), *Bm = static_cast<const TIn *>(a.B), *Cm = static_cast<const TIn *>(a.C);
   const TIn *g = static_cast<const TIn *>(a.dout);
   const int64_t PN = s.P * s.N;
@@ -682,6 +794,9 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
   }
   err = cudaMemsetAsync(w.carry, 0, size_t(s.b * s.H * PN) * sizeof(float), st);
   if (err != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(w.status, 0, 2 * sizeof(int), st)) != cudaSuccess) return err;
+  if (ordered && (err = cudaMemsetAsync(w.sem, 0, size_t(ordered_tiles(s)) * sizeof(int), st)) != cudaSuccess)
+    return err;
   if (atomic) {
     const size_t nbg = size_t(s.b * s.T * s.G * s.N) * sizeof(float);
     if ((err = cudaMemsetAsync(a.dB, 0, nbg, st)) != cudaSuccess) return err;
@@ -731,6 +846,18 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
     dbdc_kernel<TIn, true><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, a.dB, a.dC);
     tr.mark(st);
+  } else if (ordered) {
+    tr.mark(st);
+    const int64_t units = ordered_tiles(s) * s.hpg;
+    const size_t shm = size_t(2 * kOrdTile * s.N) * sizeof(float);
+    if (shm > 48 * 1024 &&
+        (err = cudaFuncSetAttribute(dbdc_ordered_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(shm))) != cudaSuccess)
+      return err;
+    dbdc_ordered_kernel<TIn><<<unsigned(units), bs, shm, st>>>(
+        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.status,
+        w.sem, spin_limit, a.dB, a.dC);
+    tr.mark(st);
   } else {
     tr.mark(st);
     dbdc_kernel<TIn, false><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
@@ -753,9 +880,11 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, bool atomi
     cumsum_bwd_kernel<false><<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(
         s, a.dt, a.A, w.dAcs, w.u, w.gx, w.vin, w.dEpass, a.seq_idx, first, w.ddt_part, a.ddt, w.dA_part, w.dD_part);
     tr.mark(st);
-    tr.mark(st);
-    reduce_heads_kernel<<<grid1(s.b * s.T * s.G * s.N, bs), bs, 0, st>>>(s, w.slot_b, w.slot_c, a.dB, a.dC);
-    tr.mark(st);
+    if (!ordered) {
+      tr.mark(st);
+      reduce_heads_kernel<<<grid1(s.b * s.T * s.G * s.N, bs), bs, 0, st>>>(s, w.slot_b, w.slot_c, a.dB, a.dC);
+      tr.mark(st);
+    }
     tr.mark(st);
     reduce_heads_scalars_kernel<<<grid1(s.H, bs), bs, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
     tr.mark(st);
@@ -771,20 +900,24 @@ size_t simt_fwd_workspace(const Shape &s) {
   return cv.bytes();
 }
 
-size_t simt_bwd_workspace(const Shape &s, bool atomic) {
+size_t simt_bwd_workspace(const Shape &s, int variant) {
   Carver cv(nullptr);
-  carve_bwd(cv, s, atomic);
+  carve_bwd(cv, s, variant);
   return cv.bytes();
 }
 
-int simt_bwd_launches(const Shape &, bool atomic, bool seq) { return (atomic ? 9 : 11) + (seq ? 2 : 0); }
+int simt_bwd_launches(const Shape &, int variant, bool seq) {
+  return (variant == 1 ? 9 : (variant == 2 ? 10 : 11)) + (seq ? 2 : 0);
+}
 
-const char *simt_bwd_launch_name(bool atomic, bool seq, int k) {
+const char *simt_bwd_launch_name(int variant, bool seq, int k) {
   static const char *det[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc",
                               "ddt_dacs", "cumsum_bwd", "reduce_heads", "reduce_heads_scalars"};
   static const char *atm[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc_atomic",
                               "ddt_dacs", "cumsum_bwd_atomic"};
-  const int n = atomic ? 9 : 11;
+  static const char *ord[] = {"cumsum_fwd", "cb", "mwg", "dhscan", "state_passing_bwd", "dx", "dbdc_ordered",
+                              "ddt_dacs", "cumsum_bwd", "reduce_heads_scalars"};
+  const int n = variant == 1 ? 9 : (variant == 2 ? 10 : 11);
   if (k < 0 || k >= n + (seq ? 2 : 0)) return "invalid";
   if (seq) {
     // seq_first runs first, dinit_mid right after the reverse state passing
@@ -792,17 +925,17 @@ const char *simt_bwd_launch_name(bool atomic, bool seq, int k) {
     if (k == 6) return "dinit_mid";
     k = k < 6 ? k - 1 : k - 2;
   }
-  return atomic ? atm[k] : det[k];
+  return variant == 1 ? atm[k] : (variant == 2 ? ord[k] : det[k]);
 }
 
 cudaError_t simt_fwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, cudaStream_t st) {
   return bf16 ? fwd_impl<__nv_bfloat16>(s, a, ws, block, st) : fwd_impl<float>(s, a, ws, block, st);
 }
 
-cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, bool atomic, cudaStream_t st,
-                     Trace &tr) {
-  return bf16 ? bwd_impl<__nv_bfloat16>(s, a, ws, block, atomic, st, tr)
-              : bwd_impl<float>(s, a, ws, block, atomic, st, tr);
+cudaError_t simt_bwd(const Shape &s, bool bf16, const Args &a, void *ws, int block, int variant, uint32_t spin_limit,
+                     cudaStream_t st, Trace &tr) {
+  return bf16 ? bwd_impl<__nv_bfloat16>(s, a, ws, block, variant, spin_limit, st, tr)
+              : bwd_impl<float>(s, a, ws, block, variant, spin_limit, st, tr);
 }
 
 }  // namespace ssd

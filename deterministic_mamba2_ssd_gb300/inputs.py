@@ -44,11 +44,14 @@ WORKLOADS = {
     "bf16_T16384": Workload("bf16_T16384", 1, 16384, 128, 256, 64, 8, 128, torch.bfloat16, 4.0, "normal"),
     "bf16_varlen_T32768": Workload("bf16_varlen_T32768", 1, 32768, 256, 128, 64, 1, 256, torch.bfloat16,
                                    4.0, "normal", seq_lens=(4096, 8192, 8192, 12288), with_init=True),
+    # fp32 inputs on the 2K shape: runs the general CUDA-core path (fp32 tolerance rules out
+    # tensor-core operands); used to compare its two deterministic dB/dC folds
+    "fp32_T2048": Workload("fp32_T2048", 1, 2048, 128, 256, 64, 8, 128, torch.float32, 4.0, "normal"),
 }
 
 #: seed offset per preset, in the order the presets are listed above
 SEED_BASE = 1234
-WORKLOAD_ORDER = ["tiny_fp32", "bf16_T2048", "bf16_T4096", "bf16_T16384", "bf16_varlen_T32768"]
+WORKLOAD_ORDER = ["tiny_fp32", "bf16_T2048", "bf16_T4096", "bf16_T16384", "bf16_varlen_T32768", "fp32_T2048"]
 
 
 def seed_of(name: str) -> int:

@@ -65,7 +65,13 @@ typedef enum {
 
 typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
 
-typedef enum { SSD_VARIANT_DETERMINISTIC = 0, SSD_VARIANT_ATOMIC = 1 } ssd_variant;
+/* Backward variants.  DETERMINISTIC (the product) and ORDERED give the same
+ * bits; ORDERED replaces the general path's per-head dB/dC slots by an
+ * ordered-semaphore fold (the CTA of head k of a group adds its tile after
+ * the CTA of head k-1 has published; the ordered accumulation of
+ * "FlashAttention 2 deterministic backward"), general path only.  ATOMIC
+ * exists only to measure the cost of determinism. */
+typedef enum { SSD_VARIANT_DETERMINISTIC = 0, SSD_VARIANT_ATOMIC = 1, SSD_VARIANT_ORDERED = 2 } ssd_variant;
 
 typedef struct {
   int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size;
@@ -153,16 +159,19 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
  * fp32 and fully overwritten: dx (b,T,H,P), ddt (b,T,H), dA (H), dB, dC
  * (b,T,G,N), dD (H), dinit (nseq,H,P,N; may be NULL; must be NULL when the
  * forward had no init_states).  workspace: >= bwd_workspace_size(config,
- * variant) bytes.  variant: SSD_VARIANT_DETERMINISTIC (the product) or
- * SSD_VARIANT_ATOMIC (same kernels with atomic accumulation; for measuring
- * the cost of determinism only, results not reproducible). */
+ * variant) bytes.  variant: SSD_VARIANT_DETERMINISTIC (the product),
+ * SSD_VARIANT_ORDERED (general path only, else SSD_ERR_UNSUPPORTED; same
+ * bits; dstate <= 512) or SSD_VARIANT_ATOMIC (same kernels with atomic
+ * accumulation; for measuring the cost of determinism only, results not
+ * reproducible). */
 ssd_status mamba2_ssd_bwd(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,
                           float *dB, float *dC, float *dD, float *dinit, void *workspace,
                           size_t workspace_bytes, int config, int variant, void *stream);
 
 /* Status of the last backward that used this workspace: reads one word
  * written by the device (synchronises `stream`).  SSD_ERR_TIMEOUT when a
- * bounded device-side wait of the fused backward ran out, SSD_ERR_UNSUPPORTED
+ * bounded device-side wait ran out (the fused backward's chain, or the
+ * ORDERED variant's semaphore), SSD_ERR_UNSUPPORTED
  * when the fused kernel found its dynamic shared memory not 1 KB aligned and
  * did no work (outputs invalid in both cases), SSD_OK otherwise. */
 ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *workspace, void *stream);

@@ -143,6 +143,21 @@ def test_any_start_dims_take_the_general_path(L):
     assert ssd.bwd_num_launches(anyst, 0, 0) == ssd.bwd_num_launches(plain, 0, 0) + 2
 
 
+def test_ordered_variant_only_on_the_general_path(L):
+    fused = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128)
+    simt = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, dtype=torch.float32)
+    assert ssd.bwd_workspace_size(fused, 0, 2) == 0 and ssd.bwd_num_launches(fused, 0, 2) == 0
+    assert ssd.bwd_workspace_size(simt, 0, 2) > 0
+    names = ssd.bwd_launch_names(simt, 0, 2)
+    assert "dbdc_ordered" in names and "reduce_heads" not in names and "dbdc" not in names
+    assert "invalid" not in names and names[-1] == "reduce_heads_scalars"
+    # no per-head slots: smaller workspace than the slot fold
+    assert ssd.bwd_workspace_size(simt, 0, 2) < ssd.bwd_workspace_size(simt, 0, 0)
+    big_n = ssd.make_dims(1, 256, 4, 16, 1, 1024, 64, dtype=torch.float32)
+    assert ssd.bwd_workspace_size(big_n, 0, 2) == 0 and ssd.bwd_workspace_size(big_n, 0, 0) > 0
+    assert ssd.bwd_workspace_size(simt, 0, 3) == 0
+
+
 def test_binding_refuses_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ssd, "_lib", None)
     monkeypatch.setattr(ssd, "LIB_PATH", str(tmp_path / "missing.so"))

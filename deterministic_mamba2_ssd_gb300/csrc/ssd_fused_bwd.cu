@@ -941,9 +941,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float off = 0.f;
           for (int w = 3; w > q; --w) off += sm->red[w];
           const float su = ((sm->red[4] + sm->red[5]) + sm->red[6]) + sm->red[7];
-          float hsum = 0.f;
+          // <H, dS> from the 16 per-warp partials: a fixed shuffle tree within each
+          // 16-lane half (every lane ends with the same total)
+          float hsum = sm->red[40 + (lane & (kEpiWarps - 1))];
 #pragma unroll
-          for (int w = 0; w < kEpiWarps; ++w) hsum += sm->red[40 + w];
+          for (int o = kEpiWarps / 2; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
           const float K = su + umma::ex2_approx(a2E5) * hsum;   // + dEpass = exp(E) <H, dS>
           const float da = (sfx + off) + K;
           __stcg(p.ddt + (row0 + r) * s.H + h, fmaf(Ah, da, dintra + eEA5 * sxy5));

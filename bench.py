@@ -483,8 +483,12 @@ def main():
             if k >= args.warmup:
                 e_ms.append(e0.elapsed_time(e1))
         em = max_over_ranks(statistics.mean(e_ms), world, dev)
+        # value from the mean step time; the median and the slowest step show how much of the
+        # mean comes from occasional slow steps of the host copies (seen at 80-130 ms against a
+        # steady 18.8 ms on a shared machine)
         e2e = {"value": world * tokens / (em / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": em}
+               "d2h_bytes_per_step": d2h, "ms_per_step": em, "ms_per_step_median": statistics.median(e_ms),
+               "ms_per_step_max": max(e_ms)}
 
     line = None
     if rank == 0:

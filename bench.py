@@ -454,41 +454,86 @@ def main():
         atomic_ms = statistics.mean(ta)
         del ws_a, out_a
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step copies its inputs from
+    # pinned host memory, runs mamba2_ssd_bwd and copies every gradient back.  Steps are
+    # pipelined over two buffer sets and three streams (inputs of step k+1 travel while step k
+    # computes and its gradients travel back), as a training loop's data path would run them;
+    # the serial step time (copies, backward and copies back on one stream) is reported beside.
     e2e = None
     if not args.no_e2e:
         host = {k: v.pin_memory() for k, v in d.items() if v is not None}
         host["states"] = saved.states.cpu().pin_memory()
-        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
         d2h = sum(v.numel() * v.element_size() for v in out.values())
-        # saved struct that points at the freshly copied device inputs
-        _, saved_e = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
-                             chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"))
-        saved_e.struct.states = dev_in["states"].data_ptr()
-        saved_e.tensors["states"] = dev_in["states"]
-        e_ms = []
-        for k in range(args.warmup + args.steps):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for key, v in host.items():
-                dev_in[key].copy_(v, non_blocking=True)
-            ssd.bwd(saved_e, dev_in["dout"], config=args.config, out=out, workspace=ws)
-            for key, v in out.items():
-                host_out[key].copy_(v, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if k >= args.warmup:
-                e_ms.append(e0.elapsed_time(e1))
-        em = max_over_ranks(statistics.mean(e_ms), world, dev)
-        # value from the mean step time; the median and the slowest step show how much of the
-        # mean comes from occasional slow steps of the host copies (seen at 80-130 ms against a
-        # steady 18.8 ms on a shared machine)
-        e2e = {"value": world * tokens / (em / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": em, "ms_per_step_median": statistics.median(e_ms),
-               "ms_per_step_max": max(e_ms)}
+        sets = []
+        for _ in range(2):
+            dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+            # saved struct that points at this set's device inputs
+            _, saved_e = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
+                                 chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"))
+            saved_e.struct.states = dev_in["states"].data_ptr()
+            saved_e.tensors["states"] = dev_in["states"]
+            out_e = {k: torch.empty_like(v) for k, v in out.items()}
+            ws_e = torch.empty_like(ws)
+            host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+            sets.append((dev_in, saved_e, out_e, ws_e, host_out))
+        torch.cuda.synchronize()
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+        def run_steps(n, serial):
+            """Mean ms per step over n steps, and the median interval between step completions."""
+            ev_cmp = [None, None]   # compute of the step that last used each set (inputs read)
+            ev_out = [None, None]   # copy-back of the step that last used each set (outputs read)
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            done = []
+            start.record(s_in)
+            for k in range(n):
+                i = k % 2
+                dev_in, saved_e, out_e, ws_e, host_out = sets[i]
+                si, sc, so = (s_in, s_in, s_in) if serial else (s_in, s_cmp, s_out)
+                if ev_cmp[i] is not None:
+                    si.wait_event(ev_cmp[i])
+                with torch.cuda.stream(si):
+                    for key, v in host.items():
+                        dev_in[key].copy_(v, non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(si)
+                sc.wait_event(e_in)
+                if ev_out[i] is not None:
+                    sc.wait_event(ev_out[i])
+                ssd.bwd(saved_e, dev_in["dout"], config=args.config, out=out_e, workspace=ws_e, stream=sc)
+                ev_cmp[i] = torch.cuda.Event()
+                ev_cmp[i].record(sc)
+                so.wait_event(ev_cmp[i])
+                with torch.cuda.stream(so):
+                    for key, v in out_e.items():
+                        host_out[key].copy_(v, non_blocking=True)
+                ev_out[i] = torch.cuda.Event(enable_timing=True)
+                ev_out[i].record(so)
+                done.append(ev_out[i])
+            for e in ev_out:
+                if e is not None:
+                    s_in.wait_event(e)
+            end.record(s_in)
+            end.synchronize()
+            t = [start.elapsed_time(e) for e in done]
+            gaps = [b - a for a, b in zip([0.0] + t[:-1], t)]
+            return start.elapsed_time(end) / n, statistics.median(gaps)
+
+        run_steps(args.warmup, serial=False)
+        pipe_ms, pipe_med = run_steps(args.steps, serial=False)
+        pipe_ms = max_over_ranks(pipe_ms, world, dev)
+        run_steps(2, serial=True)
+        serial_ms, serial_med = run_steps(args.steps, serial=True)
+        serial_ms = max_over_ranks(serial_ms, world, dev)
+        # value from the mean over all steps; the medians show how much of it comes from
+        # occasional stalls of the host copies (steps of 80-200 ms seen on a shared machine)
+        e2e = {"value": world * tokens / (pipe_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "pipelined": True,
+               "ms_per_step_median": pipe_med, "serial_ms_per_step": serial_ms,
+               "serial_ms_per_step_median": serial_med}
+        del sets
 
     line = None
     if rank == 0:

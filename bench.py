@@ -72,6 +72,11 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of independent replicas: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def barrier(world: int, device=None):
     if world > 1:
         import torch.distributed as dist
@@ -421,7 +426,7 @@ def main():
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
     tokens = w.batch * w.seqlen
-    value = world * tokens / (ms_max / 1e3)
+    value = job_throughput(tokens, world, ms_max)
 
     # dominant kernel and its roofline
     tot = {key: sum(v) for key, v in per_kernel.items()}

@@ -86,6 +86,8 @@ def lib():
         L.mamba2_ssd_bwd_fault_test.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 9 + [sz, i64, ctypes.c_uint32,
                                                                                            vp]
         L.mamba2_ssd_bwd_fault_test.restype = ci
+        L.mamba2_ssd_states_unpack.argtypes = [ctypes.POINTER(SavedStruct), vp, vp]
+        L.mamba2_ssd_states_unpack.restype = ci
         L.mamba2_ssd_selftest_umma.argtypes = [vp] * 3 + [ci] * 6 + [vp]
         L.mamba2_ssd_selftest_umma.restype = ci
         L.mamba2_ssd_static_scratch_bytes.argtypes = []
@@ -176,7 +178,16 @@ class Saved:
 
     @property
     def states(self):
+        """The saved-state buffer as the backward takes it (packed on the fused shapes)."""
         return self.tensors["states"]
+
+    def states_fp32(self, stream=None):
+        """fp32 (b, nc, H, P, N) view of the saved chunk states (a new tensor)."""
+        out = torch.empty_like(self.tensors["states"])
+        rc = lib().mamba2_ssd_states_unpack(ctypes.byref(self.struct), _ptr(out), _stream(stream))
+        if rc:
+            raise SsdError(rc, "mamba2_ssd_states_unpack")
+        return out
 
 
 def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=None, any_start=False):

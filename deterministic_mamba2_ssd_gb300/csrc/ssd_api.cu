@@ -198,12 +198,26 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.D = D;
   a.init = init_states; a.seq_idx = seq_idx; a.y = y; a.states_out = states;
   if (ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st) != cudaSuccess) return SSD_ERR_CUDA;
+  // the fused backward takes each saved state as a packed bf16 hi | lo operand pair
+  if (use_fused(dims) && ssd::fused_pack_states(s, states, st) != cudaSuccess) return SSD_ERR_CUDA;
   saved_out->dims = *dims;
   saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
   saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;
   saved_out->magic = kSavedMagic;
   saved_out->flags = 0;
   return SSD_OK;
+}
+
+ssd_status mamba2_ssd_states_unpack(const ssd_saved *saved, float *out, void *stream) {
+  if (!saved || saved->magic != kSavedMagic || !dims_ok(&saved->dims)) return SSD_ERR_HANDLE;
+  if (!saved->states || !out || !aligned16(out)) return SSD_ERR_INVALID_ARG;
+  const ssd::Shape s = shape_of(&saved->dims);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_fused(&saved->dims))
+    return ssd::fused_unpack_states(s, saved->states, out, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+  const size_t bytes = size_t(s.b * s.nc * s.H * s.P * s.N) * sizeof(float);
+  return cudaMemcpyAsync(out, saved->states, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? SSD_OK
+                                                                                                 : SSD_ERR_CUDA;
 }
 
 ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float *dx, float *ddt, float *dA,

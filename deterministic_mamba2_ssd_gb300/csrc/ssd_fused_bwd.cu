@@ -53,8 +53,9 @@ constexpr int kThreads = kEpiThreads + 64;
 constexpr uint32_t OFF_B = 0;          // B chunk  [t][n] bf16, 2 panels x 16 KB
 constexpr uint32_t OFF_C = 32768;      // C chunk  [t][n] bf16, 2 panels
 constexpr uint32_t OFF_XG = 65536;     // x [t][p] 16 KB, g 16 KB (bf16 from TMA, then scaled fp16 in place)
-constexpr uint32_t OFF_STG = 98304;    // fp32 [p][n] 32 KB: the state tile entering the chunk, then dS (bulk copies)
-constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [n][p] bf16, 16 KB each; later dS [n][p] (hi half)
+constexpr uint32_t OFF_STG = 98304;    // fp32 [p][n] 32 KB: dS, the chained state gradient (bulk copy)
+constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [n][p] bf16, 16 KB each (bulk copy of the packed
+                                       // saved state); later dS [n][p] (hi half)
 constexpr uint32_t OFF_GW = 163840;    // exp(Acs) o g hi | lo: [t][p] bf16; later w o x (hi half) + scratch (lo half)
 constexpr uint32_t OFF_M16 = 196608;   // scaled M: [t][s] fp16, 2 panels x 16 KB
 constexpr uint32_t OFF_SMALL = 229376;
@@ -73,7 +74,7 @@ constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
 constexpr uint32_t T_DH = T_RA, T_CH = T_RA + 64, T_Y = T_RA, T_D1 = T_RA + 64;
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, E_HCONV, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_HCONV || i == E_GXL || i == E_RING || i == E_DS0 || i == E_DS1) ? kEpiWarps : 1);  // per-warp arrivals
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_GXL || i == E_RING || i == E_DS0 || i == E_DS1) ? kEpiWarps : 1);  // per-warp arrivals
     umma::fence_mbar_init();
     sm->unit = atomicAdd(p.ticket, 1);
     sm->abort = 0;
@@ -348,10 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_bar(&bars[E_RING], uint32_t((k - 1) & 1), p.err);
           if (sm->abort) break;
           if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h - 1), 1);
+          // the products that read head k-1's dS from the H tiles (Y, dB) are done
+          wait_bar(&bars[B_G4], uint32_t((k - 1) & 1), p.err);
+          if (sm->abort) break;
         }
-        // the state tile entering the chunk, fp32, into the staging buffer
+        // the state tile entering the chunk, saved by the forward as the bf16 hi | lo pair of
+        // [n][p] tiles in the 128-byte swizzled operand layout: one copy straight into place
         umma::mbar_expect_tx(&bars[B_H], kP * kN * 4);
-        umma::bulk_load(sm_base + OFF_STG, states + h * kP * kN, kP * kN * 4, &bars[B_H]);
+        umma::bulk_load(sm_base + OFF_HD, states + h * kP * kN, kP * kN * 4, &bars[B_H]);
         ++n_h;
         if (k + 1 < hpg) umma::prefetch_l2(states + (h + 1) * kP * kN, kP * kN * 4);
         // x and g of this head once the previous head's are consumed
@@ -368,9 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma::tma_prefetch_2d(&tm_g, int((h + 1) * kP), int(row0));
         }
         if (has_next) {
-          // dS = dH of the chunk after, once its unit has published it and the
-          // state tile has been converted out of the staging buffer
-          wait_bar(&bars[E_HCONV], par, p.err);
+          // dS = dH of the chunk after, once its unit has published it (the staging
+          // buffer was freed by the E_RING wait above)
           const int *flag = p.flags + ((bi * s.nc + c + 1) * s.H + h);
           uint32_t it = 0;
           while (!sm->abort && ld_acquire_gpu(flag) == 0) {
@@ -452,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kP; kk += 16)
           umma::mma_bf16(tmem + T_RA + 64, kdesc(aG, 16384, kk), kdesc(aX + 8192, 16384, kk), id_kk64, kk > 0);
         umma::mma_commit(&bars[B_G1R]);
-        wait_bar(&bars[E_X16], par, p.err);  // G~ and H (hi, lo) in smem
+        wait_bar(&bars[E_X16], par, p.err);  // G~ in smem
+        wait_bar(&bars[B_H], par, p.err);    // H (hi, lo) landed
         umma::fence_after_sync();
         // dC += G~ H^T  (M = t, N = n, K = p): hi*hi + hi*lo + lo*hi; runs while the epilogue reads g x^T
         for (int part = 0; part < 3; ++part) {
@@ -612,21 +617,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with both factors at most one (kept in dtu until E3 reuses it).
       if (cq == 0) sm->dtu[r] = umma::ex2_approx(sm->a2[r | 15] - sm->a2[r]);
 
-      // H (fp32 [p][n] state entering the chunk, staging buffer) -> bf16 hi + lo,
-      // stored [n][p]: this thread takes state index n and its 16 p values
-      {
-        const float *hs = reinterpret_cast<const float *>(sm_base + OFF_STG);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int pg = 2 * cq + u;   // group of 8 p values
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = hs[(8 * pg + i) * kN + n];
-          st8_bf16_hilo(sm_base + OFF_HD, sm_base + OFF_HD + 16384, n, 8 * pg, v);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) umma::mbar_arrive(&bars[E_HCONV]);   // the staging buffer may take dS now
       // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |g| for the fp16 scaling of g; g . x
       float gmax = 0.f, gx = 0.f;
 #pragma unroll
@@ -1020,6 +1010,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The saved state of each (batch, chunk, head), as the fused backward takes it:
+// the fp32 (P, N) tile H = hi + lo rounded to a bf16 pair (hi = round(H),
+// lo = round(H - hi)), each half a [n][p] bf16 tile in the 128-byte swizzled
+// layout of a tensor-core operand (row n at n * 128 bytes, its 16-byte chunk
+// j at position j ^ (n & 7)), hi then lo: the same 32 KB per tile, packed in
+// place.  One CTA per tile.
+__global__ void __launch_bounds__(256) pack_states_kernel(float *__restrict__ states) {
+  __shared__ float tile[kP * kN];
+  float *g = states + int64_t(blockIdx.x) * kP * kN;
+  for (int i = threadIdx.x; i < kP * kN / 4; i += blockDim.x)
+    reinterpret_cast<float4 *>(tile)[i] = reinterpret_cast<const float4 *>(g)[i];
+  __syncthreads();
+  uint8_t *out = reinterpret_cast<uint8_t *>(g);
+  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {   // (row n, 8-column group)
+    const int n = i >> 3, c0 = 8 * (i & 7);
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[(c0 + e) * kN + n];
+    st8_bf16_hilo(out, out + 16384, n, c0, v);
+  }
+}
+
+// fp32 [p][n] view (hi + lo) of packed saved states, for inspection.
+__global__ void __launch_bounds__(256) unpack_states_kernel(const float *__restrict__ packed, float *__restrict__ out) {
+  const uint8_t *in = reinterpret_cast<const uint8_t *>(packed + int64_t(blockIdx.x) * kP * kN);
+  float *o = out + int64_t(blockIdx.x) * kP * kN;
+  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {
+    const int n = i >> 3, c0 = 8 * (i & 7);
+    float hi[8], lo[8];
+    ld8_bf16(in, n, c0, hi);
+    ld8_bf16(in + 16384, n, c0, lo);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[(c0 + e) * kN + n] = hi[e] + lo[e];
+  }
+}
+
 // dA[h], dD[h]: per-(batch, chunk) partials summed in ascending order.
 __global__ void fold_scalars_kernel(Shape s, const float *__restrict__ dA_part, const float *__restrict__ dD_part,
                                     float *__restrict__ dA, float *__restrict__ dD) {
@@ -1051,6 +1077,16 @@ FusedWs carve_fused(Carver &cv, const Shape &s, int ring_depth) {
 }
 
 }  // namespace
+
+cudaError_t fused_pack_states(const Shape &s, float *states, cudaStream_t st) {
+  pack_states_kernel<<<unsigned(s.b * s.nc * s.H), 256, 0, st>>>(states);
+  return cudaGetLastError();
+}
+
+cudaError_t fused_unpack_states(const Shape &s, const float *packed, float *out, cudaStream_t st) {
+  unpack_states_kernel<<<unsigned(s.b * s.nc * s.H), 256, 0, st>>>(packed, out);
+  return cudaGetLastError();
+}
 
 bool fused_bwd_supported(const Shape &s, bool bf16) {
   return bf16 && s.Q == kQ && s.N == kN && s.P == kP && s.T % kQ == 0 && s.hpg >= 1 &&

@@ -26,6 +26,11 @@ struct FusedOptions {
   int64_t silent_chunk = -1;       // fault injection: units of this chunk never publish
 };
 bool fused_bwd_supported(const Shape &s, bool bf16);
+// Saved states of the fused family: fp32 (P, N) tiles packed in place into the
+// bf16 hi | lo operand tiles the fused backward copies straight into shared
+// memory (same 32 KB per tile), and the fp32 view of them (hi + lo).
+cudaError_t fused_pack_states(const Shape &s, float *states, cudaStream_t st);
+cudaError_t fused_unpack_states(const Shape &s, const float *packed, float *out, cudaStream_t st);
 size_t fused_bwd_workspace(const Shape &s, int ring_depth);
 cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
 

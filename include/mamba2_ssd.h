@@ -102,7 +102,8 @@ typedef struct {
   const float *D;             /* (H) fp32 skip weight */
   const int32_t *seq_idx;     /* (b,T) int32 or NULL */
   const float *init_states;   /* (nseq,H,P,N) fp32 or NULL */
-  const float *states;        /* (b,nc,H,P,N) fp32: state entering each chunk */
+  const float *states;        /* (b,nc,H,P,N) states entering each chunk (packed on the fused shapes;
+                                 see mamba2_ssd_fwd and mamba2_ssd_states_unpack) */
   uint32_t magic;
   uint32_t flags;
 } ssd_saved;
@@ -147,13 +148,26 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
  * else SSD_ERR_UNSUPPORTED; checked with one synchronous device-to-host copy
  * of seq_idx, the only synchronisation in this library);
  * init_states (nseq,H,P,N) fp32 (nullable: zero initial states).
- * Outputs: y (b,T,H,P) in dtype; states (b,nc,H,P,N) fp32, the state
- * entering each chunk (init/zero at a sequence start); *saved_out (host
- * struct) filled for the backward.  workspace: >= fwd_workspace_size bytes. */
+ * Outputs: y (b,T,H,P) in dtype; states: b*nc*H*P*N fp32-sized elements
+ * holding the state entering each chunk (init/zero at a sequence start), the
+ * (P,N) fp32 tile of (b,c,h) at element offset ((b*nc+c)*H+h)*P*N.  On the
+ * shapes that run the fused backward (mamba2_ssd_config_name "fused/...")
+ * each tile is stored packed instead, in the same 32 KB: the bf16 pair
+ * hi = round(S), lo = round(S - hi) as two [N][P] tiles in the 128-byte
+ * swizzled tensor-core operand layout (row n at n*128 bytes, its 16-byte
+ * chunk j at position j ^ (n % 8)), hi first -- the operand the fused
+ * backward copies straight into shared memory.  mamba2_ssd_states_unpack
+ * gives the fp32 (b,nc,H,P,N) view of either form.  *saved_out (host struct)
+ * filled for the backward.  workspace: >= fwd_workspace_size bytes. */
 ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                           const void *B, const void *C, const float *D, const int32_t *seq_idx,
                           const float *init_states, void *y, float *states, void *workspace,
                           size_t workspace_bytes, void *stream, ssd_saved *saved_out);
+
+/* fp32 (b,nc,H,P,N) copy of the saved chunk states (hi + lo of the packed
+ * form on the fused shapes, the states themselves otherwise) into `out`
+ * (device, 16-byte aligned), enqueued on `stream`. */
+ssd_status mamba2_ssd_states_unpack(const ssd_saved *saved, float *out, void *stream);
 
 /* Backward of L = sum(y * dout).  dout (b,T,H,P) in dtype.  Outputs, all
  * fp32 and fully overwritten: dx (b,T,H,P), ddt (b,T,H), dA (H), dB, dC

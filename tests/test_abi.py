@@ -199,3 +199,14 @@ def test_adjacent_steps_reject_bad_arguments_on_host(L):
     assert L.mamba2_ssd_gate_bwd(16, 0, p(0), p(1), p(2), p(3), None, None) == 1
     assert L.mamba2_ssd_gate_fwd(0, 1, None, None, None, None) == 0
     assert L.mamba2_ssd_gate_bwd(-1, 1, p(0), p(1), p(2), p(3), p(4), None) == 1
+
+
+def test_states_unpack_rejects_bad_arguments_on_host(L):
+    sv = ssd.SavedStruct()
+    assert L.mamba2_ssd_states_unpack(None, ctypes.c_void_p(FAKE), None) == 6
+    assert L.mamba2_ssd_states_unpack(ctypes.byref(sv), ctypes.c_void_p(FAKE), None) == 6   # not from fwd
+    sv.dims = ssd.make_dims(1, 256, 4, 64, 1, 128, 128)
+    sv.magic = 0x53534432
+    sv.states = FAKE
+    assert L.mamba2_ssd_states_unpack(ctypes.byref(sv), None, None) == 1
+    assert L.mamba2_ssd_states_unpack(ctypes.byref(sv), ctypes.c_void_p(FAKE + 4), None) == 1

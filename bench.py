@@ -193,8 +193,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "939a44777cfe424d3b613b98d6cb568e5c4b5046a0bc2a0f01cfcbe9152afa39": {
-        "bytes_per_token": (2.29e9 + 1.67e9) / 16384,
+    "3233a502d6428c0f9f62b702d8bc4d3c058b54c7a5425212de58e5c647f4d579": {
+        "bytes_per_token": (2.29e9 + 1.65e9) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

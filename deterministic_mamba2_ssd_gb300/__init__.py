@@ -16,7 +16,7 @@ import torch
 
 __all__ = ["lib", "fwd", "bwd", "Saved", "SsdError", "make_dims", "num_configs", "config_name",
            "bwd_workspace_size", "fwd_workspace_size", "bwd_num_launches", "bwd_launch_names", "LIB_PATH",
-           "dt_fwd", "dt_bwd", "gate_fwd", "gate_bwd"]
+           "dt_fwd", "dt_bwd", "gate_fwd", "gate_bwd", "SSDFunction", "ssd"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba2_ssd.so")
 
@@ -336,3 +336,32 @@ def gate_bwd(y, z, dout, stream=None):
     if rc:
         raise SsdError(rc, "mamba2_ssd_gate_bwd")
     return dy, dz
+
+
+# ---- autograd -------------------------------------------------------------
+
+class SSDFunction(torch.autograd.Function):
+    """y = SSD(x, dt, A, B, C, D) as a differentiable op: the forward and the
+    deterministic backward are the library's (mamba2_ssd_fwd / mamba2_ssd_bwd);
+    this class only hands tensors across.  The library's gradients are fp32;
+    autograd casts each to its input's dtype."""
+
+    @staticmethod
+    def forward(ctx, x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, any_start=False):
+        y, saved = fwd(x, dt, A, B, C, D, chunk_size, seq_idx=seq_idx, init_states=init_states,
+                       any_start=any_start)
+        ctx.ssd_saved = saved
+        ctx.has_init = init_states is not None
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        saved = ctx.ssd_saved
+        g = bwd(saved, dy.contiguous())
+        dinit = g.get("dinit") if ctx.has_init else None
+        return g["dx"], g["ddt"], g["dA"], g["dB"], g["dC"], g["dD"], None, None, dinit, None
+
+
+def ssd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, any_start=False):
+    """Differentiable Mamba2 SSD chunked scan (see SSDFunction)."""
+    return SSDFunction.apply(x, dt, A, B, C, D, chunk_size, seq_idx, init_states, any_start)

@@ -210,3 +210,23 @@ def test_states_unpack_rejects_bad_arguments_on_host(L):
     sv.states = FAKE
     assert L.mamba2_ssd_states_unpack(ctypes.byref(sv), None, None) == 1
     assert L.mamba2_ssd_states_unpack(ctypes.byref(sv), ctypes.c_void_p(FAKE + 4), None) == 1
+
+
+def test_binding_checks_shapes_before_calling_the_library():
+    x = torch.zeros(1, 8, 2, 4)
+    dt = torch.zeros(1, 8, 2)
+    A = torch.zeros(2)
+    Bm = torch.zeros(1, 8, 1, 4)
+    D = torch.zeros(2)
+    with pytest.raises(ValueError, match="bf16 or fp32"):
+        ssd.fwd(x.half(), dt, A, Bm.half(), Bm.half(), D, 4)
+    with pytest.raises(ValueError, match="B"):
+        ssd.fwd(x, dt, A, torch.zeros(1, 7, 1, 4), Bm, D, 4)
+    with pytest.raises(ValueError, match="dt"):
+        ssd.fwd(x, dt[:, :, :1].contiguous(), A, Bm, Bm, D, 4)
+    with pytest.raises(ValueError, match="any_start"):
+        ssd.fwd(x, dt, A, Bm, Bm, D, 4, any_start=True)
+    with pytest.raises(ValueError, match="z"):
+        ssd.gate_fwd(x, torch.zeros(1, 8, 2, 5))
+    with pytest.raises(ValueError, match="dt_raw"):
+        ssd.dt_fwd(torch.zeros(5))

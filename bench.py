@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
     ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd"],
                     help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()

@@ -42,7 +42,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks_agree_on_the_slowest_time():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork: the parent may hold threads
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0] == out[1]
     m, v = out[0]

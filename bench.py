@@ -440,6 +440,24 @@ def main():
     achieved = alg / (dom_ms / 1e3) / 1e9 if alg else None
     shares = {n: round(tot[(j, n)] / sum(tot.values()), 4) for (j, n) in tot}
 
+    # bitwise repeat (after the timed region): 20 more backward passes, each compared bit for bit
+    # with the first, and one pass under every other launch configuration
+    def bits_of(o):
+        return {k: v.view(torch.int32).clone() for k, v in o.items()}
+    ref_bits = bits_of(out)
+    repeats_equal = 0
+    for _ in range(20):
+        ssd.bwd(saved, g["dout"], config=args.config, variant=args.variant, out=out, workspace=ws)
+        repeats_equal += all(torch.equal(ref_bits[k], v.view(torch.int32)) for k, v in out.items())
+    configs_equal = []
+    for cfg in range(ssd.num_configs(saved.dims)):
+        o = ssd.bwd(saved, g["dout"], config=cfg, variant=args.variant)
+        configs_equal.append(all(torch.equal(ref_bits[k], v.view(torch.int32)) for k, v in o.items()))
+    determinism = {"repeats": 20, "bitwise_equal_repeats": int(repeats_equal),
+                   "configs": [ssd.config_name(saved.dims, c) for c in range(len(configs_equal))],
+                   "bitwise_equal_across_configs": all(configs_equal)}
+    del ref_bits
+
     # determinism overhead: the same kernels with atomic accumulation
     atomic_ms = None
     if not args.no_atomic and args.variant == 0:
@@ -565,6 +583,7 @@ def main():
             "bwd_roofline_8TBps_frac": (api_bytes(w, es) / 8e12) / (ms_max / 1e3),
             "kernel_share": shares,
             "gpu_launches": nl * args.steps,
+            "bitwise_repeat": determinism,
             "deterministic_vs_atomic": {"det_ms": ms_max, "atomic_ms": atomic_ms,
                                         "overhead": (ms_max / atomic_ms - 1.0) if atomic_ms else None},
             "wall_s_timed_region": wall,

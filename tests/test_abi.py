@@ -230,3 +230,9 @@ def test_binding_checks_shapes_before_calling_the_library():
         ssd.gate_fwd(x, torch.zeros(1, 8, 2, 5))
     with pytest.raises(ValueError, match="dt_raw"):
         ssd.dt_fwd(torch.zeros(5))
+
+
+def test_binding_declares_argument_types_of_every_entry_point(L):
+    # ctypes would otherwise pass Python ints as C int and floats as double
+    missing = [n for n in declared_functions() if getattr(L, n).argtypes is None]
+    assert not missing, missing

@@ -193,8 +193,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "3233a502d6428c0f9f62b702d8bc4d3c058b54c7a5425212de58e5c647f4d579": {
-        "bytes_per_token": (2.29e9 + 1.65e9) / 16384,
+    "468b3ff713589a7a20e82dc7672c7acbe23f14cc87a3bbed2c60ece8ed9a0ab3": {
+        "bytes_per_token": (2283227648 + 1238003200) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

@@ -94,6 +94,8 @@ def lib():
         L.mamba2_ssd_static_scratch_bytes.restype = sz
         L.mamba2_ssd_bwd_static_scratch.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 8 + [ci, vp]
         L.mamba2_ssd_bwd_static_scratch.restype = ci
+        L.mamba2_ssd_static_scratch_check.argtypes = [pd, ci, vp]
+        L.mamba2_ssd_static_scratch_check.restype = ci
         f32 = ctypes.c_float
         L.mamba2_ssd_dt_fwd.argtypes = [i64, i64, vp, vp, ci, f32, f32, vp, vp]
         L.mamba2_ssd_dt_fwd.restype = ci

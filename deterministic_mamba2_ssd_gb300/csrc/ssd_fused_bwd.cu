@@ -742,7 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const bool has_next = sm->has_next != 0;
-      if (has_next) ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
+      if (has_next) {
+        ewait(&bars[B_DSL], par, p.err);   // dS in the staging buffer
+        // The ring slot has been copied for the last time: its L2 lines are
+        // dropped rather than written back to DRAM (the slot is next written
+        // after this chunk's flag is published, which these threads precede).
+        if (tid < kP * kN / 32 && !sm->abort)
+          umma::discard_l2_line(p.ring + ((((c + 1) % p.ring_depth) * s.b + bi) * s.H + h) * (kP * kN) + 32 * tid);
+      }
       float hdot = 0.f;
       float ds[16];   // this thread's dS values (state index n, 16 p values)
       {
@@ -779,6 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // per-warp partials of <H, dS>, folded in fixed order in E5
       hdot = warp_sum(hdot);
       if (lane == 0) sm->red[40 + warp] = hdot;
+      // atomic variant: every warp adds its own share of dA as soon as it has
+      // it (exp(E) <H, dS> times the chunk's total step), in whatever order
+      // the warps and CTAs get there
+      if (p.atomic && lane == 0) atomicAdd(p.dA + h, eE * hdot * sm->red[36 + (k & 1)]);
 
       ewait(&bars[B_CH], par, p.err);   // C H done: H (hi tile) may now give way to dS
       umma::fence_after_sync();
@@ -922,6 +933,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             sm->red[4 + q] = wu;
             sm->red[8 + q] = wg;
             sm->red[12 + q] = wc;
+            if (p.atomic) {   // this warp's share of dA and dD, added straight away
+              atomicAdd(p.dA + h, fmaf(wu, sm->red[36 + (k & 1)], wc));
+              atomicAdd(p.dD + h, wg);
+            }
           }
         }
         ep_sync();
@@ -939,17 +954,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float K = su + umma::ex2_approx(a2E5) * hsum;   // + dEpass = exp(E) <H, dS>
           const float da = (sfx + off) + K;
           __stcg(p.ddt + (row0 + r) * s.H + h, fmaf(Ah, da, dintra + eEA5 * sxy5));
-          if (tid == 0) {
+          if (tid == 0 && !p.atomic) {
             const float sg = ((sm->red[8] + sm->red[9]) + sm->red[10]) + sm->red[11];
             const float sc = ((sm->red[12] + sm->red[13]) + sm->red[14]) + sm->red[15];
             const float dap = fmaf(K, sm->red[36 + (k & 1)], sc);
-            if (p.atomic) {
-              atomicAdd(p.dA + h, dap);
-              atomicAdd(p.dD + h, sg);
-            } else {
-              __stcg(p.dA_part + (bi * s.nc + c) * s.H + h, dap);
-              __stcg(p.dD_part + (bi * s.nc + c) * s.H + h, sg);
-            }
+            __stcg(p.dA_part + (bi * s.nc + c) * s.H + h, dap);
+            __stcg(p.dD_part + (bi * s.nc + c) * s.H + h, sg);
           }
         }
       }

@@ -13,7 +13,10 @@
 // Set-up: the first call on a device, with that device current, looks the
 // array's device address up (cudaGetSymbolAddress) and caches it; later
 // calls reuse it.  That first call should therefore come before any stream
-// capture on the device.  Calls share the array and it keeps the previous
+// capture on the device.  The cached address belongs to the device context
+// it was looked up in: after cudaDeviceReset (or any teardown of the primary
+// context) the module is loaded again at a new address, and this entry point
+// must not be called again in that process.  Calls share the array and it keeps the previous
 // call's contents; the backward clears what must start at zero itself.  Calls
 // whose work overlaps on the GPU (different streams without ordering) race
 // on the array and must not be made.
@@ -67,6 +70,16 @@ ssd_status mamba2_ssd_bwd_static_scratch(const ssd_saved *saved, const void *dou
   if (st != SSD_OK) return st;
   return mamba2_ssd_bwd(saved, dout, dx, ddt, dA, dB, dC, dD, dinit, ws, kStaticScratchBytes, config,
                         SSD_VARIANT_DETERMINISTIC, stream);
+}
+
+// The backward's device-side status word lives at the start of its workspace,
+// here the static array; this reads it the way mamba2_ssd_bwd_check does.
+ssd_status mamba2_ssd_static_scratch_check(const ssd_dims *dims, int config, void *stream) {
+  if (config < 0 || config >= mamba2_ssd_num_configs(dims)) return SSD_ERR_INVALID_ARG;   // 0 configs: bad dims
+  void *ws = nullptr;
+  const ssd_status st = scratch_address(&ws);
+  if (st != SSD_OK) return st;
+  return mamba2_ssd_bwd_check(dims, config, ws, stream);
 }
 
 }  // extern "C"

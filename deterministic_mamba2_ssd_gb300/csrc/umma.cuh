@@ -312,6 +312,12 @@ __device__ __forceinline__ void prefetch_l2(const void *gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gptr)), "r"(bytes)
                : "memory");
 }
+// Drops one 128-byte line (128-byte aligned address) from L2 without writing
+// it back: its contents become undefined.  For scratch that has been read for
+// the last time before it is overwritten.
+__device__ __forceinline__ void discard_l2_line(const void *gptr) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(gptr)) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

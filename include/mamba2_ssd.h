@@ -242,6 +242,17 @@ ssd_status mamba2_ssd_bwd_static_scratch(const ssd_saved *saved, const void *dou
                                          float *dA, float *dB, float *dC, float *dD, float *dinit, int config,
                                          void *stream);
 
+/* Status of the last mamba2_ssd_bwd_static_scratch call on the current
+ * device: the counterpart of mamba2_ssd_bwd_check for callers that never see
+ * the workspace (the device status word sits at the start of the static
+ * array).  Same results and synchronisation as mamba2_ssd_bwd_check: reads
+ * one word after synchronising `stream`; SSD_ERR_TIMEOUT or
+ * SSD_ERR_UNSUPPORTED mean the gradients of that call are invalid.  dims and
+ * config must be those of the call being checked.  The cached address of the
+ * array is only valid in the device context it was looked up in: after
+ * cudaDeviceReset neither static-scratch entry point may be called again. */
+ssd_status mamba2_ssd_static_scratch_check(const ssd_dims *dims, int config, void *stream);
+
 /* ---- Steps either side of the scan ------------------------------------
  * The step-size preprocessing that Mamba2 folds into its chunk_cumsum (whose
  * backward "Deterministic bwd kernel for mamba2" lists as chunk_cumsum_bwd)

@@ -171,6 +171,10 @@ def test_selftest_and_static_entry_reject_bad_arguments_on_host(L):
     assert L.mamba2_ssd_selftest_umma(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, None) == 1
     assert L.mamba2_ssd_static_scratch_bytes() == 32 << 20
     assert L.mamba2_ssd_bwd_static_scratch(None, None, None, None, None, None, None, None, None, 0, None) == 6
+    # its status check validates dims and config before looking the array up
+    assert L.mamba2_ssd_static_scratch_check(None, 0, None) == 1
+    fused = ssd.make_dims(1, 256, 4, 64, 1, 128, 128)
+    assert L.mamba2_ssd_static_scratch_check(ctypes.byref(fused), 2, None) == 1
 
 
 def test_adjacent_steps_reject_bad_arguments_on_host(L):

@@ -112,7 +112,7 @@ int64_t mamba2_ssd_num_chunks(const ssd_dims *dims) {
 
 size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
   if (!dims_ok(dims)) return 0;
-  return ssd::simt_fwd_workspace(shape_of(dims));
+  return use_fused(dims) ? ssd::fused_fwd_workspace(shape_of(dims)) : ssd::simt_fwd_workspace(shape_of(dims));
 }
 
 int mamba2_ssd_num_configs(const ssd_dims *dims) {
@@ -174,8 +174,7 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   if (!seq_idx && dims->nseq != dims->batch) return SSD_ERR_INVALID_ARG;
   if ((seq_idx != nullptr) != ((dims->flags & SSD_DIMS_SEQ_IDX) != 0)) return SSD_ERR_INVALID_ARG;
   const ssd::Shape s = shape_of(dims);
-  const size_t need = ssd::simt_fwd_workspace(s);
-  if (workspace_bytes < need) return SSD_ERR_WORKSPACE;
+  if (workspace_bytes < mamba2_ssd_fwd_workspace_size(dims)) return SSD_ERR_WORKSPACE;
   if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (seq_idx) {
@@ -197,9 +196,11 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   ssd::Args a{};
   a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.D = D;
   a.init = init_states; a.seq_idx = seq_idx; a.y = y; a.states_out = states;
-  if (ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st) != cudaSuccess) return SSD_ERR_CUDA;
-  // the fused backward takes each saved state as a packed bf16 hi | lo operand pair
-  if (use_fused(dims) && ssd::fused_pack_states(s, states, st) != cudaSuccess) return SSD_ERR_CUDA;
+  // The fused shape family runs the tensor-core forward, which writes each saved state as the
+  // packed bf16 hi | lo operand pair the fused backward takes; every other shape the general one.
+  const cudaError_t err = use_fused(dims) ? ssd::fused_fwd(s, a, workspace, st)
+                                          : ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
+  if (err != cudaSuccess) return SSD_ERR_CUDA;
   saved_out->dims = *dims;
   saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
   saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;

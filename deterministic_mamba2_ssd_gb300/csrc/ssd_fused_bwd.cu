@@ -36,6 +36,7 @@
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
+#include "tile_io.cuh"
 #include "tmap.h"
 #include "umma.cuh"
 
@@ -122,15 +123,6 @@ struct Params {
 __device__ __forceinline__ void ep_sync() { umma::named_bar(1, kEpiThreads); }
 __device__ __forceinline__ void scan_sync() { umma::named_bar(2, 128); }  // warps 8-11 (column quarter 2)
 
-__device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
 
 __device__ __forceinline__ void st_row16_bf16(uint8_t *panel, int r, int c0, const float (&v)[16]) {
 #pragma unroll
@@ -154,24 +146,6 @@ __device__ __forceinline__ void f16x8_to_f32(uint4 u, float *f) {
   }
 }
 
-// v -> bf16 hi + lo (hi = round(v), lo = round(v - hi)) as packed pairs, and
-// both stored as 8 consecutive elements of row r of two 64-column panels
-__device__ __forceinline__ void st8_bf16_hilo(uint8_t *panel_hi, uint8_t *panel_lo, int r, int c0,
-                                              const float (&v)[8]) {
-  uint4 uh, ul;
-  uint32_t *ph = reinterpret_cast<uint32_t *>(&uh), *pl = reinterpret_cast<uint32_t *>(&ul);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
-    ph[i] = *reinterpret_cast<const uint32_t *>(&h);
-    pl[i] = *reinterpret_cast<const uint32_t *>(&l);
-  }
-  const uint32_t off = r * 128 + (((c0 >> 3) ^ (r & 7)) << 4);
-  *reinterpret_cast<uint4 *>(panel_hi + off) = uh;
-  *reinterpret_cast<uint4 *>(panel_lo + off) = ul;
-}
 
 __device__ __forceinline__ void st_row8_f16(uint8_t *panel, int r, int c0, const float (&v)[8]) {
   uint4 u;
@@ -182,10 +156,6 @@ __device__ __forceinline__ void st_row8_f16(uint8_t *panel, int r, int c0, const
   *reinterpret_cast<uint4 *>(panel + r * 128 + chunk * 16) = u;
 }
 
-// 8 consecutive elements (one 16-byte chunk) of row r, columns c0..c0+7 (c0 % 8 == 0)
-__device__ __forceinline__ void ld8_bf16(const uint8_t *panel, int r, int c0, float (&v)[8]) {
-  bf16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
-}
 __device__ __forceinline__ void ld8_f16(const uint8_t *panel, int r, int c0, float (&v)[8]) {
   f16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
 }
@@ -1020,28 +990,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// The saved state of each (batch, chunk, head), as the fused backward takes it:
-// the fp32 (P, N) tile H = hi + lo rounded to a bf16 pair (hi = round(H),
-// lo = round(H - hi)), each half a [n][p] bf16 tile in the 128-byte swizzled
-// layout of a tensor-core operand (row n at n * 128 bytes, its 16-byte chunk
-// j at position j ^ (n & 7)), hi then lo: the same 32 KB per tile, packed in
-// place.  One CTA per tile.
-__global__ void __launch_bounds__(256) pack_states_kernel(float *__restrict__ states) {
-  __shared__ float tile[kP * kN];
-  float *g = states + int64_t(blockIdx.x) * kP * kN;
-  for (int i = threadIdx.x; i < kP * kN / 4; i += blockDim.x)
-    reinterpret_cast<float4 *>(tile)[i] = reinterpret_cast<const float4 *>(g)[i];
-  __syncthreads();
-  uint8_t *out = reinterpret_cast<uint8_t *>(g);
-  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {   // (row n, 8-column group)
-    const int n = i >> 3, c0 = 8 * (i & 7);
-    float v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = tile[(c0 + e) * kN + n];
-    st8_bf16_hilo(out, out + 16384, n, c0, v);
-  }
-}
-
 // fp32 [p][n] view (hi + lo) of packed saved states, for inspection.
 __global__ void __launch_bounds__(256) unpack_states_kernel(const float *__restrict__ packed, float *__restrict__ out) {
   const uint8_t *in = reinterpret_cast<const uint8_t *>(packed + int64_t(blockIdx.x) * kP * kN);
@@ -1087,11 +1035,6 @@ FusedWs carve_fused(Carver &cv, const Shape &s, int ring_depth) {
 }
 
 }  // namespace
-
-cudaError_t fused_pack_states(const Shape &s, float *states, cudaStream_t st) {
-  pack_states_kernel<<<unsigned(s.b * s.nc * s.H), 256, 0, st>>>(states);
-  return cudaGetLastError();
-}
 
 cudaError_t fused_unpack_states(const Shape &s, const float *packed, float *out, cudaStream_t st) {
   unpack_states_kernel<<<unsigned(s.b * s.nc * s.H), 256, 0, st>>>(packed, out);

@@ -1,0 +1,533 @@
+// ssd_fused_fwd.cu -- tensor-core forward of the Mamba2 SSD for the shape
+// family of the fused backward (bf16 inputs, chunk 128, dstate 128, headdim
+// 64, sequence starts at chunk boundaries).
+//
+// The forward is the chunked scan whose backward "Deterministic bwd kernel
+// for mamba2" (Mamba PR #827) breaks down per kernel; its three steps here:
+//   1. chunk states   S_c = sum_t exp(E - Acs_t) dt_t x_t B_t^T      (tcgen05)
+//   2. state passing  H_{c+1} = exp(E_c) H_c + S_c, reset to the initial
+//                     state (or zero) where a sequence starts          (CUDA cores)
+//   3. chunk scan     y_t = sum_{s<=t} (C_t.B_s) exp(Acs_t - Acs_s) dt_s x_s
+//                           + exp(Acs_t) H_c C_t + D x_t               (tcgen05)
+// with Acs the in-chunk cumulative sum of dt*A and E its value at the chunk's
+// last token.  Step 2 writes each state entering a chunk straight into the
+// packed operand form the fused backward copies into shared memory: the bf16
+// pair hi = round(H), lo = round(H - hi), two [n][p] tiles in the 128-byte
+// swizzled layout.
+//
+// Operand precision: B, C, x are the bf16 inputs themselves; every computed
+// operand (w o x, the intra-chunk matrix, the states) enters the tensor cores
+// as a bf16 hi + lo pair, so products keep about 16 significant bits before
+// the fp32 accumulation.  The prefix sums use one fixed shuffle tree per
+// chunk (the same for every launch).
+#include <cstring>
+
+#include "ssd_common.cuh"
+#include "ssd_internal.h"
+#include "tile_io.cuh"
+#include "tmap.h"
+#include "umma.cuh"
+
+namespace ssd {
+
+namespace {
+
+constexpr int kQ = 128, kN = 128, kP = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr long long kWaitCycles = 2000000000LL;  // about one second
+
+// Bounded mbarrier wait (records error bit 2 and gives up after about a
+// second instead of hanging; results are then invalid).
+__device__ __forceinline__ void fwait(uint64_t *b, uint32_t parity, int *err) {
+  if (umma::mbar_try_wait(b, parity)) return;
+  const long long t0 = clock64();
+  while (!umma::mbar_try_wait_sleep(b, parity, 20000u)) {
+    if (clock64() - t0 > kWaitCycles) {
+      if (err) atomicOr(err, 2);
+      return;
+    }
+  }
+}
+
+// 1 KB-aligned start of the dynamic shared memory (the swizzled tiles need it;
+// every launch reserves 1 KB of slack for this).
+__device__ __forceinline__ uint8_t *align1k(uint8_t *p) {
+  const uint32_t a = umma::smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+// K-major / MN-major shared-memory descriptors of K step kk (as in the backward)
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, uint32_t panel_bytes, int kk) {
+  return umma::smem_desc_sw128(base, 16, 1024) + uint64_t((uint32_t(kk / 64) * panel_bytes + uint32_t(kk % 64) * 2) >> 4);
+}
+__device__ __forceinline__ uint64_t mdesc(uint32_t base, uint32_t panel_bytes, int kk) {
+  return umma::smem_desc_sw128(base, panel_bytes, 1024) + uint64_t((uint32_t(kk) * 128) >> 4);
+}
+
+// Inclusive prefix sum of v over the 128 tokens of a chunk held by the
+// threads [g0, g0 + 128) (thread g0 + t holds token t): shuffle tree inside
+// each warp, then the warp totals of the lower warps added in warp order.
+// wtot: 4 floats of shared memory owned by this group; `sync` is a barrier
+// over every thread that calls this.
+template <class Sync>
+__device__ __forceinline__ float chunk_scan128(float v, float *wtot, int t, Sync sync) {
+  const int lane = t & 31, w = t >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) wtot[w] = v;
+  sync();
+  float pre = 0.f;
+  for (int k = 0; k < w; ++k) pre += wtot[k];
+  return v + pre;
+}
+
+struct FwdParams {
+  Shape s;
+  const float *dt, *A, *D, *init;
+  const int32_t *seq_idx;
+  float *ST;        // (b, nc, H, N, P) fp32: chunk states, transposed, n-major
+  float *decay;     // (b, nc, H): exp(E) of each chunk
+  float *states;    // (b, nc, H) packed 32 KB tiles: the state entering each chunk
+  __nv_bfloat16 *y;
+  int *err;
+};
+
+// =============================================== 1. chunk states (tcgen05) ==
+// One CTA of 128 threads per (batch row, chunk, group); thread t owns token t
+// (and TMEM lane t = state row n for the result).  Per head: w = exp(E - Acs)
+// dt, w o x as a bf16 hi/lo pair in shared memory, S^T = B^T (w o x) on the
+// tensor cores (M = n, N = p, K = t) into one of two TMEM buffers, and the
+// previous head's S^T stored while this head's product runs.
+constexpr uint32_t K1_B = 0;         // B chunk [t][n] bf16, 2 panels
+constexpr uint32_t K1_X = 32768;     // x [t][p] bf16, 2 stages of 16 KB
+constexpr uint32_t K1_WH = 65536;    // (w o x) hi [t][p]
+constexpr uint32_t K1_WL = 81920;    // (w o x) lo
+constexpr uint32_t K1_SMALL = 98304;
+struct K1Small {
+  float wtot[2][4];
+  uint64_t bfull, xfull[2], mma;
+  uint32_t tmem;
+};
+constexpr uint32_t K1_SMEM = K1_SMALL + 256 + 1024;
+
+__global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_x,
+                                                        const __grid_constant__ CUtensorMap tm_b) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *const base = align1k(smem_raw);
+  K1Small *sm = reinterpret_cast<K1Small *>(base + K1_SMALL);
+  const Shape &s = p.s;
+  const int t = threadIdx.x, warp = t >> 5;
+  const int unit = blockIdx.x;
+  const int g = unit % int(s.G), c = (unit / int(s.G)) % int(s.nc), bi = unit / int(s.G * s.nc);
+  const int row0 = bi * int(s.T) + c * kQ;
+  const int hpg = int(s.hpg);
+
+  if (warp == 0) {
+    umma::tmem_alloc(&sm->tmem, 128);
+    umma::tmem_relinquish();
+  }
+  if (t == 0) {
+    umma::mbar_init(&sm->bfull, 1);
+    umma::mbar_init(&sm->xfull[0], 1);
+    umma::mbar_init(&sm->xfull[1], 1);
+    umma::mbar_init(&sm->mma, 1);
+    umma::fence_mbar_init();
+    umma::mbar_expect_tx(&sm->bfull, 32768);
+    for (int j = 0; j < 2; ++j)
+      umma::tma_load_2d(base + K1_B + j * 16384, &tm_b, g * kN + j * 64, row0, &sm->bfull);
+    for (int k = 0; k < 2 && k < hpg; ++k) {
+      umma::mbar_expect_tx(&sm->xfull[k], 16384);
+      umma::tma_load_2d(base + K1_X + k * 16384, &tm_x, (g * hpg + k) * kP, row0, &sm->xfull[k]);
+    }
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = sm->tmem;
+  const uint32_t lane_off = uint32_t(32 * warp) << 16;
+  const uint32_t aB = umma::smem_u32(base + K1_B), aWh = umma::smem_u32(base + K1_WH),
+                 aWl = umma::smem_u32(base + K1_WL);
+  constexpr uint32_t id_mm64 = umma::idesc_bf16_f32(128, 64, 1, 1);
+
+  // S^T of head k from TMEM buffer k & 1 to ST (row n = t: 64 contiguous floats)
+  auto store_state = [&](int k) {
+    const int64_t h = int64_t(g) * hpg + k;
+    float *o = p.ST + (((int64_t(bi) * s.nc + c) * s.H + h) * kN + t) * kP;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float v[16];
+      umma::tmem_ld16(tmem + lane_off + 64 * (k & 1) + 16 * j, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        __stcg(reinterpret_cast<float4 *>(o + 16 * j + 4 * i), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+    }
+  };
+
+  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + g * hpg);
+  for (int k = 0; k < hpg; ++k) {
+    const int64_t h = int64_t(g) * hpg + k;
+    const float dtv = dt_next;
+    if (k + 1 < hpg) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
+    const float Ah = __ldg(p.A + h) * kLog2e;
+    float *wt = sm->wtot[k & 1];
+    const float cum = chunk_scan128(dtv, wt, t, [] { __syncthreads(); });
+    const float cumE = ((wt[0] + wt[1]) + wt[2]) + wt[3];   // the same bits as token 127's cum
+    const float w = umma::ex2_approx((cumE - cum) * Ah) * dtv;   // exp(E - Acs_t) dt_t
+    if (t == 0) __stcg(p.decay + (int64_t(bi) * s.nc + c) * s.H + h, umma::ex2_approx(cumE * Ah));
+    fwait(&sm->xfull[k & 1], uint32_t((k >> 1) & 1), p.err);
+    if (k >= 1) {
+      fwait(&sm->mma, uint32_t((k - 1) & 1), p.err);   // the product of head k-1 has read w o x
+      umma::fence_after_sync();
+    }
+    {
+      const uint8_t *xs = base + K1_X + (k & 1) * 16384;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float v[8];
+        ld8_bf16(xs, t, 8 * c8, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] *= w;
+        st8_bf16_hilo(base + K1_WH, base + K1_WL, t, 8 * c8, v);
+      }
+    }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+    if (t == 0) {
+      if (k + 2 < hpg) {   // x of head k has been read: stage k & 1 takes head k + 2
+        umma::mbar_expect_tx(&sm->xfull[k & 1], 16384);
+        umma::tma_load_2d(base + K1_X + (k & 1) * 16384, &tm_x, int(h + 2) * kP, row0, &sm->xfull[k & 1]);
+      }
+      if (k == 0) fwait(&sm->bfull, 0, p.err);
+      umma::fence_after_sync();
+      for (int part = 0; part < 2; ++part)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + 64 * (k & 1), mdesc(aB, 16384, kk), mdesc(part ? aWl : aWh, 16384, kk), id_mm64,
+                         (part > 0) || (kk > 0));
+      umma::mma_commit(&sm->mma);
+    }
+    __syncwarp();
+    if (k >= 1) store_state(k - 1);   // its product completed before this head's w o x was written
+    umma::fence_before_sync();
+  }
+  fwait(&sm->mma, uint32_t((hpg - 1) & 1), p.err);
+  umma::fence_after_sync();
+  store_state(hpg - 1);
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, 128);
+  }
+}
+
+// ============================================ 2. state passing (CUDA cores) ==
+// Thread per (batch row, head, state row n, 8 consecutive p); serial over
+// chunks: the state entering chunk c (the initial state or zero where chunk c
+// starts a sequence) is written in packed form, then carried:
+// H <- exp(E_c) H + S_c.
+__global__ void __launch_bounds__(256) fwd_pass_kernel(const FwdParams p) {
+  const Shape &s = p.s;
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= s.b * s.H * kN * 8) return;
+  const int oct = int(idx & 7), n = int((idx >> 3) % kN);
+  const int64_t h = (idx >> 3) / kN % s.H, bi = (idx >> 3) / (kN * s.H);
+  const int p0 = 8 * oct;
+  float carry[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) carry[i] = 0.f;
+  const float *st = p.ST + ((bi * s.nc * s.H + h) * kN + n) * kP + p0;   // chunk 0
+  float4 s0 = __ldcs(reinterpret_cast<const float4 *>(st)), s1 = __ldcs(reinterpret_cast<const float4 *>(st + 4));
+  for (int64_t c = 0; c < s.nc; ++c) {
+    const int64_t t0 = c * kQ;
+    if (is_seq_start(p.seq_idx, bi, s.T, t0)) {
+      const float *in = p.init ? p.init + ((seq_of(p.seq_idx, bi, s.T, t0) * s.H + h) * kP + p0) * kN + n : nullptr;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) carry[i] = in ? __ldg(in + i * kN) : 0.f;
+    }
+    uint8_t *tile = reinterpret_cast<uint8_t *>(p.states + ((bi * s.nc + c) * s.H + h) * (kP * kN));
+    st8_bf16_hilo(tile, tile + 16384, n, p0, carry);
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    if (c + 1 < s.nc) {   // next chunk's S in flight while this one is folded in
+      const float *nx = st + (c + 1) * s.H * kN * kP;
+      s0 = __ldcs(reinterpret_cast<const float4 *>(nx));
+      s1 = __ldcs(reinterpret_cast<const float4 *>(nx + 4));
+    }
+    const float e = __ldg(p.decay + (bi * s.nc + c) * s.H + h);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) carry[i] = fmaf(e, carry[i], sv[i]);
+  }
+}
+
+// ================================================= 3. chunk scan (tcgen05) ==
+// One CTA of 256 threads per (batch row, chunk, group).  Warp w handles TMEM
+// lane quadrant q = w % 4 (tokens 32q..32q+31) and half w / 4 of the columns.
+// Per head: the intra-chunk matrix M'[t,s] = (C_t.B_s) exp(Acs_t - Acs_s) dt_s
+// for s <= t (plus D on the diagonal, which folds the skip term into the
+// product) as a bf16 hi/lo pair; Y = M' x and C H (saved state, packed pair)
+// on the tensor cores; y = Y + exp(Acs_t) (C H)_t, stored while the next
+// head's products run.  TMEM: C B^T (columns 0-127), then two head buffers of
+// 128 columns (Y at +0, C H at +64).
+constexpr uint32_t K3_B = 0, K3_C = 32768;   // [t][n] bf16, 2 panels each
+constexpr uint32_t K3_X = 65536;             // x [t][p], 2 stages of 16 KB
+constexpr uint32_t K3_H = 98304;             // packed states, 2 stages of 32 KB (hi | lo)
+constexpr uint32_t K3_MH = 163840;           // M' hi [t][s], 2 panels
+constexpr uint32_t K3_ML = 196608;           // M' lo
+constexpr uint32_t K3_SMALL = 229376;
+struct K3Small {
+  float a2[kQ];      // Acs in log2 units, current head
+  float dtv[kQ];     // step sizes, current head
+  float wtot[2][2][4];
+  uint64_t bcfull, cbdone, xfull[2], hfull[2], mma;
+  uint32_t tmem;
+};
+constexpr uint32_t K3_SMEM = K3_SMALL + 1536 + 1024;
+static_assert(sizeof(K3Small) <= 1536, "small region");
+static_assert(K3_SMEM <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_x,
+                                                          const __grid_constant__ CUtensorMap tm_b,
+                                                          const __grid_constant__ CUtensorMap tm_c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *const base = align1k(smem_raw);
+  K3Small *sm = reinterpret_cast<K3Small *>(base + K3_SMALL);
+  const Shape &s = p.s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3, half = warp >> 2;
+  const int r = 32 * q + lane;   // token row of this thread
+  const int unit = blockIdx.x;
+  const int g = unit % int(s.G), c = (unit / int(s.G)) % int(s.nc), bi = unit / int(s.G * s.nc);
+  const int row0 = bi * int(s.T) + c * kQ;
+  const int hpg = int(s.hpg);
+  const float *states = p.states + ((int64_t(bi) * s.nc + c) * s.H + int64_t(g) * hpg) * (kP * kN);
+
+  if (warp == 0) {
+    umma::tmem_alloc(&sm->tmem, 512);
+    umma::tmem_relinquish();
+  }
+  if (tid == 0) {
+    umma::mbar_init(&sm->bcfull, 1);
+    umma::mbar_init(&sm->cbdone, 1);
+    for (int j = 0; j < 2; ++j) {
+      umma::mbar_init(&sm->xfull[j], 1);
+      umma::mbar_init(&sm->hfull[j], 1);
+    }
+    umma::mbar_init(&sm->mma, 1);
+    umma::fence_mbar_init();
+    umma::mbar_expect_tx(&sm->bcfull, 65536);
+    for (int j = 0; j < 2; ++j) {
+      umma::tma_load_2d(base + K3_B + j * 16384, &tm_b, g * kN + j * 64, row0, &sm->bcfull);
+      umma::tma_load_2d(base + K3_C + j * 16384, &tm_c, g * kN + j * 64, row0, &sm->bcfull);
+    }
+    for (int k = 0; k < 2 && k < hpg; ++k) {
+      umma::mbar_expect_tx(&sm->xfull[k], 16384);
+      umma::tma_load_2d(base + K3_X + k * 16384, &tm_x, (g * hpg + k) * kP, row0, &sm->xfull[k]);
+      umma::mbar_expect_tx(&sm->hfull[k], kP * kN * 4);
+      umma::bulk_load(base + K3_H + k * 32768, states + int64_t(k) * kP * kN, kP * kN * 4, &sm->hfull[k]);
+    }
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = sm->tmem;
+  const uint32_t lane_off = uint32_t(32 * q) << 16;
+  const uint32_t aB = umma::smem_u32(base + K3_B), aC = umma::smem_u32(base + K3_C);
+  const uint32_t aMh = umma::smem_u32(base + K3_MH), aMl = umma::smem_u32(base + K3_ML);
+  constexpr uint32_t id_kk128 = umma::idesc_bf16_f32(128, 128, 0, 0);
+  constexpr uint32_t id_km64 = umma::idesc_bf16_f32(128, 64, 0, 1);
+  if (tid == 0) {
+    fwait(&sm->bcfull, 0, p.err);
+    umma::fence_after_sync();
+    for (int kk = 0; kk < kN; kk += 16) umma::mma_bf16(tmem, kdesc(aC, 16384, kk), kdesc(aB, 16384, kk), id_kk128, kk > 0);
+    umma::mma_commit(&sm->cbdone);
+  }
+  __syncwarp();
+  if (lane == 0) fwait(&sm->cbdone, 0, p.err);
+  __syncwarp();
+  umma::fence_after_sync();
+
+  // y of head k from TMEM buffer k & 1: this thread's row, 32 columns
+  auto store_y = [&](int k, float eacs) {
+    const int64_t h = int64_t(g) * hpg + k;
+    const uint32_t buf = 128 + 128 * uint32_t(k & 1);
+    __nv_bfloat16 *o = p.y + (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float yv[16], ch[16];
+      umma::tmem_ld16(tmem + lane_off + buf + 32 * half + 16 * j, yv);
+      umma::tmem_ld16(tmem + lane_off + buf + 64 + 32 * half + 16 * j, ch);
+      uint4 u[2];
+      __nv_bfloat162 *hb = reinterpret_cast<__nv_bfloat162 *>(u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        hb[i] = __floats2bfloat162_rn(fmaf(eacs, ch[2 * i], yv[2 * i]), fmaf(eacs, ch[2 * i + 1], yv[2 * i + 1]));
+      *reinterpret_cast<uint4 *>(o + 16 * j) = u[0];
+      *reinterpret_cast<uint4 *>(o + 16 * j + 8) = u[1];
+    }
+  };
+
+  float eacs_prev = 0.f;
+  const int grp = tid >> 7, t = tid & 127;   // two groups of 128 threads run the same scan
+  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + g * hpg);
+  for (int k = 0; k < hpg; ++k) {
+    const int64_t h = int64_t(g) * hpg + k;
+    const float dtv = dt_next;
+    if (k + 1 < hpg) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
+    const float Ah = __ldg(p.A + h) * kLog2e, Dh = __ldg(p.D + h);
+    // ---- step sizes: cumulative decay (both groups compute identical bits)
+    const float cum = chunk_scan128(dtv, sm->wtot[k & 1][grp], t, [] { __syncthreads(); });
+    const float a2t = cum * Ah;
+    if (grp == 0) {
+      sm->a2[t] = a2t;
+      sm->dtv[t] = dtv;
+    }
+    if (k >= 1 && lane == 0) fwait(&sm->mma, uint32_t((k - 1) & 1), p.err);   // head k-1 products done
+    __syncwarp();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const float a2r = sm->a2[r];
+    const float eacs = umma::ex2_approx(a2r);
+
+    // ---- M' of this head: blocks of 16 columns j = half, half + 2, ... (balanced within a quadrant)
+#pragma unroll
+    for (int jb = 0; jb < 4; ++jb) {
+      const int s0 = 16 * (2 * jb + half);
+      uint8_t *ph = base + K3_MH + (s0 >> 6) * 16384, *pl = base + K3_ML + (s0 >> 6) * 16384;
+      const int cc = s0 & 63;
+      if (s0 > 32 * q + 31) {   // strictly above the diagonal for the whole quadrant
+        const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st8_bf16_hilo(ph, pl, r, cc, z);
+        st8_bf16_hilo(ph, pl, r, cc + 8, z);
+        continue;
+      }
+      float cb[16];
+      umma::tmem_ld16(tmem + lane_off + s0, cb);
+#pragma unroll
+      for (int e8 = 0; e8 < 2; ++e8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int sc = s0 + 8 * e8 + i;
+          const float m = (sc <= r) ? cb[8 * e8 + i] * umma::ex2_approx(a2r - sm->a2[sc]) * sm->dtv[sc] : 0.f;
+          v[i] = (sc == r) ? m + Dh : m;
+        }
+        st8_bf16_hilo(ph, pl, r, cc + 8 * e8, v);
+      }
+    }
+    umma::fence_proxy_async_smem();
+    umma::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      // products of head k: C H and Y = M' x into buffer k & 1
+      const uint32_t buf = 128 + 128 * uint32_t(k & 1);
+      const uint32_t aH = umma::smem_u32(base + K3_H + (k & 1) * 32768);
+      const uint32_t aX = umma::smem_u32(base + K3_X + (k & 1) * 16384);
+      fwait(&sm->hfull[k & 1], uint32_t((k >> 1) & 1), p.err);
+      fwait(&sm->xfull[k & 1], uint32_t((k >> 1) & 1), p.err);
+      umma::fence_after_sync();
+      for (int part = 0; part < 2; ++part)
+        for (int kk = 0; kk < kN; kk += 16)
+          umma::mma_bf16(tmem + buf + 64, kdesc(aC, 16384, kk), mdesc(aH + part * 16384, 16384, kk), id_km64,
+                         (part > 0) || (kk > 0));
+      for (int part = 0; part < 2; ++part)
+        for (int kk = 0; kk < kQ; kk += 16)
+          umma::mma_bf16(tmem + buf, kdesc(part ? aMl : aMh, 16384, kk), mdesc(aX, 16384, kk), id_km64,
+                         (part > 0) || (kk > 0));
+      umma::mma_commit(&sm->mma);
+    }
+    __syncwarp();
+    // ---- y of the previous head while this head's products run
+    if (k >= 1) store_y(k - 1, eacs_prev);
+    eacs_prev = eacs;
+    umma::fence_before_sync();
+    __syncthreads();
+    if (tid == 0 && k >= 1 && k + 1 < hpg) {
+      // head k-1's products are done (waited above): its x and H stages take head k + 1
+      const int st = (k + 1) & 1;
+      umma::mbar_expect_tx(&sm->xfull[st], 16384);
+      umma::tma_load_2d(base + K3_X + st * 16384, &tm_x, int(h + 1) * kP, row0, &sm->xfull[st]);
+      umma::mbar_expect_tx(&sm->hfull[st], kP * kN * 4);
+      umma::bulk_load(base + K3_H + st * 32768, states + int64_t(k + 1) * kP * kN, kP * kN * 4, &sm->hfull[st]);
+      if (k + 2 < hpg) {
+        umma::tma_prefetch_2d(&tm_x, int(h + 2) * kP, row0);
+        umma::prefetch_l2(states + int64_t(k + 2) * kP * kN, kP * kN * 4);
+      }
+    }
+  }
+  if (lane == 0) fwait(&sm->mma, uint32_t((hpg - 1) & 1), p.err);
+  __syncwarp();
+  umma::fence_after_sync();
+  store_y(hpg - 1, eacs_prev);
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    umma::fence_after_sync();
+    umma::tmem_dealloc(tmem, 512);
+  }
+}
+
+struct FwdWs {
+  int *status;
+  float *ST, *decay;
+};
+
+FwdWs carve_fwd_fused(Carver &cv, const Shape &s) {
+  FwdWs w;
+  w.status = cv.take<int>(64);
+  w.ST = cv.take<float>(s.b * s.nc * s.H * kN * kP);
+  w.decay = cv.take<float>(s.b * s.nc * s.H);
+  return w;
+}
+
+}  // namespace
+
+size_t fused_fwd_workspace(const Shape &s) {
+  Carver cv(nullptr);
+  carve_fwd_fused(cv, s);
+  return cv.bytes();
+}
+
+cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st) {
+  Carver cv(ws);
+  FwdWs w = carve_fwd_fused(cv, s);
+  CUtensorMap tm_x, tm_b, tm_c;
+  const uint64_t rows = uint64_t(s.b * s.T);
+  if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
+                    128, true) ||
+      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+                    128, true) ||
+      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+                    128, true))
+    return cudaErrorInvalidValue;
+  cudaError_t err = cudaMemsetAsync(w.status, 0, 64 * sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.s = s;
+  p.dt = a.dt;
+  p.A = a.A;
+  p.D = a.D;
+  p.init = a.init;
+  p.seq_idx = a.seq_idx;
+  p.ST = w.ST;
+  p.decay = w.decay;
+  p.states = a.states_out;
+  p.y = static_cast<__nv_bfloat16 *>(a.y);
+  p.err = w.status;
+  if ((err = cudaFuncSetAttribute(fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_SMEM)) !=
+          cudaSuccess ||
+      (err = cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM)) !=
+          cudaSuccess)
+    return err;
+  const unsigned units = unsigned(s.b * s.nc * s.G);
+  fwd_state_kernel<<<units, 128, K1_SMEM, st>>>(p, tm_x, tm_b);
+  fwd_pass_kernel<<<unsigned((s.b * s.H * kN * 8 + 255) / 256), 256, 0, st>>>(p);
+  fwd_scan_kernel<<<units, 256, K3_SMEM, st>>>(p, tm_x, tm_b, tm_c);
+  return cudaGetLastError();
+}
+
+}  // namespace ssd

@@ -26,12 +26,15 @@ struct FusedOptions {
   int64_t silent_chunk = -1;       // fault injection: units of this chunk never publish
 };
 bool fused_bwd_supported(const Shape &s, bool bf16);
-// Saved states of the fused family: fp32 (P, N) tiles packed in place into the
-// bf16 hi | lo operand tiles the fused backward copies straight into shared
-// memory (same 32 KB per tile), and the fp32 view of them (hi + lo).
-cudaError_t fused_pack_states(const Shape &s, float *states, cudaStream_t st);
+// Saved states of the fused family are the bf16 hi | lo operand tiles the
+// fused backward copies straight into shared memory (32 KB per (P, N) tile,
+// written by fused_fwd); this gives the fp32 view of them (hi + lo).
 cudaError_t fused_unpack_states(const Shape &s, const float *packed, float *out, cudaStream_t st);
 size_t fused_bwd_workspace(const Shape &s, int ring_depth);
+// Tensor-core forward of the same family: y, and the states entering each
+// chunk written directly in the packed form above.
+size_t fused_fwd_workspace(const Shape &s);
+cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st);
 cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
 
 }  // namespace ssd

@@ -1,0 +1,45 @@
+// tile_io.cuh -- element access to the 128-byte swizzled bf16 operand
+// panels shared by the fused kernels: rows of 128 bytes (64 bf16), the
+// 16-byte chunk j of row r stored at position j ^ (r % 8).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ssd {
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 u, float *f) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// v -> bf16 hi + lo (hi = round(v), lo = round(v - hi)) as packed pairs, and
+// both stored as 8 consecutive elements of row r of two 64-column panels
+__device__ __forceinline__ void st8_bf16_hilo(uint8_t *panel_hi, uint8_t *panel_lo, int r, int c0,
+                                              const float (&v)[8]) {
+  uint4 uh, ul;
+  uint32_t *ph = reinterpret_cast<uint32_t *>(&uh), *pl = reinterpret_cast<uint32_t *>(&ul);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+    ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+    pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+  }
+  const uint32_t off = r * 128 + (((c0 >> 3) ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4 *>(panel_hi + off) = uh;
+  *reinterpret_cast<uint4 *>(panel_lo + off) = ul;
+}
+
+// 8 consecutive elements (one 16-byte chunk) of row r, columns c0..c0+7 (c0 % 8 == 0)
+__device__ __forceinline__ void ld8_bf16(const uint8_t *panel, int r, int c0, float (&v)[8]) {
+  bf16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
+}
+
+}  // namespace ssd

@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
+    ap.add_argument("--no-others", action="store_true", help="skip the other workload presets")
     ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd"],
                     help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()
@@ -155,6 +156,30 @@ def api_bytes(w, es):
     return rd + wr
 
 
+def algorithmic_flops(w):
+    """Tensor-core FLOPs of one backward (elementwise work excluded): per
+    (batch, chunk, head) the two Q x Q x P products (g x^T and the intra-chunk
+    dx) and the four Q x N x P products (state dx, dHscan, inter-chunk dC,
+    state dB); per (batch, chunk, group) the three Q x Q x N products (C B^T
+    and the head-summed intra-chunk dC and dB)."""
+    b, T, H, P, G, N, Q = w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk
+    nc = -(-T // Q)
+    per_head = 2 * Q * Q * P * 2 + 2 * Q * N * P * 4
+    per_group = 2 * Q * Q * N * 3
+    return b * nc * (H * per_head + G * per_group)
+
+
+def north_star_roofline(w, es, ms, tensor_peak_tflops):
+    """The slower of HBM bytes at 8 TB/s and tensor FLOPs at the tensor peak,
+    as a fraction of the measured backward time."""
+    t_hbm = api_bytes(w, es) / 8e12
+    t_tc = algorithmic_flops(w) / (tensor_peak_tflops * 1e12)
+    bound = max(t_hbm, t_tc)
+    return {"bound": "hbm" if t_hbm >= t_tc else "tensor", "t_hbm_us": t_hbm * 1e6, "t_tensor_us": t_tc * 1e6,
+            "roofline_us": bound * 1e6, "frac": bound / (ms / 1e3), "algorithmic_bytes": api_bytes(w, es),
+            "algorithmic_flops": algorithmic_flops(w), "hbm_tbps": 8.0, "tensor_peak_tflops": tensor_peak_tflops}
+
+
 def kernel_bytes(name, w, es):
     """Algorithmic bytes of one launch of a kernel of the general path: the
     arrays it must read and write, each once."""
@@ -218,6 +243,33 @@ def load_peaks():
         return float(p["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def load_tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: the backward is one short kernel)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def cpu_model():
+    """Model name of the host CPU (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
 
 
 # ------------------------------------------------------- CPU oracle ----
@@ -359,6 +411,56 @@ def run_adjacent(args):
     return 0
 
 
+# ------------------------------------------------- other workloads ----
+def time_workload(ssd, name, dev, steps, warmup=3, repeats=5):
+    """Backward (and forward) time of another workload preset, inputs resident
+    in HBM, L2 flushed between steps; bitwise repeat over `repeats` runs."""
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS[name]
+    es = 2 if w.dtype == torch.bfloat16 else 4
+    d = workload_inputs(name)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def fwd():
+        return ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk, seq_idx=g["seq_idx"],
+                       init_states=g["init"])
+    y, saved = fwd()
+    out = ssd.bwd(saved, g["dout"])
+    ws = torch.empty(max(16, ssd.bwd_workspace_size(saved.dims, 0, 0)), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        flush.fill_(1.0)
+        ssd.bwd(saved, g["dout"], out=out, workspace=ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        flush.fill_(1.0)
+        a.record()
+        ssd.bwd(saved, g["dout"], out=out, workspace=ws)
+        b.record()
+    fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(max(2, steps // 2))]
+    for a, b in fe:
+        flush.fill_(1.0)
+        a.record()
+        fwd()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fe)
+    ref = {k: v.view(torch.int32).clone() for k, v in out.items()}
+    same = 0
+    for _ in range(repeats):
+        o = ssd.bwd(saved, g["dout"], workspace=ws)
+        same += all(torch.equal(ref[k], v.view(torch.int32)) for k, v in o.items())
+    peak, peak_kind = load_peaks()
+    tpeak, _ = load_tensor_peak()
+    tokens = w.batch * w.seqlen
+    return {"workload": name, "launch_config": ssd.config_name(saved.dims, 0), "bwd_ms": ms,
+            "tokens_per_s": tokens / (ms / 1e3), "fwd_ms": fwd_ms, "steps": steps,
+            "bwd_hbm_frac": api_bytes(w, es) / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
+            "north_star_roofline": north_star_roofline(w, es, ms, tpeak),
+            "bitwise_equal_repeats": "%d/%d" % (same, repeats)}
+
+
 # ------------------------------------------------------------- ours ----
 def main():
     args = parse()
@@ -383,6 +485,15 @@ def main():
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
                        seq_idx=g["seq_idx"], init_states=g["init"])
+    # the forward that produces the saved states (untimed by the metric), timed on its own
+    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+    for a, b in fwd_ev:
+        a.record()
+        y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
+                           seq_idx=g["seq_idx"], init_states=g["init"])
+        b.record()
+    torch.cuda.synchronize()
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev[1:])
     out = ssd.bwd(saved, g["dout"], config=args.config, variant=args.variant)
     ws = torch.empty(max(16, ssd.bwd_workspace_size(saved.dims, args.config, args.variant)), dtype=torch.uint8,
                      device=dev)
@@ -558,14 +669,28 @@ def main():
                "serial_ms_per_step_median": serial_med}
         del sets
 
+    # the other workload presets (the 2K and 4K rows of the pages' tables and the packed
+    # variable-length batch), timed after the headline run, single GPU only
+    others = None
+    if world == 1 and not args.no_others and args.workload == "bf16_T16384":
+        others = [time_workload(ssd, n, dev, steps=st) for n, st in
+                  (("bf16_T2048", 20), ("bf16_T4096", 20), ("bf16_varlen_T32768", 2))]
+
     line = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             v, secs, nt = oracle_tokens_per_s(w, args.cpu_sample_tokens)
-            cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle",
+            cpu = {"value": v, "unit": UNIT, "cores": nt, "kind": "oracle", "cpu_model": cpu_model(),
                    "sample": "first %d tokens of the workload, all %d heads, fp64 forward+backward, %.1f s" %
                              (min(args.cpu_sample_tokens, w.seqlen), w.nheads, secs)}
+            # one thread on the 2K workload (a 512-token sample of it)
+            from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS
+            w1 = WORKLOADS["bf16_T2048"]
+            v1, secs1, _ = oracle_tokens_per_s(w1, 512, nthreads=1)
+            cpu["one_thread"] = {"value": v1, "unit": UNIT, "threads": 1,
+                                 "sample": "first 512 tokens of bf16_T2048, all %d heads, fp64 forward+backward, "
+                                           "%.1f s" % (w1.nheads, secs1)}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -580,7 +705,9 @@ def main():
                          "frac": (achieved / peak) if achieved else None,
                          "traffic": fused_traffic(w.batch * w.seqlen) if ndom == "fused_bwd" else None,
                          "algorithmic_bytes_per_launch": alg, "launch_ms": dom_ms},
-            "bwd_roofline_8TBps_frac": (api_bytes(w, es) / 8e12) / (ms_max / 1e3),
+            "north_star_roofline": north_star_roofline(w, es, ms_max, load_tensor_peak()[0]),
+            "fwd_ms": fwd_ms,
+            "other_workloads": others,
             "kernel_share": shares,
             "gpu_launches": nl * args.steps,
             "bitwise_repeat": determinism,

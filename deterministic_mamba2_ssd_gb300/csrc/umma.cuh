@@ -291,6 +291,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                "r"(c0), "r"(c1), "r"(smem_u32(src))
                : "memory");
 }
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from shared to global memory (bulk-group completion).
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared-memory sources of all committed stores have been read.
 __device__ __forceinline__ void tma_store_wait_read() {

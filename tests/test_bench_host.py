@@ -32,3 +32,30 @@ def test_peaks_from_the_measured_file_or_fallback(tmp_path, monkeypatch):
     assert bench.load_peaks() == (6800.0, "fallback")
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6784.2}))
     assert bench.load_peaks() == (6784.2, "measured")
+
+
+def test_algorithmic_flops_of_the_pages_workloads():
+    # per (chunk, head): 2 Q^2 P x 2 + 2 Q N P x 4; per (chunk, group): 2 Q^2 N x 3
+    w = WORKLOADS["bf16_T16384"]
+    per_head = 2 * 128 * 128 * 64 * 2 + 2 * 128 * 128 * 64 * 4
+    per_group = 2 * 128 * 128 * 128 * 3
+    assert bench.algorithmic_flops(w) == 128 * (256 * per_head + 8 * per_group)
+    assert bench.algorithmic_flops(w) / 1e9 == pytest.approx(425.2, abs=0.05)
+    assert bench.algorithmic_flops(WORKLOADS["bf16_varlen_T32768"]) / 1e9 == pytest.approx(837.5, abs=0.05)
+
+
+def test_north_star_roofline_takes_the_slower_bound():
+    w = WORKLOADS["bf16_T16384"]
+    r = bench.north_star_roofline(w, 2, 1.0, 1950.0)
+    assert r["bound"] == "hbm" and r["t_hbm_us"] == pytest.approx(432.0, abs=0.1)
+    assert r["t_tensor_us"] == pytest.approx(218.1, abs=0.1)
+    assert r["frac"] == pytest.approx(0.432, abs=1e-3)
+    v = bench.north_star_roofline(WORKLOADS["bf16_varlen_T32768"], 2, 1.0, 1950.0)
+    assert v["bound"] == "tensor" and v["roofline_us"] == pytest.approx(429.5, abs=0.2)
+
+
+def test_tensor_peak_from_the_measured_file_or_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_tensor_peak() == (1900.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1872.3}))
+    assert bench.load_tensor_peak() == (1872.3, "measured")

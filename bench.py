@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
     ap.add_argument("--no-others", action="store_true", help="skip the other workload presets")
-    ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd"],
+    ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd", "conv1d_bwd"],
                     help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()
 
@@ -340,7 +340,42 @@ def run_adjacent(args):
     es = 2 if w.dtype == torch.bfloat16 else 4
     rows = w.batch * w.seqlen
     gen = torch.Generator().manual_seed(4321)
-    if args.op == "dt_bwd":
+    atomic_step = None
+    if args.op == "conv1d_bwd":
+        # the conv before the scan on the same workload: its channels are the scan's x, B and C
+        # concatenated (nheads * headdim + 2 * ngroups * dstate), width 4, silu
+        from deterministic_mamba2_ssd_gb300.inputs import make_conv_inputs
+        C = w.nheads * w.headdim + 2 * w.ngroups * w.dstate
+        cd = make_conv_inputs(w.batch, w.seqlen, C, 4, dtype=w.dtype, seed=4321, seq_lens=w.seq_lens)
+        cg = {k: (v.to(dev) if v is not None else None) for k, v in cd.items()}
+        n = w.batch * w.seqlen * C
+        dxc = torch.empty((w.batch, w.seqlen, C), dtype=torch.float32, device=dev)
+        dwc = torch.empty_like(cg["w"])
+        dbc = torch.empty_like(cg["bias"])
+        need = ssd.lib().mamba2_ssd_conv1d_bwd_workspace_size(w.batch, w.seqlen, C, 4)
+        wsc = torch.empty(max(16, need), dtype=torch.uint8, device=dev)
+        import ctypes
+        st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        dtc = 1 if w.dtype == torch.bfloat16 else 0
+
+        def conv_step(variant):
+            rc = ssd.lib().mamba2_ssd_conv1d_bwd(w.batch, w.seqlen, C, 4, dtc, 1, ptr(cg["x"]), ptr(cg["w"]),
+                                                 ptr(cg["bias"]), ptr(cg["seq_idx"]), ptr(cg["dy"]), ptr(dxc),
+                                                 ptr(dwc), ptr(dbc), ptr(wsc), wsc.numel(), 0, variant, st)
+            if rc:
+                raise ssd.SsdError(rc, "mamba2_ssd_conv1d_bwd")
+
+        def step():
+            conv_step(0)
+
+        def atomic_step():
+            conv_step(1)
+        alg = 2 * n * es + n * 4 + 2 * C * 4 * 4 + 2 * C * 4
+        launches = 2
+        kernel = "conv1d_bwd"
+        dtype = "bf16" if es == 2 else "f32"
+    elif args.op == "dt_bwd":
         raw = (torch.randn((rows, w.nheads), generator=gen) - 4.0).to(dev)
         bias = torch.randn((w.nheads,), generator=gen).to(dev)
         ddt = torch.randn((rows, w.nheads), generator=gen).to(dev)
@@ -397,6 +432,18 @@ def run_adjacent(args):
     ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), world, dev)
     peak, peak_kind = load_peaks()
     achieved = alg / (ms / 1e3) / 1e9
+    det_vs_atomic = None
+    if atomic_step is not None:
+        ta = []
+        for _ in range(max(3, args.steps // 2)):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            atomic_step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ta.append(a.elapsed_time(b))
+        det_vs_atomic = {"det_ms": ms, "atomic_ms": statistics.mean(ta), "overhead": ms / statistics.mean(ta) - 1.0}
     if rank == 0:
         print(json.dumps({
             "metric": "%s tokens/s @ seqlen %d" % (kernel, w.seqlen), "value": world * rows / (ms / 1e3),
@@ -407,7 +454,8 @@ def run_adjacent(args):
             "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                          "algorithmic_bytes_per_launch": alg},
-            "gpu_launches": launches * args.steps, "clocks": clocks, "e2e": None, "cpu_baseline": None}))
+            "gpu_launches": launches * args.steps, "clocks": clocks, "e2e": None, "cpu_baseline": None,
+            "deterministic_vs_atomic": det_vs_atomic}))
     return 0
 
 

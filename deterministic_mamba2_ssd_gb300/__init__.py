@@ -16,7 +16,7 @@ import torch
 
 __all__ = ["lib", "fwd", "bwd", "Saved", "SsdError", "make_dims", "num_configs", "config_name",
            "bwd_workspace_size", "fwd_workspace_size", "bwd_num_launches", "bwd_launch_names", "LIB_PATH",
-           "dt_fwd", "dt_bwd", "gate_fwd", "gate_bwd", "SSDFunction", "ssd"]
+           "dt_fwd", "dt_bwd", "gate_fwd", "gate_bwd", "conv1d_fwd", "conv1d_bwd", "SSDFunction", "ssd"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmamba2_ssd.so")
 
@@ -107,6 +107,15 @@ def lib():
         L.mamba2_ssd_gate_fwd.restype = ci
         L.mamba2_ssd_gate_bwd.argtypes = [i64, ctypes.c_int32, vp, vp, vp, vp, vp, vp]
         L.mamba2_ssd_gate_bwd.restype = ci
+        i32 = ctypes.c_int32
+        L.mamba2_ssd_conv1d_num_configs.argtypes = []
+        L.mamba2_ssd_conv1d_num_configs.restype = ci
+        L.mamba2_ssd_conv1d_fwd.argtypes = [i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, ci, vp]
+        L.mamba2_ssd_conv1d_fwd.restype = ci
+        L.mamba2_ssd_conv1d_bwd_workspace_size.argtypes = [i64, i64, i64, i32]
+        L.mamba2_ssd_conv1d_bwd_workspace_size.restype = sz
+        L.mamba2_ssd_conv1d_bwd.argtypes = [i64, i64, i64, i32, i32, i32] + [vp] * 9 + [sz, ci, ci, vp]
+        L.mamba2_ssd_conv1d_bwd.restype = ci
         _lib = L
     return _lib
 
@@ -338,6 +347,52 @@ def gate_bwd(y, z, dout, stream=None):
     if rc:
         raise SsdError(rc, "mamba2_ssd_gate_bwd")
     return dy, dz
+
+
+# ---- causal conv1d before the scan -------------------------------------------
+
+def _conv_check(x, weight, bias, seq_idx):
+    if x.dim() != 3 or x.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("x must be (batch, seqlen, channels) bf16 or fp32")
+    b, T, C = x.shape
+    _check(x, "x", (b, T, C), x.dtype, x.device)
+    if weight.dim() != 2 or weight.shape[0] != C:
+        raise ValueError("weight must be (channels, width)")
+    _check(weight, "weight", (C, weight.shape[1]), torch.float32, x.device)
+    if bias is not None:
+        _check(bias, "bias", (C,), torch.float32, x.device)
+    if seq_idx is not None:
+        _check(seq_idx, "seq_idx", (b, T), torch.int32, x.device)
+    return b, T, C, int(weight.shape[1]), SSD_BF16 if x.dtype == torch.bfloat16 else SSD_F32
+
+
+def conv1d_fwd(x, weight, bias=None, seq_idx=None, activation="silu", config=0, stream=None):
+    """y = act(bias + causal depthwise conv of x with weight (channels, width)), same dtype as x."""
+    b, T, C, K, dt = _conv_check(x, weight, bias, seq_idx)
+    y = torch.empty_like(x)
+    rc = lib().mamba2_ssd_conv1d_fwd(b, T, C, K, dt, 1 if activation == "silu" else 0, _ptr(x), _ptr(weight),
+                                     _ptr(bias), _ptr(seq_idx), _ptr(y), config, _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_conv1d_fwd")
+    return y
+
+
+def conv1d_bwd(x, weight, dy, bias=None, seq_idx=None, activation="silu", config=0, variant=VARIANT_DETERMINISTIC,
+               stream=None, want_bias_grad=True):
+    """(dx fp32, dweight fp32, dbias fp32 or None) of sum(conv1d_fwd(...) * dy)."""
+    b, T, C, K, dt = _conv_check(x, weight, bias, seq_idx)
+    _check(dy, "dy", tuple(x.shape), x.dtype, x.device)
+    dx = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    dw = torch.empty_like(weight)
+    db = torch.empty((C,), dtype=torch.float32, device=x.device) if want_bias_grad else None
+    need = lib().mamba2_ssd_conv1d_bwd_workspace_size(b, T, C, K)
+    ws = torch.empty(max(16, need), dtype=torch.uint8, device=x.device)
+    rc = lib().mamba2_ssd_conv1d_bwd(b, T, C, K, dt, 1 if activation == "silu" else 0, _ptr(x), _ptr(weight),
+                                     _ptr(bias), _ptr(seq_idx), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(ws),
+                                     ws.numel(), config, variant, _stream(stream))
+    if rc:
+        raise SsdError(rc, "mamba2_ssd_conv1d_bwd")
+    return dx, dw, db
 
 
 # ---- autograd -------------------------------------------------------------

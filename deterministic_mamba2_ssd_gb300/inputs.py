@@ -94,3 +94,33 @@ def workload_inputs(name: str, seqlen: int | None = None, seed: int | None = Non
     return make_inputs(w.batch, T, w.nheads, w.headdim, w.ngroups, w.dstate, dtype=w.dtype,
                        seed=seed_of(name) if seed is None else seed, dt_shift=w.dt_shift,
                        d_mode=w.d_mode, seq_lens=seq_lens, with_init=w.with_init)
+
+
+def make_conv_inputs(batch, seqlen, channels, width, *, dtype=torch.bfloat16, seed=0, seq_lens=()):
+    """Inputs of the causal depthwise conv before the scan, drawn in the order
+    x, weight, bias, dy: x, dy ~ N(0,1) in ``dtype`` (batch, seqlen,
+    channels); weight (channels, width) and bias (channels) ~ U(-1/sqrt(width),
+    1/sqrt(width)) fp32 (the usual initialisation of a depthwise conv with
+    `width` inputs per output); seq_idx (1, seqlen) int32 for a packed batch."""
+    g = torch.Generator().manual_seed(int(seed))
+    bound = 1.0 / math.sqrt(width)
+    x = torch.randn((batch, seqlen, channels), generator=g)
+    w = (torch.rand((channels, width), generator=g) * 2 - 1) * bound
+    bias = (torch.rand((channels,), generator=g) * 2 - 1) * bound
+    dy = torch.randn((batch, seqlen, channels), generator=g)
+    seq_idx = None
+    if seq_lens:
+        assert batch == 1 and sum(seq_lens) == seqlen
+        seq_idx = torch.repeat_interleave(torch.arange(len(seq_lens), dtype=torch.int32),
+                                          torch.tensor(seq_lens)).reshape(1, seqlen).contiguous()
+    return dict(x=x.to(dtype).contiguous(), w=w.float().contiguous(), bias=bias.float().contiguous(),
+                dy=dy.to(dtype).contiguous(), seq_idx=seq_idx)
+
+
+#: the conv before the scan on the two workloads of this library: its channels are the
+#: concatenated x, B, C inputs of the scan (nheads * headdim + 2 * ngroups * dstate), width 4
+CONV_WORKLOADS = {
+    "conv_T16384": dict(batch=1, seqlen=16384, channels=256 * 64 + 2 * 8 * 128, width=4, seq_lens=()),
+    "conv_varlen_T32768": dict(batch=1, seqlen=32768, channels=128 * 64 + 2 * 1 * 256, width=4,
+                               seq_lens=(4096, 8192, 8192, 12288)),
+}

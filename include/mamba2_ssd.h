@@ -291,6 +291,44 @@ ssd_status mamba2_ssd_gate_fwd(int64_t n, int32_t dtype, const void *y, const vo
 ssd_status mamba2_ssd_gate_bwd(int64_t n, int32_t dtype, const void *y, const void *z, const void *dout, void *dy,
                                float *dz, void *stream);
 
+/* ---- Causal depthwise conv1d before the scan ---------------------------
+ * "Deterministic bwd kernel for mamba2" (Mamba PR #827), section "Atomic add
+ * non-determinism", names the atomics of causal-conv1d next to the SSD
+ * backward's.  Per batch row b, token t, channel c (x, y, dy laid out
+ * (batch, seqlen, channels), densely packed):
+ *     pre[b,t,c] = bias[c] + sum_{k<width} weight[c,k] x[b, t-width+1+k, c]
+ *     y = pre (activation 0) or silu(pre) = pre / (1 + e^-pre) (activation 1)
+ * where a tap before the row start reads zero and, when seq_idx (batch,
+ * seqlen) int32 is given (batch 1, non-decreasing ids), a tap in another
+ * sequence than t reads zero.  Sizes: channels a multiple of 4, width 1..4,
+ * batch * ceil(seqlen / 128) <= 65535.  weight (channels, width) and bias
+ * (channels, may be NULL) fp32; x, y, dy in `dtype` (ssd_dtype); dx, dweight,
+ * dbias fp32.  All pointers device, 16-byte aligned.  config in
+ * [0, mamba2_ssd_conv1d_num_configs()) picks the block size only: every
+ * config gives the same bits.  Enqueued on `stream`; a bad size, pointer or
+ * config returns SSD_ERR_INVALID_ARG and launches nothing. */
+int mamba2_ssd_conv1d_num_configs(void);
+ssd_status mamba2_ssd_conv1d_fwd(int64_t batch, int64_t seqlen, int64_t channels, int32_t width, int32_t dtype,
+                                 int32_t activation, const void *x, const float *weight, const float *bias,
+                                 const int32_t *seq_idx, void *y, int config, void *stream);
+
+/* Workspace bytes of the deterministic conv1d backward (0 for bad sizes):
+ * one slot of (width + 1) x channels partial sums per 128-token tile. */
+size_t mamba2_ssd_conv1d_bwd_workspace_size(int64_t batch, int64_t seqlen, int64_t channels, int32_t width);
+
+/* Backward of L = sum(y * dy): dx (batch, seqlen, channels), dweight
+ * (channels, width), dbias (channels; may be NULL), all fully overwritten.
+ * dweight and dbias sum over every token: each 128-token tile's partial sums
+ * (in token order) go to its own slot of the workspace and are folded in
+ * ascending tile order -- bitwise reproducible for every run and config.
+ * variant SSD_VARIANT_ATOMIC adds the partial sums with atomics instead (no
+ * workspace needed; results not reproducible; for measuring the cost of
+ * determinism only). */
+ssd_status mamba2_ssd_conv1d_bwd(int64_t batch, int64_t seqlen, int64_t channels, int32_t width, int32_t dtype,
+                                 int32_t activation, const void *x, const float *weight, const float *bias,
+                                 const int32_t *seq_idx, const void *dy, float *dx, float *dweight, float *dbias,
+                                 void *workspace, size_t workspace_bytes, int config, int variant, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

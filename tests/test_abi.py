@@ -240,3 +240,25 @@ def test_binding_declares_argument_types_of_every_entry_point(L):
     # ctypes would otherwise pass Python ints as C int and floats as double
     missing = [n for n in declared_functions() if getattr(L, n).argtypes is None]
     assert not missing, missing
+
+
+def test_conv1d_rejects_bad_arguments_on_host(L):
+    p = lambda k: ctypes.c_void_p(FAKE + 256 * k)
+    assert L.mamba2_ssd_conv1d_num_configs() == 2
+    need = L.mamba2_ssd_conv1d_bwd_workspace_size(1, 300, 64, 4)
+    assert need == 3 * 5 * 64 * 4          # 3 tiles of 128 tokens, (width + 1) x channels each
+    assert L.mamba2_ssd_conv1d_bwd_workspace_size(1, 300, 62, 4) == 0    # channels not a multiple of 4
+    assert L.mamba2_ssd_conv1d_bwd_workspace_size(1, 300, 64, 5) == 0    # width above 4
+    # bad width, dtype, activation, config, misaligned pointer, seq_idx with batch > 1
+    assert L.mamba2_ssd_conv1d_fwd(1, 300, 64, 0, 1, 1, p(0), p(1), None, None, p(2), 0, None) == 1
+    assert L.mamba2_ssd_conv1d_fwd(1, 300, 64, 4, 7, 1, p(0), p(1), None, None, p(2), 0, None) == 1
+    assert L.mamba2_ssd_conv1d_fwd(1, 300, 64, 4, 1, 2, p(0), p(1), None, None, p(2), 0, None) == 1
+    assert L.mamba2_ssd_conv1d_fwd(1, 300, 64, 4, 1, 1, p(0), p(1), None, None, p(2), 2, None) == 1
+    assert L.mamba2_ssd_conv1d_fwd(1, 300, 64, 4, 1, 1, ctypes.c_void_p(FAKE + 8), p(1), None, None, p(2), 0,
+                                   None) == 1
+    assert L.mamba2_ssd_conv1d_fwd(2, 300, 64, 4, 1, 1, p(0), p(1), None, p(3), p(2), 0, None) == 1
+    # workspace too small (deterministic variant); bad variant
+    assert L.mamba2_ssd_conv1d_bwd(1, 300, 64, 4, 1, 1, p(0), p(1), None, None, p(2), p(3), p(4), p(5), p(6),
+                                   need - 1, 0, 0, None) == 3
+    assert L.mamba2_ssd_conv1d_bwd(1, 300, 64, 4, 1, 1, p(0), p(1), None, None, p(2), p(3), p(4), p(5), p(6),
+                                   need, 0, 2, None) == 1

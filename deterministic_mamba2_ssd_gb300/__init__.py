@@ -42,7 +42,7 @@ class Dims(ctypes.Structure):
 
 class SavedStruct(ctypes.Structure):
     _fields_ = [("dims", Dims)] + [(n, ctypes.c_void_p) for n in
-                                   ("x", "dt", "A", "B", "C", "D", "seq_idx", "init_states", "states")] + \
+                                   ("x", "dt", "A", "B", "C", "D", "seq_idx", "init_states", "states", "aux")] + \
                [("magic", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
 
 

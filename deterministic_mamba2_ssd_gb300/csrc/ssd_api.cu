@@ -57,11 +57,18 @@ constexpr int kNumSimt = 2;
 constexpr int kFusedRings[] = {4, 2};
 constexpr int kNumFused = 2;
 
-// The fused kernel resets the state at chunk boundaries only, so sequence
-// starts inside a chunk always take the general path.
-bool use_fused(const ssd_dims *d) {
-  return !(d->flags & SSD_DIMS_SEQ_ANY_START) && ssd::fused_bwd_supported(shape_of(d), d->dtype == SSD_BF16);
+// Which backward a shape runs.  The fused kernels reset the state at chunk
+// boundaries only, so sequence starts inside a chunk always take the general
+// path; dstate 256 with one group runs the fused kernels once per state half.
+enum Kind { kSimt = 0, kFused = 1, kSplit = 2 };
+Kind kind_of(const ssd_dims *d) {
+  if (d->flags & SSD_DIMS_SEQ_ANY_START) return kSimt;
+  const ssd::Shape s = shape_of(d);
+  if (ssd::fused_bwd_supported(s, d->dtype == SSD_BF16)) return kFused;
+  if (ssd::fused_split_supported(s, d->dtype == SSD_BF16)) return kSplit;
+  return kSimt;
 }
+bool use_fused(const ssd_dims *d) { return kind_of(d) != kSimt; }
 
 bool has_seq(const ssd_dims *d) { return (d->flags & SSD_DIMS_SEQ_IDX) != 0; }
 
@@ -81,9 +88,8 @@ constexpr uint32_t kOrderedSpinLimit = 1u << 24;   // polls before an ordered-fo
 
 ssd::FusedOptions fused_options(const ssd_dims *d, int config, int variant) {
   ssd::FusedOptions o;
-  // with sequence starts the chain can be cut, so every chunk gets its own slot
-  o.ring_depth = (d->flags & SSD_DIMS_SEQ_IDX) ? int((d->seqlen + d->chunk_size - 1) / d->chunk_size)
-                                                : kFusedRings[config];
+  // with sequence starts the chain can be cut, so every (128-token) chunk gets its own slot
+  o.ring_depth = (d->flags & SSD_DIMS_SEQ_IDX) ? int((d->seqlen + 127) / 128) : kFusedRings[config];
   o.atomic = variant == SSD_VARIANT_ATOMIC;
   return o;
 }
@@ -112,7 +118,11 @@ int64_t mamba2_ssd_num_chunks(const ssd_dims *dims) {
 
 size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
   if (!dims_ok(dims)) return 0;
-  return use_fused(dims) ? ssd::fused_fwd_workspace(shape_of(dims)) : ssd::simt_fwd_workspace(shape_of(dims));
+  switch (kind_of(dims)) {
+    case kFused: return ssd::fused_fwd_workspace(shape_of(dims));
+    case kSplit: return ssd::fused_fwd_split_workspace(shape_of(dims));
+    default: return ssd::simt_fwd_workspace(shape_of(dims));
+  }
 }
 
 int mamba2_ssd_num_configs(const ssd_dims *dims) {
@@ -122,6 +132,7 @@ int mamba2_ssd_num_configs(const ssd_dims *dims) {
 
 const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
+  if (kind_of(dims) == kSplit) return config == 0 ? "fused-split/ring4" : "fused-split/ring2";
   if (use_fused(dims)) return config == 0 ? "fused/ring4" : "fused/ring2";
   return config == 0 ? "simt/block256" : "simt/block128";
 }
@@ -129,6 +140,8 @@ const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
 size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (!variant_ok(dims, variant)) return 0;
+  if (kind_of(dims) == kSplit)
+    return ssd::fused_bwd_split_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
   if (use_fused(dims)) return ssd::fused_bwd_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
   return ssd::simt_bwd_workspace(shape_of(dims), variant);
 }
@@ -136,6 +149,7 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
 int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (!variant_ok(dims, variant)) return 0;
+  if (kind_of(dims) == kSplit) return variant == SSD_VARIANT_ATOMIC ? 3 : 4;
   if (use_fused(dims)) return variant == SSD_VARIANT_ATOMIC ? 1 : 2;
   return ssd::simt_bwd_launches(shape_of(dims), variant, has_seq(dims));
 }
@@ -143,6 +157,12 @@ int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
   if (!variant_ok(dims, variant)) return "invalid";
+  if (kind_of(dims) == kSplit) {   // one fused launch per state half, then the fold
+    static const char *det[] = {"fused_bwd", "fused_bwd", "split_fold", "split_scalars"};
+    static const char *atm[] = {"fused_bwd_atomic", "fused_bwd_atomic", "split_fold"};
+    if (variant == SSD_VARIANT_ATOMIC) return (k >= 0 && k < 3) ? atm[k] : "invalid";
+    return (k >= 0 && k < 4) ? det[k] : "invalid";
+  }
   if (use_fused(dims)) {
     if (variant == SSD_VARIANT_ATOMIC) return k == 0 ? "fused_bwd_atomic" : "invalid";
     return k == 0 ? "fused_bwd" : (k == 1 ? "fold_scalars" : "invalid");
@@ -197,10 +217,14 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   a.x = x; a.B = B; a.C = C; a.dt = dt; a.A = A; a.D = D;
   a.init = init_states; a.seq_idx = seq_idx; a.y = y; a.states_out = states;
   // The fused shape family runs the tensor-core forward, which writes each saved state as the
-  // packed bf16 hi | lo operand pair the fused backward takes; every other shape the general one.
-  const cudaError_t err = use_fused(dims) ? ssd::fused_fwd(s, a, workspace, st)
-                                          : ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
+  // packed bf16 hi | lo operand pair the fused backward takes; dstate 256 runs it per state half
+  // (packed states of both halves kept in the workspace); every other shape the general one.
+  const Kind kind = kind_of(dims);
+  const cudaError_t err = kind == kFused   ? ssd::fused_fwd(s, a, workspace, st)
+                          : kind == kSplit ? ssd::fused_fwd_split(s, a, workspace, st)
+                                           : ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
   if (err != cudaSuccess) return SSD_ERR_CUDA;
+  saved_out->aux = kind == kSplit ? ssd::fused_split_aux(s, workspace) : nullptr;
   saved_out->dims = *dims;
   saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
   saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;
@@ -214,7 +238,7 @@ ssd_status mamba2_ssd_states_unpack(const ssd_saved *saved, float *out, void *st
   if (!saved->states || !out || !aligned16(out)) return SSD_ERR_INVALID_ARG;
   const ssd::Shape s = shape_of(&saved->dims);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_fused(&saved->dims))
+  if (kind_of(&saved->dims) == kFused)
     return ssd::fused_unpack_states(s, saved->states, out, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
   const size_t bytes = size_t(s.b * s.nc * s.H * s.P * s.N) * sizeof(float);
   return cudaMemcpyAsync(out, saved->states, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess ? SSD_OK
@@ -250,7 +274,11 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   tr.events = reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events));
   tr.count = num_events;
   cudaError_t err;
-  if (use_fused(dims))
+  if (kind_of(dims) == kSplit) {
+    if (!saved->aux) return SSD_ERR_HANDLE;   // the packed states live in the forward's workspace
+    a.states_in = saved->aux;
+    err = ssd::fused_bwd_split(s, a, workspace, fused_options(dims, config, variant), st, tr);
+  } else if (use_fused(dims))
     err = ssd::fused_bwd(s, a, workspace, fused_options(dims, config, variant), st, tr);
   else
     err = ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], variant, kOrderedSpinLimit, st,
@@ -264,7 +292,7 @@ ssd_status mamba2_ssd_bwd_fault_test(const ssd_saved *saved, const void *dout, f
                                      void *stream) {
   if (!saved || saved->magic != kSavedMagic || !dims_ok(&saved->dims)) return SSD_ERR_HANDLE;
   const ssd_dims *dims = &saved->dims;
-  if (!use_fused(dims)) return SSD_ERR_UNSUPPORTED;
+  if (kind_of(dims) != kFused) return SSD_ERR_UNSUPPORTED;
   const void *req[] = {saved->x, saved->dt, saved->A, saved->B, saved->C, saved->D, saved->states,
                        dout, dx, ddt, dA, dB, dC, dD};
   for (const void *p : req)

@@ -1042,6 +1042,7 @@ cudaError_t fused_unpack_states(const Shape &s, const float *packed, float *out,
 }
 
 bool fused_bwd_supported(const Shape &s, bool bf16) {
+  // (dstate 256 with one group runs this kernel once per state half: fused_bwd_split)
   return bf16 && s.Q == kQ && s.N == kN && s.P == kP && s.T % kQ == 0 && s.hpg >= 1 &&
          s.b * s.nc * s.G <= (int64_t(1) << 30) && s.b * s.T <= (int64_t(1) << 30);
 }
@@ -1052,33 +1053,29 @@ size_t fused_bwd_workspace(const Shape &s, int ring_depth) {
   return cv.bytes();
 }
 
-cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
-                      Trace &tr) {
-  Carver cv(ws);
-  FusedWs w = carve_fused(cv, s, opt.ring_depth);
+namespace {
+
+// One launch of the fused kernel.  `bc_pitch`: elements per token row of B and C
+// (the kernel reads columns [g * 128, g * 128 + 128) from `a.B`, `a.C`); `pass`
+// picks the ticket counter (status[1 + pass]) so that consecutive launches on
+// one workspace do not share one.
+cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const FusedOptions &opt, int64_t bc_pitch,
+                        int pass, cudaStream_t st, Trace &tr) {
   CUtensorMap tm_x, tm_g, tm_b, tm_c, tm_dx;
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
                     128, true) ||
       !make_tmap_2d(&tm_g, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP),
                     64, 128, true) ||
-      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(bc_pitch), 64,
                     128, true) ||
-      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(s.G * kN), 64,
+      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(bc_pitch), 64,
                     128, true) ||
       !make_tmap_2d(&tm_dx, a.dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 32,
                     128, true))
     return cudaErrorInvalidValue;
-  cudaError_t err = cudaMemsetAsync(w.status, 0, 64 * sizeof(int), st);
-  if (err != cudaSuccess) return err;
+  cudaError_t err;
   if ((err = cudaMemsetAsync(w.flags, 0, size_t(s.b * s.nc * s.H) * sizeof(int), st)) != cudaSuccess) return err;
-  if (a.dinit && (err = cudaMemsetAsync(a.dinit, 0, size_t(s.nseq * s.H * kP * kN) * sizeof(float), st)) !=
-                     cudaSuccess)
-    return err;
-  if (opt.atomic) {
-    if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
-    if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
-  }
   if ((err = cudaFuncSetAttribute(fused_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
       cudaSuccess)
     return err;
@@ -1101,7 +1098,7 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
   p.ring_depth = opt.ring_depth;
   p.flags = w.flags;
   p.err = w.status;
-  p.ticket = w.status + 1;
+  p.ticket = w.status + 1 + pass;
   p.dA_part = w.dA_part;
   p.dD_part = w.dD_part;
   p.dA = a.dA;
@@ -1113,9 +1110,183 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
   tr.mark(st);
   fused_bwd_kernel<<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   tr.mark(st);
+  return cudaGetLastError();
+}
+
+// ---- dstate 256, one group: two state halves (see fused_fwd_split) --------
+struct SplitBwdWs {
+  FusedWs w;                       // shared by both passes, except the dA/dD partials
+  float *dA_part1, *dD_part1, *dD_scratch, *zeros;
+  float *dx1, *ddt1;               // the second half's dx and ddt
+  float *dBh[2], *dCh[2], *dinit_h[2];
+};
+
+Shape split_half(const Shape &s) {
+  Shape h = s;
+  h.N = kN;
+  h.Q = kQ;
+  h.nc = s.T / kQ;
+  return h;
+}
+
+SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
+  const Shape h = split_half(s);
+  SplitBwdWs w;
+  w.w = carve_fused(cv, h, ring_depth);
+  w.dA_part1 = cv.take<float>(h.b * h.nc * h.H);
+  w.dD_part1 = cv.take<float>(h.b * h.nc * h.H);
+  w.dD_scratch = cv.take<float>(h.H);
+  w.zeros = cv.take<float>(h.H);
+  w.dx1 = cv.take<float>(s.b * s.T * s.H * kP);
+  w.ddt1 = cv.take<float>(s.b * s.T * s.H);
+  for (int j = 0; j < 2; ++j) {
+    w.dBh[j] = cv.take<float>(s.b * s.T * kN);
+    w.dCh[j] = cv.take<float>(s.b * s.T * kN);
+    w.dinit_h[j] = cv.take<float>(s.nseq * s.H * kP * kN);
+  }
+  return w;
+}
+
+// dx += dx of the second half, ddt likewise; dB, dC and dinit assembled from
+// their halves (grid-stride over float4 groups of each array in turn)
+__global__ void split_fold_kernel(int64_t n_dx4, int64_t n_ddt4, int64_t rows, int64_t init_rows, float *__restrict__ dx,
+                                  const float *__restrict__ dx1, float *__restrict__ ddt,
+                                  const float *__restrict__ ddt1, float *__restrict__ dB, float *__restrict__ dC,
+                                  const float *__restrict__ dB0, const float *__restrict__ dB1,
+                                  const float *__restrict__ dC0, const float *__restrict__ dC1,
+                                  float *__restrict__ dinit, const float *__restrict__ di0,
+                                  const float *__restrict__ di1) {
+  const int64_t q = kN / 4;   // float4 groups in a 128-wide half row
+  const int64_t n_bc = rows * 2 * q, n_in = init_rows * 2 * q;
+  const int64_t total = n_dx4 + n_ddt4 + 2 * n_bc + n_in;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    int64_t k = i;
+    if (k < n_dx4) {
+      float4 a = reinterpret_cast<float4 *>(dx)[k];
+      const float4 b = __ldcs(reinterpret_cast<const float4 *>(dx1) + k);
+      a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+      reinterpret_cast<float4 *>(dx)[k] = a;
+      continue;
+    }
+    k -= n_dx4;
+    if (k < n_ddt4) {
+      float4 a = reinterpret_cast<float4 *>(ddt)[k];
+      const float4 b = __ldcs(reinterpret_cast<const float4 *>(ddt1) + k);
+      a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+      reinterpret_cast<float4 *>(ddt)[k] = a;
+      continue;
+    }
+    k -= n_ddt4;
+    // output float4 k of a 256-wide row array: row k / (2q), half j, group within the half
+    const float *src0, *src1;
+    float *out;
+    if (k < n_bc) {
+      src0 = dB0, src1 = dB1, out = dB;
+    } else if (k < 2 * n_bc) {
+      k -= n_bc;
+      src0 = dC0, src1 = dC1, out = dC;
+    } else {
+      k -= 2 * n_bc;
+      src0 = di0, src1 = di1, out = dinit;
+    }
+    const int64_t row = k / (2 * q), rem = k % (2 * q), j = rem / q, g4 = rem % q;
+    reinterpret_cast<float4 *>(out)[k] = __ldcs(reinterpret_cast<const float4 *>(j ? src1 : src0) + row * q + g4);
+  }
+}
+
+// dA[h]: both halves' per-(batch, chunk) partials, half 0 then half 1, each in
+// ascending chunk order; dD[h] from half 0 (its g . x terms do not depend on
+// the state half).
+__global__ void split_scalars_kernel(Shape h, const float *__restrict__ a0, const float *__restrict__ a1,
+                                     const float *__restrict__ d0, float *__restrict__ dA, float *__restrict__ dD) {
+  const int64_t hd = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (hd >= h.H) return;
+  float a = 0.f, d = 0.f;
+  for (int64_t bc = 0; bc < h.b * h.nc; ++bc) {
+    a += a0[bc * h.H + hd];
+    d += d0[bc * h.H + hd];
+  }
+  for (int64_t bc = 0; bc < h.b * h.nc; ++bc) a += a1[bc * h.H + hd];
+  dA[hd] = a;
+  dD[hd] = d;
+}
+
+}  // namespace
+
+cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
+                      Trace &tr) {
+  Carver cv(ws);
+  FusedWs w = carve_fused(cv, s, opt.ring_depth);
+  cudaError_t err = cudaMemsetAsync(w.status, 0, 64 * sizeof(int), st);
+  if (err != cudaSuccess) return err;
+  if (a.dinit && (err = cudaMemsetAsync(a.dinit, 0, size_t(s.nseq * s.H * kP * kN) * sizeof(float), st)) !=
+                     cudaSuccess)
+    return err;
+  if (opt.atomic) {
+    if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  }
+  if ((err = launch_pass(s, a, w, opt, s.G * kN, 0, st, tr)) != cudaSuccess) return err;
   if (!opt.atomic) {
     tr.mark(st);
     fold_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
+    tr.mark(st);
+  }
+  return cudaGetLastError();
+}
+
+size_t fused_bwd_split_workspace(const Shape &s, int ring_depth) {
+  Carver cv(nullptr);
+  carve_split(cv, s, ring_depth);
+  return cv.bytes();
+}
+
+cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
+                            Trace &tr) {
+  const Shape h = split_half(s);
+  Carver cv(ws);
+  SplitBwdWs w = carve_split(cv, s, opt.ring_depth);
+  cudaError_t err;
+  if ((err = cudaMemsetAsync(w.w.status, 0, 64 * sizeof(int), st)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(w.zeros, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  for (int j = 0; j < 2 && a.dinit; ++j)
+    if ((err = cudaMemsetAsync(w.dinit_h[j], 0, size_t(s.nseq * s.H * kP * kN) * sizeof(float), st)) != cudaSuccess)
+      return err;
+  if (opt.atomic) {
+    if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+    if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  }
+  const int64_t tiles = h.b * h.nc * h.H * kP * kN;
+  for (int j = 0; j < 2; ++j) {
+    Args aj = a;
+    aj.B = static_cast<const __nv_bfloat16 *>(a.B) + j * kN;
+    aj.C = static_cast<const __nv_bfloat16 *>(a.C) + j * kN;
+    aj.states_in = a.states_in + j * tiles;
+    aj.dB = w.dBh[j];
+    aj.dC = w.dCh[j];
+    aj.dinit = a.dinit ? w.dinit_h[j] : nullptr;
+    FusedWs wj = w.w;
+    if (j == 1) {
+      aj.D = w.zeros;          // the skip term D x belongs to one half only
+      aj.dx = w.dx1;
+      aj.ddt = w.ddt1;
+      aj.dD = w.dD_scratch;    // (atomic variant) g . x is counted by half 0
+      wj.dA_part = w.dA_part1;
+      wj.dD_part = w.dD_part1;
+    }
+    if ((err = launch_pass(h, aj, wj, opt, 2 * kN, j, st, tr)) != cudaSuccess) return err;
+  }
+  const int64_t n_dx4 = s.b * s.T * s.H * kP / 4, n_ddt4 = s.b * s.T * s.H / 4;
+  const int64_t rows = s.b * s.T, init_rows = a.dinit ? s.nseq * s.H * kP : 0;
+  tr.mark(st);
+  split_fold_kernel<<<unsigned(8 * 152), 256, 0, st>>>(n_dx4, n_ddt4, rows, init_rows, a.dx, w.dx1, a.ddt, w.ddt1,
+                                                       a.dB, a.dC, w.dBh[0], w.dBh[1], w.dCh[0], w.dCh[1], a.dinit,
+                                                       w.dinit_h[0], w.dinit_h[1]);
+  tr.mark(st);
+  if (!opt.atomic) {
+    tr.mark(st);
+    split_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(h, w.w.dA_part, w.dA_part1, w.w.dD_part, a.dA,
+                                                                       a.dD);
     tr.mark(st);
   }
   return cudaGetLastError();

@@ -92,6 +92,8 @@ struct FwdParams {
   float *decay;     // (b, nc, H): exp(E) of each chunk
   float *states;    // (b, nc, H) packed 32 KB tiles: the state entering each chunk
   __nv_bfloat16 *y;
+  float *y_acc;     // fp32 partial y (state halves of a 256-wide state, see fused_fwd_split)
+  int y_mode;       // 0: y in bf16; 1: partial y to y_acc; 2: y = y_acc + this partial, in bf16
   int *err;
 };
 
@@ -353,19 +355,37 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
   auto store_y = [&](int k, float eacs) {
     const int64_t h = int64_t(g) * hpg + k;
     const uint32_t buf = 128 + 128 * uint32_t(k & 1);
-    __nv_bfloat16 *o = p.y + (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
+    const int64_t e0 = (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float yv[16], ch[16];
       umma::tmem_ld16(tmem + lane_off + buf + 32 * half + 16 * j, yv);
       umma::tmem_ld16(tmem + lane_off + buf + 64 + 32 * half + 16 * j, ch);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) yv[i] = fmaf(eacs, ch[i], yv[i]);
+      if (p.y_mode == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          __stcg(reinterpret_cast<float4 *>(p.y_acc + e0 + 16 * j + 4 * i),
+                 make_float4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]));
+        continue;
+      }
+      if (p.y_mode == 2) {   // the other state half's partial first, then this one
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 a = __ldcs(reinterpret_cast<const float4 *>(p.y_acc + e0 + 16 * j + 4 * i));
+          yv[4 * i] = a.x + yv[4 * i];
+          yv[4 * i + 1] = a.y + yv[4 * i + 1];
+          yv[4 * i + 2] = a.z + yv[4 * i + 2];
+          yv[4 * i + 3] = a.w + yv[4 * i + 3];
+        }
+      }
       uint4 u[2];
       __nv_bfloat162 *hb = reinterpret_cast<__nv_bfloat162 *>(u);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        hb[i] = __floats2bfloat162_rn(fmaf(eacs, ch[2 * i], yv[2 * i]), fmaf(eacs, ch[2 * i + 1], yv[2 * i + 1]));
-      *reinterpret_cast<uint4 *>(o + 16 * j) = u[0];
-      *reinterpret_cast<uint4 *>(o + 16 * j + 8) = u[1];
+      for (int i = 0; i < 8; ++i) hb[i] = __floats2bfloat162_rn(yv[2 * i], yv[2 * i + 1]);
+      *reinterpret_cast<uint4 *>(p.y + e0 + 16 * j) = u[0];
+      *reinterpret_cast<uint4 *>(p.y + e0 + 16 * j + 8) = u[1];
     }
   };
 
@@ -527,6 +547,150 @@ cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st) 
   fwd_state_kernel<<<units, 128, K1_SMEM, st>>>(p, tm_x, tm_b);
   fwd_pass_kernel<<<unsigned((s.b * s.H * kN * 8 + 255) / 256), 256, 0, st>>>(p);
   fwd_scan_kernel<<<units, 256, K3_SMEM, st>>>(p, tm_x, tm_b, tm_c);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// dstate 256 (one group), chunk 128 or 256: the recurrence never mixes state
+// dimensions, so the scan is the sum of two scans over the state halves
+// n < 128 and n >= 128 (B, C split the same way), with D counted once.  Each
+// half runs the kernels above as a dstate-128 problem in 128-token chunks (the
+// chunked form is exact for any chunk length); the halves' y are added in
+// fp32 before the single rounding to bf16.  The saved states of both halves
+// (packed, every 128 tokens) live in the forward workspace (`aux`), and the
+// caller's state buffer receives the fp32 (b, nc, H, P, 256) states entering
+// each chunk of the caller's chunk length.
+namespace {
+
+Shape half_shape(const Shape &s) {
+  Shape h = s;
+  h.N = kN;
+  h.Q = kQ;
+  h.nc = s.T / kQ;
+  return h;
+}
+
+struct SplitFwdWs {
+  float *aux;   // packed states of both halves: [half][b][nc'][H] tiles of P x 128
+  FwdWs k;      // status, ST, decay of one half at a time
+  float *y_acc, *init_half, *zeros;
+};
+
+SplitFwdWs carve_fwd_split(Carver &cv, const Shape &s) {
+  const Shape h = half_shape(s);
+  SplitFwdWs w;
+  w.aux = cv.take<float>(2 * h.b * h.nc * h.H * kP * kN);
+  w.k = carve_fwd_fused(cv, h);
+  w.y_acc = cv.take<float>(s.b * s.T * s.H * kP);
+  w.init_half = cv.take<float>(s.nseq * s.H * kP * kN);
+  w.zeros = cv.take<float>(s.H);
+  return w;
+}
+
+// init (nseq, H, P, 256) -> its half j as (nseq, H, P, 128)
+__global__ void init_half_kernel(int64_t rows, int j, const float *__restrict__ init, float *__restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;   // one float4 of the half
+  if (i >= rows * (kN / 4)) return;
+  const int64_t row = i / (kN / 4), q = i % (kN / 4);
+  reinterpret_cast<float4 *>(out)[i] = __ldg(reinterpret_cast<const float4 *>(init + row * 2 * kN + j * kN) + q);
+}
+
+// fp32 (b, nc, H, P, 256) states entering each caller chunk (ratio = caller
+// chunk / 128) from the packed halves; one CTA per (b, caller chunk, head, half)
+__global__ void __launch_bounds__(256) states_view_kernel(Shape s, int ratio, const float *__restrict__ aux,
+                                                           float *__restrict__ out) {
+  const int64_t tile = blockIdx.x;   // ((b * nc + c) * H + h) * 2 + j
+  const int j = int(tile & 1);
+  const int64_t h = (tile >> 1) % s.H, c = (tile >> 1) / s.H % s.nc, bi = (tile >> 1) / (s.H * s.nc);
+  const int64_t nch = s.T / kQ;
+  const uint8_t *in = reinterpret_cast<const uint8_t *>(
+      aux + (((int64_t(j) * s.b + bi) * nch + c * ratio) * s.H + h) * (kP * kN));
+  float *o = out + (((bi * s.nc + c) * s.H + h) * kP) * (2 * kN) + j * kN;
+  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {
+    const int n = i >> 3, c0 = 8 * (i & 7);
+    float hi[8], lo[8];
+    ld8_bf16(in, n, c0, hi);
+    ld8_bf16(in + 16384, n, c0, lo);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[(c0 + e) * (2 * kN) + n] = hi[e] + lo[e];
+  }
+}
+
+}  // namespace
+
+bool fused_split_supported(const Shape &s, bool bf16) {
+  return bf16 && s.N == 2 * kN && s.G == 1 && s.P == kP && (s.Q == kQ || s.Q == 2 * kQ) && s.T % s.Q == 0 &&
+         s.b * (s.T / kQ) <= (int64_t(1) << 30) && s.b * s.T <= (int64_t(1) << 30);
+}
+
+size_t fused_fwd_split_workspace(const Shape &s) {
+  Carver cv(nullptr);
+  carve_fwd_split(cv, s);
+  return cv.bytes();
+}
+
+float *fused_split_aux(const Shape &s, void *ws) {
+  Carver cv(ws);
+  return carve_fwd_split(cv, s).aux;
+}
+
+cudaError_t fused_fwd_split(const Shape &s, const Args &a, void *ws, cudaStream_t st) {
+  const Shape h = half_shape(s);
+  Carver cv(ws);
+  SplitFwdWs w = carve_fwd_split(cv, s);
+  const uint64_t rows = uint64_t(s.b * s.T);
+  CUtensorMap tm_x, tm_b[2], tm_c[2];
+  if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
+                    128, true))
+    return cudaErrorInvalidValue;
+  for (int j = 0; j < 2; ++j) {
+    // the half j of each token's 256 state values: 128 columns at offset 128 j, row pitch 256
+    const __nv_bfloat16 *Bj = static_cast<const __nv_bfloat16 *>(a.B) + j * kN;
+    const __nv_bfloat16 *Cj = static_cast<const __nv_bfloat16 *>(a.C) + j * kN;
+    if (!make_tmap_2d(&tm_b[j], Bj, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, kN, 2 * kN, 64, 128, true) ||
+        !make_tmap_2d(&tm_c[j], Cj, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, kN, 2 * kN, 64, 128, true))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t err;
+  if ((err = cudaMemsetAsync(w.k.status, 0, 64 * sizeof(int), st)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(w.zeros, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  if ((err = cudaFuncSetAttribute(fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K1_SMEM)) !=
+          cudaSuccess ||
+      (err = cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM)) !=
+          cudaSuccess)
+    return err;
+  const unsigned units = unsigned(h.b * h.nc);
+  const int64_t tiles = h.b * h.nc * h.H * kP * kN;
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.s = h;
+  p.dt = a.dt;
+  p.A = a.A;
+  p.seq_idx = a.seq_idx;
+  p.ST = w.k.ST;
+  p.decay = w.k.decay;
+  p.y = static_cast<__nv_bfloat16 *>(a.y);
+  p.y_acc = w.y_acc;
+  p.err = w.k.status;
+  // chunk states and state passing, one half at a time
+  for (int j = 0; j < 2; ++j) {
+    if (a.init) {
+      const int64_t rws = s.nseq * s.H * kP;
+      init_half_kernel<<<unsigned((rws * (kN / 4) + 255) / 256), 256, 0, st>>>(rws, j, a.init, w.init_half);
+    }
+    p.init = a.init ? w.init_half : nullptr;
+    p.states = w.aux + j * tiles;
+    fwd_state_kernel<<<units, 128, K1_SMEM, st>>>(p, tm_x, tm_b[j]);
+    fwd_pass_kernel<<<unsigned((h.b * h.H * kN * 8 + 255) / 256), 256, 0, st>>>(p);
+  }
+  states_view_kernel<<<unsigned(s.b * s.nc * s.H * 2), 256, 0, st>>>(s, int(s.Q / kQ), w.aux, a.states_out);
+  // y: half 0 (with D) into fp32, then half 1 (no D) added and rounded once
+  for (int j = 0; j < 2; ++j) {
+    p.states = w.aux + j * tiles;
+    p.D = j == 0 ? a.D : w.zeros;
+    p.y_mode = j == 0 ? 1 : 2;
+    fwd_scan_kernel<<<units, 256, K3_SMEM, st>>>(p, tm_x, tm_b[j], tm_c[j]);
+  }
   return cudaGetLastError();
 }
 

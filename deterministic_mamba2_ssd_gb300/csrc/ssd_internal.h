@@ -35,6 +35,19 @@ size_t fused_bwd_workspace(const Shape &s, int ring_depth);
 // chunk written directly in the packed form above.
 size_t fused_fwd_workspace(const Shape &s);
 cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st);
+
+// dstate 256 with one group (chunk 128 or 256): the same kernels run once per
+// state half (n < 128, n >= 128) as dstate-128 problems in 128-token chunks,
+// their contributions summed in a fixed order.  The forward keeps the packed
+// states of both halves in its workspace (fused_split_aux); the caller's state
+// buffer gets the fp32 states entering each chunk.
+bool fused_split_supported(const Shape &s, bool bf16);
+size_t fused_fwd_split_workspace(const Shape &s);
+float *fused_split_aux(const Shape &s, void *ws);
+cudaError_t fused_fwd_split(const Shape &s, const Args &a, void *ws, cudaStream_t st);
+size_t fused_bwd_split_workspace(const Shape &s, int ring_depth);
+cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
+                            Trace &tr);
 cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
 
 }  // namespace ssd

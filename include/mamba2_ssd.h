@@ -104,6 +104,9 @@ typedef struct {
   const float *init_states;   /* (nseq,H,P,N) fp32 or NULL */
   const float *states;        /* (b,nc,H,P,N) states entering each chunk (packed on the fused shapes;
                                  see mamba2_ssd_fwd and mamba2_ssd_states_unpack) */
+  const float *aux;           /* dstate-256 fused shapes: the packed states of both state halves, inside
+                                 the forward's workspace (which must then stay alive and unmodified until
+                                 the backward has run); NULL otherwise */
   uint32_t magic;
   uint32_t flags;
 } ssd_saved;
@@ -124,9 +127,13 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
 /* Number of selectable launch configurations for these dims (>= 1, or 0 if
  * the dims are invalid).  All configurations give bitwise-identical
  * results; they differ in launch shape and scheduling only.  bf16 problems
- * with chunk 128, dstate 128, headdim 64 and seqlen a multiple of 128 run
- * the fused tensor-core backward (unless SSD_DIMS_SEQ_ANY_START is set);
- * every other shape runs the general CUDA-core backward. */
+ * with headdim 64, seqlen a multiple of the chunk, and either chunk 128 and
+ * dstate 128 ("fused/...") or one group, chunk 128 or 256 and dstate 256
+ * ("fused-split/...": the recurrence never mixes state dimensions, so the
+ * fused kernels run once per 128-wide state half, in 128-token chunks, and
+ * the halves' contributions are summed in a fixed order) run the fused
+ * tensor-core forward and backward (unless SSD_DIMS_SEQ_ANY_START is set);
+ * every other shape runs the general CUDA-core ones. */
 int mamba2_ssd_num_configs(const ssd_dims *dims);
 
 /* Name of the backward algorithm a configuration selects (static string). */
@@ -157,8 +164,11 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
  * swizzled tensor-core operand layout (row n at n*128 bytes, its 16-byte
  * chunk j at position j ^ (n % 8)), hi first -- the operand the fused
  * backward copies straight into shared memory.  mamba2_ssd_states_unpack
- * gives the fp32 (b,nc,H,P,N) view of either form.  *saved_out (host struct)
- * filled for the backward.  workspace: >= fwd_workspace_size bytes. */
+ * gives the fp32 (b,nc,H,P,N) view of either form.  On the "fused-split"
+ * shapes `states` holds the fp32 states themselves and the packed ones stay
+ * in the workspace, which must then live, unmodified, until the backward
+ * (ssd_saved.aux).  *saved_out (host struct) filled for the backward.
+ * workspace: >= fwd_workspace_size bytes. */
 ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                           const void *B, const void *C, const float *D, const int32_t *seq_idx,
                           const float *init_states, void *y, float *states, void *workspace,

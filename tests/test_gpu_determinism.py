@@ -36,7 +36,7 @@ def repeat_digests(d, chunk, n, config=0, variant=0):
     return out
 
 
-@pytest.mark.parametrize("name", ["bf16_T2048", "bf16_T16384"])
+@pytest.mark.parametrize("name", ["bf16_T2048", "bf16_T16384", "bf16_varlen_T32768"])
 def test_bitwise_repeat_20(name):
     w = WORKLOADS[name]
     assert w.nheads // w.ngroups > 1 and w.seqlen // w.chunk > 1   # several writers per reduced element

@@ -246,6 +246,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ============================================================== kernel ===
+// kDxAdd: add dx into the existing dx (the second state half of a 256-wide
+// state, one add per element) instead of storing it.
+template <bool kDxAdd>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_bwd_kernel(const Params p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
@@ -861,8 +864,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 128) {
         umma::mbar_arrive(&bars[E_RA]);
         umma::mbar_arrive(&bars[E_XG]);
-        umma::tma_store_2d(&tm_dx, sm_base + OFF_M16, int(h * kP), int(row0));
-        umma::tma_store_2d(&tm_dx, sm_base + OFF_M16 + 16384, int(h * kP + 32), int(row0));
+        if (kDxAdd) {
+          umma::tma_reduce_add_2d(&tm_dx, sm_base + OFF_M16, int(h * kP), int(row0));
+          umma::tma_reduce_add_2d(&tm_dx, sm_base + OFF_M16 + 16384, int(h * kP + 32), int(row0));
+        } else {
+          umma::tma_store_2d(&tm_dx, sm_base + OFF_M16, int(h * kP), int(row0));
+          umma::tma_store_2d(&tm_dx, sm_base + OFF_M16 + 16384, int(h * kP + 32), int(row0));
+        }
         umma::tma_store_commit();
       }
 
@@ -1060,7 +1068,7 @@ namespace {
 // picks the ticket counter (status[1 + pass]) so that consecutive launches on
 // one workspace do not share one.
 cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const FusedOptions &opt, int64_t bc_pitch,
-                        int pass, cudaStream_t st, Trace &tr) {
+                        int pass, bool dx_add, cudaStream_t st, Trace &tr) {
   CUtensorMap tm_x, tm_g, tm_b, tm_c, tm_dx;
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
@@ -1076,8 +1084,10 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
     return cudaErrorInvalidValue;
   cudaError_t err;
   if ((err = cudaMemsetAsync(w.flags, 0, size_t(s.b * s.nc * s.H) * sizeof(int), st)) != cudaSuccess) return err;
-  if ((err = cudaFuncSetAttribute(fused_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
-      cudaSuccess)
+  if ((err = cudaFuncSetAttribute(fused_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
+          cudaSuccess ||
+      (err = cudaFuncSetAttribute(fused_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
+          cudaSuccess)
     return err;
   Params p;
   memset(&p, 0, sizeof(p));
@@ -1108,7 +1118,10 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
   p.silent_chunk = opt.silent_chunk;
   const unsigned units = unsigned(s.b * s.nc * s.G);
   tr.mark(st);
-  fused_bwd_kernel<<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
+  if (dx_add)
+    fused_bwd_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
+  else
+    fused_bwd_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   tr.mark(st);
   return cudaGetLastError();
 }
@@ -1117,7 +1130,7 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
 struct SplitBwdWs {
   FusedWs w;                       // shared by both passes, except the dA/dD partials
   float *dA_part1, *dD_part1, *dD_scratch, *zeros;
-  float *dx1, *ddt1;               // the second half's dx and ddt
+  float *ddt1;                     // the second half's ddt
   float *dBh[2], *dCh[2], *dinit_h[2];
 };
 
@@ -1137,7 +1150,6 @@ SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   w.dD_part1 = cv.take<float>(h.b * h.nc * h.H);
   w.dD_scratch = cv.take<float>(h.H);
   w.zeros = cv.take<float>(h.H);
-  w.dx1 = cv.take<float>(s.b * s.T * s.H * kP);
   w.ddt1 = cv.take<float>(s.b * s.T * s.H);
   for (int j = 0; j < 2; ++j) {
     w.dBh[j] = cv.take<float>(s.b * s.T * kN);
@@ -1147,10 +1159,9 @@ SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   return w;
 }
 
-// dx += dx of the second half, ddt likewise; dB, dC and dinit assembled from
-// their halves (grid-stride over float4 groups of each array in turn)
-__global__ void split_fold_kernel(int64_t n_dx4, int64_t n_ddt4, int64_t rows, int64_t init_rows, float *__restrict__ dx,
-                                  const float *__restrict__ dx1, float *__restrict__ ddt,
+// ddt += ddt of the second half; dB, dC and dinit assembled from their
+// halves (grid-stride over float4 groups of each array in turn)
+__global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_rows, float *__restrict__ ddt,
                                   const float *__restrict__ ddt1, float *__restrict__ dB, float *__restrict__ dC,
                                   const float *__restrict__ dB0, const float *__restrict__ dB1,
                                   const float *__restrict__ dC0, const float *__restrict__ dC1,
@@ -1158,17 +1169,9 @@ __global__ void split_fold_kernel(int64_t n_dx4, int64_t n_ddt4, int64_t rows, i
                                   const float *__restrict__ di1) {
   const int64_t q = kN / 4;   // float4 groups in a 128-wide half row
   const int64_t n_bc = rows * 2 * q, n_in = init_rows * 2 * q;
-  const int64_t total = n_dx4 + n_ddt4 + 2 * n_bc + n_in;
+  const int64_t total = n_ddt4 + 2 * n_bc + n_in;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
     int64_t k = i;
-    if (k < n_dx4) {
-      float4 a = reinterpret_cast<float4 *>(dx)[k];
-      const float4 b = __ldcs(reinterpret_cast<const float4 *>(dx1) + k);
-      a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
-      reinterpret_cast<float4 *>(dx)[k] = a;
-      continue;
-    }
-    k -= n_dx4;
     if (k < n_ddt4) {
       float4 a = reinterpret_cast<float4 *>(ddt)[k];
       const float4 b = __ldcs(reinterpret_cast<const float4 *>(ddt1) + k);
@@ -1226,7 +1229,7 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
     if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
   }
-  if ((err = launch_pass(s, a, w, opt, s.G * kN, 0, st, tr)) != cudaSuccess) return err;
+  if ((err = launch_pass(s, a, w, opt, s.G * kN, 0, false, st, tr)) != cudaSuccess) return err;
   if (!opt.atomic) {
     tr.mark(st);
     fold_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
@@ -1268,20 +1271,20 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
     FusedWs wj = w.w;
     if (j == 1) {
       aj.D = w.zeros;          // the skip term D x belongs to one half only
-      aj.dx = w.dx1;
       aj.ddt = w.ddt1;
       aj.dD = w.dD_scratch;    // (atomic variant) g . x is counted by half 0
       wj.dA_part = w.dA_part1;
       wj.dD_part = w.dD_part1;
     }
-    if ((err = launch_pass(h, aj, wj, opt, 2 * kN, j, st, tr)) != cudaSuccess) return err;
+    // the second half adds its dx onto the first half's (finished: same stream), one add per element
+    if ((err = launch_pass(h, aj, wj, opt, 2 * kN, j, j == 1, st, tr)) != cudaSuccess) return err;
   }
-  const int64_t n_dx4 = s.b * s.T * s.H * kP / 4, n_ddt4 = s.b * s.T * s.H / 4;
+  const int64_t n_ddt4 = s.b * s.T * s.H / 4;
   const int64_t rows = s.b * s.T, init_rows = a.dinit ? s.nseq * s.H * kP : 0;
   tr.mark(st);
-  split_fold_kernel<<<unsigned(8 * 152), 256, 0, st>>>(n_dx4, n_ddt4, rows, init_rows, a.dx, w.dx1, a.ddt, w.ddt1,
-                                                       a.dB, a.dC, w.dBh[0], w.dBh[1], w.dCh[0], w.dCh[1], a.dinit,
-                                                       w.dinit_h[0], w.dinit_h[1]);
+  split_fold_kernel<<<unsigned(8 * 152), 256, 0, st>>>(n_ddt4, rows, init_rows, a.ddt, w.ddt1, a.dB, a.dC, w.dBh[0],
+                                                       w.dBh[1], w.dCh[0], w.dCh[1], a.dinit, w.dinit_h[0],
+                                                       w.dinit_h[1]);
   tr.mark(st);
   if (!opt.atomic) {
     tr.mark(st);

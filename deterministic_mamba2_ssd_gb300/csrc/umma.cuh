@@ -298,6 +298,15 @@ __device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, uint32_
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// 2-D tiled add of a shared-memory box into global memory (fp32 add in L2,
+// bulk-group completion).  With one such add per element it is a plain
+// deterministic sum of the existing value and the box.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, const void *src, int32_t c0, int32_t c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(smem_u32(src))
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the shared-memory sources of all committed stores have been read.
 __device__ __forceinline__ void tma_store_wait_read() {

@@ -33,6 +33,7 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "ssd_common.cuh"
 #include "ssd_internal.h"
@@ -1128,8 +1129,8 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
 
 // ---- dstate 256, one group: two state halves (see fused_fwd_split) --------
 struct SplitBwdWs {
-  FusedWs w;                       // shared by both passes, except the dA/dD partials
-  float *dA_part1, *dD_part1, *dD_scratch, *zeros;
+  FusedWs w, w1;                   // one per state half (the halves run concurrently)
+  float *dD_scratch, *zeros;
   float *ddt1;                     // the second half's ddt
   float *dBh[2], *dCh[2], *dinit_h[2];
 };
@@ -1146,8 +1147,7 @@ SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   const Shape h = split_half(s);
   SplitBwdWs w;
   w.w = carve_fused(cv, h, ring_depth);
-  w.dA_part1 = cv.take<float>(h.b * h.nc * h.H);
-  w.dD_part1 = cv.take<float>(h.b * h.nc * h.H);
+  w.w1 = carve_fused(cv, h, ring_depth);
   w.dD_scratch = cv.take<float>(h.H);
   w.zeros = cv.take<float>(h.H);
   w.ddt1 = cv.take<float>(s.b * s.T * s.H);
@@ -1244,14 +1244,36 @@ size_t fused_bwd_split_workspace(const Shape &s, int ring_depth) {
   return cv.bytes();
 }
 
+// A second stream per device on which the second state half runs next to the
+// first (created once, kept for the life of the process).
+cudaError_t side_stream(cudaStream_t *out) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev]) {
+    const cudaError_t err = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+    if (err != cudaSuccess) return err;
+  }
+  *out = streams[dev];
+  return cudaSuccess;
+}
+
 cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
                             Trace &tr) {
   const Shape h = split_half(s);
   Carver cv(ws);
   SplitBwdWs w = carve_split(cv, s, opt.ring_depth);
   cudaError_t err;
+  cudaStream_t side;
+  if ((err = side_stream(&side)) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(w.w.status, 0, 64 * sizeof(int), st)) != cudaSuccess) return err;
+  if ((err = cudaMemsetAsync(w.w1.status, 0, 64 * sizeof(int), st)) != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(w.zeros, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
+  // both halves add their dx into zeros: with two addends onto zero the sum is
+  // the same bits in either order (0 + a = a exactly, and a + b = b + a)
+  if ((err = cudaMemsetAsync(a.dx, 0, size_t(s.b * s.T * s.H * kP) * sizeof(float), st)) != cudaSuccess) return err;
   for (int j = 0; j < 2 && a.dinit; ++j)
     if ((err = cudaMemsetAsync(w.dinit_h[j], 0, size_t(s.nseq * s.H * kP * kN) * sizeof(float), st)) != cudaSuccess)
       return err;
@@ -1259,8 +1281,17 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
     if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
   }
+  // fork: the second half runs on the side stream once everything above is done
+  cudaEvent_t fork, join;
+  if ((err = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming)) != cudaSuccess) return err;
+  if ((err = cudaEventCreateWithFlags(&join, cudaEventDisableTiming)) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    return err;
+  }
+  err = cudaEventRecord(fork, st);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(side, fork, 0);
   const int64_t tiles = h.b * h.nc * h.H * kP * kN;
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < 2 && err == cudaSuccess; ++j) {
     Args aj = a;
     aj.B = static_cast<const __nv_bfloat16 *>(a.B) + j * kN;
     aj.C = static_cast<const __nv_bfloat16 *>(a.C) + j * kN;
@@ -1268,17 +1299,20 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
     aj.dB = w.dBh[j];
     aj.dC = w.dCh[j];
     aj.dinit = a.dinit ? w.dinit_h[j] : nullptr;
-    FusedWs wj = w.w;
     if (j == 1) {
       aj.D = w.zeros;          // the skip term D x belongs to one half only
       aj.ddt = w.ddt1;
       aj.dD = w.dD_scratch;    // (atomic variant) g . x is counted by half 0
-      wj.dA_part = w.dA_part1;
-      wj.dD_part = w.dD_part1;
     }
-    // the second half adds its dx onto the first half's (finished: same stream), one add per element
-    if ((err = launch_pass(h, aj, wj, opt, 2 * kN, j, j == 1, st, tr)) != cudaSuccess) return err;
+    FusedWs wj = j ? w.w1 : w.w;
+    wj.status = w.w.status;    // one status word (ticket status[1 + j] per half) for the check
+    err = launch_pass(h, aj, wj, opt, 2 * kN, j, true, j ? side : st, tr);
   }
+  if (err == cudaSuccess) err = cudaEventRecord(join, side);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(st, join, 0);   // join before the fold
+  cudaEventDestroy(fork);
+  cudaEventDestroy(join);
+  if (err != cudaSuccess) return err;
   const int64_t n_ddt4 = s.b * s.T * s.H / 4;
   const int64_t rows = s.b * s.T, init_rows = a.dinit ? s.nseq * s.H * kP : 0;
   tr.mark(st);
@@ -1288,8 +1322,8 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
   tr.mark(st);
   if (!opt.atomic) {
     tr.mark(st);
-    split_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(h, w.w.dA_part, w.dA_part1, w.w.dD_part, a.dA,
-                                                                       a.dD);
+    split_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(h, w.w.dA_part, w.w1.dA_part, w.w.dD_part,
+                                                                       a.dA, a.dD);
     tr.mark(st);
   }
   return cudaGetLastError();

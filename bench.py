@@ -51,8 +51,6 @@ def parse():
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
     ap.add_argument("--no-others", action="store_true", help="skip the other workload presets")
-    ap.add_argument("--seqlen", type=int, default=None,
-                    help="shorten the workload to this many tokens (one sequence; for small profiling cases)")
     ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd", "conv1d_bwd"],
                     help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()
@@ -225,6 +223,101 @@ FUSED_TRAFFIC_PER_TOKEN = {
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }
+
+
+def fused_traffic(tokens):
+    import hashlib
+    path = os.path.join(ROOT, "deterministic_mamba2_ssd_gb300", "csrc", "ssd_fused_bwd.cu")
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    rec = FUSED_TRAFFIC_PER_TOKEN.get(digest)
+    return None if rec is None else rec["bytes_per_token"] * tokens
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def load_tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: the backward is one short kernel)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def cpu_model():
+    """Model name of the host CPU (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+# ------------------------------------------------------- CPU oracle ----
+def oracle_tokens_per_s(w, sample_tokens, nthreads=None):
+    """Times the fp64 CPU oracle (forward + backward: its backward recomputes
+    the forward) on the first ``sample_tokens`` tokens of the workload, all
+    heads.  Returns (tokens/s, seconds, threads)."""
+    import oracle
+    from deterministic_mamba2_ssd_gb300.inputs import workload_inputs
+    T = min(sample_tokens, w.seqlen)
+    d = workload_inputs(w.name, seqlen=T)
+    if w.with_init:
+        d["init"] = d["init"][:1].contiguous()
+    nt = nthreads or oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], init=d["init"], nthreads=nt)
+    oracle.bwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["dout"], init=d["init"], nthreads=nt)
+    dt = time.perf_counter() - t0
+    return w.batch * T / dt, dt, nt
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    sample = 256
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, sample)
+    times = []
+    nt = None
+    for _ in range(args.steps):
+        _, dt, nt = oracle_tokens_per_s(w, sample)
+        times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    value = w.batch * min(sample, w.seqlen) / (ms / 1e3)
+    desc = "first %d tokens of the workload, all %d heads, fwd+bwd in fp64 per step" % (min(sample, w.seqlen),
+                                                                                         w.nheads)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": w.seqlen, "global_batch": w.batch,
+                       "sample_tokens_per_step": min(sample, w.seqlen)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
@@ -435,11 +528,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = WORKLOADS[args.workload]
-    if args.seqlen:
-        import dataclasses
-        w = dataclasses.replace(w, seqlen=args.seqlen, seq_lens=())
     es = 2 if w.dtype == torch.bfloat16 else 4
-    d = workload_inputs(w.name, seqlen=args.seqlen)
+    d = workload_inputs(w.name)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
                        seq_idx=g["seq_idx"], init_states=g["init"])

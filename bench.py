@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-atomic", action="store_true", help="skip the atomic-variant overhead run")
     ap.add_argument("--cpu-sample-tokens", type=int, default=8192)
     ap.add_argument("--no-others", action="store_true", help="skip the other workload presets")
+    ap.add_argument("--seqlen", type=int, default=None,
+                    help="shorten the workload to this many tokens (one sequence; for small profiling cases)")
     ap.add_argument("--op", default="ssd_bwd", choices=["ssd_bwd", "dt_bwd", "gate_bwd", "conv1d_bwd"],
                     help="what one step runs: the scan's backward (default) or an adjacent step's backward")
     return ap.parse_args()
@@ -528,8 +530,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = WORKLOADS[args.workload]
+    if args.seqlen:
+        import dataclasses
+        w = dataclasses.replace(w, seqlen=args.seqlen, seq_lens=())
     es = 2 if w.dtype == torch.bfloat16 else 4
-    d = workload_inputs(w.name)
+    d = workload_inputs(w.name, seqlen=args.seqlen)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
                        seq_idx=g["seq_idx"], init_states=g["init"])

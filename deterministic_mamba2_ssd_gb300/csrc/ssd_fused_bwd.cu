@@ -247,9 +247,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ============================================================== kernel ===
-// kDxAdd: add dx into the existing dx (the second state half of a 256-wide
-// state, one add per element) instead of storing it.
-template <bool kDxAdd>
+// kDxAdd: add dx into the existing dx (the state halves of a 256-wide state:
+// two adds onto zero per element) instead of storing it.  kSliceShift: the
+// heads of a group are split into 2^kSliceShift slices, one unit each (unit
+// group g covers heads [g * hpg, (g + 1) * hpg) and reads the B, C columns of
+// group g >> kSliceShift; its dB, dC are that slice's partial sums).
+template <bool kDxAdd, int kSliceShift>
 __global__ void __launch_bounds__(kThreads, 1)
     fused_bwd_kernel(const Params p, const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_g,
                      const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c,
@@ -306,8 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::tma_prefetch_desc(&tm_c);
       umma::mbar_expect_tx(&bars[B_BC], 65536);
       for (int j = 0; j < 2; ++j) {
-        umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int(g * kN + j * 64), int(row0), &bars[B_BC]);
-        umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int(g * kN + j * 64), int(row0), &bars[B_BC]);
+        umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int((g >> kSliceShift) * kN + j * 64), int(row0),
+                          &bars[B_BC]);
+        umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int((g >> kSliceShift) * kN + j * 64), int(row0),
+                          &bars[B_BC]);
       }
       const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
       // this thread also publishes each head's state gradient to the chunk before
@@ -1070,25 +1075,26 @@ namespace {
 // one workspace do not share one.
 cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const FusedOptions &opt, int64_t bc_pitch,
                         int pass, bool dx_add, cudaStream_t st, Trace &tr) {
+  // (dx_add: the sliced instantiation; the unit groups of `s` are then head slices, two per group)
   CUtensorMap tm_x, tm_g, tm_b, tm_c, tm_dx;
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
                     128, true) ||
       !make_tmap_2d(&tm_g, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP),
                     64, 128, true) ||
-      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(bc_pitch), 64,
-                    128, true) ||
-      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.G * kN), uint64_t(bc_pitch), 64,
-                    128, true) ||
+      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((dx_add ? s.G / 2 : s.G) * kN),
+                    uint64_t(bc_pitch), 64, 128, true) ||
+      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((dx_add ? s.G / 2 : s.G) * kN),
+                    uint64_t(bc_pitch), 64, 128, true) ||
       !make_tmap_2d(&tm_dx, a.dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 32,
                     128, true))
     return cudaErrorInvalidValue;
   cudaError_t err;
   if ((err = cudaMemsetAsync(w.flags, 0, size_t(s.b * s.nc * s.H) * sizeof(int), st)) != cudaSuccess) return err;
-  if ((err = cudaFuncSetAttribute(fused_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
-          cudaSuccess ||
-      (err = cudaFuncSetAttribute(fused_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
-          cudaSuccess)
+  if ((err = cudaFuncSetAttribute(fused_bwd_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SMEM_BYTES)) != cudaSuccess ||
+      (err = cudaFuncSetAttribute(fused_bwd_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SMEM_BYTES)) != cudaSuccess)
     return err;
   Params p;
   memset(&p, 0, sizeof(p));
@@ -1120,9 +1126,9 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
   const unsigned units = unsigned(s.b * s.nc * s.G);
   tr.mark(st);
   if (dx_add)
-    fused_bwd_kernel<true><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
+    fused_bwd_kernel<true, 1><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   else
-    fused_bwd_kernel<false><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
+    fused_bwd_kernel<false, 0><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   tr.mark(st);
   return cudaGetLastError();
 }
@@ -1143,6 +1149,16 @@ Shape split_half(const Shape &s) {
   return h;
 }
 
+// The half as the kernel sees it: the group's heads in two slices (two units
+// per chunk and half: the units are half as long, so the grid packs the SMs
+// more evenly); dB and dC are then per-slice partial sums.
+Shape split_units(const Shape &s) {
+  Shape h = split_half(s);
+  h.G = 2 * s.G;
+  h.hpg = s.hpg / 2;
+  return h;
+}
+
 SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   const Shape h = split_half(s);
   SplitBwdWs w;
@@ -1151,16 +1167,17 @@ SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   w.dD_scratch = cv.take<float>(h.H);
   w.zeros = cv.take<float>(h.H);
   w.ddt1 = cv.take<float>(s.b * s.T * s.H);
-  for (int j = 0; j < 2; ++j) {
-    w.dBh[j] = cv.take<float>(s.b * s.T * kN);
-    w.dCh[j] = cv.take<float>(s.b * s.T * kN);
+  for (int j = 0; j < 2; ++j) {   // dB, dC: (b, T, slice, 128) partial sums of each half
+    w.dBh[j] = cv.take<float>(s.b * s.T * 2 * kN);
+    w.dCh[j] = cv.take<float>(s.b * s.T * 2 * kN);
     w.dinit_h[j] = cv.take<float>(s.nseq * s.H * kP * kN);
   }
   return w;
 }
 
-// ddt += ddt of the second half; dB, dC and dinit assembled from their
-// halves (grid-stride over float4 groups of each array in turn)
+// ddt += ddt of the second half; dB, dC assembled from their halves (each the
+// sum of its two head slices, slice 0 first) and dinit from its halves
+// (grid-stride over float4 groups of each array in turn)
 __global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_rows, float *__restrict__ ddt,
                                   const float *__restrict__ ddt1, float *__restrict__ dB, float *__restrict__ dC,
                                   const float *__restrict__ dB0, const float *__restrict__ dB1,
@@ -1193,7 +1210,13 @@ __global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_row
       src0 = di0, src1 = di1, out = dinit;
     }
     const int64_t row = k / (2 * q), rem = k % (2 * q), j = rem / q, g4 = rem % q;
-    reinterpret_cast<float4 *>(out)[k] = __ldcs(reinterpret_cast<const float4 *>(j ? src1 : src0) + row * q + g4);
+    const float4 *src = reinterpret_cast<const float4 *>(j ? src1 : src0);
+    if (out == dinit) {
+      reinterpret_cast<float4 *>(out)[k] = __ldcs(src + row * q + g4);
+    } else {   // head slice 0 then slice 1
+      const float4 a = __ldcs(src + (row * 2) * q + g4), b = __ldcs(src + (row * 2 + 1) * q + g4);
+      reinterpret_cast<float4 *>(out)[k] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    }
   }
 }
 
@@ -1262,7 +1285,7 @@ cudaError_t side_stream(cudaStream_t *out) {
 
 cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
                             Trace &tr) {
-  const Shape h = split_half(s);
+  const Shape h = split_half(s), hu = split_units(s);
   Carver cv(ws);
   SplitBwdWs w = carve_split(cv, s, opt.ring_depth);
   cudaError_t err;
@@ -1306,7 +1329,7 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
     }
     FusedWs wj = j ? w.w1 : w.w;
     wj.status = w.w.status;    // one status word (ticket status[1 + j] per half) for the check
-    err = launch_pass(h, aj, wj, opt, 2 * kN, j, true, j ? side : st, tr);
+    err = launch_pass(hu, aj, wj, opt, 2 * kN, j, true, j ? side : st, tr);
   }
   if (err == cudaSuccess) err = cudaEventRecord(join, side);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(st, join, 0);   // join before the fold

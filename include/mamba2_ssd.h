@@ -128,7 +128,8 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
  * the dims are invalid).  All configurations give bitwise-identical
  * results; they differ in launch shape and scheduling only.  bf16 problems
  * with headdim 64, seqlen a multiple of the chunk, and either chunk 128 and
- * dstate 128 ("fused/...") or one group, chunk 128 or 256 and dstate 256
+ * dstate 128 ("fused/...") or one group, an even number of heads, chunk 128
+ * or 256 and dstate 256
  * ("fused-split/...": the recurrence never mixes state dimensions, so the
  * fused kernels run once per 128-wide state half, in 128-token chunks, and
  * the halves' contributions are summed in a fixed order) run the fused

@@ -262,3 +262,16 @@ def test_conv1d_rejects_bad_arguments_on_host(L):
                                    need - 1, 0, 0, None) == 3
     assert L.mamba2_ssd_conv1d_bwd(1, 300, 64, 4, 1, 1, p(0), p(1), None, None, p(2), p(3), p(4), p(5), p(6),
                                    need, 0, 2, None) == 1
+
+
+def test_dstate_256_shapes_pick_the_split_fused_path_or_the_general_one():
+    # one group, even head count, chunk 128 or 256: the fused kernels once per state half
+    assert ssd.config_name(ssd.make_dims(1, 512, 4, 64, 1, 256, 256), 0) == "fused-split/ring4"
+    assert ssd.config_name(ssd.make_dims(1, 512, 4, 64, 1, 256, 128), 1) == "fused-split/ring2"
+    assert ssd.bwd_launch_names(ssd.make_dims(1, 512, 4, 64, 1, 256, 256)) == [
+        "fused_bwd", "fused_bwd", "split_fold", "split_scalars"]
+    # odd head count, two groups, fp32, or a ragged length: the general path
+    for dims in (ssd.make_dims(1, 512, 3, 64, 1, 256, 256), ssd.make_dims(1, 512, 4, 64, 2, 256, 256),
+                 ssd.make_dims(1, 512, 4, 64, 1, 256, 256, dtype=torch.float32),
+                 ssd.make_dims(1, 500, 4, 64, 1, 256, 256)):
+        assert ssd.config_name(dims, 0).startswith("simt"), dims

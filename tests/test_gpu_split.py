@@ -19,7 +19,7 @@ TOL = 2e-3
 
 @pytest.mark.parametrize("case", [
     dict(b=1, T=512, H=4, Q=256),
-    dict(b=2, T=256, H=3, Q=128, with_init=True),
+    dict(b=2, T=256, H=4, Q=128, with_init=True),
     dict(b=1, T=1024, H=6, Q=256, seq_lens=(256, 512, 256), with_init=True),
     dict(b=1, T=768, H=2, Q=256, dt_shift=2.0),      # strong decay
 ])

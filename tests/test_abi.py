@@ -264,7 +264,7 @@ def test_conv1d_rejects_bad_arguments_on_host(L):
                                    need, 0, 2, None) == 1
 
 
-def test_dstate_256_shapes_pick_the_split_fused_path_or_the_general_one():
+def test_dstate_256_shapes_pick_the_split_fused_path_or_the_general_one(L):
     # one group, even head count, chunk 128 or 256: the fused kernels once per state half
     assert ssd.config_name(ssd.make_dims(1, 512, 4, 64, 1, 256, 256), 0) == "fused-split/ring4"
     assert ssd.config_name(ssd.make_dims(1, 512, 4, 64, 1, 256, 128), 1) == "fused-split/ring2"

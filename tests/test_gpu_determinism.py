@@ -60,12 +60,12 @@ def test_bitwise_across_every_config():
         assert len(flat) == 1, digests
 
 
-@pytest.mark.parametrize("name", ["bf16_T16384", "simt_bf16"])
+@pytest.mark.parametrize("name", ["bf16_T16384", "bf16_varlen_T32768", "simt_bf16"])
 def test_atomic_variant_shows_the_test_has_teeth(name):
     """The same kernels with atomic accumulation: expected to differ between
-    runs at these shapes (fused path: dA/dD; general path: dB/dC/dA/dD).  If
-    they happen not to, the repeat test above is not proof of anything and
-    this test says so."""
+    runs at these shapes (fused paths: per-warp dA/dD shares; general path:
+    dB/dC/dA/dD).  If they happen not to, the repeat test above is not proof
+    of anything and this test says so."""
     if name == "simt_bf16":
         d, Q = make_inputs(1, 2000, 64, 64, 2, 128, dtype=torch.bfloat16, seed=8, dt_shift=4.0), 128
     else:

@@ -53,6 +53,42 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, const float (&v)[4]) {
   *reinterpret_cast<uint2 *>(p) = u;
 }
 
+// Each thread streams the rows it will read next into its own slots of a
+// shared-memory ring with asynchronous copies, kDepth tokens ahead: the loads
+// are in flight without holding registers.  Slot (d, a) of thread i is the
+// 16-byte word at ((d * 2 + a) * blockDim.x + i) * 16 (a = 0: x, 1: dy).
+constexpr int kDepth = 8;
+
+__device__ __forceinline__ uint32_t ring_slot(uint32_t base, int d, int a) {
+  return base + uint32_t(((d * 2 + a) * int(blockDim.x) + int(threadIdx.x)) * 16);
+}
+// Copy the 4 channels of one token (8 bytes of bf16 or 16 of fp32) into a ring
+// slot, or zeros when `valid` is false (nothing is read then).
+template <class TIn>
+__device__ __forceinline__ void stream_row(uint32_t dst, const TIn *src, bool valid) {
+  if (sizeof(TIn) == 2)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(valid ? 8 : 0) : "memory");
+  else
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void stream_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// the oldest of the kDepth groups in flight has landed
+__device__ __forceinline__ void stream_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kDepth - 1) : "memory"); }
+
+__device__ __forceinline__ void read_slot(uint32_t a, const float *, float (&v)[4]) {
+  float4 u;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w) : "r"(a));
+  v[0] = u.x, v[1] = u.y, v[2] = u.z, v[3] = u.w;
+}
+__device__ __forceinline__ void read_slot(uint32_t a, const __nv_bfloat16 *, float (&v)[4]) {
+  uint32_t lo, hi;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(lo), "=r"(hi) : "r"(a));
+  const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&lo));
+  const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&hi));
+  v[0] = p.x, v[1] = p.y, v[2] = q.x, v[3] = q.y;
+}
+
 // logistic function, no overflow for either sign of v
 __device__ __forceinline__ float sigmoid(float v) {
   const float e = expf(-fabsf(v));
@@ -92,23 +128,31 @@ __global__ void conv_fwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
   for (int k = 0; k < K; ++k)
 #pragma unroll
     for (int i = 0; i < kVec; ++i) win[k][i] = 0.f;
-  for (int64_t t = t0 - (K - 1); t < t1; ++t) {
+  extern __shared__ __align__(16) uint8_t ring_raw[];
+  const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
+  const int64_t u0 = t0 - (K - 1);
+  auto issue = [&](int64_t u) {
+    const bool ok = u >= 0 && u < t1;
+    stream_row(ring_slot(ring, int((u - u0) % kDepth), 0), x + (ok ? (bi * s.T + u) * s.C + c0 : c0), ok);
+    stream_commit();
+  };
+  for (int j = 0; j < kDepth; ++j) issue(u0 + j);
+  for (int64_t t = u0; t < t1; ++t) {
 #pragma unroll
     for (int k = 0; k + 1 < K; ++k)
 #pragma unroll
       for (int i = 0; i < kVec; ++i) win[k][i] = win[k + 1][i];
-    if (t < 0) {
-#pragma unroll
-      for (int i = 0; i < kVec; ++i) win[K - 1][i] = 0.f;
-      continue;
-    }
+    stream_wait();
+    const uint32_t slot = ring_slot(ring, int((t - u0) % kDepth), 0);
+    read_slot(slot, x, win[K - 1]);   // zeros before the row start
+    issue(t + kDepth);                // the slot just read takes the token kDepth ahead
+    if (t < 0) continue;
     if (starts_seq(seq_idx, bi, s.T, t)) {   // earlier taps belong to another sequence
 #pragma unroll
       for (int k = 0; k + 1 < K; ++k)
 #pragma unroll
         for (int i = 0; i < kVec; ++i) win[k][i] = 0.f;
     }
-    load4(x + (bi * s.T + t) * s.C + c0, win[K - 1]);
     if (t < t0) continue;
     float out[kVec];
 #pragma unroll
@@ -120,6 +164,7 @@ __global__ void conv_fwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
     }
     store4(y + (bi * s.T + t) * s.C + c0, out);
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Backward of one (tile, 4 channels): dpre of the tile's tokens and of the
@@ -156,8 +201,20 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
 #pragma unroll
   for (int i = 0; i < kVec; ++i) dbp[i] = 0.f;
   // tokens past the row end take part as zeros, so that dx of the tile's last
-  // tokens comes out of the same loop (every window index stays static)
-  for (int64_t u = t0 - (K - 1); u < t1 + (K - 1); ++u) {
+  // tokens comes out of the same loop (every window index stays static); x and
+  // dy of the next kDepth tokens stream into this thread's ring slots meanwhile
+  extern __shared__ __align__(16) uint8_t ring_raw[];
+  const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
+  const int64_t u0 = t0 - (K - 1), u1 = t1 + (K - 1);
+  auto issue = [&](int64_t u) {
+    const int d = int((u - u0) % kDepth);
+    const bool okx = u >= 0 && u < s.T && u < u1, okg = okx && u >= t0;
+    stream_row(ring_slot(ring, d, 0), x + (okx ? (bi * s.T + u) * s.C + c0 : c0), okx);
+    stream_row(ring_slot(ring, d, 1), dy + (okg ? (bi * s.T + u) * s.C + c0 : c0), okg);
+    stream_commit();
+  };
+  for (int j = 0; j < kDepth; ++j) issue(u0 + j);
+  for (int64_t u = u0; u < u1; ++u) {
 #pragma unroll
     for (int k = 0; k + 1 < K; ++k)
 #pragma unroll
@@ -166,8 +223,16 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
         dz[k][i] = dz[k + 1][i];
       }
     st >>= 1;
+    float g[kVec];
+    stream_wait();
+    {
+      const int d = int((u - u0) % kDepth);
+      read_slot(ring_slot(ring, d, 0), x, xw[K - 1]);   // zeros outside the row
+      read_slot(ring_slot(ring, d, 1), dy, g);          // zeros before the tile and outside the row
+    }
+    issue(u + kDepth);
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) xw[K - 1][i] = dz[K - 1][i] = 0.f;
+    for (int i = 0; i < kVec; ++i) dz[K - 1][i] = 0.f;
     if (u >= 0 && u < s.T) {
       if (starts_seq(seq_idx, bi, s.T, u)) {
         st |= 1u << (K - 1);
@@ -176,10 +241,7 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
 #pragma unroll
           for (int i = 0; i < kVec; ++i) xw[k][i] = 0.f;
       }
-      load4(x + (bi * s.T + u) * s.C + c0, xw[K - 1]);
       if (u >= t0) {
-        float g[kVec];
-        load4(dy + (bi * s.T + u) * s.C + c0, g);
 #pragma unroll
         for (int i = 0; i < kVec; ++i) {
           float acc = bv[i];
@@ -220,6 +282,7 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
       store4(dx + (bi * s.T + sx) * s.C + c0, o);
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   if (kAtomic) {
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
@@ -251,6 +314,8 @@ __global__ void conv_fold_kernel(int64_t C, int K, int64_t tiles, const float *_
 }
 
 constexpr int kConvBlocks[] = {128, 256};
+// dynamic shared memory of a block: each thread's kDepth x {x, dy} 16-byte slots
+size_t ring_bytes(int block) { return size_t(kDepth) * 2 * 16 * size_t(block); }
 constexpr int kNumConvConfigs = 2;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -273,18 +338,27 @@ bool conv_shape(int64_t batch, int64_t seqlen, int64_t channels, int32_t width, 
   return true;
 }
 
+// Launch with the block's ring of shared memory (above the 48 KB default for 256 threads).
+template <class Kern, class... Args>
+cudaError_t launch_ring(Kern kernel, dim3 grid, int block, cudaStream_t st, Args... args) {
+  const size_t smem = ring_bytes(block);
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (err != cudaSuccess) return err;
+  kernel<<<grid, block, smem, st>>>(args...);
+  return cudaGetLastError();
+}
+
 template <class TIn>
 cudaError_t launch_fwd(const ConvShape &s, int K, dim3 grid, int block, const void *x, const float *w,
                        const float *bias, const int32_t *seq_idx, void *y, cudaStream_t st) {
   const TIn *xx = static_cast<const TIn *>(x);
   TIn *yy = static_cast<TIn *>(y);
   switch (K) {
-    case 1: conv_fwd_kernel<TIn, 1><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, yy); break;
-    case 2: conv_fwd_kernel<TIn, 2><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, yy); break;
-    case 3: conv_fwd_kernel<TIn, 3><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, yy); break;
-    default: conv_fwd_kernel<TIn, 4><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, yy); break;
+    case 1: return launch_ring(conv_fwd_kernel<TIn, 1>, grid, block, st, s, xx, w, bias, seq_idx, yy);
+    case 2: return launch_ring(conv_fwd_kernel<TIn, 2>, grid, block, st, s, xx, w, bias, seq_idx, yy);
+    case 3: return launch_ring(conv_fwd_kernel<TIn, 3>, grid, block, st, s, xx, w, bias, seq_idx, yy);
+    default: return launch_ring(conv_fwd_kernel<TIn, 4>, grid, block, st, s, xx, w, bias, seq_idx, yy);
   }
-  return cudaGetLastError();
 }
 
 template <class TIn, bool kAtomic>
@@ -293,12 +367,11 @@ cudaError_t launch_bwd(const ConvShape &s, int K, dim3 grid, int block, const vo
                        float *dbias, cudaStream_t st) {
   const TIn *xx = static_cast<const TIn *>(x), *gg = static_cast<const TIn *>(dy);
   switch (K) {
-    case 1: conv_bwd_kernel<TIn, 1, kAtomic><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias); break;
-    case 2: conv_bwd_kernel<TIn, 2, kAtomic><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias); break;
-    case 3: conv_bwd_kernel<TIn, 3, kAtomic><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias); break;
-    default: conv_bwd_kernel<TIn, 4, kAtomic><<<grid, block, 0, st>>>(s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias); break;
+    case 1: return launch_ring(conv_bwd_kernel<TIn, 1, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
+    case 2: return launch_ring(conv_bwd_kernel<TIn, 2, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
+    case 3: return launch_ring(conv_bwd_kernel<TIn, 3, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
+    default: return launch_ring(conv_bwd_kernel<TIn, 4, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

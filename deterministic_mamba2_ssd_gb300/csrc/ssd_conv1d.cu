@@ -58,6 +58,7 @@ __device__ __forceinline__ void store4(__nv_bfloat16 *p, const float (&v)[4]) {
 // are in flight without holding registers.  Slot (d, a) of thread i is the
 // 16-byte word at ((d * 2 + a) * blockDim.x + i) * 16 (a = 0: x, 1: dy).
 constexpr int kDepth = 8;
+static_assert((kDepth & (kDepth - 1)) == 0, "ring depth: a power of two");
 
 __device__ __forceinline__ uint32_t ring_slot(uint32_t base, int d, int a) {
   return base + uint32_t(((d * 2 + a) * int(blockDim.x) + int(threadIdx.x)) * 16);
@@ -131,21 +132,22 @@ __global__ void conv_fwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
   extern __shared__ __align__(16) uint8_t ring_raw[];
   const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
   const int64_t u0 = t0 - (K - 1);
-  auto issue = [&](int64_t u) {
+  const TIn *row = x + (bi * s.T + u0) * s.C + c0;   // token u0 (read only where it exists)
+  auto issue = [&](int64_t u, int d, const TIn *p) {
     const bool ok = u >= 0 && u < t1;
-    stream_row(ring_slot(ring, int((u - u0) % kDepth), 0), x + (ok ? (bi * s.T + u) * s.C + c0 : c0), ok);
+    stream_row(ring_slot(ring, d, 0), ok ? p : x, ok);
     stream_commit();
   };
-  for (int j = 0; j < kDepth; ++j) issue(u0 + j);
-  for (int64_t t = u0; t < t1; ++t) {
+  for (int j = 0; j < kDepth; ++j) issue(u0 + j, j, row + j * s.C);
+  int d = 0;   // ring slot of token t
+  for (int64_t t = u0; t < t1; ++t, d = (d + 1) & (kDepth - 1), row += s.C) {
 #pragma unroll
     for (int k = 0; k + 1 < K; ++k)
 #pragma unroll
       for (int i = 0; i < kVec; ++i) win[k][i] = win[k + 1][i];
     stream_wait();
-    const uint32_t slot = ring_slot(ring, int((t - u0) % kDepth), 0);
-    read_slot(slot, x, win[K - 1]);   // zeros before the row start
-    issue(t + kDepth);                // the slot just read takes the token kDepth ahead
+    read_slot(ring_slot(ring, d, 0), x, win[K - 1]);   // zeros before the row start
+    issue(t + kDepth, d, row + kDepth * s.C);          // the slot just read takes the token kDepth ahead
     if (t < 0) continue;
     if (starts_seq(seq_idx, bi, s.T, t)) {   // earlier taps belong to another sequence
 #pragma unroll
@@ -162,7 +164,7 @@ __global__ void conv_fwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
       for (int k = 0; k < K; ++k) acc = fmaf(wv[k][i], win[k][i], acc);
       out[i] = s.silu ? acc * sigmoid(acc) : acc;
     }
-    store4(y + (bi * s.T + t) * s.C + c0, out);
+    store4(y + (row - x) , out);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -206,15 +208,17 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
   extern __shared__ __align__(16) uint8_t ring_raw[];
   const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
   const int64_t u0 = t0 - (K - 1), u1 = t1 + (K - 1);
-  auto issue = [&](int64_t u) {
-    const int d = int((u - u0) % kDepth);
+  const int64_t off0 = (bi * s.T + u0) * s.C + c0;   // element offset of token u0 (read only where it exists)
+  auto issue = [&](int64_t u, int d, int64_t off) {
     const bool okx = u >= 0 && u < s.T && u < u1, okg = okx && u >= t0;
-    stream_row(ring_slot(ring, d, 0), x + (okx ? (bi * s.T + u) * s.C + c0 : c0), okx);
-    stream_row(ring_slot(ring, d, 1), dy + (okg ? (bi * s.T + u) * s.C + c0 : c0), okg);
+    stream_row(ring_slot(ring, d, 0), okx ? x + off : x, okx);
+    stream_row(ring_slot(ring, d, 1), okg ? dy + off : dy, okg);
     stream_commit();
   };
-  for (int j = 0; j < kDepth; ++j) issue(u0 + j);
-  for (int64_t u = u0; u < u1; ++u) {
+  for (int j = 0; j < kDepth; ++j) issue(u0 + j, j, off0 + j * s.C);
+  int dslot = 0;   // ring slot of token u
+  int64_t off = off0;
+  for (int64_t u = u0; u < u1; ++u, dslot = (dslot + 1) & (kDepth - 1), off += s.C) {
 #pragma unroll
     for (int k = 0; k + 1 < K; ++k)
 #pragma unroll
@@ -225,12 +229,9 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
     st >>= 1;
     float g[kVec];
     stream_wait();
-    {
-      const int d = int((u - u0) % kDepth);
-      read_slot(ring_slot(ring, d, 0), x, xw[K - 1]);   // zeros outside the row
-      read_slot(ring_slot(ring, d, 1), dy, g);          // zeros before the tile and outside the row
-    }
-    issue(u + kDepth);
+    read_slot(ring_slot(ring, dslot, 0), x, xw[K - 1]);   // zeros outside the row
+    read_slot(ring_slot(ring, dslot, 1), dy, g);          // zeros before the tile and outside the row
+    issue(u + kDepth, dslot, off + kDepth * s.C);
 #pragma unroll
     for (int i = 0; i < kVec; ++i) dz[K - 1][i] = 0.f;
     if (u >= 0 && u < s.T) {
@@ -279,7 +280,7 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
           for (int i = 0; i < kVec; ++i) o[i] = fmaf(wv[K - 1 - j][i], dz[j][i], o[i]);
         }
       }
-      store4(dx + (bi * s.T + sx) * s.C + c0, o);
+      store4(dx + off - (K - 1) * s.C, o);   // token sx = u - (K - 1)
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");

@@ -220,8 +220,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "39f33f083ffe38dfa1044afd4a22f2224d819f14cd3d32ebd9fc1b983ea777b0": {
-        "bytes_per_token": (2283985920 + 1239201024) / 16384,
+    "e94f21ef22f37d2ef5725b9f543ed32c4a88938fb9e9c14778645fd27e912502": {
+        "bytes_per_token": (2283359744 + 1248142336) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

@@ -88,6 +88,10 @@ def lib():
         L.mamba2_ssd_bwd_fault_test.restype = ci
         L.mamba2_ssd_states_unpack.argtypes = [ctypes.POINTER(SavedStruct), vp, vp]
         L.mamba2_ssd_states_unpack.restype = ci
+        L.mamba2_ssd_padded_chunks.argtypes = [pd]
+        L.mamba2_ssd_padded_chunks.restype = i64
+        L.mamba2_ssd_padded_piece_table.argtypes = [pd, vp, vp]
+        L.mamba2_ssd_padded_piece_table.restype = ci
         L.mamba2_ssd_selftest_umma.argtypes = [vp] * 3 + [ci] * 6 + [vp]
         L.mamba2_ssd_selftest_umma.restype = ci
         L.mamba2_ssd_static_scratch_bytes.argtypes = []

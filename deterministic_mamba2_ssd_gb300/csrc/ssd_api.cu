@@ -4,6 +4,7 @@
 // check in the forward).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "mamba2_ssd.h"
@@ -58,17 +59,29 @@ constexpr int kFusedRings[] = {4, 2};
 constexpr int kNumFused = 2;
 
 // Which backward a shape runs.  The fused kernels reset the state at chunk
-// boundaries only, so sequence starts inside a chunk always take the general
-// path; dstate 256 with one group runs the fused kernels once per state half.
-enum Kind { kSimt = 0, kFused = 1, kSplit = 2 };
+// starts only; dstate 256 with one group runs them once per state half.
+// Sequence starts inside a chunk run them on a padded copy of the problem
+// (every piece of a sequence inside one 128-token chunk padded to a chunk of
+// its own) when the padding at most doubles the chunk count, and take the
+// general path otherwise.
+enum Kind { kSimt = 0, kFused = 1, kSplit = 2, kFusedPad = 3, kSplitPad = 4 };
 Kind kind_of(const ssd_dims *d) {
-  if (d->flags & SSD_DIMS_SEQ_ANY_START) return kSimt;
   const ssd::Shape s = shape_of(d);
-  if (ssd::fused_bwd_supported(s, d->dtype == SSD_BF16)) return kFused;
-  if (ssd::fused_split_supported(s, d->dtype == SSD_BF16)) return kSplit;
+  const bool bf16 = d->dtype == SSD_BF16;
+  if (d->flags & SSD_DIMS_SEQ_ANY_START) {
+    if (d->batch != 1 || !bf16 || s.nseq - 1 > (s.T + 127) / 128) return kSimt;
+    const ssd::Shape p = ssd::padded_shape(s);
+    if (s.Q == 128 && ssd::fused_bwd_supported(p, bf16)) return kFusedPad;
+    if ((s.Q == 128 || s.Q == 256) && ssd::fused_split_supported(p, bf16)) return kSplitPad;
+    return kSimt;
+  }
+  if (ssd::fused_bwd_supported(s, bf16)) return kFused;
+  if (ssd::fused_split_supported(s, bf16)) return kSplit;
   return kSimt;
 }
 bool use_fused(const ssd_dims *d) { return kind_of(d) != kSimt; }
+bool is_split(Kind k) { return k == kSplit || k == kSplitPad; }
+bool is_padded(Kind k) { return k == kFusedPad || k == kSplitPad; }
 
 bool has_seq(const ssd_dims *d) { return (d->flags & SSD_DIMS_SEQ_IDX) != 0; }
 
@@ -90,6 +103,7 @@ ssd::FusedOptions fused_options(const ssd_dims *d, int config, int variant) {
   ssd::FusedOptions o;
   // with sequence starts the chain can be cut, so every (128-token) chunk gets its own slot
   o.ring_depth = (d->flags & SSD_DIMS_SEQ_IDX) ? int((d->seqlen + 127) / 128) : kFusedRings[config];
+  if (is_padded(kind_of(d))) o.ring_depth = int(ssd::padded_chunks(shape_of(d)));
   o.atomic = variant == SSD_VARIANT_ATOMIC;
   return o;
 }
@@ -121,6 +135,8 @@ size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
   switch (kind_of(dims)) {
     case kFused: return ssd::fused_fwd_workspace(shape_of(dims));
     case kSplit: return ssd::fused_fwd_split_workspace(shape_of(dims));
+    case kFusedPad: return ssd::padded_fwd_workspace(shape_of(dims), false);
+    case kSplitPad: return ssd::padded_fwd_workspace(shape_of(dims), true);
     default: return ssd::simt_fwd_workspace(shape_of(dims));
   }
 }
@@ -132,40 +148,61 @@ int mamba2_ssd_num_configs(const ssd_dims *dims) {
 
 const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
-  if (kind_of(dims) == kSplit) return config == 0 ? "fused-split/ring4" : "fused-split/ring2";
-  if (use_fused(dims)) return config == 0 ? "fused/ring4" : "fused/ring2";
+  switch (kind_of(dims)) {
+    case kSplit: return config == 0 ? "fused-split/ring4" : "fused-split/ring2";
+    case kFused: return config == 0 ? "fused/ring4" : "fused/ring2";
+    // (with seq_idx every chunk has its own ring slot, so both configurations run the same launches)
+    case kSplitPad: return config == 0 ? "fused-split-padded/0" : "fused-split-padded/1";
+    case kFusedPad: return config == 0 ? "fused-padded/0" : "fused-padded/1";
+    default: break;
+  }
   return config == 0 ? "simt/block256" : "simt/block128";
 }
 
 size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (!variant_ok(dims, variant)) return 0;
-  if (kind_of(dims) == kSplit)
-    return ssd::fused_bwd_split_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
-  if (use_fused(dims)) return ssd::fused_bwd_workspace(shape_of(dims), fused_options(dims, config, variant).ring_depth);
+  const int ring = fused_options(dims, config, variant).ring_depth;
+  switch (kind_of(dims)) {
+    case kSplit: return ssd::fused_bwd_split_workspace(shape_of(dims), ring);
+    case kFused: return ssd::fused_bwd_workspace(shape_of(dims), ring);
+    case kFusedPad: return ssd::padded_bwd_workspace(shape_of(dims), false, ring);
+    case kSplitPad: return ssd::padded_bwd_workspace(shape_of(dims), true, ring);
+    default: break;
+  }
   return ssd::simt_bwd_workspace(shape_of(dims), variant);
 }
 
 int mamba2_ssd_bwd_num_launches(const ssd_dims *dims, int config, int variant) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return 0;
   if (!variant_ok(dims, variant)) return 0;
-  if (kind_of(dims) == kSplit) return variant == SSD_VARIANT_ATOMIC ? 3 : 4;
-  if (use_fused(dims)) return variant == SSD_VARIANT_ATOMIC ? 1 : 2;
+  const Kind kind = kind_of(dims);
+  if (kind != kSimt) {
+    const int core = is_split(kind) ? (variant == SSD_VARIANT_ATOMIC ? 3 : 4) : (variant == SSD_VARIANT_ATOMIC ? 1 : 2);
+    return core + (is_padded(kind) ? 2 : 0);   // (padded: the dout gather before, the gradient scatter after)
+  }
   return ssd::simt_bwd_launches(shape_of(dims), variant, has_seq(dims));
 }
 
 const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int variant, int k) {
   if (!dims_ok(dims) || config < 0 || config >= mamba2_ssd_num_configs(dims)) return "invalid";
   if (!variant_ok(dims, variant)) return "invalid";
-  if (kind_of(dims) == kSplit) {   // one fused launch per state half, then the fold
-    static const char *det[] = {"fused_bwd", "fused_bwd", "split_fold", "split_scalars"};
-    static const char *atm[] = {"fused_bwd_atomic", "fused_bwd_atomic", "split_fold"};
-    if (variant == SSD_VARIANT_ATOMIC) return (k >= 0 && k < 3) ? atm[k] : "invalid";
-    return (k >= 0 && k < 4) ? det[k] : "invalid";
-  }
-  if (use_fused(dims)) {
-    if (variant == SSD_VARIANT_ATOMIC) return k == 0 ? "fused_bwd_atomic" : "invalid";
-    return k == 0 ? "fused_bwd" : (k == 1 ? "fold_scalars" : "invalid");
+  const Kind kind = kind_of(dims);
+  if (kind != kSimt) {
+    const int n = mamba2_ssd_bwd_num_launches(dims, config, variant);
+    if (k < 0 || k >= n) return "invalid";
+    if (is_padded(kind)) {   // the gather and the scatter around the launches of the unpadded form
+      if (k == 0) return "pad_gather";
+      if (k == n - 1) return "pad_scatter";
+      --k;
+    }
+    if (is_split(kind)) {   // one fused launch per state half, then the fold
+      static const char *det[] = {"fused_bwd", "fused_bwd", "split_fold", "split_scalars"};
+      static const char *atm[] = {"fused_bwd_atomic", "fused_bwd_atomic", "split_fold"};
+      return variant == SSD_VARIANT_ATOMIC ? atm[k] : det[k];
+    }
+    if (variant == SSD_VARIANT_ATOMIC) return "fused_bwd_atomic";
+    return k == 0 ? "fused_bwd" : "fold_scalars";
   }
   return ssd::simt_bwd_launch_name(variant, has_seq(dims), k);
 }
@@ -197,12 +234,14 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   if (workspace_bytes < mamba2_ssd_fwd_workspace_size(dims)) return SSD_ERR_WORKSPACE;
   if (!workspace || !aligned16(workspace)) return SSD_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t> host_seq;
   if (seq_idx) {
     // Ids must be valid and non-decreasing; without SSD_DIMS_SEQ_ANY_START
     // every sequence start must also fall on a chunk start (the fused
     // backward resets the state there only).  One synchronous copy, documented.
     if (dims->batch != 1) return SSD_ERR_UNSUPPORTED;
-    std::vector<int32_t> h(size_t(s.T));
+    std::vector<int32_t> &h = host_seq;
+    h.resize(size_t(s.T));
     if (cudaMemcpyAsync(h.data(), seq_idx, size_t(s.T) * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
       return SSD_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
@@ -219,17 +258,40 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   // The fused shape family runs the tensor-core forward, which writes each saved state as the
   // packed bf16 hi | lo operand pair the fused backward takes; dstate 256 runs it per state half
   // (packed states of both halves kept in the workspace); every other shape the general one.
+  // Sequence starts inside a chunk run the fused kernels on a padded copy kept in the workspace.
   const Kind kind = kind_of(dims);
-  const cudaError_t err = kind == kFused   ? ssd::fused_fwd(s, a, workspace, st)
-                          : kind == kSplit ? ssd::fused_fwd_split(s, a, workspace, st)
-                                           : ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
+  cudaError_t err;
+  switch (kind) {
+    case kFused: err = ssd::fused_fwd(s, a, workspace, st); break;
+    case kSplit: err = ssd::fused_fwd_split(s, a, workspace, st); break;
+    case kFusedPad:
+    case kSplitPad: err = ssd::padded_fwd(s, kind == kSplitPad, a, host_seq.data(), workspace, st); break;
+    default: err = ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
+  }
   if (err != cudaSuccess) return SSD_ERR_CUDA;
-  saved_out->aux = kind == kSplit ? ssd::fused_split_aux(s, workspace) : nullptr;
+  saved_out->aux = kind == kSplit ? ssd::fused_split_aux(s, workspace) : is_padded(kind) ? static_cast<const float *>(workspace)
+                                                                         : nullptr;
   saved_out->dims = *dims;
   saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
   saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;
   saved_out->magic = kSavedMagic;
   saved_out->flags = 0;
+  return SSD_OK;
+}
+
+int64_t mamba2_ssd_padded_chunks(const ssd_dims *dims) {
+  if (!dims_ok(dims) || !is_padded(kind_of(dims))) return 0;
+  return ssd::padded_chunks(shape_of(dims));
+}
+
+ssd_status mamba2_ssd_padded_piece_table(const ssd_dims *dims, const int32_t *seq_idx, int32_t *table) {
+  if (!dims_ok(dims) || !is_padded(kind_of(dims)) || !seq_idx || !table) return SSD_ERR_INVALID_ARG;
+  const ssd::Shape s = shape_of(dims);
+  for (int64_t t = 0; t < s.T; ++t)
+    if (seq_idx[t] < 0 || seq_idx[t] >= s.nseq || (t > 0 && seq_idx[t] < seq_idx[t - 1])) return SSD_ERR_INVALID_ARG;
+  std::vector<int32_t> tab;
+  if (!ssd::build_piece_table(s, seq_idx, tab)) return SSD_ERR_INVALID_ARG;
+  std::copy(tab.begin(), tab.end(), table);
   return SSD_OK;
 }
 
@@ -274,11 +336,16 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   tr.events = reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events));
   tr.count = num_events;
   cudaError_t err;
-  if (kind_of(dims) == kSplit) {
+  const Kind kind = kind_of(dims);
+  if (is_padded(kind) || kind == kSplit) {
     if (!saved->aux) return SSD_ERR_HANDLE;   // the packed states live in the forward's workspace
+  }
+  if (is_padded(kind)) {
+    err = ssd::padded_bwd(s, kind == kSplitPad, a, saved->aux, workspace, fused_options(dims, config, variant), st, tr);
+  } else if (kind == kSplit) {
     a.states_in = saved->aux;
     err = ssd::fused_bwd_split(s, a, workspace, fused_options(dims, config, variant), st, tr);
-  } else if (use_fused(dims))
+  } else if (kind == kFused)
     err = ssd::fused_bwd(s, a, workspace, fused_options(dims, config, variant), st, tr);
   else
     err = ssd::simt_bwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[config], variant, kOrderedSpinLimit, st,

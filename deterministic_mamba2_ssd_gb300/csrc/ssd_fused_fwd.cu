@@ -685,7 +685,8 @@ cudaError_t fused_fwd_split(const Shape &s, const Args &a, void *ws, cudaStream_
     fwd_state_kernel<<<units, 128, K1_SMEM, st>>>(p, tm_x, tm_b[j]);
     fwd_pass_kernel<<<unsigned((h.b * h.H * kN * 8 + 255) / 256), 256, 0, st>>>(p);
   }
-  states_view_kernel<<<unsigned(s.b * s.nc * s.H * 2), 256, 0, st>>>(s, int(s.Q / kQ), w.aux, a.states_out);
+  if (a.states_out)   // (a caller that reads the packed states itself passes none)
+    states_view_kernel<<<unsigned(s.b * s.nc * s.H * 2), 256, 0, st>>>(s, int(s.Q / kQ), w.aux, a.states_out);
   // y: half 0 (with D) into fp32, then half 1 (no D) added and rounded once
   for (int j = 0; j < 2; ++j) {
     p.states = w.aux + j * tiles;

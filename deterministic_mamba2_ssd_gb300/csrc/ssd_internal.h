@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <vector>
+
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -49,5 +51,24 @@ size_t fused_bwd_split_workspace(const Shape &s, int ring_depth);
 cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st,
                             Trace &tr);
 cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
+
+// Packed batches (batch 1, seq_idx) whose sequences may start inside a chunk:
+// the token stream is cut at every sequence start and every 128 tokens, each
+// piece padded to a 128-token chunk with tokens that leave the state and all
+// real gradients unchanged, and the fused kernels above run the padded
+// problem (`split`: the dstate-256 form).  The forward keeps the padded inputs
+// and packed states in its workspace for the backward; the caller's state
+// buffer gets the fp32 states entering each of its chunks.
+int64_t padded_chunks(const Shape &s);   // ceil(T / 128) + nseq - 1
+Shape padded_shape(const Shape &s);      // batch 1, padded_chunks chunks of 128 tokens
+// Piece table from the host copy of seq_idx: start[npc] | len[npc] | id[npc] |
+// map[nc] (caller chunk -> padded chunk); false if the ids change more often
+// than nseq allows.
+bool build_piece_table(const Shape &s, const int32_t *seq, std::vector<int32_t> &tab);
+size_t padded_fwd_workspace(const Shape &s, bool split);
+size_t padded_bwd_workspace(const Shape &s, bool split, int ring_depth);
+cudaError_t padded_fwd(const Shape &s, bool split, const Args &a, const int32_t *host_seq, void *ws, cudaStream_t st);
+cudaError_t padded_bwd(const Shape &s, bool split, const Args &a, const void *fwd_ws, void *ws,
+                       const FusedOptions &opt, cudaStream_t st, Trace &tr);
 
 }  // namespace ssd

@@ -85,9 +85,14 @@ typedef struct {
 /* ssd_dims.flags (with SSD_DIMS_SEQ_IDX): sequences may start anywhere, not
  * only at multiples of chunk_size.  A sequence that starts inside a chunk
  * begins from its own initial state (or zero) exactly as the recurrence
- * says; decay terms never cross a sequence start.  These dims always run the
- * general CUDA-core backward (the fused one resets states at chunk starts
- * only). */
+ * says; decay terms never cross a sequence start.  The fused kernels reset
+ * states at chunk starts only, so these dims run them on a padded copy of the
+ * problem (mamba2_ssd_padded_chunks) when they are bf16 with batch 1,
+ * headdim 64, nseq - 1 <= ceil(seqlen / 128), and either chunk 128 and
+ * dstate 128 ("fused-padded") or one group, an even head count, chunk 128 or
+ * 256 and dstate 256 ("fused-split-padded"); seqlen need not be a multiple
+ * of the chunk there.  Every other such shape runs the general CUDA-core
+ * kernels. */
 #define SSD_DIMS_SEQ_ANY_START 2
 
 /* What the backward needs from the forward.  Filled by mamba2_ssd_fwd; it
@@ -105,8 +110,9 @@ typedef struct {
   const float *states;        /* (b,nc,H,P,N) states entering each chunk (packed on the fused shapes;
                                  see mamba2_ssd_fwd and mamba2_ssd_states_unpack) */
   const float *aux;           /* dstate-256 fused shapes: the packed states of both state halves, inside
-                                 the forward's workspace (which must then stay alive and unmodified until
-                                 the backward has run); NULL otherwise */
+                                 the forward's workspace; "-padded" shapes: the forward's workspace itself
+                                 (the padded problem); either must then stay alive and unmodified until
+                                 the backward has run; NULL otherwise */
   uint32_t magic;
   uint32_t flags;
 } ssd_saved;
@@ -133,8 +139,9 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
  * ("fused-split/...": the recurrence never mixes state dimensions, so the
  * fused kernels run once per 128-wide state half, in 128-token chunks, and
  * the halves' contributions are summed in a fixed order) run the fused
- * tensor-core forward and backward (unless SSD_DIMS_SEQ_ANY_START is set);
- * every other shape runs the general CUDA-core ones. */
+ * tensor-core forward and backward (with SSD_DIMS_SEQ_ANY_START set, the
+ * "-padded" forms of both, see there); every other shape runs the general
+ * CUDA-core ones. */
 int mamba2_ssd_num_configs(const ssd_dims *dims);
 
 /* Name of the backward algorithm a configuration selects (static string). */
@@ -166,14 +173,38 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
  * chunk j at position j ^ (n % 8)), hi first -- the operand the fused
  * backward copies straight into shared memory.  mamba2_ssd_states_unpack
  * gives the fp32 (b,nc,H,P,N) view of either form.  On the "fused-split"
- * shapes `states` holds the fp32 states themselves and the packed ones stay
- * in the workspace, which must then live, unmodified, until the backward
+ * and "-padded" shapes `states` holds the fp32 states themselves and the
+ * packed ones (and, padded, the padded copies of x, dt, B, C and seq_idx)
+ * stay in the workspace, which must then live, unmodified, until the backward
  * (ssd_saved.aux).  *saved_out (host struct) filled for the backward.
  * workspace: >= fwd_workspace_size bytes. */
 ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A,
                           const void *B, const void *C, const float *D, const int32_t *seq_idx,
                           const float *init_states, void *y, float *states, void *workspace,
                           size_t workspace_bytes, void *stream, ssd_saved *saved_out);
+
+/* The padded form that runs packed batches whose sequences start inside a
+ * chunk on the fused kernels ("fused-padded/..." and "fused-split-padded/..."
+ * configurations; see SSD_DIMS_SEQ_ANY_START): the token stream is cut at
+ * every sequence start and every multiple of 128 tokens, and piece k becomes
+ * chunk k of a padded problem in 128-token chunks, its tokens first, then
+ * tokens with dt = 0 and x = B = C = dout = 0, which leave the state and
+ * every gradient of the real tokens unchanged.  The padded problem has
+ * ceil(seqlen / 128) + nseq - 1 chunks (trailing ones all padding, inside the
+ * last sequence); this returns that count, or 0 for dims that do not run the
+ * padded form. */
+int64_t mamba2_ssd_padded_chunks(const ssd_dims *dims);
+
+/* The piece table of the padded form for a HOST copy of seq_idx (seqlen
+ * int32), written to host `table` (3 * padded_chunks + num_chunks int32):
+ * start[k], len[k] (0..128) and id[k] of every padded chunk k -- its first
+ * token, its count of real tokens and its sequence id -- then, for every
+ * chunk c of the caller's chunking, the padded chunk that begins with token
+ * c * chunk_size.  Host code only (the forward builds the same table from its
+ * own copy of seq_idx).  SSD_ERR_INVALID_ARG for dims that do not run the
+ * padded form, null pointers, or ids that are negative, >= nseq or
+ * decreasing. */
+ssd_status mamba2_ssd_padded_piece_table(const ssd_dims *dims, const int32_t *seq_idx, int32_t *table);
 
 /* fp32 (b,nc,H,P,N) copy of the saved chunk states (hi + lo of the packed
  * form on the fused shapes, the states themselves otherwise) into `out`

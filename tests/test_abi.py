@@ -129,10 +129,13 @@ def test_bwd_argument_checks(L):
     assert L.mamba2_ssd_bwd(*args(sv, o, need)) == 1
 
 
-def test_any_start_dims_take_the_general_path(L):
+def test_any_start_dims_take_the_padded_fused_path_or_the_general_one(L):
     fused = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, seq_idx=True)
-    anyst = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, seq_idx=True, any_start=True)
-    assert ssd.config_name(fused, 0).startswith("fused")
+    padded = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, seq_idx=True, any_start=True)
+    assert ssd.config_name(fused, 0) == "fused/ring4"
+    assert ssd.config_name(padded, 0) == "fused-padded/0"
+    # fp32: the general path, with its sequence-start kernels
+    anyst = ssd.make_dims(1, 1024, 8, 64, 2, 128, 128, nseq=3, dtype=torch.float32, seq_idx=True, any_start=True)
     assert ssd.config_name(anyst, 0).startswith("simt")
     for var in (0, 1):
         names = ssd.bwd_launch_names(anyst, 0, var)

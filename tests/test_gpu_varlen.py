@@ -6,15 +6,17 @@ Cases cover a start at the second and at the last token of a chunk, a
 sequence wholly inside one chunk, a one-token sequence, a sequence that
 starts inside a chunk and runs through several, a ragged tail, ids with a
 gap (a sequence with no token keeps a zero initial-state gradient), runs
-with and without initial states, and bf16 inputs on the shape the fused
-backward would take (these dims always run the general path).
+with and without initial states.  fp32 inputs run the general CUDA-core
+path; bf16 inputs on the fused shapes run the fused kernels on the padded
+form (every piece of a sequence inside one 128-token chunk padded to a chunk
+of its own), dstate 128 and the dstate-256 split alike.
 """
 import numpy as np
 import pytest
 import torch
 
 import deterministic_mamba2_ssd_gb300 as ssd
-from _helpers import GRADS, relerr, run_gpu, run_oracle, same_bits, to_dev
+from _helpers import GRADS, relerr, run_gpu, run_oracle, same_bits, to_dev, y_relerr
 from deterministic_mamba2_ssd_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -23,7 +25,7 @@ pytestmark = pytest.mark.gpu
 def check(d, chunk, tol, config=0):
     y, saved, g = run_gpu(d, chunk, config=config, any_start=True)
     ref = run_oracle(d, chunk=chunk)
-    errs = {"y": relerr(y, ref["y"]), "states": relerr(saved.states_fp32(), ref["states"])}
+    errs = {"y": y_relerr(y, ref["y"]), "states": relerr(saved.states_fp32(), ref["states"])}
     for k in GRADS:
         errs[k] = relerr(g[k], ref[k])
     if d["init"] is not None:
@@ -60,14 +62,85 @@ def test_fp32_mid_chunk_ids_with_gap():
     assert torch.count_nonzero(g["dinit"][1]) == 0
 
 
-def test_bf16_mid_chunk_on_fused_shape():
-    lens = (100, 300, 1, 111)
-    d = make_inputs(1, sum(lens), 4, 64, 1, 128, dtype=torch.bfloat16, seed=11, dt_shift=4.0, d_mode="normal",
-                    seq_lens=lens, with_init=True)
-    dims = ssd.make_dims(1, sum(lens), 4, 64, 1, 128, 128, nseq=len(lens), dtype=torch.bfloat16, seq_idx=True,
+BF16_CASES = [
+    # (lens, H, G, N, Q, init)
+    ((100, 300, 1, 111), 4, 1, 128, 128, True),
+    ((1, 127, 128, 2, 1, 253, 400), 4, 1, 128, 128, False),   # one-token sequences, starts at local 1 and 127
+    ((5, 3, 7, 1, 9, 2, 13, 1000), 8, 2, 128, 128, True),     # many starts in one chunk; two groups
+    ((50, 17, 100, 133), 6, 3, 128, 128, True),               # ragged length 300
+    ((1, 128, 128, 128, 127), 4, 1, 128, 128, True),          # the padding bound is reached
+    ((100, 300, 1, 111), 4, 1, 256, 256, True),               # dstate 256, chunk 256 (split)
+    ((300, 212, 600), 4, 1, 256, 128, False),                 # dstate 256, chunk 128; ragged
+]
+
+
+@pytest.mark.parametrize("lens,H,G,N,Q,init", BF16_CASES)
+def test_bf16_mid_chunk_on_fused_shapes(lens, H, G, N, Q, init):
+    T = sum(lens)
+    d = make_inputs(1, T, H, 64, G, N, dtype=torch.bfloat16, seed=T + H + N, dt_shift=4.0, d_mode="normal",
+                    seq_lens=lens, with_init=init)
+    dims = ssd.make_dims(1, T, H, 64, G, N, Q, nseq=len(lens), dtype=torch.bfloat16, seq_idx=True,
                          any_start=True)
-    assert ssd.config_name(dims, 0).startswith("simt")
-    check(d, 128, 2e-3)
+    assert ssd.config_name(dims, 0) == ("fused-padded/0" if N == 128 else "fused-split-padded/0")
+    check(d, Q, 2e-3)
+
+
+def test_bf16_mid_chunk_ids_with_gap_on_the_padded_path():
+    lens = (40, 300, 58)
+    d = make_inputs(1, sum(lens), 4, 64, 1, 128, dtype=torch.bfloat16, seed=78, dt_shift=4.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    d["seq_idx"] = torch.where(d["seq_idx"] >= 1, d["seq_idx"] + 1, d["seq_idx"]).contiguous()
+    d["init"] = torch.cat([d["init"][:1], torch.randn_like(d["init"][:1]), d["init"][1:]]).contiguous()
+    g = check(d, 128, 2e-3)
+    assert torch.count_nonzero(g["dinit"][1]) == 0
+
+
+@pytest.mark.parametrize("N,Q", [(128, 128), (256, 256)])
+def test_padded_path_bitwise_repeat_configs_and_atomic_teeth(N, Q):
+    lens = (1000, 1, 517, 2000, 3, 700)
+    d = make_inputs(1, sum(lens), 8, 64, 1, N, dtype=torch.bfloat16, seed=6, dt_shift=4.0, d_mode="normal",
+                    seq_lens=lens, with_init=True)
+    g = to_dev(d)
+    runs = [run_gpu(d, Q, config=c, g=g, any_start=True)[2] for c in (0, 0, 0, 1, 1)]
+    for r in runs[1:]:
+        assert same_bits(runs[0], r)
+    # the same launches with dA (and dD) added by atomics: the order varies between runs
+    digests = {hash(run_gpu(d, Q, variant=1, g=g, any_start=True)[2]["dA"].cpu().numpy().tobytes())
+               for _ in range(20)}
+    if len(digests) == 1:
+        pytest.skip("atomic variant was reproducible in 20 runs")
+    assert len(digests) > 1
+
+
+def test_bf16_varlen_T32768_mid_chunk_starts_sampled_sequences():
+    """The packed varlen workload's shape (chunk 256, dstate 256, one group,
+    128 heads, 32768 tokens, initial states) with every sequence start inside
+    a 128-token chunk.  Sequences never interact, so the oracle runs two of
+    them alone, in full, on their own tokens and initial state."""
+    from deterministic_mamba2_ssd_gb300.inputs import WORKLOADS, workload_inputs
+    w = WORKLOADS["bf16_varlen_T32768"]
+    lens = (9001, 7000, 333, 16434)
+    assert sum(lens) == w.seqlen
+    d = workload_inputs("bf16_varlen_T32768")
+    d["seq_idx"] = torch.from_numpy(np.repeat(np.arange(4, dtype=np.int32), lens)[None, :]).contiguous()
+    dims = ssd.make_dims(1, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, w.chunk, nseq=4,
+                         dtype=torch.bfloat16, seq_idx=True, any_start=True)
+    assert ssd.config_name(dims, 0) == "fused-split-padded/0"
+    y, _, g = run_gpu(d, w.chunk, any_start=True)
+    y2, _, g2 = run_gpu(d, w.chunk, any_start=True)
+    assert same_bits(g, g2) and torch.equal(y, y2)
+    off = np.cumsum((0,) + lens)
+    for s in (1, 2):
+        sl = slice(int(off[s]), int(off[s + 1]))
+        part = dict(x=d["x"][:, sl].contiguous(), dt=d["dt"][:, sl].contiguous(), A=d["A"],
+                    B=d["B"][:, sl].contiguous(), C=d["C"][:, sl].contiguous(), D=d["D"],
+                    dout=d["dout"][:, sl].contiguous(), seq_idx=None, init=d["init"][s:s + 1].contiguous())
+        ref = run_oracle(part)
+        errs = {k: relerr(g[k][:, sl], ref[k]) for k in ("dx", "ddt", "dB", "dC")}
+        errs["dinit"] = relerr(g["dinit"][s:s + 1], ref["dinit"])
+        errs["y"] = y_relerr(y[:, sl], ref["y"])
+        bad = {k: v for k, v in errs.items() if not v < 2e-3}
+        assert not bad, (s, bad, errs)
 
 
 def test_mid_chunk_start_without_flag_is_unsupported():

@@ -474,7 +474,7 @@ def time_workload(ssd, name, dev, steps, warmup=3, repeats=5):
 
     def fwd():
         return ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk, seq_idx=g["seq_idx"],
-                       init_states=g["init"])
+                       init_states=g["init"], any_start=w.any_start)
     y, saved = fwd()
     out = ssd.bwd(saved, g["dout"])
     ws = torch.empty(max(16, ssd.bwd_workspace_size(saved.dims, 0, 0)), dtype=torch.uint8, device=dev)
@@ -537,13 +537,13 @@ def main():
     d = workload_inputs(w.name, seqlen=args.seqlen)
     g = {k: (v.to(dev) if v is not None else None) for k, v in d.items()}
     y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
-                       seq_idx=g["seq_idx"], init_states=g["init"])
+                       seq_idx=g["seq_idx"], init_states=g["init"], any_start=w.any_start)
     # the forward that produces the saved states (untimed by the metric), timed on its own
     fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
     for a, b in fwd_ev:
         a.record()
         y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=w.chunk,
-                           seq_idx=g["seq_idx"], init_states=g["init"])
+                           seq_idx=g["seq_idx"], init_states=g["init"], any_start=w.any_start)
         b.record()
     torch.cuda.synchronize()
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev[1:])
@@ -675,7 +675,8 @@ def main():
                 dev_in[k].copy_(v)
             # saved struct that points at this set's device inputs
             _, saved_e = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
-                                 chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"))
+                                 chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"),
+                                 any_start=w.any_start)
             saved_e.struct.states = dev_in["states"].data_ptr()
             saved_e.tensors["states"] = dev_in["states"]
             out_e = {k: torch.empty_like(v) for k, v in out.items()}
@@ -745,7 +746,8 @@ def main():
     others = None
     if world == 1 and not args.no_others and args.workload == "bf16_T16384":
         others = [time_workload(ssd, n, dev, steps=st) for n, st in
-                  (("bf16_T2048", 20), ("bf16_T4096", 20), ("bf16_varlen_T32768", 2))]
+                  (("bf16_T2048", 20), ("bf16_T4096", 20), ("bf16_varlen_T32768", 2),
+                   ("bf16_varlen_T32768_midchunk", 2))]
 
     line = None
     if rank == 0:

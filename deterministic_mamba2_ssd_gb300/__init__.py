@@ -209,7 +209,8 @@ def fwd(x, dt, A, B, C, D, chunk_size, seq_idx=None, init_states=None, stream=No
     """Forward.  Returns (y, saved).  x (b,T,H,P) and B, C (b,T,G,N) in
     bf16 or fp32; dt (b,T,H), A (H), D (H), init_states (nseq,H,P,N) fp32;
     seq_idx (1,T) int32, non-decreasing, with sequence starts at multiples of
-    chunk_size unless ``any_start`` (which selects the general backward)."""
+    chunk_size unless ``any_start`` (starts anywhere: the padded fused form on
+    the bf16 fused shapes, the general kernels otherwise)."""
     b, T, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     dev = x.device

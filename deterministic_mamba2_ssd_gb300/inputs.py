@@ -35,6 +35,7 @@ class Workload:
     d_mode: str                 # "one" or "normal"
     seq_lens: tuple = field(default=())   # packed variable-length batch (batch must be 1)
     with_init: bool = False
+    any_start: bool = False     # sequence starts may fall inside a chunk
 
 
 WORKLOADS = {
@@ -44,6 +45,10 @@ WORKLOADS = {
     "bf16_T16384": Workload("bf16_T16384", 1, 16384, 128, 256, 64, 8, 128, torch.bfloat16, 4.0, "normal"),
     "bf16_varlen_T32768": Workload("bf16_varlen_T32768", 1, 32768, 256, 128, 64, 1, 256, torch.bfloat16,
                                    4.0, "normal", seq_lens=(4096, 8192, 8192, 12288), with_init=True),
+    # the packed batch with every sequence start inside a 128-token chunk
+    "bf16_varlen_T32768_midchunk": Workload("bf16_varlen_T32768_midchunk", 1, 32768, 256, 128, 64, 1, 256,
+                                            torch.bfloat16, 4.0, "normal", seq_lens=(9001, 7000, 333, 16434),
+                                            with_init=True, any_start=True),
     # fp32 inputs on the 2K shape: runs the general CUDA-core path (fp32 tolerance rules out
     # tensor-core operands); used to compare its two deterministic dB/dC folds
     "fp32_T2048": Workload("fp32_T2048", 1, 2048, 128, 256, 64, 8, 128, torch.float32, 4.0, "normal"),
@@ -51,7 +56,8 @@ WORKLOADS = {
 
 #: seed offset per preset, in the order the presets are listed above
 SEED_BASE = 1234
-WORKLOAD_ORDER = ["tiny_fp32", "bf16_T2048", "bf16_T4096", "bf16_T16384", "bf16_varlen_T32768", "fp32_T2048"]
+WORKLOAD_ORDER = ["tiny_fp32", "bf16_T2048", "bf16_T4096", "bf16_T16384", "bf16_varlen_T32768", "fp32_T2048",
+                  "bf16_varlen_T32768_midchunk"]
 
 
 def seed_of(name: str) -> int:

@@ -60,6 +60,67 @@ __device__ __forceinline__ int64_t local_start(const int32_t *seq_idx, const int
   return f > 0 ? f : 0;
 }
 
+// ------------------------------------------------------------ tile products --
+// The per-chunk products below are computed by CTAs of 256 threads, each
+// producing a tile of (16 RA) x 64 outputs D[r][q] = sum_k A(r, k) B(q, k) with
+// the operands staged through shared memory in k blocks of 16.  Every output
+// element is still one sequential fmaf chain over its k index, ascending, one
+// term per k (terms outside a product's range are exact zeros), so its bits
+// depend neither on the tiling nor on the launch configuration.  Thread
+// (ty, tx) = (tid / 16, tid % 16) holds rows ty + 16 a and columns tx + 16 b.
+constexpr int kTileThreads = 256, kTK = 16, kTC = 64;
+
+template <int RA>
+struct TileBuf {
+  float a[kTK][16 * RA + 4];
+  float b[kTK][kTC + 4];
+};
+
+// fa(r, k) = A(r, k), fb(q, k) = B(q, k) (0 outside their ranges);
+// kAKFast / kBKFast: consecutive k adjacent in memory (else consecutive r, q),
+// which picks the thread order of the loads so that they coalesce.
+template <int RA, bool kAKFast, bool kBKFast, class FA, class FB>
+__device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, TileBuf<RA> &sb,
+                                        float (&acc)[RA][4]) {
+  constexpr int R = 16 * RA;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+#pragma unroll
+  for (int a = 0; a < RA; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+  for (int64_t k0 = 0; k0 < K; k0 += kTK) {
+#pragma unroll
+    for (int e0 = 0; e0 < R * kTK; e0 += kTileThreads) {
+      const int e = e0 + tid;
+      const int r = kAKFast ? e / kTK : e % R, kk = kAKFast ? e % kTK : e / R;
+      sb.a[kk][r] = (k0 + kk < K) ? fa(r, k0 + kk) : 0.f;
+    }
+#pragma unroll
+    for (int e0 = 0; e0 < kTC * kTK; e0 += kTileThreads) {
+      const int e = e0 + tid;
+      const int q = kBKFast ? e / kTK : e % kTC, kk = kBKFast ? e % kTK : e / kTC;
+      sb.b[kk][q] = (k0 + kk < K) ? fb(q, k0 + kk) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kTK; ++kk) {
+      float av[RA], bv[4];
+#pragma unroll
+      for (int a = 0; a < RA; ++a) av[a] = sb.a[kk][ty + 16 * a];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bv[b] = sb.b[kk][tx + 16 * b];
+#pragma unroll
+      for (int a = 0; a < RA; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(av[a], bv[b], acc[a][b]);
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ int tile_tx() { return threadIdx.x & 15; }
+__device__ __forceinline__ int tile_ty() { return threadIdx.x >> 4; }
+
 // ---------------------------------------------------------------- cumsum --
 // Acs (b,H,nc,Q) as hi + lo: left-to-right compensated (two-sum) prefix sum
 // of a_i = dt_i * A_h, one thread per (b, c, h), entries past the chunk end
@@ -90,13 +151,16 @@ __global__ void cumsum_fwd_kernel(Shape s, const float *__restrict__ dt, const f
 
 // ------------------------------------------------------ chunk_state (fwd) --
 // S[b,c,h,p,n] = sum_i exp(E - Acs_i) dt_i x_i[p] B_i[n] over the tokens of
-// the sequence holding the chunk's last token (i >= fe); one thread per (p,n).
+// the sequence holding the chunk's last token (i >= fe), i ascending; a CTA
+// per (b, c, h) and 64 x 64 tile of (p, n).
 template <class TIn>
-__global__ void chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Bm,
-                                       const float *__restrict__ dt, const float *__restrict__ acs_hi,
-                                       const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                                       const int32_t *__restrict__ first, float *__restrict__ S) {
+__global__ void __launch_bounds__(kTileThreads)
+    chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Bm, const float *__restrict__ dt,
+                           const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                           const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                           float *__restrict__ S) {
   extern __shared__ float w[];
+  __shared__ TileBuf<4> sb;
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
@@ -107,15 +171,22 @@ __global__ void chunk_state_fwd_kernel(Shape s, const TIn *__restrict__ x, const
     w[i] = i < fe ? 0.f
                   : __fmul_rn(expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])), dt[(bi * s.T + t0 + i) * s.H + h]);
   __syncthreads();
-  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
-  if (e >= s.P * s.N) return;
-  const int64_t p = e / s.N, n = e % s.N;
-  float acc = 0.f;
-  for (int64_t i = 0; i < Lc; ++i) {
-    const int64_t t = t0 + i;
-    acc = fmaf(w[i] * ld(x + ((bi * s.T + t) * s.H + h) * s.P + p), ld(Bm + ((bi * s.T + t) * s.G + g) * s.N + n), acc);
-  }
-  S[(((bi * s.nc + c) * s.H + h) * s.P + p) * s.N + n] = acc;
+  const int64_t ntn = cdiv(s.N, kTC);
+  const int64_t p0 = (blockIdx.y / ntn) * 64, n0 = (blockIdx.y % ntn) * kTC;
+  const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;   // token i: xc + i * H P
+  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;  // token i: bc + i * G N
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  float acc[4][4];
+  tile_mm<4, false, false>(
+      Lc, [&](int r, int64_t i) { const int64_t p = p0 + r; return p < s.P ? w[i] * ld(xc + i * HP + p) : 0.f; },
+      [&](int q, int64_t i) { const int64_t n = n0 + q; return n < s.N ? ld(bc + i * GN + n) : 0.f; }, sb, acc);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t p = p0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      if (p < s.P && n < s.N) S[(unit * s.P + p) * s.N + n] = acc[a][b];
+    }
 }
 
 // ------------------------------------------------ state passing (fwd) --
@@ -151,106 +222,163 @@ __global__ void state_passing_fwd_kernel(Shape s, const float *__restrict__ S, c
 }
 
 // -------------------------------------------------------------- C . B^T --
-// CB[b,c,g,i,j] = C_i . B_j for j <= i < Lc, else 0.  One thread per (i,j).
+// CB[b,c,g,i,j] = C_i . B_j for j <= i < Lc, else 0; a CTA per (b, c, g) and
+// 64 x 64 tile of (i, j) (tiles above the diagonal are zeros).
 template <class TIn>
-__global__ void cb_kernel(Shape s, const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, float *__restrict__ CB) {
+__global__ void __launch_bounds__(kTileThreads)
+    cb_kernel(Shape s, const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, float *__restrict__ CB) {
+  __shared__ TileBuf<4> sb;
   const int64_t unit = blockIdx.x;  // (b, c, g)
   const int64_t g = unit % s.G, c = (unit / s.G) % s.nc, bi = unit / (s.G * s.nc);
-  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
-  if (e >= s.Q * s.Q) return;
-  const int64_t i = e / s.Q, j = e % s.Q;
-  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
-  float acc = 0.f;
-  if (j <= i && i < Lc) {
-    const TIn *ci = Cm + ((bi * s.T + t0 + i) * s.G + g) * s.N;
-    const TIn *bj = Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N;
-    for (int64_t n = 0; n < s.N; ++n) acc = fmaf(ld(ci + n), ld(bj + n), acc);
-  }
-  CB[((bi * s.nc + c) * s.G + g) * s.Q * s.Q + e] = acc;
+  const int64_t nt = cdiv(s.Q, 64);
+  const int64_t i0 = (blockIdx.y / nt) * 64, j0 = (blockIdx.y % nt) * 64;
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), GN = s.G * s.N;
+  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
+  float acc[4][4] = {};
+  if (j0 <= i0 && i0 < Lc)   // the tile reaches the lower triangle (same for the whole CTA)
+    tile_mm<4, true, true>(
+        s.N, [&](int r, int64_t n) { const int64_t i = i0 + r; return i < Lc ? ld(cc + i * GN + n) : 0.f; },
+        [&](int q, int64_t n) { const int64_t j = j0 + q; return j < Lc ? ld(bc + j * GN + n) : 0.f; }, sb, acc);
+  float *o = CB + unit * s.Q * s.Q;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t i = i0 + tile_ty() + 16 * a, j = j0 + tile_tx() + 16 * b;
+      if (i < s.Q && j < s.Q) o[i * s.Q + j] = (j <= i && i < Lc) ? acc[a][b] : 0.f;
+    }
 }
 
 // ------------------------------------------------------- chunk_scan (fwd) --
 // y_i[p] = sum_{f<=j<=i} CB[i,j] exp(Acs_i - Acs_j) dt_j x_j[p]
 //        + din_i sum_n Hin[p,n] C_i[n] + D x_i[p], f = local_start(i): Hin = states
 // and din_i = exp(Acs_i) when f = 0, else Hin = init[seq] (or 0) and
-// din_i = exp(Acs_i - Acs_{f-1}).  One thread per (b,t,h,p).
+// din_i = exp(Acs_i - Acs_{f-1}).  A CTA per (b, c, h) and 64 x 64 tile of (i, p).
 template <class TIn>
-__global__ void chunk_scan_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Cm,
-                                      const float *__restrict__ dt, const float *__restrict__ D,
-                                      const float *__restrict__ CB, const float *__restrict__ acs_hi,
-                                      const float *__restrict__ acs_lo, const float *__restrict__ states,
-                                      const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                                      const float *__restrict__ init, TIn *__restrict__ y) {
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= s.b * s.T * s.H * s.P) return;
-  const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
-  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, g = h / s.hpg;
-  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
+__global__ void __launch_bounds__(kTileThreads)
+    chunk_scan_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Cm, const float *__restrict__ dt,
+                          const float *__restrict__ D, const float *__restrict__ CB, const float *__restrict__ acs_hi,
+                          const float *__restrict__ acs_lo, const float *__restrict__ states,
+                          const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                          const float *__restrict__ init, TIn *__restrict__ y) {
+  __shared__ TileBuf<4> sb;
+  __shared__ int fr[64];   // local sequence start of each row of the tile
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+  const int64_t ntp = cdiv(s.P, kTC);
+  const int64_t i0 = (blockIdx.y / ntp) * 64, p0 = (blockIdx.y % ntp) * kTC;
+  if (i0 >= Lc) return;   // (the whole CTA)
+  for (int r = threadIdx.x; r < 64; r += blockDim.x)
+    fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
+  __syncthreads();
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float *cb = CB + (((bi * s.nc + c) * s.G + g) * s.Q + i) * s.Q;
-  float acc = 0.f;
-  for (int64_t j = f; j <= i; ++j) {
-    const float wgt = cb[j] * expf(acs_diff(ah[i], al[i], ah[j], al[j])) * dt[(bi * s.T + t0 + j) * s.H + h];
-    acc = fmaf(wgt, ld(x + ((bi * s.T + t0 + j) * s.H + h) * s.P + p), acc);
-  }
-  const float *hs = f == 0 ? states + (((bi * s.nc + c) * s.H + h) * s.P + p) * s.N
-                           : (init ? init + ((seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P + p) * s.N : nullptr);
-  const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
-  float inter = 0.f;
-  if (hs)
-    for (int64_t n = 0; n < s.N; ++n) inter = fmaf(hs[n], ld(ci + n), inter);
-  const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
-  const float xv = ld(x + idx);
-  const float out = fmaf(din, inter, acc) + D[h] * xv;
-  st(y + idx, out);
+  const float *cb = CB + ((bi * s.nc + c) * s.G + g) * s.Q * s.Q;
+  const float *dtc = dt + (bi * s.T + t0) * s.H + h;      // token j: dtc[j * H]
+  const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;  // token j: xc + j * H P
+  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N; // token i: cc + i * G N
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  float acc[4][4], inter[4][4];
+  tile_mm<4, true, false>(
+      Lc,
+      [&](int r, int64_t j) {
+        const int64_t i = i0 + r;
+        if (i >= Lc || j > i || j < fr[r]) return 0.f;
+        return cb[i * s.Q + j] * expf(acs_diff(ah[i], al[i], ah[j], al[j])) * dtc[j * s.H];
+      },
+      [&](int q, int64_t j) { const int64_t p = p0 + q; return p < s.P ? ld(xc + j * HP + p) : 0.f; }, sb, acc);
+  const float *hst = states + unit * s.P * s.N;
+  tile_mm<4, true, true>(
+      s.N, [&](int r, int64_t n) { const int64_t i = i0 + r; return i < Lc ? ld(cc + i * GN + n) : 0.f; },
+      [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? hst[p * s.N + n] : 0.f; }, sb, inter);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t i = i0 + tile_ty() + 16 * a, p = p0 + tile_tx() + 16 * b;
+      if (i >= Lc || p >= s.P) continue;
+      const int64_t t = t0 + i, f = fr[tile_ty() + 16 * a];
+      float in = inter[a][b];
+      if (f > 0) {   // a sequence that started inside the chunk: its own initial state
+        in = 0.f;
+        if (init) {
+          const float *hs = init + ((seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P + p) * s.N;
+          const TIn *ci = cc + i * GN;
+          for (int64_t n = 0; n < s.N; ++n) in = fmaf(hs[n], ld(ci + n), in);
+        }
+      }
+      const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+      const int64_t idx = ((bi * s.T + t) * s.H + h) * s.P + p;
+      const float xv = ld(x + idx);
+      st(y + idx, fmaf(din, in, acc[a][b]) + D[h] * xv);
+    }
 }
 
 // ============================================================ backward ====
 
 // Per (b,c,h,i,j) with local_start(i) <= j <= i < Lc (same sequence):
 // L = exp(Acs_i - Acs_j), Gx = g_i . x_j, M = CB[i,j] L, W = L Gx dt_j,
-// MG = M Gx; zero elsewhere.
+// MG = M Gx; zero elsewhere.  A CTA per (b, c, h) and 64 x 64 tile of (i, j).
 template <class TIn>
-__global__ void mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
-                           const float *__restrict__ dt, const float *__restrict__ CB,
-                           const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
-                           const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                           float *__restrict__ Mm, float *__restrict__ Wm, float *__restrict__ MGm) {
+__global__ void __launch_bounds__(kTileThreads)
+    mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const float *__restrict__ dt,
+               const float *__restrict__ CB, const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+               const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first, float *__restrict__ Mm,
+               float *__restrict__ Wm, float *__restrict__ MGm) {
+  __shared__ TileBuf<4> sb;
+  __shared__ int fr[64];
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
-  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
-  if (e >= s.Q * s.Q) return;
-  const int64_t i = e / s.Q, j = e % s.Q;
-  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
-  float M = 0.f, W = 0.f, MG = 0.f;
-  if (j <= i && i < Lc && j >= local_start(seq_idx, first, bi, s.T, t0 + i, t0)) {
-    const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
-    const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-    const float L = expf(acs_diff(ah[i], al[i], ah[j], al[j]));
-    const TIn *gi = dout + ((bi * s.T + t0 + i) * s.H + h) * s.P;
-    const TIn *xj = x + ((bi * s.T + t0 + j) * s.H + h) * s.P;
-    float gx = 0.f;
-    for (int64_t p = 0; p < s.P; ++p) gx = fmaf(ld(gi + p), ld(xj + p), gx);
-    const float cbv = CB[(((bi * s.nc + c) * s.G + g) * s.Q + i) * s.Q + j];
-    M = cbv * L;
-    W = L * gx * dt[(bi * s.T + t0 + j) * s.H + h];
-    MG = M * gx;
-  }
-  const int64_t o = unit * s.Q * s.Q + e;
-  Mm[o] = M;
-  Wm[o] = W;
-  MGm[o] = MG;
+  const int64_t nt = cdiv(s.Q, 64);
+  const int64_t i0 = (blockIdx.y / nt) * 64, j0 = (blockIdx.y % nt) * 64;
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg, HP = s.H * s.P;
+  for (int r = threadIdx.x; r < 64; r += blockDim.x)
+    fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
+  __syncthreads();
+  const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
+  const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;
+  const bool live = j0 <= i0 && i0 < Lc;   // (the whole CTA)
+  float acc[4][4] = {};
+  if (live)
+    tile_mm<4, true, true>(
+        s.P, [&](int r, int64_t p) { const int64_t i = i0 + r; return i < Lc ? ld(gc + i * HP + p) : 0.f; },
+        [&](int q, int64_t p) { const int64_t j = j0 + q; return j < Lc ? ld(xc + j * HP + p) : 0.f; }, sb, acc);
+  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  const float *cb = CB + ((bi * s.nc + c) * s.G + g) * s.Q * s.Q;
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t i = i0 + tile_ty() + 16 * a, j = j0 + tile_tx() + 16 * b;
+      if (i >= s.Q || j >= s.Q) continue;
+      float M = 0.f, W = 0.f, MG = 0.f;
+      if (live && j <= i && i < Lc && j >= fr[tile_ty() + 16 * a]) {
+        const float L = expf(acs_diff(ah[i], al[i], ah[j], al[j]));
+        const float gx = acc[a][b];
+        M = cb[i * s.Q + j] * L;
+        W = L * gx * dt[(bi * s.T + t0 + j) * s.H + h];
+        MG = M * gx;
+      }
+      const int64_t o = unit * s.Q * s.Q + i * s.Q + j;
+      Mm[o] = M;
+      Wm[o] = W;
+      MGm[o] = MG;
+    }
 }
 
 // dHscan[b,c,h,p,n] = sum_i exp(Acs_i) g_i[p] C_i[n] over the tokens that see
-// the state entering the chunk (local_start(i) == 0); one thread per (p,n).
+// the state entering the chunk (local_start(i) == 0), i ascending; a CTA per
+// (b, c, h) and 64 x 64 tile of (p, n).
 template <class TIn>
-__global__ void dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Cm,
-                              const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
-                              const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                              float *__restrict__ dH) {
+__global__ void __launch_bounds__(kTileThreads)
+    dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Cm, const float *__restrict__ acs_hi,
+                  const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                  const int32_t *__restrict__ first, float *__restrict__ dH) {
   extern __shared__ float ea[];
+  __shared__ TileBuf<4> sb;
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
@@ -259,15 +387,22 @@ __global__ void dhscan_kernel(Shape s, const TIn *__restrict__ dout, const TIn *
   for (int64_t i = threadIdx.x; i < Lc; i += blockDim.x)
     ea[i] = local_start(seq_idx, first, bi, s.T, t0 + i, t0) == 0 ? expf(__fadd_rn(ah[i], al[i])) : 0.f;
   __syncthreads();
-  const int64_t e = int64_t(blockIdx.y) * blockDim.x + threadIdx.x;
-  if (e >= s.P * s.N) return;
-  const int64_t p = e / s.N, n = e % s.N;
-  float acc = 0.f;
-  for (int64_t i = 0; i < Lc; ++i) {
-    const int64_t t = t0 + i;
-    acc = fmaf(ea[i] * ld(dout + ((bi * s.T + t) * s.H + h) * s.P + p), ld(Cm + ((bi * s.T + t) * s.G + g) * s.N + n), acc);
-  }
-  dH[(((bi * s.nc + c) * s.H + h) * s.P + p) * s.N + n] = acc;
+  const int64_t ntn = cdiv(s.N, kTC);
+  const int64_t p0 = (blockIdx.y / ntn) * 64, n0 = (blockIdx.y % ntn) * kTC;
+  const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
+  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  float acc[4][4];
+  tile_mm<4, false, false>(
+      Lc, [&](int r, int64_t i) { const int64_t p = p0 + r; return p < s.P ? ea[i] * ld(gc + i * HP + p) : 0.f; },
+      [&](int q, int64_t i) { const int64_t n = n0 + q; return n < s.N ? ld(cc + i * GN + n) : 0.f; }, sb, acc);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t p = p0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      if (p < s.P && n < s.N) dH[(unit * s.P + p) * s.N + n] = acc[a][b];
+    }
 }
 
 // Fixed-shape block sum: each warp folds by xor-shuffle, then warp sums are
@@ -363,82 +498,168 @@ __global__ void dinit_mid_kernel(Shape s, const TIn *__restrict__ dout, const TI
 
 // dx_i[p] = dt_i sum_{j>=i} M[j,i] g_j[p] + w_i sum_n B_i[n] dS[p,n] + D g_i[p],
 // w_i = exp(E - Acs_i) dt_i for the tokens of the sequence holding the
-// chunk's last token (i >= fe), else 0.  One thread per (b,t,h,p).
+// chunk's last token (i >= fe), else 0.  A CTA per (b, c, h) and 64 x 64 tile
+// of (i, p).
 template <class TIn>
-__global__ void dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
-                          const float *__restrict__ dt, const float *__restrict__ D, const float *__restrict__ Mm,
-                          const float *__restrict__ dS, const float *__restrict__ acs_hi,
-                          const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                          const int32_t *__restrict__ first, float *__restrict__ dx) {
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= s.b * s.T * s.H * s.P) return;
-  const int64_t p = idx % s.P, h = (idx / s.P) % s.H, t = (idx / (s.P * s.H)) % s.T, bi = idx / (s.P * s.H * s.T);
-  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
-  const int64_t unit = (bi * s.nc + c) * s.H + h;
+__global__ void __launch_bounds__(kTileThreads)
+    dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm, const float *__restrict__ dt,
+              const float *__restrict__ D, const float *__restrict__ Mm, const float *__restrict__ dS,
+              const float *__restrict__ acs_hi, const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+              const int32_t *__restrict__ first, float *__restrict__ dx) {
+  __shared__ TileBuf<4> sb;
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const int64_t ntp = cdiv(s.P, kTC);
+  const int64_t i0 = (blockIdx.y / ntp) * 64, p0 = (blockIdx.y % ntp) * kTC;
+  if (i0 >= Lc) return;   // (the whole CTA)
   const float *M = Mm + unit * s.Q * s.Q;
-  float d1 = 0.f;
-  for (int64_t j = i; j < Lc; ++j) d1 = fmaf(M[j * s.Q + i], ld(dout + ((bi * s.T + t0 + j) * s.H + h) * s.P + p), d1);
-  const float *ds = dS + (unit * s.P + p) * s.N;
-  const TIn *bi_ = Bm + ((bi * s.T + t) * s.G + g) * s.N;
-  float y = 0.f;
-  for (int64_t n = 0; n < s.N; ++n) y = fmaf(ld(bi_ + n), ds[n], y);
+  const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
+  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const float *ds = dS + unit * s.P * s.N;
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  float d1[4][4], yv[4][4];
+  tile_mm<4, false, false>(
+      Lc, [&](int r, int64_t j) { const int64_t i = i0 + r; return i < Lc ? M[j * s.Q + i] : 0.f; },
+      [&](int q, int64_t j) { const int64_t p = p0 + q; return p < s.P ? ld(gc + j * HP + p) : 0.f; }, sb, d1);
+  tile_mm<4, true, true>(
+      s.N, [&](int r, int64_t n) { const int64_t i = i0 + r; return i < Lc ? ld(bc + i * GN + n) : 0.f; },
+      [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? ds[p * s.N + n] : 0.f; }, sb, yv);
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float dti = dt[(bi * s.T + t) * s.H + h];
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
-  const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
-  dx[idx] = fmaf(dti, d1, fmaf(wi, y, D[h] * ld(dout + idx)));
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int64_t i = i0 + tile_ty() + 16 * a;
+    if (i >= Lc) continue;
+    const int64_t t = t0 + i;
+    const float dti = dt[(bi * s.T + t) * s.H + h];
+    const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t p = p0 + tile_tx() + 16 * b;
+      if (p >= s.P) continue;
+      const int64_t idx = ((bi * s.T + t) * s.H + h) * s.P + p;
+      dx[idx] = fmaf(dti, d1[a][b], fmaf(wi, yv[a][b], D[h] * ld(dout + idx)));
+    }
+  }
 }
 
-// Per-head dB / dC rows, one thread per (b,t,h,n):
+// Per-head dB / dC rows of tokens i0 .. i0 + 16 RA - 1 of chunk c, state
+// columns n0 .. n0 + 63 (shared by the slot and the ordered fold, so both
+// produce the same bits):
 //   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + din_i sum_p Hin[p,n] g_i[p]
 //   dB_h[i,n] = sum_{j>=i} W[j,i] C_j[n] + w_i sum_p dS[p,n] x_i[p]
-// (din_i, Hin as in chunk_scan_fwd; w_i as in dx_kernel).  Deterministic
-// variant: written to per-head slots (b,T,H,N); atomic variant: added into
-// dB/dC (b,T,G,N) with atomics.
-template <class TIn, bool kAtomic>
-__global__ void dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
-                            const TIn *__restrict__ Bm, const TIn *__restrict__ Cm, const float *__restrict__ dt,
-                            const float *__restrict__ Wm, const float *__restrict__ states,
-                            const float *__restrict__ dS, const float *__restrict__ acs_hi,
-                            const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                            const int32_t *__restrict__ first, const float *__restrict__ init,
-                            float *__restrict__ dBo, float *__restrict__ dCo) {
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= s.b * s.T * s.H * s.N) return;
-  const int64_t n = idx % s.N, h = (idx / s.N) % s.H, t = (idx / (s.N * s.H)) % s.T, bi = idx / (s.N * s.H * s.T);
-  const int64_t c = t / s.Q, i = t % s.Q, t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+// (din_i, Hin as in chunk_scan_fwd; w_i as in dx_kernel; fr[r]: local start
+// of row i0 + r).
+template <int RA, class TIn>
+__device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
+                                          const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
+                                          const float *__restrict__ dt, const float *__restrict__ Wm,
+                                          const float *__restrict__ states, const float *__restrict__ dS,
+                                          const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                                          const int32_t *__restrict__ seq_idx, const float *__restrict__ init,
+                                          int64_t bi, int64_t c, int64_t h, int64_t i0, int64_t n0, const int *fr,
+                                          int64_t fe, TileBuf<RA> &sb, float (&dcv)[RA][4], float (&dbv)[RA][4]) {
+  const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
   const int64_t unit = (bi * s.nc + c) * s.H + h;
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
   const float *W = Wm + unit * s.Q * s.Q;
-  float dc = 0.f, db = 0.f;
-  for (int64_t j = 0; j <= i; ++j) dc = fmaf(W[i * s.Q + j], ld(Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), dc);
-  for (int64_t j = i; j < Lc; ++j) db = fmaf(W[j * s.Q + i], ld(Cm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), db);
-  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
-  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
-  const float *hs = f == 0 ? states + unit * s.P * s.N + n
-                           : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N + n : nullptr);
-  const float *ds = dS + unit * s.P * s.N + n;
-  const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
-  const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
-  float hg = 0.f, sx = 0.f;
-  for (int64_t p = 0; p < s.P; ++p) {
-    if (hs) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
-    sx = fmaf(ds[p * s.N], ld(xi + p), sx);
-  }
+  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
+  const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;
+  const float *hst = states + unit * s.P * s.N, *ds = dS + unit * s.P * s.N;
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
-  const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
-  dc = fmaf(din, hg, dc);
-  db = fmaf(wi, sx, db);
-  if (kAtomic) {
-    const int64_t o = ((bi * s.T + t) * s.G + g) * s.N + n;
-    atomicAdd(dBo + o, db);
-    atomicAdd(dCo + o, dc);
-  } else {
-    dBo[idx] = db;
-    dCo[idx] = dc;
+  float t1[RA][4];
+  auto row_ok = [&](int r) { return i0 + r < Lc; };
+  tile_mm<RA, true, false>(
+      Lc, [&](int r, int64_t j) { return row_ok(r) ? W[(i0 + r) * s.Q + j] : 0.f; },
+      [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(bc + j * GN + n) : 0.f; }, sb, dcv);
+  tile_mm<RA, true, false>(
+      s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(gc + (i0 + r) * HP + p) : 0.f; },
+      [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? hst[p * s.N + n] : 0.f; }, sb, t1);
+#pragma unroll
+  for (int a = 0; a < RA; ++a) {
+    const int64_t i = i0 + tile_ty() + 16 * a;
+    if (i >= Lc) continue;
+    const int64_t f = fr[tile_ty() + 16 * a];
+    const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t n = n0 + tile_tx() + 16 * b;
+      if (n >= s.N) continue;
+      float hg = t1[a][b];
+      if (f > 0) {   // a sequence that started inside the chunk: its own initial state
+        hg = 0.f;
+        if (init) {
+          const float *hs = init + (seq_of(seq_idx, bi, s.T, t0 + i) * s.H + h) * s.P * s.N + n;
+          const TIn *gi = gc + i * HP;
+          for (int64_t p = 0; p < s.P; ++p) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+        }
+      }
+      dcv[a][b] = fmaf(din, hg, dcv[a][b]);
+    }
   }
+  tile_mm<RA, false, false>(
+      Lc, [&](int r, int64_t j) { return row_ok(r) ? W[j * s.Q + i0 + r] : 0.f; },
+      [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(cc + j * GN + n) : 0.f; }, sb, dbv);
+  tile_mm<RA, true, false>(
+      s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(xc + (i0 + r) * HP + p) : 0.f; },
+      [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? ds[p * s.N + n] : 0.f; }, sb, t1);
+#pragma unroll
+  for (int a = 0; a < RA; ++a) {
+    const int64_t i = i0 + tile_ty() + 16 * a;
+    if (i >= Lc) continue;
+    const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t0 + i) * s.H + h];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) dbv[a][b] = fmaf(wi, t1[a][b], dbv[a][b]);
+  }
+}
+
+// Deterministic variant: per-head slots (b,T,H,N); atomic variant: added into
+// dB/dC (b,T,G,N) with atomics.  A CTA per (b, c, h) and 64 x 64 tile of (i, n).
+template <class TIn, bool kAtomic>
+__global__ void __launch_bounds__(kTileThreads)
+    dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
+                const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ Wm,
+                const float *__restrict__ states, const float *__restrict__ dS, const float *__restrict__ acs_hi,
+                const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                const int32_t *__restrict__ first, const float *__restrict__ init, float *__restrict__ dBo,
+                float *__restrict__ dCo) {
+  __shared__ TileBuf<4> sb;
+  __shared__ int fr[64];
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const int64_t ntn = cdiv(s.N, kTC);
+  const int64_t i0 = (blockIdx.y / ntn) * 64, n0 = (blockIdx.y % ntn) * kTC;
+  if (i0 >= Lc) return;   // (the whole CTA)
+  for (int r = threadIdx.x; r < 64; r += blockDim.x)
+    fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
+  __syncthreads();
+  const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+  float dcv[4][4], dbv[4][4];
+  dbdc_tile<4, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h, i0, n0, fr, fe,
+                    sb, dcv, dbv);
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t i = i0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      if (i >= Lc || n >= s.N) continue;
+      const int64_t t = t0 + i;
+      if (kAtomic) {
+        const int64_t o = ((bi * s.T + t) * s.G + g) * s.N + n;
+        atomicAdd(dBo + o, dbv[a][b]);
+        atomicAdd(dCo + o, dcv[a][b]);
+      } else {
+        const int64_t o = ((bi * s.T + t) * s.H + h) * s.N + n;
+        dBo[o] = dbv[a][b];
+        dCo[o] = dcv[a][b];
+      }
+    }
 }
 
 constexpr int kOrdTile = 32;   // tokens per tile of the ordered dB/dC fold
@@ -456,21 +677,23 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
 // Ordered dB/dC fold.  Work unit = (b, c, g, token tile tt, head k of the
 // group), k fastest, handed out in that order by an atomic ticket, so a CTA
 // only ever waits for units with smaller tickets, which are already running.
-// The CTA computes its tile's per-head dB/dC rows exactly as dbdc_kernel does
-// (same terms, same order) into shared memory, waits until the tile's
-// semaphore reads k (a bounded spin: past spin_limit polls it sets status
-// bit 1 and skips its add), then stores (k = 0) or adds its rows into dB/dC,
-// and releases the semaphore to k + 1.
+// The CTA computes its tile's per-head dB/dC rows with dbdc_tile (the same
+// terms in the same order as the slot fold) into shared memory, waits until
+// the tile's semaphore reads k (a bounded spin: past spin_limit polls it sets
+// status bit 1 and skips its add), then stores (k = 0) or adds its rows into
+// dB/dC, and releases the semaphore to k + 1.
 template <class TIn>
-__global__ void dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
-                                    const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
-                                    const float *__restrict__ dt, const float *__restrict__ Wm,
-                                    const float *__restrict__ states, const float *__restrict__ dS,
-                                    const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
-                                    const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                                    const float *__restrict__ init, int *__restrict__ status, int *__restrict__ sem,
-                                    uint32_t spin_limit, float *__restrict__ dBo, float *__restrict__ dCo) {
+__global__ void __launch_bounds__(kTileThreads)
+    dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
+                        const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ Wm,
+                        const float *__restrict__ states, const float *__restrict__ dS,
+                        const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                        const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                        const float *__restrict__ init, int *__restrict__ status, int *__restrict__ sem,
+                        uint32_t spin_limit, float *__restrict__ dBo, float *__restrict__ dCo) {
   extern __shared__ float tile[];   // [2][kOrdTile][N]: dB rows then dC rows
+  __shared__ TileBuf<kOrdTile / 16> sb;
+  __shared__ int fr[kOrdTile];
   __shared__ int s_unit, s_go;
   if (threadIdx.x == 0) s_unit = atomicAdd(status + 1, 1);
   __syncthreads();
@@ -481,31 +704,25 @@ __global__ void dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TI
   const int64_t bi = tileid / (ntt * s.G * s.nc);
   const int64_t h = g * s.hpg + k, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
   const int64_t i0 = tt * kOrdTile, i1 = min(Lc, i0 + kOrdTile);
-  const int64_t hunit = (bi * s.nc + c) * s.H + h;
-  const float *W = Wm + hunit * s.Q * s.Q;
-  const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
-  const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
+  for (int r = threadIdx.x; r < kOrdTile; r += blockDim.x)
+    fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
+  __syncthreads();
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
-  for (int64_t e = threadIdx.x; e < (i1 - i0) * s.N; e += blockDim.x) {
-    const int64_t i = i0 + e / s.N, n = e % s.N, t = t0 + i;
-    float dc = 0.f, db = 0.f;
-    for (int64_t j = 0; j <= i; ++j) dc = fmaf(W[i * s.Q + j], ld(Bm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), dc);
-    for (int64_t j = i; j < Lc; ++j) db = fmaf(W[j * s.Q + i], ld(Cm + ((bi * s.T + t0 + j) * s.G + g) * s.N + n), db);
-    const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
-    const float *hs = f == 0 ? states + hunit * s.P * s.N + n
-                             : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N + n : nullptr);
-    const float *ds = dS + hunit * s.P * s.N + n;
-    const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
-    const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
-    float hg = 0.f, sx = 0.f;
-    for (int64_t p = 0; p < s.P; ++p) {
-      if (hs) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
-      sx = fmaf(ds[p * s.N], ld(xi + p), sx);
+  if (i0 < Lc) {   // (the whole CTA)
+    for (int64_t n0 = 0; n0 < s.N; n0 += kTC) {
+      float dcv[kOrdTile / 16][4], dbv[kOrdTile / 16][4];
+      dbdc_tile<kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h,
+                                    i0, n0, fr, fe, sb, dcv, dbv);
+#pragma unroll
+      for (int a = 0; a < kOrdTile / 16; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int64_t r = tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+          if (n >= s.N) continue;
+          tile[r * s.N + n] = dbv[a][b];
+          tile[kOrdTile * s.N + r * s.N + n] = dcv[a][b];
+        }
     }
-    const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t) * s.H + h];
-    const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
-    tile[e] = fmaf(wi, sx, db);
-    tile[kOrdTile * s.N + e] = fmaf(din, hg, dc);
   }
   __syncthreads();
   int *sm_flag = sem + tileid;
@@ -546,21 +763,79 @@ __global__ void dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TI
 // with sx_i = x_i . (dS B_i) (din_i, Hin as in chunk_scan_fwd; w_i and the
 // exp(E - Acs_i) factor zero before fe).  Also gx_i = g_i . x_i for dD, and
 // vin_i = v_i for tokens of a sequence that started inside the chunk (their
-// decay exp(Acs_i - Acs_{f-1}) also depends on Acs_{f-1}), else 0.
+// decay exp(Acs_i - Acs_{f-1}) also depends on Acs_{f-1}), else 0.  A CTA per
+// (b, c, h) and 64 tokens: the products C Hin^T and B dS^T of its tokens come
+// out of tile products (64 state columns p at a time), the per-token sums
+// from one thread per token, p ascending.
 template <class TIn>
-__global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
-                                const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
-                                const float *__restrict__ dt, const float *__restrict__ MGm,
-                                const float *__restrict__ states, const float *__restrict__ dS,
-                                const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
-                                const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                                const float *__restrict__ init, float *__restrict__ ddt_part,
-                                float *__restrict__ dAcs, float *__restrict__ u_buf, float *__restrict__ gx_buf,
-                                float *__restrict__ vin_buf) {
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= s.b * s.H * s.nc * s.Q) return;
-  const int64_t i = idx % s.Q, c = (idx / s.Q) % s.nc, h = (idx / (s.Q * s.nc)) % s.H, bi = idx / (s.Q * s.nc * s.H);
-  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg, t = t0 + i;
+__global__ void __launch_bounds__(kTileThreads)
+    ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
+                    const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ MGm,
+                    const float *__restrict__ states, const float *__restrict__ dS, const float *__restrict__ acs_hi,
+                    const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
+                    const int32_t *__restrict__ first, const float *__restrict__ init, float *__restrict__ ddt_part,
+                    float *__restrict__ dAcs, float *__restrict__ u_buf, float *__restrict__ gx_buf,
+                    float *__restrict__ vin_buf) {
+  __shared__ TileBuf<4> sb;
+  __shared__ float chs[64][kTC + 1], ys[64][kTC + 1];
+  const int64_t unit = blockIdx.x;  // (b, c, h)
+  const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
+  const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
+  const int64_t i0 = int64_t(blockIdx.y) * 64;
+  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
+  const float *hst = states + unit * s.P * s.N, *ds = dS + unit * s.P * s.N;
+  // this thread's token (threads 0..63) and what it needs across the state tiles
+  const int r = threadIdx.x;
+  const int64_t i = i0 + r, t = t0 + i;
+  const bool mine = r < 64 && i < Lc;
+  const int64_t f = mine ? local_start(seq_idx, first, bi, s.T, t, t0) : 0;
+  const float *hsi = nullptr;   // initial state of a sequence that started inside the chunk
+  if (mine && f > 0 && init) hsi = init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N;
+  const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
+  const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
+  const TIn *ci = cc + i * GN;
+  float inter = 0.f, sx = 0.f, gx = 0.f;
+  if (i0 < Lc) {   // (the whole CTA)
+    for (int64_t p0 = 0; p0 < s.P; p0 += kTC) {
+      float acc[4][4];
+      tile_mm<4, true, true>(
+          s.N, [&](int rr, int64_t n) { const int64_t ii = i0 + rr; return ii < Lc ? ld(cc + ii * GN + n) : 0.f; },
+          [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? hst[p * s.N + n] : 0.f; }, sb, acc);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) chs[tile_ty() + 16 * a][tile_tx() + 16 * b] = acc[a][b];
+      tile_mm<4, true, true>(
+          s.N, [&](int rr, int64_t n) { const int64_t ii = i0 + rr; return ii < Lc ? ld(bc + ii * GN + n) : 0.f; },
+          [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? ds[p * s.N + n] : 0.f; }, sb, acc);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) ys[tile_ty() + 16 * a][tile_tx() + 16 * b] = acc[a][b];
+      __syncthreads();
+      if (mine) {
+        const int64_t pe = min(int64_t(kTC), s.P - p0);
+        for (int64_t pp = 0; pp < pe; ++pp) {
+          const int64_t p = p0 + pp;
+          float hc = chs[r][pp];
+          if (f > 0) {   // a sequence that started inside the chunk: its own initial state
+            hc = 0.f;
+            if (hsi)
+              for (int64_t n = 0; n < s.N; ++n) hc = fmaf(hsi[p * s.N + n], ld(ci + n), hc);
+          }
+          const float gp = ld(gi + p), xp = ld(xi + p);
+          inter = fmaf(gp, hc, inter);
+          sx = fmaf(xp, ys[r][pp], sx);
+          gx = fmaf(gp, xp, gx);
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (r >= 64 || i >= s.Q) return;
+  const int64_t idx = ((bi * s.H + h) * s.nc + c) * s.Q + i;
   if (i >= Lc) {
     dAcs[idx] = 0.f;
     u_buf[idx] = 0.f;
@@ -568,7 +843,6 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
     vin_buf[idx] = 0.f;
     return;
   }
-  const int64_t unit = (bi * s.nc + c) * s.H + h;
   const float *MG = MGm + unit * s.Q * s.Q;
   const float *dtc = dt + (bi * s.T + t0) * s.H + h;  // dtc[j * H]
   float col = 0.f, row = 0.f;
@@ -576,27 +850,7 @@ __global__ void ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *_
   for (int64_t j = i + 1; j < Lc; ++j) col += MG[j * s.Q + i];
   for (int64_t j = 0; j < i; ++j) row = fmaf(MG[i * s.Q + j], dtc[j * s.H], row);
   const float dti = dtc[i * s.H];
-  const int64_t f = local_start(seq_idx, first, bi, s.T, t, t0);
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
-  const float *hs = f == 0 ? states + unit * s.P * s.N
-                           : (init ? init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N : nullptr);
-  const float *ds = dS + unit * s.P * s.N;
-  const TIn *ci = Cm + ((bi * s.T + t) * s.G + g) * s.N;
-  const TIn *b_i = Bm + ((bi * s.T + t) * s.G + g) * s.N;
-  const TIn *gi = dout + ((bi * s.T + t) * s.H + h) * s.P;
-  const TIn *xi = x + ((bi * s.T + t) * s.H + h) * s.P;
-  float inter = 0.f, sx = 0.f, gx = 0.f;
-  for (int64_t p = 0; p < s.P; ++p) {
-    float hc = 0.f, dsb = 0.f;
-    for (int64_t n = 0; n < s.N; ++n) {
-      if (hs) hc = fmaf(hs[p * s.N + n], ld(ci + n), hc);
-      dsb = fmaf(ds[p * s.N + n], ld(b_i + n), dsb);
-    }
-    const float gp = ld(gi + p), xp = ld(xi + p);
-    inter = fmaf(gp, hc, inter);
-    sx = fmaf(xp, dsb, sx);
-    gx = fmaf(gp, xp, gx);
-  }
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float eEi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i]));
@@ -767,12 +1021,15 @@ cudaError_t fwd_impl(const Shape &s, const Args &a, void *ws, int bs, cudaStream
     if (err != cudaSuccess) return err;
   }
   cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
-  chunk_state_fwd_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.H), grid1(s.P * s.N, bs)), bs, s.Q * sizeof(float), st>>>(
+  const unsigned nbch = unsigned(s.b * s.nc * s.H);
+  const unsigned tiles_pn = unsigned(cdiv(s.P, 64) * cdiv(s.N, kTC)), tiles_qq = unsigned(cdiv(s.Q, 64) * cdiv(s.Q, 64));
+  const unsigned tiles_qp = unsigned(cdiv(s.Q, 64) * cdiv(s.P, kTC));
+  chunk_state_fwd_kernel<TIn><<<dim3(nbch, tiles_pn), kTileThreads, s.Q * sizeof(float), st>>>(
       s, x, Bm, a.dt, w.acs_hi, w.acs_lo, a.seq_idx, first, w.S);
   state_passing_fwd_kernel<<<grid1(s.b * s.H * s.P * s.N, bs), bs, 0, st>>>(s, w.S, w.acs_hi, w.acs_lo, a.seq_idx,
                                                                             first, a.init, a.states_out);
-  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
-  chunk_scan_fwd_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(
+  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), tiles_qq), kTileThreads, 0, st>>>(s, Bm, Cm, w.CB);
+  chunk_scan_fwd_kernel<TIn><<<dim3(nbch, tiles_qp), kTileThreads, 0, st>>>(
       s, x, Cm, a.dt, a.D, w.CB, w.acs_hi, w.acs_lo, a.states_out, a.seq_idx, first, a.init,
       static_cast<TIn *>(a.y));
   return cudaGetLastError();
@@ -805,6 +1062,8 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
     if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
   }
   const unsigned nbch = unsigned(s.b * s.nc * s.H);
+  const unsigned tiles_pn = unsigned(cdiv(s.P, 64) * cdiv(s.N, kTC)), tiles_qq = unsigned(cdiv(s.Q, 64) * cdiv(s.Q, 64));
+  const unsigned tiles_qp = unsigned(cdiv(s.Q, 64) * cdiv(s.P, kTC)), tiles_qn = unsigned(cdiv(s.Q, 64) * cdiv(s.N, kTC));
   const int32_t *first = a.seq_idx ? w.first : nullptr;
   if (a.seq_idx) {
     tr.mark(st);
@@ -815,15 +1074,15 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   cumsum_fwd_kernel<<<grid1(s.b * s.nc * s.H, bs), bs, 0, st>>>(s, a.dt, a.A, w.acs_hi, w.acs_lo);
   tr.mark(st);
   tr.mark(st);
-  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, Bm, Cm, w.CB);
+  cb_kernel<TIn><<<dim3(unsigned(s.b * s.nc * s.G), tiles_qq), kTileThreads, 0, st>>>(s, Bm, Cm, w.CB);
   tr.mark(st);
   tr.mark(st);
-  mwg_kernel<TIn><<<dim3(nbch, grid1(s.Q * s.Q, bs)), bs, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo,
-                                                                    a.seq_idx, first, w.Mm, w.Wm, w.MGm);
+  mwg_kernel<TIn><<<dim3(nbch, tiles_qq), kTileThreads, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo, a.seq_idx,
+                                                                  first, w.Mm, w.Wm, w.MGm);
   tr.mark(st);
   tr.mark(st);
-  dhscan_kernel<TIn><<<dim3(nbch, grid1(PN, bs)), bs, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo,
-                                                                                 a.seq_idx, first, w.buf);
+  dhscan_kernel<TIn><<<dim3(nbch, tiles_pn), kTileThreads, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo,
+                                                                                      a.seq_idx, first, w.buf);
   tr.mark(st);
   tr.mark(st);
   // fixed block: this kernel folds per-thread partial dot products, so its
@@ -838,35 +1097,35 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
     tr.mark(st);
   }
   tr.mark(st);
-  dx_kernel<TIn><<<grid1(s.b * s.T * s.H * s.P, bs), bs, 0, st>>>(s, g, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi,
-                                                                  w.acs_lo, a.seq_idx, first, a.dx);
+  dx_kernel<TIn><<<dim3(nbch, tiles_qp), kTileThreads, 0, st>>>(s, g, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi, w.acs_lo,
+                                                                a.seq_idx, first, a.dx);
   tr.mark(st);
   if (atomic) {
     tr.mark(st);
-    dbdc_kernel<TIn, true><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
+    dbdc_kernel<TIn, true><<<dim3(nbch, tiles_qn), kTileThreads, 0, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, a.dB, a.dC);
     tr.mark(st);
   } else if (ordered) {
     tr.mark(st);
     const int64_t units = ordered_tiles(s) * s.hpg;
     const size_t shm = size_t(2 * kOrdTile * s.N) * sizeof(float);
-    if (shm > 48 * 1024 &&
-        (err = cudaFuncSetAttribute(dbdc_ordered_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // (the kernel's static tile buffers come on top of this)
+    if ((err = cudaFuncSetAttribute(dbdc_ordered_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     int(shm))) != cudaSuccess)
       return err;
-    dbdc_ordered_kernel<TIn><<<unsigned(units), bs, shm, st>>>(
+    dbdc_ordered_kernel<TIn><<<unsigned(units), kTileThreads, shm, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.status,
         w.sem, spin_limit, a.dB, a.dC);
     tr.mark(st);
   } else {
     tr.mark(st);
-    dbdc_kernel<TIn, false><<<grid1(s.b * s.T * s.H * s.N, bs), bs, 0, st>>>(
+    dbdc_kernel<TIn, false><<<dim3(nbch, tiles_qn), kTileThreads, 0, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.slot_b,
         w.slot_c);
     tr.mark(st);
   }
   tr.mark(st);
-  ddt_dacs_kernel<TIn><<<grid1(s.b * s.H * s.nc * s.Q, bs), bs, 0, st>>>(
+  ddt_dacs_kernel<TIn><<<dim3(nbch, unsigned(cdiv(s.Q, 64))), kTileThreads, 0, st>>>(
       s, x, g, Bm, Cm, a.dt, w.MGm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.ddt_part,
       w.dAcs, w.u, w.gx, w.vin);
   tr.mark(st);

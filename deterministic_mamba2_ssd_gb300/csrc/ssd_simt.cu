@@ -67,13 +67,25 @@ __device__ __forceinline__ int64_t local_start(const int32_t *seq_idx, const int
 // element is still one sequential fmaf chain over its k index, ascending, one
 // term per k (terms outside a product's range are exact zeros), so its bits
 // depend neither on the tiling nor on the launch configuration.  Thread
-// (ty, tx) = (tid / 16, tid % 16) holds rows ty + 16 a and columns tx + 16 b.
+// (ty, tx) = (tid / 16, tid % 16) holds rows RA ty + a and columns 4 tx + b,
+// read from shared memory as vectors.
 constexpr int kTileThreads = 256, kTK = 16, kTC = 64;
 
 template <int RA>
 struct TileBuf {
   float a[kTK][16 * RA + 4];
   float b[kTK][kTC + 4];
+};
+
+template <int RA>
+struct RowVec;
+template <>
+struct RowVec<4> {
+  using T = float4;
+};
+template <>
+struct RowVec<2> {
+  using T = float2;
 };
 
 // fa(r, k) = A(r, k), fb(q, k) = B(q, k) (0 outside their ranges);
@@ -104,11 +116,10 @@ __device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, T
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
-      float av[RA], bv[4];
-#pragma unroll
-      for (int a = 0; a < RA; ++a) av[a] = sb.a[kk][ty + 16 * a];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) bv[b] = sb.b[kk][tx + 16 * b];
+      const typename RowVec<RA>::T avv = *reinterpret_cast<const typename RowVec<RA>::T *>(&sb.a[kk][RA * ty]);
+      const float4 bvv = *reinterpret_cast<const float4 *>(&sb.b[kk][4 * tx]);
+      const float *av = reinterpret_cast<const float *>(&avv);
+      const float bv[4] = {bvv.x, bvv.y, bvv.z, bvv.w};
 #pragma unroll
       for (int a = 0; a < RA; ++a)
 #pragma unroll
@@ -118,8 +129,10 @@ __device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, T
   }
 }
 
-__device__ __forceinline__ int tile_tx() { return threadIdx.x & 15; }
-__device__ __forceinline__ int tile_ty() { return threadIdx.x >> 4; }
+// row and column of this thread's output (a, b) within the tile
+template <int RA>
+__device__ __forceinline__ int tile_row(int a) { return RA * int(threadIdx.x >> 4) + a; }
+__device__ __forceinline__ int tile_col(int b) { return 4 * int(threadIdx.x & 15) + b; }
 
 // ---------------------------------------------------------------- cumsum --
 // Acs (b,H,nc,Q) as hi + lo: left-to-right compensated (two-sum) prefix sum
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t p = p0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      const int64_t p = p0 + tile_row<4>(a), n = n0 + tile_col(b);
       if (p < s.P && n < s.N) S[(unit * s.P + p) * s.N + n] = acc[a][b];
     }
 }
@@ -245,7 +258,7 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t i = i0 + tile_ty() + 16 * a, j = j0 + tile_tx() + 16 * b;
+      const int64_t i = i0 + tile_row<4>(a), j = j0 + tile_col(b);
       if (i < s.Q && j < s.Q) o[i * s.Q + j] = (j <= i && i < Lc) ? acc[a][b] : 0.f;
     }
 }
@@ -297,9 +310,9 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t i = i0 + tile_ty() + 16 * a, p = p0 + tile_tx() + 16 * b;
+      const int64_t i = i0 + tile_row<4>(a), p = p0 + tile_col(b);
       if (i >= Lc || p >= s.P) continue;
-      const int64_t t = t0 + i, f = fr[tile_ty() + 16 * a];
+      const int64_t t = t0 + i, f = fr[tile_row<4>(a)];
       float in = inter[a][b];
       if (f > 0) {   // a sequence that started inside the chunk: its own initial state
         in = 0.f;
@@ -321,14 +334,21 @@ __global__ void __launch_bounds__(kTileThreads)
 // Per (b,c,h,i,j) with local_start(i) <= j <= i < Lc (same sequence):
 // L = exp(Acs_i - Acs_j), Gx = g_i . x_j, M = CB[i,j] L, W = L Gx dt_j,
 // MG = M Gx; zero elsewhere.  A CTA per (b, c, h) and 64 x 64 tile of (i, j).
+// MG is only needed through its sums, so it is not stored: each tile leaves,
+// per row i, its part of sum_{j<i} MG[i,j] dt_j (rowp[unit][tile column][i]),
+// per column j its part of sum_{i>j} MG[i,j] (colp[unit][tile row][j]), and
+// MG[i,i] (dg[unit][i]), each summed in one fixed order (the thread's four
+// elements, then a fixed shuffle tree over the tile's row or a fixed loop
+// over its column).
 template <class TIn>
 __global__ void __launch_bounds__(kTileThreads)
     mwg_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const float *__restrict__ dt,
                const float *__restrict__ CB, const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
                const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first, float *__restrict__ Mm,
-               float *__restrict__ Wm, float *__restrict__ MGm) {
+               float *__restrict__ Wm, float *__restrict__ rowp, float *__restrict__ colp, float *__restrict__ dg) {
   __shared__ TileBuf<4> sb;
   __shared__ int fr[64];
+  __shared__ float cpart[16][kTC];   // column partials of each thread row
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t nt = cdiv(s.Q, 64);
@@ -348,25 +368,47 @@ __global__ void __launch_bounds__(kTileThreads)
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *cb = CB + ((bi * s.nc + c) * s.G + g) * s.Q * s.Q;
+  float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t i = i0 + tile_ty() + 16 * a, j = j0 + tile_tx() + 16 * b;
+      const int64_t i = i0 + tile_row<4>(a), j = j0 + tile_col(b);
       if (i >= s.Q || j >= s.Q) continue;
-      float M = 0.f, W = 0.f, MG = 0.f;
-      if (live && j <= i && i < Lc && j >= fr[tile_ty() + 16 * a]) {
+      float M = 0.f, W = 0.f, MG = 0.f, dtj = 0.f;
+      if (live && j <= i && i < Lc && j >= fr[tile_row<4>(a)]) {
         const float L = expf(acs_diff(ah[i], al[i], ah[j], al[j]));
         const float gx = acc[a][b];
+        dtj = dt[(bi * s.T + t0 + j) * s.H + h];
         M = cb[i * s.Q + j] * L;
-        W = L * gx * dt[(bi * s.T + t0 + j) * s.H + h];
+        W = L * gx * dtj;
         MG = M * gx;
       }
       const int64_t o = unit * s.Q * s.Q + i * s.Q + j;
       Mm[o] = M;
       Wm[o] = W;
-      MGm[o] = MG;
+      if (j < i) rp[a] += MG * dtj;
+      if (i > j) cp[b] += MG;
+      if (i == j) dg[unit * s.Q + i] = MG;
     }
+  // row parts: the 16 threads of a tile row (lanes 16 ty .. 16 ty + 15 of one warp)
+  const int64_t nt2 = cdiv(s.Q, 64), it = blockIdx.y / nt2, jt = blockIdx.y % nt2;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float v = rp[a];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int64_t i = i0 + tile_row<4>(a);
+    if ((threadIdx.x & 15) == 0 && i < s.Q) rowp[(unit * nt2 + jt) * s.Q + i] = v;
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) cpart[threadIdx.x >> 4][tile_col(b)] = cp[b];
+  __syncthreads();
+  if (threadIdx.x < kTC && j0 + threadIdx.x < s.Q) {
+    float v = 0.f;
+    for (int r = 0; r < 16; ++r) v += cpart[r][threadIdx.x];
+    colp[(unit * nt2 + it) * s.Q + j0 + threadIdx.x] = v;
+  }
 }
 
 // dHscan[b,c,h,p,n] = sum_i exp(Acs_i) g_i[p] C_i[n] over the tokens that see
@@ -400,7 +442,7 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t p = p0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      const int64_t p = p0 + tile_row<4>(a), n = n0 + tile_col(b);
       if (p < s.P && n < s.N) dH[(unit * s.P + p) * s.N + n] = acc[a][b];
     }
 }
@@ -419,7 +461,7 @@ __device__ float block_sum(float v, float *red) {
   return tot;  // valid in thread 0
 }
 
-// Reverse state passing, one CTA per (b,h), in place on buf:
+// Reverse state passing, in place on buf:
 //   in:  buf[c] = dHscan_c;  out: buf[c] = dS_c = gradient reaching the end
 //   state of chunk c (dH_{c+1}, or 0 where chunk c+1 starts a sequence);
 //   dH_c = dHscan_c + exp(E_c) dS_c when the sequence holding the chunk's
@@ -428,16 +470,51 @@ __device__ float block_sum(float v, float *red) {
 //   exp(E_c - Acs_{fe-1}) <init[seq], dS_c> (fe >= 1: the carried part of the
 //   chunk-end state then starts from that sequence's initial state);
 //   dinit[seq] += dH_c where chunk c starts a sequence at its first token.
-__global__ void state_passing_bwd_kernel(Shape s, float *__restrict__ buf, float *__restrict__ carry,
-                                         const float *__restrict__ states, const float *__restrict__ acs_hi,
-                                         const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                                         const int32_t *__restrict__ first, const float *__restrict__ init,
-                                         float *__restrict__ dEpass, float *__restrict__ dinit) {
+// The recurrence is elementwise in (p, n): a CTA per (b, h) and slice of
+// kPassSlice state elements walks the chunks in reverse with the running dH
+// of its elements in registers; dEpass is left as one partial per slice
+// (dEpart[b,h,c,slice], the slice's block sum times the decay factor), which
+// the cumsum backward adds in slice order.
+constexpr int kPassSlice = 4 * kPassThreads;
+
+__global__ void __launch_bounds__(kPassThreads)
+    state_passing_bwd_kernel(Shape s, float *__restrict__ buf, const float *__restrict__ states,
+                             const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                             const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                             const float *__restrict__ init, float *__restrict__ dEpart, float *__restrict__ dinit) {
   __shared__ float red[32];
   const int64_t h = blockIdx.x % s.H, bi = blockIdx.x / s.H;
-  const int64_t PN = s.P * s.N;
-  float *cr = carry + (bi * s.H + h) * PN;
+  const int64_t PN = s.P * s.N, nsl = cdiv(PN, kPassSlice), sl = blockIdx.y;
+  const int64_t e0 = sl * kPassSlice + threadIdx.x;
+  float cr[4] = {0.f, 0.f, 0.f, 0.f};   // dH of the chunk after, per owned element
+  // Chunk c's dHscan and carried-in state (the state entering the chunk, or the
+  // initial state of the sequence holding its last token) for the owned elements.
+  auto hin_of = [&](int64_t c) -> const float * {
+    const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
+    const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
+    return fe == 0 ? states + ((bi * s.nc + c) * s.H + h) * PN
+                   : (init ? init + (seq_of(seq_idx, bi, s.T, t0 + Lc - 1) * s.H + h) * PN : nullptr);
+  };
+  auto load = [&](int64_t c, float (&dh)[4], float (&hv)[4]) {
+    const float *bc = buf + ((bi * s.nc + c) * s.H + h) * PN;
+    const float *hin = hin_of(c);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t e = e0 + k * kPassThreads;
+      dh[k] = e < PN ? bc[e] : 0.f;
+      hv[k] = (hin && e < PN) ? hin[e] : 0.f;
+    }
+  };
+  float dh_n[4], hv_n[4];   // the next chunk down, loaded one step ahead
+  load(s.nc - 1, dh_n, hv_n);
   for (int64_t c = s.nc - 1; c >= 0; --c) {
+    float dh[4], hv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      dh[k] = dh_n[k];
+      hv[k] = hv_n[k];
+    }
+    if (c > 0) load(c - 1, dh_n, hv_n);
     const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
     const bool nxt_start = (c + 1 >= s.nc) || is_seq_start(seq_idx, bi, s.T, (c + 1) * s.Q);
     const bool here_start = is_seq_start(seq_idx, bi, s.T, t0);
@@ -446,22 +523,23 @@ __global__ void state_passing_bwd_kernel(Shape s, float *__restrict__ buf, float
     const float eE = expf(__fadd_rn(acs_hi[q], acs_lo[q]));
     const float eIn = fe == 0 ? eE : expf(acs_diff(acs_hi[q], acs_lo[q], acs_hi[q0 + fe - 1], acs_lo[q0 + fe - 1]));
     const float eCarry = fe == 0 ? eE : 0.f;
+    const bool has_hin = hin_of(c) != nullptr;
     float *bc = buf + ((bi * s.nc + c) * s.H + h) * PN;
-    const float *hin = fe == 0 ? states + ((bi * s.nc + c) * s.H + h) * PN
-                               : (init ? init + (seq_of(seq_idx, bi, s.T, t0 + Lc - 1) * s.H + h) * PN : nullptr);
     float *di = (here_start && dinit) ? dinit + (seq_of(seq_idx, bi, s.T, t0) * s.H + h) * PN : nullptr;
     float part = 0.f;
-    for (int64_t e = threadIdx.x; e < PN; e += blockDim.x) {
-      const float cur = nxt_start ? 0.f : cr[e];
-      const float dh = bc[e];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t e = e0 + k * kPassThreads;
+      if (e >= PN) continue;
+      const float cur = nxt_start ? 0.f : cr[k];
       bc[e] = cur;
-      if (hin) part = fmaf(hin[e], cur, part);
-      const float dHc = fmaf(eCarry, cur, dh);
-      cr[e] = dHc;
+      if (has_hin) part = fmaf(hv[k], cur, part);
+      const float dHc = fmaf(eCarry, cur, dh[k]);
+      cr[k] = dHc;
       if (di) di[e] += dHc;
     }
     const float tot = block_sum(part, red);
-    if (threadIdx.x == 0) dEpass[(bi * s.H + h) * s.nc + c] = eIn * tot;
+    if (threadIdx.x == 0) dEpart[((bi * s.H + h) * s.nc + c) * nsl + sl] = eIn * tot;
   }
 }
 
@@ -530,14 +608,14 @@ __global__ void __launch_bounds__(kTileThreads)
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    const int64_t i = i0 + tile_ty() + 16 * a;
+    const int64_t i = i0 + tile_row<4>(a);
     if (i >= Lc) continue;
     const int64_t t = t0 + i;
     const float dti = dt[(bi * s.T + t) * s.H + h];
     const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dti;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t p = p0 + tile_tx() + 16 * b;
+      const int64_t p = p0 + tile_col(b);
       if (p >= s.P) continue;
       const int64_t idx = ((bi * s.T + t) * s.H + h) * s.P + p;
       dx[idx] = fmaf(dti, d1[a][b], fmaf(wi, yv[a][b], D[h] * ld(dout + idx)));
@@ -582,13 +660,13 @@ __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict_
       [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? hst[p * s.N + n] : 0.f; }, sb, t1);
 #pragma unroll
   for (int a = 0; a < RA; ++a) {
-    const int64_t i = i0 + tile_ty() + 16 * a;
+    const int64_t i = i0 + tile_row<RA>(a);
     if (i >= Lc) continue;
-    const int64_t f = fr[tile_ty() + 16 * a];
+    const int64_t f = fr[tile_row<RA>(a)];
     const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t n = n0 + tile_tx() + 16 * b;
+      const int64_t n = n0 + tile_col(b);
       if (n >= s.N) continue;
       float hg = t1[a][b];
       if (f > 0) {   // a sequence that started inside the chunk: its own initial state
@@ -610,7 +688,7 @@ __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict_
       [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? ds[p * s.N + n] : 0.f; }, sb, t1);
 #pragma unroll
   for (int a = 0; a < RA; ++a) {
-    const int64_t i = i0 + tile_ty() + 16 * a;
+    const int64_t i = i0 + tile_row<RA>(a);
     if (i >= Lc) continue;
     const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t0 + i) * s.H + h];
 #pragma unroll
@@ -647,7 +725,7 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const int64_t i = i0 + tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+      const int64_t i = i0 + tile_row<4>(a), n = n0 + tile_col(b);
       if (i >= Lc || n >= s.N) continue;
       const int64_t t = t0 + i;
       if (kAtomic) {
@@ -717,7 +795,7 @@ __global__ void __launch_bounds__(kTileThreads)
       for (int a = 0; a < kOrdTile / 16; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const int64_t r = tile_ty() + 16 * a, n = n0 + tile_tx() + 16 * b;
+          const int64_t r = tile_row<kOrdTile / 16>(a), n = n0 + tile_col(b);
           if (n >= s.N) continue;
           tile[r * s.N + n] = dbv[a][b];
           tile[kOrdTile * s.N + r * s.N + n] = dcv[a][b];
@@ -763,33 +841,35 @@ __global__ void __launch_bounds__(kTileThreads)
 // with sx_i = x_i . (dS B_i) (din_i, Hin as in chunk_scan_fwd; w_i and the
 // exp(E - Acs_i) factor zero before fe).  Also gx_i = g_i . x_i for dD, and
 // vin_i = v_i for tokens of a sequence that started inside the chunk (their
-// decay exp(Acs_i - Acs_{f-1}) also depends on Acs_{f-1}), else 0.  A CTA per
-// (b, c, h) and 64 tokens: the products C Hin^T and B dS^T of its tokens come
-// out of tile products (64 state columns p at a time), the per-token sums
-// from one thread per token, p ascending.
+// decay exp(Acs_i - Acs_{f-1}) also depends on Acs_{f-1}), else 0.  The MG
+// sums come from mwg_kernel's tile parts (tiles in ascending order).  A CTA
+// per (b, c, h) and 64 tokens: the products C Hin^T and B dS^T of its tokens
+// come out of tile products (64 state columns p at a time); four threads per
+// token each sum a quarter of every p tile, p ascending, and the quarters are
+// added in a fixed tree.
 template <class TIn>
 __global__ void __launch_bounds__(kTileThreads)
     ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
-                    const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ MGm,
-                    const float *__restrict__ states, const float *__restrict__ dS, const float *__restrict__ acs_hi,
-                    const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-                    const int32_t *__restrict__ first, const float *__restrict__ init, float *__restrict__ ddt_part,
-                    float *__restrict__ dAcs, float *__restrict__ u_buf, float *__restrict__ gx_buf,
-                    float *__restrict__ vin_buf) {
+                    const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ rowp,
+                    const float *__restrict__ colp, const float *__restrict__ dg, const float *__restrict__ states,
+                    const float *__restrict__ dS, const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+                    const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
+                    const float *__restrict__ init, float *__restrict__ ddt_part, float *__restrict__ dAcs,
+                    float *__restrict__ u_buf, float *__restrict__ gx_buf, float *__restrict__ vin_buf) {
   __shared__ TileBuf<4> sb;
   __shared__ float chs[64][kTC + 1], ys[64][kTC + 1];
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
   const int64_t i0 = int64_t(blockIdx.y) * 64;
-  const int64_t HP = s.H * s.P, GN = s.G * s.N;
+  const int64_t GN = s.G * s.N;
   const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
   const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
   const float *hst = states + unit * s.P * s.N, *ds = dS + unit * s.P * s.N;
-  // this thread's token (threads 0..63) and what it needs across the state tiles
-  const int r = threadIdx.x;
+  // this thread's token and quarter of the state columns
+  const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int64_t i = i0 + r, t = t0 + i;
-  const bool mine = r < 64 && i < Lc;
+  const bool mine = i < Lc;
   const int64_t f = mine ? local_start(seq_idx, first, bi, s.T, t, t0) : 0;
   const float *hsi = nullptr;   // initial state of a sequence that started inside the chunk
   if (mine && f > 0 && init) hsi = init + (seq_of(seq_idx, bi, s.T, t) * s.H + h) * s.P * s.N;
@@ -806,18 +886,18 @@ __global__ void __launch_bounds__(kTileThreads)
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) chs[tile_ty() + 16 * a][tile_tx() + 16 * b] = acc[a][b];
+        for (int b = 0; b < 4; ++b) chs[tile_row<4>(a)][tile_col(b)] = acc[a][b];
       tile_mm<4, true, true>(
           s.N, [&](int rr, int64_t n) { const int64_t ii = i0 + rr; return ii < Lc ? ld(bc + ii * GN + n) : 0.f; },
           [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? ds[p * s.N + n] : 0.f; }, sb, acc);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) ys[tile_ty() + 16 * a][tile_tx() + 16 * b] = acc[a][b];
+        for (int b = 0; b < 4; ++b) ys[tile_row<4>(a)][tile_col(b)] = acc[a][b];
       __syncthreads();
       if (mine) {
         const int64_t pe = min(int64_t(kTC), s.P - p0);
-        for (int64_t pp = 0; pp < pe; ++pp) {
+        for (int64_t pp = 16 * part; pp < min(pe, int64_t(16 * part + 16)); ++pp) {
           const int64_t p = p0 + pp;
           float hc = chs[r][pp];
           if (f > 0) {   // a sequence that started inside the chunk: its own initial state
@@ -834,7 +914,14 @@ __global__ void __launch_bounds__(kTileThreads)
       __syncthreads();
     }
   }
-  if (r >= 64 || i >= s.Q) return;
+  // the four quarters of each token (lanes 4 r .. 4 r + 3 of one warp), fixed tree
+  inter += __shfl_xor_sync(0xffffffffu, inter, 1);
+  sx += __shfl_xor_sync(0xffffffffu, sx, 1);
+  gx += __shfl_xor_sync(0xffffffffu, gx, 1);
+  inter += __shfl_xor_sync(0xffffffffu, inter, 2);
+  sx += __shfl_xor_sync(0xffffffffu, sx, 2);
+  gx += __shfl_xor_sync(0xffffffffu, gx, 2);
+  if (part != 0 || i >= s.Q) return;
   const int64_t idx = ((bi * s.H + h) * s.nc + c) * s.Q + i;
   if (i >= Lc) {
     dAcs[idx] = 0.f;
@@ -843,12 +930,14 @@ __global__ void __launch_bounds__(kTileThreads)
     vin_buf[idx] = 0.f;
     return;
   }
-  const float *MG = MGm + unit * s.Q * s.Q;
-  const float *dtc = dt + (bi * s.T + t0) * s.H + h;  // dtc[j * H]
+  const int64_t nt = cdiv(s.Q, 64);
   float col = 0.f, row = 0.f;
-  const float diag = MG[i * s.Q + i];
-  for (int64_t j = i + 1; j < Lc; ++j) col += MG[j * s.Q + i];
-  for (int64_t j = 0; j < i; ++j) row = fmaf(MG[i * s.Q + j], dtc[j * s.H], row);
+  for (int64_t k = 0; k < nt; ++k) {
+    row += rowp[(unit * nt + k) * s.Q + i];
+    col += colp[(unit * nt + k) * s.Q + i];
+  }
+  const float diag = dg[unit * s.Q + i];
+  const float *dtc = dt + (bi * s.T + t0) * s.H + h;  // dtc[j * H]
   const float dti = dtc[i * s.H];
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
@@ -889,7 +978,9 @@ __global__ void cumsum_bwd_kernel(Shape s, const float *__restrict__ dt, const f
     sg += gx_buf[base + i];
   }
   const float Ah = A[h];
-  const float dEp = dEpass[(bi * s.H + h) * s.nc + c];
+  const int64_t nsl = cdiv(s.P * s.N, kPassSlice);
+  float dEp = 0.f;   // the slices' parts of exp(E) <Hin, dS>, in slice order
+  for (int64_t k = 0; k < nsl; ++k) dEp += dEpass[((bi * s.H + h) * s.nc + c) * nsl + k];
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
   float da = su + dEp;
   float pend = fe > 0 ? dEp : 0.f;  // owed by Acs_{f-1} of the sequence being walked
@@ -948,7 +1039,7 @@ __global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ d
 
 struct BwdWs {
   int *status;   // [0] error bits (bit 1: an ordered-fold wait gave up), [1] ticket; first in the workspace
-  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *MGm, *buf, *carry, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
+  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *rowp, *colp, *dg, *buf, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
       *dD_part, *slot_b, *slot_c;
   int32_t *first;
   int *sem;
@@ -966,10 +1057,12 @@ BwdWs carve_bwd(Carver &cv, const Shape &s, int variant) {
   w.CB = cv.take<float>(s.b * s.nc * s.G * s.Q * s.Q);
   w.Mm = cv.take<float>(qq);
   w.Wm = cv.take<float>(qq);
-  w.MGm = cv.take<float>(qq);
+  const int64_t parts = s.b * s.nc * s.H * cdiv(s.Q, 64) * s.Q;   // MG sums, per 64-wide tile
+  w.rowp = cv.take<float>(parts);
+  w.colp = cv.take<float>(parts);
+  w.dg = cv.take<float>(s.b * s.nc * s.H * s.Q);
   w.buf = cv.take<float>(s.b * s.nc * s.H * s.P * s.N);
-  w.carry = cv.take<float>(s.b * s.H * s.P * s.N);
-  w.dEpass = cv.take<float>(s.b * s.H * s.nc);
+  w.dEpass = cv.take<float>(s.b * s.H * s.nc * cdiv(s.P * s.N, kPassSlice));
   w.dAcs = cv.take<float>(acs);
   w.u = cv.take<float>(acs);
   w.gx = cv.take<float>(acs);
@@ -1049,8 +1142,6 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
     err = cudaMemsetAsync(a.dinit, 0, size_t(s.nseq * s.H * PN) * sizeof(float), st);
     if (err != cudaSuccess) return err;
   }
-  err = cudaMemsetAsync(w.carry, 0, size_t(s.b * s.H * PN) * sizeof(float), st);
-  if (err != cudaSuccess) return err;
   if ((err = cudaMemsetAsync(w.status, 0, 2 * sizeof(int), st)) != cudaSuccess) return err;
   if (ordered && (err = cudaMemsetAsync(w.sem, 0, size_t(ordered_tiles(s)) * sizeof(int), st)) != cudaSuccess)
     return err;
@@ -1078,7 +1169,7 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   tr.mark(st);
   tr.mark(st);
   mwg_kernel<TIn><<<dim3(nbch, tiles_qq), kTileThreads, 0, st>>>(s, x, g, a.dt, w.CB, w.acs_hi, w.acs_lo, a.seq_idx,
-                                                                  first, w.Mm, w.Wm, w.MGm);
+                                                                  first, w.Mm, w.Wm, w.rowp, w.colp, w.dg);
   tr.mark(st);
   tr.mark(st);
   dhscan_kernel<TIn><<<dim3(nbch, tiles_pn), kTileThreads, s.Q * sizeof(float), st>>>(s, g, Cm, w.acs_hi, w.acs_lo,
@@ -1087,8 +1178,8 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   tr.mark(st);
   // fixed block: this kernel folds per-thread partial dot products, so its
   // shape must not follow the launch configuration
-  state_passing_bwd_kernel<<<unsigned(s.b * s.H), kPassThreads, 0, st>>>(
-      s, w.buf, w.carry, a.states_in, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.dEpass, a.dinit);
+  state_passing_bwd_kernel<<<dim3(unsigned(s.b * s.H), unsigned(cdiv(PN, kPassSlice))), kPassThreads, 0, st>>>(
+      s, w.buf, a.states_in, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.dEpass, a.dinit);
   tr.mark(st);
   if (a.seq_idx) {
     tr.mark(st);
@@ -1126,7 +1217,7 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   }
   tr.mark(st);
   ddt_dacs_kernel<TIn><<<dim3(nbch, unsigned(cdiv(s.Q, 64))), kTileThreads, 0, st>>>(
-      s, x, g, Bm, Cm, a.dt, w.MGm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.ddt_part,
+      s, x, g, Bm, Cm, a.dt, w.rowp, w.colp, w.dg, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.ddt_part,
       w.dAcs, w.u, w.gx, w.vin);
   tr.mark(st);
   if (atomic) {

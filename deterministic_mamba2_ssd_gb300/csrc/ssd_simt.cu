@@ -100,20 +100,40 @@ __device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, T
   for (int a = 0; a < RA; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+  // the next k block is read from global memory into registers while the
+  // current one is multiplied out of shared memory
+  constexpr int NA = R * kTK / kTileThreads, NB = kTC * kTK / kTileThreads;
+  float ra[NA], rb[NB];
+  auto fetch = [&](int64_t k0) {
+#pragma unroll
+    for (int u = 0; u < NA; ++u) {
+      const int e = u * kTileThreads + tid;
+      const int r = kAKFast ? e / kTK : e % R, kk = kAKFast ? e % kTK : e / R;
+      ra[u] = (k0 + kk < K) ? fa(r, k0 + kk) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < NB; ++u) {
+      const int e = u * kTileThreads + tid;
+      const int q = kBKFast ? e / kTK : e % kTC, kk = kBKFast ? e % kTK : e / kTC;
+      rb[u] = (k0 + kk < K) ? fb(q, k0 + kk) : 0.f;
+    }
+  };
+  if (K > 0) fetch(0);
   for (int64_t k0 = 0; k0 < K; k0 += kTK) {
 #pragma unroll
-    for (int e0 = 0; e0 < R * kTK; e0 += kTileThreads) {
-      const int e = e0 + tid;
+    for (int u = 0; u < NA; ++u) {
+      const int e = u * kTileThreads + tid;
       const int r = kAKFast ? e / kTK : e % R, kk = kAKFast ? e % kTK : e / R;
-      sb.a[kk][r] = (k0 + kk < K) ? fa(r, k0 + kk) : 0.f;
+      sb.a[kk][r] = ra[u];
     }
 #pragma unroll
-    for (int e0 = 0; e0 < kTC * kTK; e0 += kTileThreads) {
-      const int e = e0 + tid;
+    for (int u = 0; u < NB; ++u) {
+      const int e = u * kTileThreads + tid;
       const int q = kBKFast ? e / kTK : e % kTC, kk = kBKFast ? e % kTK : e / kTC;
-      sb.b[kk][q] = (k0 + kk < K) ? fb(q, k0 + kk) : 0.f;
+      sb.b[kk][q] = rb[u];
     }
     __syncthreads();
+    if (k0 + kTK < K) fetch(k0 + kTK);
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
       const typename RowVec<RA>::T avv = *reinterpret_cast<const typename RowVec<RA>::T *>(&sb.a[kk][RA * ty]);
@@ -269,7 +289,7 @@ __global__ void __launch_bounds__(kTileThreads)
 // and din_i = exp(Acs_i) when f = 0, else Hin = init[seq] (or 0) and
 // din_i = exp(Acs_i - Acs_{f-1}).  A CTA per (b, c, h) and 64 x 64 tile of (i, p).
 template <class TIn>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 3)
     chunk_scan_fwd_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ Cm, const float *__restrict__ dt,
                           const float *__restrict__ D, const float *__restrict__ CB, const float *__restrict__ acs_hi,
                           const float *__restrict__ acs_lo, const float *__restrict__ states,
@@ -579,7 +599,7 @@ __global__ void dinit_mid_kernel(Shape s, const TIn *__restrict__ dout, const TI
 // chunk's last token (i >= fe), else 0.  A CTA per (b, c, h) and 64 x 64 tile
 // of (i, p).
 template <class TIn>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 3)
     dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm, const float *__restrict__ dt,
               const float *__restrict__ D, const float *__restrict__ Mm, const float *__restrict__ dS,
               const float *__restrict__ acs_hi, const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
@@ -626,11 +646,11 @@ __global__ void __launch_bounds__(kTileThreads)
 // Per-head dB / dC rows of tokens i0 .. i0 + 16 RA - 1 of chunk c, state
 // columns n0 .. n0 + 63 (shared by the slot and the ordered fold, so both
 // produce the same bits):
-//   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + din_i sum_p Hin[p,n] g_i[p]
-//   dB_h[i,n] = sum_{j>=i} W[j,i] C_j[n] + w_i sum_p dS[p,n] x_i[p]
+//   dC_h[i,n] = sum_{j<=i} W[i,j] B_j[n] + din_i sum_p Hin[p,n] g_i[p]   (kDB false)
+//   dB_h[i,n] = sum_{j>=i} W[j,i] C_j[n] + w_i sum_p dS[p,n] x_i[p]      (kDB true)
 // (din_i, Hin as in chunk_scan_fwd; w_i as in dx_kernel; fr[r]: local start
 // of row i0 + r).
-template <int RA, class TIn>
+template <bool kDB, int RA, class TIn>
 __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict__ x, const TIn *__restrict__ dout,
                                           const TIn *__restrict__ Bm, const TIn *__restrict__ Cm,
                                           const float *__restrict__ dt, const float *__restrict__ Wm,
@@ -638,68 +658,74 @@ __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict_
                                           const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
                                           const int32_t *__restrict__ seq_idx, const float *__restrict__ init,
                                           int64_t bi, int64_t c, int64_t h, int64_t i0, int64_t n0, const int *fr,
-                                          int64_t fe, TileBuf<RA> &sb, float (&dcv)[RA][4], float (&dbv)[RA][4]) {
+                                          int64_t fe, TileBuf<RA> &sb, float (&res)[RA][4]) {
   const int64_t g = h / s.hpg, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
   const int64_t unit = (bi * s.nc + c) * s.H + h;
   const int64_t HP = s.H * s.P, GN = s.G * s.N;
   const float *W = Wm + unit * s.Q * s.Q;
-  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
-  const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
-  const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
-  const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;
-  const float *hst = states + unit * s.P * s.N, *ds = dS + unit * s.P * s.N;
   const float *ah = acs_hi + ((bi * s.H + h) * s.nc + c) * s.Q;
   const float *al = acs_lo + ((bi * s.H + h) * s.nc + c) * s.Q;
   float t1[RA][4];
   auto row_ok = [&](int r) { return i0 + r < Lc; };
-  tile_mm<RA, true, false>(
-      Lc, [&](int r, int64_t j) { return row_ok(r) ? W[(i0 + r) * s.Q + j] : 0.f; },
-      [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(bc + j * GN + n) : 0.f; }, sb, dcv);
-  tile_mm<RA, true, false>(
-      s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(gc + (i0 + r) * HP + p) : 0.f; },
-      [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? hst[p * s.N + n] : 0.f; }, sb, t1);
+  if (!kDB) {
+    const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
+    const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
+    const float *hst = states + unit * s.P * s.N;
+    tile_mm<RA, true, false>(
+        Lc, [&](int r, int64_t j) { return row_ok(r) ? W[(i0 + r) * s.Q + j] : 0.f; },
+        [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(bc + j * GN + n) : 0.f; }, sb, res);
+    tile_mm<RA, true, false>(
+        s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(gc + (i0 + r) * HP + p) : 0.f; },
+        [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? hst[p * s.N + n] : 0.f; }, sb, t1);
 #pragma unroll
-  for (int a = 0; a < RA; ++a) {
-    const int64_t i = i0 + tile_row<RA>(a);
-    if (i >= Lc) continue;
-    const int64_t f = fr[tile_row<RA>(a)];
-    const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
+    for (int a = 0; a < RA; ++a) {
+      const int64_t i = i0 + tile_row<RA>(a);
+      if (i >= Lc) continue;
+      const int64_t f = fr[tile_row<RA>(a)];
+      const float din = expf(f == 0 ? __fadd_rn(ah[i], al[i]) : acs_diff(ah[i], al[i], ah[f - 1], al[f - 1]));
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int64_t n = n0 + tile_col(b);
-      if (n >= s.N) continue;
-      float hg = t1[a][b];
-      if (f > 0) {   // a sequence that started inside the chunk: its own initial state
-        hg = 0.f;
-        if (init) {
-          const float *hs = init + (seq_of(seq_idx, bi, s.T, t0 + i) * s.H + h) * s.P * s.N + n;
-          const TIn *gi = gc + i * HP;
-          for (int64_t p = 0; p < s.P; ++p) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+      for (int b = 0; b < 4; ++b) {
+        const int64_t n = n0 + tile_col(b);
+        if (n >= s.N) continue;
+        float hg = t1[a][b];
+        if (f > 0) {   // a sequence that started inside the chunk: its own initial state
+          hg = 0.f;
+          if (init) {
+            const float *hs = init + (seq_of(seq_idx, bi, s.T, t0 + i) * s.H + h) * s.P * s.N + n;
+            const TIn *gi = gc + i * HP;
+            for (int64_t p = 0; p < s.P; ++p) hg = fmaf(hs[p * s.N], ld(gi + p), hg);
+          }
         }
+        res[a][b] = fmaf(din, hg, res[a][b]);
       }
-      dcv[a][b] = fmaf(din, hg, dcv[a][b]);
     }
-  }
-  tile_mm<RA, false, false>(
-      Lc, [&](int r, int64_t j) { return row_ok(r) ? W[j * s.Q + i0 + r] : 0.f; },
-      [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(cc + j * GN + n) : 0.f; }, sb, dbv);
-  tile_mm<RA, true, false>(
-      s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(xc + (i0 + r) * HP + p) : 0.f; },
-      [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? ds[p * s.N + n] : 0.f; }, sb, t1);
+  } else {
+    const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
+    const TIn *xc = x + ((bi * s.T + t0) * s.H + h) * s.P;
+    const float *ds = dS + unit * s.P * s.N;
+    tile_mm<RA, false, false>(
+        Lc, [&](int r, int64_t j) { return row_ok(r) ? W[j * s.Q + i0 + r] : 0.f; },
+        [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(cc + j * GN + n) : 0.f; }, sb, res);
+    tile_mm<RA, true, false>(
+        s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(xc + (i0 + r) * HP + p) : 0.f; },
+        [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? ds[p * s.N + n] : 0.f; }, sb, t1);
 #pragma unroll
-  for (int a = 0; a < RA; ++a) {
-    const int64_t i = i0 + tile_row<RA>(a);
-    if (i >= Lc) continue;
-    const float wi = i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t0 + i) * s.H + h];
+    for (int a = 0; a < RA; ++a) {
+      const int64_t i = i0 + tile_row<RA>(a);
+      if (i >= Lc) continue;
+      const float wi =
+          i < fe ? 0.f : expf(acs_diff(ah[Lc - 1], al[Lc - 1], ah[i], al[i])) * dt[(bi * s.T + t0 + i) * s.H + h];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) dbv[a][b] = fmaf(wi, t1[a][b], dbv[a][b]);
+      for (int b = 0; b < 4; ++b) res[a][b] = fmaf(wi, t1[a][b], res[a][b]);
+    }
   }
 }
 
 // Deterministic variant: per-head slots (b,T,H,N); atomic variant: added into
-// dB/dC (b,T,G,N) with atomics.  A CTA per (b, c, h) and 64 x 64 tile of (i, n).
+// dB/dC (b,T,G,N) with atomics.  A CTA per (b, c, h), 64 x 64 tile of (i, n)
+// and output (blockIdx.z: 0 dC, 1 dB).
 template <class TIn, bool kAtomic>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 3)
     dbdc_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
                 const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ Wm,
                 const float *__restrict__ states, const float *__restrict__ dS, const float *__restrict__ acs_hi,
@@ -718,9 +744,15 @@ __global__ void __launch_bounds__(kTileThreads)
     fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
   __syncthreads();
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
-  float dcv[4][4], dbv[4][4];
-  dbdc_tile<4, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h, i0, n0, fr, fe,
-                    sb, dcv, dbv);
+  const bool is_db = blockIdx.z != 0;
+  float res[4][4];
+  if (is_db)
+    dbdc_tile<true, 4, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h, i0, n0,
+                            fr, fe, sb, res);
+  else
+    dbdc_tile<false, 4, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h, i0, n0,
+                             fr, fe, sb, res);
+  float *out = is_db ? dBo : dCo;
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -728,15 +760,10 @@ __global__ void __launch_bounds__(kTileThreads)
       const int64_t i = i0 + tile_row<4>(a), n = n0 + tile_col(b);
       if (i >= Lc || n >= s.N) continue;
       const int64_t t = t0 + i;
-      if (kAtomic) {
-        const int64_t o = ((bi * s.T + t) * s.G + g) * s.N + n;
-        atomicAdd(dBo + o, dbv[a][b]);
-        atomicAdd(dCo + o, dcv[a][b]);
-      } else {
-        const int64_t o = ((bi * s.T + t) * s.H + h) * s.N + n;
-        dBo[o] = dbv[a][b];
-        dCo[o] = dcv[a][b];
-      }
+      if (kAtomic)
+        atomicAdd(out + ((bi * s.T + t) * s.G + g) * s.N + n, res[a][b]);
+      else
+        out[((bi * s.T + t) * s.H + h) * s.N + n] = res[a][b];
     }
 }
 
@@ -789,8 +816,10 @@ __global__ void __launch_bounds__(kTileThreads)
   if (i0 < Lc) {   // (the whole CTA)
     for (int64_t n0 = 0; n0 < s.N; n0 += kTC) {
       float dcv[kOrdTile / 16][4], dbv[kOrdTile / 16][4];
-      dbdc_tile<kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi, c, h,
-                                    i0, n0, fr, fe, sb, dcv, dbv);
+      dbdc_tile<false, kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
+                                           c, h, i0, n0, fr, fe, sb, dcv);
+      dbdc_tile<true, kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
+                                          c, h, i0, n0, fr, fe, sb, dbv);
 #pragma unroll
       for (int a = 0; a < kOrdTile / 16; ++a)
 #pragma unroll
@@ -848,7 +877,7 @@ __global__ void __launch_bounds__(kTileThreads)
 // token each sum a quarter of every p tile, p ascending, and the quarters are
 // added in a fixed tree.
 template <class TIn>
-__global__ void __launch_bounds__(kTileThreads)
+__global__ void __launch_bounds__(kTileThreads, 3)
     ddt_dacs_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
                     const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ rowp,
                     const float *__restrict__ colp, const float *__restrict__ dg, const float *__restrict__ states,
@@ -1193,7 +1222,7 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   tr.mark(st);
   if (atomic) {
     tr.mark(st);
-    dbdc_kernel<TIn, true><<<dim3(nbch, tiles_qn), kTileThreads, 0, st>>>(
+    dbdc_kernel<TIn, true><<<dim3(nbch, tiles_qn, 2), kTileThreads, 0, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, a.dB, a.dC);
     tr.mark(st);
   } else if (ordered) {
@@ -1210,7 +1239,7 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
     tr.mark(st);
   } else {
     tr.mark(st);
-    dbdc_kernel<TIn, false><<<dim3(nbch, tiles_qn), kTileThreads, 0, st>>>(
+    dbdc_kernel<TIn, false><<<dim3(nbch, tiles_qn, 2), kTileThreads, 0, st>>>(
         s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.slot_b,
         w.slot_c);
     tr.mark(st);

@@ -741,13 +741,14 @@ def main():
                "serial_ms_per_step_median": serial_med}
         del sets
 
-    # the other workload presets (the 2K and 4K rows of the pages' tables and the packed
-    # variable-length batch), timed after the headline run, single GPU only
+    # the other workload presets (the 2K and 4K rows of the pages' tables, the packed
+    # variable-length batch, and fp32 inputs on the general path), timed after the headline
+    # run, single GPU only
     others = None
     if world == 1 and not args.no_others and args.workload == "bf16_T16384":
         others = [time_workload(ssd, n, dev, steps=st) for n, st in
                   (("bf16_T2048", 20), ("bf16_T4096", 20), ("bf16_varlen_T32768", 2),
-                   ("bf16_varlen_T32768_midchunk", 2))]
+                   ("bf16_varlen_T32768_midchunk", 2), ("fp32_T2048", 10))]
 
     line = None
     if rank == 0:

@@ -135,3 +135,33 @@ def test_zero_step_gives_skip_only():
     assert torch.allclose(y.cpu(), D * d["x"], rtol=1e-6, atol=1e-6)
     assert torch.allclose(g["dx"].cpu(), D * d["dout"], rtol=1e-6, atol=1e-6)
     assert torch.count_nonzero(g["dB"]) == 0 and torch.count_nonzero(g["dC"]) == 0
+
+
+@pytest.mark.parametrize("case", [
+    # several 64-wide tiles of tokens, state columns and head dims, each with a ragged edge
+    dict(T=500, H=6, G=3, P=72, N=160, Q=192, init=True),
+    dict(T=333, H=4, G=1, P=130, N=66, Q=80, init=False),
+    dict(T=257, H=2, G=2, P=64, N=128, Q=128, init=True, lens=(40, 100, 1, 116)),
+])
+def test_fp32_multi_tile_shapes(case):
+    """The general path's tiled products with more than one tile along every
+    dimension and ragged tile edges, against the oracle; both launch
+    configurations and the ordered dB/dC fold give the same bits."""
+    lens = case.get("lens", ())
+    d = make_inputs(1, case["T"], case["H"], case["P"], case["G"], case["N"], dtype=torch.float32,
+                    seed=case["T"] + case["P"], dt_shift=2.0, d_mode="normal", seq_lens=lens,
+                    with_init=case["init"])
+    y, saved, g = run_gpu(d, case["Q"], any_start=bool(lens))
+    ref = run_oracle(d, chunk=case["Q"])
+    errs = {"y": y_relerr(y, ref["y"]), "states": relerr(saved.states_fp32(), ref["states"])}
+    for k in GRADS:
+        errs[k] = relerr(g[k], ref[k])
+    if d["init"] is not None:
+        errs["dinit"] = relerr(g["dinit"], ref["dinit"])
+    bad = {k: v for k, v in errs.items() if not v < 1e-5}
+    assert not bad, (bad, errs)
+    dev = to_dev(d)
+    for config, variant in ((1, 0), (0, 2)):
+        o = run_gpu(d, case["Q"], config=config, variant=variant, g=dev, any_start=bool(lens))[2]
+        for k in g:
+            assert torch.equal(g[k].view(torch.int32), o[k].view(torch.int32)), (config, variant, k)

@@ -1074,17 +1074,19 @@ namespace {
 // picks the ticket counter (status[1 + pass]) so that consecutive launches on
 // one workspace do not share one.
 cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const FusedOptions &opt, int64_t bc_pitch,
-                        int pass, bool dx_add, cudaStream_t st, Trace &tr) {
-  // (dx_add: the sliced instantiation; the unit groups of `s` are then head slices, two per group)
+                        int pass, int slice_shift, cudaStream_t st, Trace &tr) {
+  // (slice_shift > 0: the sliced instantiation, adding its dx into dx; the unit groups of `s` are
+  // then head slices, 2^slice_shift per group)
+  const bool dx_add = slice_shift > 0;
   CUtensorMap tm_x, tm_g, tm_b, tm_c, tm_dx;
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
                     128, true) ||
       !make_tmap_2d(&tm_g, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP),
                     64, 128, true) ||
-      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((dx_add ? s.G / 2 : s.G) * kN),
+      !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((s.G >> slice_shift) * kN),
                     uint64_t(bc_pitch), 64, 128, true) ||
-      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((dx_add ? s.G / 2 : s.G) * kN),
+      !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((s.G >> slice_shift) * kN),
                     uint64_t(bc_pitch), 64, 128, true) ||
       !make_tmap_2d(&tm_dx, a.dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 32,
                     128, true))
@@ -1094,6 +1096,8 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
   if ((err = cudaFuncSetAttribute(fused_bwd_kernel<false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   SMEM_BYTES)) != cudaSuccess ||
       (err = cudaFuncSetAttribute(fused_bwd_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  SMEM_BYTES)) != cudaSuccess ||
+      (err = cudaFuncSetAttribute(fused_bwd_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   SMEM_BYTES)) != cudaSuccess)
     return err;
   Params p;
@@ -1125,7 +1129,9 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
   p.silent_chunk = opt.silent_chunk;
   const unsigned units = unsigned(s.b * s.nc * s.G);
   tr.mark(st);
-  if (dx_add)
+  if (slice_shift == 2)
+    fused_bwd_kernel<true, 2><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
+  else if (slice_shift == 1)
     fused_bwd_kernel<true, 1><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
   else
     fused_bwd_kernel<false, 0><<<units, kThreads, SMEM_BYTES, st>>>(p, tm_x, tm_g, tm_b, tm_c, tm_dx);
@@ -1149,13 +1155,17 @@ Shape split_half(const Shape &s) {
   return h;
 }
 
-// The half as the kernel sees it: the group's heads in two slices (two units
-// per chunk and half: the units are half as long, so the grid packs the SMs
-// more evenly); dB and dC are then per-slice partial sums.
+// The half as the kernel sees it: the group's heads in 2^split_shift slices
+// (four when the head count allows, else two), one unit each per chunk and
+// half.  Shorter units pack the SMs more evenly, and more of them are
+// independent: a unit waits only for the unit of the same slice in the chunk
+// after, so more slices mean more, shorter chains of waiting units running
+// side by side.  dB and dC are then per-slice partial sums.
+int split_shift(const Shape &s) { return s.hpg % 4 == 0 ? 2 : 1; }
 Shape split_units(const Shape &s) {
   Shape h = split_half(s);
-  h.G = 2 * s.G;
-  h.hpg = s.hpg / 2;
+  h.G = s.G << split_shift(s);
+  h.hpg = s.hpg >> split_shift(s);
   return h;
 }
 
@@ -1167,18 +1177,19 @@ SplitBwdWs carve_split(Carver &cv, const Shape &s, int ring_depth) {
   w.dD_scratch = cv.take<float>(h.H);
   w.zeros = cv.take<float>(h.H);
   w.ddt1 = cv.take<float>(s.b * s.T * s.H);
+  const int64_t ns = int64_t(1) << split_shift(s);
   for (int j = 0; j < 2; ++j) {   // dB, dC: (b, T, slice, 128) partial sums of each half
-    w.dBh[j] = cv.take<float>(s.b * s.T * 2 * kN);
-    w.dCh[j] = cv.take<float>(s.b * s.T * 2 * kN);
+    w.dBh[j] = cv.take<float>(s.b * s.T * ns * kN);
+    w.dCh[j] = cv.take<float>(s.b * s.T * ns * kN);
     w.dinit_h[j] = cv.take<float>(s.nseq * s.H * kP * kN);
   }
   return w;
 }
 
 // ddt += ddt of the second half; dB, dC assembled from their halves (each the
-// sum of its two head slices, slice 0 first) and dinit from its halves
-// (grid-stride over float4 groups of each array in turn)
-__global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_rows, float *__restrict__ ddt,
+// sum of its ns head slices in ascending slice order) and dinit from its
+// halves (grid-stride over float4 groups of each array in turn)
+__global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_rows, int ns, float *__restrict__ ddt,
                                   const float *__restrict__ ddt1, float *__restrict__ dB, float *__restrict__ dC,
                                   const float *__restrict__ dB0, const float *__restrict__ dB1,
                                   const float *__restrict__ dC0, const float *__restrict__ dC1,
@@ -1213,9 +1224,13 @@ __global__ void split_fold_kernel(int64_t n_ddt4, int64_t rows, int64_t init_row
     const float4 *src = reinterpret_cast<const float4 *>(j ? src1 : src0);
     if (out == dinit) {
       reinterpret_cast<float4 *>(out)[k] = __ldcs(src + row * q + g4);
-    } else {   // head slice 0 then slice 1
-      const float4 a = __ldcs(src + (row * 2) * q + g4), b = __ldcs(src + (row * 2 + 1) * q + g4);
-      reinterpret_cast<float4 *>(out)[k] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    } else {   // head slices in ascending order
+      float4 a = __ldcs(src + (row * ns) * q + g4);
+      for (int sl = 1; sl < ns; ++sl) {
+        const float4 b = __ldcs(src + (row * ns + sl) * q + g4);
+        a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+      }
+      reinterpret_cast<float4 *>(out)[k] = a;
     }
   }
 }
@@ -1252,7 +1267,7 @@ cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOption
     if ((err = cudaMemsetAsync(a.dA, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
     if ((err = cudaMemsetAsync(a.dD, 0, size_t(s.H) * sizeof(float), st)) != cudaSuccess) return err;
   }
-  if ((err = launch_pass(s, a, w, opt, s.G * kN, 0, false, st, tr)) != cudaSuccess) return err;
+  if ((err = launch_pass(s, a, w, opt, s.G * kN, 0, 0, st, tr)) != cudaSuccess) return err;
   if (!opt.atomic) {
     tr.mark(st);
     fold_scalars_kernel<<<unsigned((s.H + 127) / 128), 128, 0, st>>>(s, w.dA_part, w.dD_part, a.dA, a.dD);
@@ -1329,7 +1344,7 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
     }
     FusedWs wj = j ? w.w1 : w.w;
     wj.status = w.w.status;    // one status word (ticket status[1 + j] per half) for the check
-    err = launch_pass(hu, aj, wj, opt, 2 * kN, j, true, j ? side : st, tr);
+    err = launch_pass(hu, aj, wj, opt, 2 * kN, j, split_shift(s), j ? side : st, tr);
   }
   if (err == cudaSuccess) err = cudaEventRecord(join, side);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(st, join, 0);   // join before the fold
@@ -1339,7 +1354,7 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
   const int64_t n_ddt4 = s.b * s.T * s.H / 4;
   const int64_t rows = s.b * s.T, init_rows = a.dinit ? s.nseq * s.H * kP : 0;
   tr.mark(st);
-  split_fold_kernel<<<unsigned(8 * 152), 256, 0, st>>>(n_ddt4, rows, init_rows, a.ddt, w.ddt1, a.dB, a.dC, w.dBh[0],
+  split_fold_kernel<<<unsigned(8 * 152), 256, 0, st>>>(n_ddt4, rows, init_rows, 1 << split_shift(s), a.ddt, w.ddt1, a.dB, a.dC, w.dBh[0],
                                                        w.dBh[1], w.dCh[0], w.dCh[1], a.dinit, w.dinit_h[0],
                                                        w.dinit_h[1]);
   tr.mark(st);

@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(256) states_view_kernel(Shape s, int ratio, co
 }  // namespace
 
 bool fused_split_supported(const Shape &s, bool bf16) {
-  // (the backward splits each group's heads into two slices: an even head count)
+  // (the backward splits each group's heads into two or four slices: an even head count)
   return bf16 && s.N == 2 * kN && s.G == 1 && s.H % 2 == 0 && s.P == kP && (s.Q == kQ || s.Q == 2 * kQ) &&
          s.T % s.Q == 0 &&
          s.b * (s.T / kQ) <= (int64_t(1) << 30) && s.b * s.T <= (int64_t(1) << 30);

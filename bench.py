@@ -220,8 +220,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "e94f21ef22f37d2ef5725b9f543ed32c4a88938fb9e9c14778645fd27e912502": {
-        "bytes_per_token": (2283359744 + 1248142336) / 16384,
+    "fe3c1bba83998f6729df71672304d566f5e4a9ad5ce647a26ec73f3ee6b2b017": {
+        "bytes_per_token": (2278705920 + 1246661120) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

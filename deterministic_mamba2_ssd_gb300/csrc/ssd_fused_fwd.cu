@@ -599,21 +599,14 @@ __global__ void init_half_kernel(int64_t rows, int j, const float *__restrict__ 
 // chunk / 128) from the packed halves; one CTA per (b, caller chunk, head, half)
 __global__ void __launch_bounds__(256) states_view_kernel(Shape s, int ratio, const float *__restrict__ aux,
                                                            float *__restrict__ out) {
+  __shared__ float t[64][129];
   const int64_t tile = blockIdx.x;   // ((b * nc + c) * H + h) * 2 + j
   const int j = int(tile & 1);
   const int64_t h = (tile >> 1) % s.H, c = (tile >> 1) / s.H % s.nc, bi = (tile >> 1) / (s.H * s.nc);
   const int64_t nch = s.T / kQ;
   const uint8_t *in = reinterpret_cast<const uint8_t *>(
       aux + (((int64_t(j) * s.b + bi) * nch + c * ratio) * s.H + h) * (kP * kN));
-  float *o = out + (((bi * s.nc + c) * s.H + h) * kP) * (2 * kN) + j * kN;
-  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {
-    const int n = i >> 3, c0 = 8 * (i & 7);
-    float hi[8], lo[8];
-    ld8_bf16(in, n, c0, hi);
-    ld8_bf16(in + 16384, n, c0, lo);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[(c0 + e) * (2 * kN) + n] = hi[e] + lo[e];
-  }
+  unpack_state_tile(in, out + (((bi * s.nc + c) * s.H + h) * kP) * (2 * kN) + j * kN, 2 * kN, t);
 }
 
 }  // namespace

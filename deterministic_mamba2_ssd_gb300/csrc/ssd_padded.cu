@@ -192,20 +192,13 @@ __global__ void __launch_bounds__(256) pad_states_view_kernel(int64_t H, int hal
                                                                const int32_t *__restrict__ map,
                                                                const float *__restrict__ packed,
                                                                float *__restrict__ out) {
+  __shared__ float t[64][129];
   const int64_t tile = blockIdx.x;
   const int j = int(tile % halves);
   const int64_t h = (tile / halves) % H, c = tile / halves / H;
   const uint8_t *in = reinterpret_cast<const uint8_t *>(packed + ((j * npc + map[c]) * H + h) * (kP * kN));
   const int64_t pitch = int64_t(halves) * kN;
-  float *o = out + (c * H + h) * kP * pitch + j * kN;
-  for (int i = threadIdx.x; i < kN * (kP / 8); i += blockDim.x) {
-    const int n = i >> 3, c0 = 8 * (i & 7);
-    float hi[8], lo[8];
-    ld8_bf16(in, n, c0, hi);
-    ld8_bf16(in + 16384, n, c0, lo);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[(c0 + e) * pitch + n] = hi[e] + lo[e];
-  }
+  unpack_state_tile(in, out + (c * H + h) * kP * pitch + j * kN, pitch, t);
 }
 
 PadTables tables_of(const PadFwdWs &f) { return PadTables{f.start, f.len, f.id}; }

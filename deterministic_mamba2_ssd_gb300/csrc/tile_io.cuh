@@ -43,3 +43,29 @@ __device__ __forceinline__ void ld8_bf16(const uint8_t *panel, int r, int c0, fl
 }
 
 }  // namespace ssd
+
+namespace ssd {
+
+// fp32 view of one packed state tile (bf16 hi then lo, each [128][64] in the
+// swizzled operand layout): out[p * pitch + n] = hi + lo for p < 64, n < 128.
+// The tile passes through shared memory (t: 64 rows of 129 floats) so that
+// the writes run along n, 128 contiguous floats per row of p; the whole CTA
+// (a multiple of 32 threads) takes part.
+__device__ __forceinline__ void unpack_state_tile(const uint8_t *__restrict__ in, float *__restrict__ out,
+                                                  int64_t pitch, float (*t)[129]) {
+  for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
+    const int n = i >> 3, c0 = 8 * (i & 7);
+    float hi[8], lo[8];
+    ld8_bf16(in, n, c0, hi);
+    ld8_bf16(in + 16384, n, c0, lo);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) t[c0 + e][n] = hi[e] + lo[e];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int p = threadIdx.x >> 5; p < 64; p += nw)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[p * pitch + lane + 32 * k] = t[p][lane + 32 * k];
+}
+
+}  // namespace ssd

@@ -171,7 +171,7 @@ def algorithmic_flops(w):
     return b * nc * (H * per_head + G * per_group)
 
 
-def north_star_roofline(w, es, ms, tensor_peak_tflops):
+def nominal_roofline(w, es, ms, tensor_peak_tflops):
     """The slower of HBM bytes at 8 TB/s and tensor FLOPs at the tensor peak,
     as a fraction of the measured backward time."""
     t_hbm = api_bytes(w, es) / 8e12
@@ -196,17 +196,19 @@ def kernel_bytes(name, w, es):
     cbq = b * nc * G * Q * Q * f4
     st = b * nc * H * P * N * f4
     slots = b * T * H * N * f4
+    # mwg leaves the sums of M o Gx per 64-wide tile (rows and columns) and its diagonal
+    parts = 2 * b * nc * H * (-(-Q // 64)) * Q * f4 + b * nc * H * Q * f4
     tab = {
         "cumsum_fwd": dt + acs,
         "cb": 2 * bc + cbq,
-        "mwg": 2 * x + cbq + acs + dt + 3 * qq,
+        "mwg": 2 * x + cbq + acs + dt + 2 * qq + parts,
         "dhscan": x + bc + acs + st,
         "state_passing_bwd": 3 * st + acs,
         "dx": x + bc + dt + qq + st + acs + b * T * H * P * f4,
         "dbdc": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * slots,
         "dbdc_atomic": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * b * T * G * N * f4,
         "dbdc_ordered": 2 * x + 2 * bc + dt + qq + 2 * st + acs + 2 * b * T * G * N * f4,
-        "ddt_dacs": 2 * x + 2 * bc + dt + qq + 2 * st + acs + dt + 3 * b * H * nc * Q * f4,
+        "ddt_dacs": 2 * x + 2 * bc + dt + parts + 2 * st + acs + dt + 4 * b * H * nc * Q * f4,
         "cumsum_bwd": 2 * dt + 4 * b * H * nc * Q * f4,
         "cumsum_bwd_atomic": 2 * dt + 4 * b * H * nc * Q * f4,
         "reduce_heads": 2 * slots + 2 * b * T * G * N * f4,
@@ -507,7 +509,7 @@ def time_workload(ssd, name, dev, steps, warmup=3, repeats=5):
     return {"workload": name, "launch_config": ssd.config_name(saved.dims, 0), "bwd_ms": ms,
             "tokens_per_s": tokens / (ms / 1e3), "fwd_ms": fwd_ms, "steps": steps,
             "bwd_hbm_frac": api_bytes(w, es) / (ms / 1e3) / 1e9 / peak, "peak_kind": peak_kind,
-            "north_star_roofline": north_star_roofline(w, es, ms, tpeak),
+            "nominal_roofline": nominal_roofline(w, es, ms, tpeak),
             "bitwise_equal_repeats": "%d/%d" % (same, repeats)}
 
 
@@ -611,7 +613,7 @@ def main():
                 "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
                 "traffic": fused_traffic(w.batch * w.seqlen) if ndom == "fused_bwd" else None,
                 "algorithmic_bytes_per_launch": alg, "launch_ms": dom_ms}
-    if north_star_roofline(w, es, 1.0, tpeak)["bound"] == "tensor" and ndom.startswith("fused_bwd"):
+    if nominal_roofline(w, es, 1.0, tpeak)["bound"] == "tensor" and ndom.startswith("fused_bwd"):
         # tensor-bound shape (dstate 256): the fused kernel runs once per state half, both halves
         # at once, so it is timed over the whole backward and held against the tensor peak
         flops = algorithmic_flops(w)
@@ -775,7 +777,7 @@ def main():
                        "launch_config": ssd.config_name(saved.dims, args.config),
                        "l2": "flushed between steps (256 MB write) and inputs larger than L2"},
             "roofline": roofline,
-            "north_star_roofline": north_star_roofline(w, es, ms_max, tpeak),
+            "nominal_roofline": nominal_roofline(w, es, ms_max, tpeak),
             "fwd_ms": fwd_ms,
             "other_workloads": others,
             "kernel_share": shares,

@@ -44,13 +44,13 @@ def test_algorithmic_flops_of_the_pages_workloads():
     assert bench.algorithmic_flops(WORKLOADS["bf16_varlen_T32768"]) / 1e9 == pytest.approx(837.5, abs=0.05)
 
 
-def test_north_star_roofline_takes_the_slower_bound():
+def test_nominal_roofline_takes_the_slower_bound():
     w = WORKLOADS["bf16_T16384"]
-    r = bench.north_star_roofline(w, 2, 1.0, 1950.0)
+    r = bench.nominal_roofline(w, 2, 1.0, 1950.0)
     assert r["bound"] == "hbm" and r["t_hbm_us"] == pytest.approx(432.0, abs=0.1)
     assert r["t_tensor_us"] == pytest.approx(218.1, abs=0.1)
     assert r["frac"] == pytest.approx(0.432, abs=1e-3)
-    v = bench.north_star_roofline(WORKLOADS["bf16_varlen_T32768"], 2, 1.0, 1950.0)
+    v = bench.nominal_roofline(WORKLOADS["bf16_varlen_T32768"], 2, 1.0, 1950.0)
     assert v["bound"] == "tensor" and v["roofline_us"] == pytest.approx(429.5, abs=0.2)
 
 

@@ -92,6 +92,28 @@ def test_bf16_T16384_sampled_group():
         assert not bad, (g0, bad)
 
 
+def test_bf16_T16384_with_initial_states_sampled_group():
+    """The benchmarked shape at full size with initial states, in the other
+    launch configuration: one whole group against the oracle, its initial-state
+    gradient included."""
+    w = WORKLOADS["bf16_T16384"]
+    d = make_inputs(w.batch, w.seqlen, w.nheads, w.headdim, w.ngroups, w.dstate, dtype=w.dtype, seed=4242,
+                    dt_shift=w.dt_shift, d_mode=w.d_mode, with_init=True)
+    y, saved, g = run_gpu(d, w.chunk, config=1)
+    hpg = w.nheads // w.ngroups
+    g0 = 3
+    sub = head_slice(d, g0, hpg)
+    ref = run_oracle(sub, chunk=w.chunk)
+    hs = slice(g0 * hpg, (g0 + 1) * hpg)
+    errs = {"y": y_relerr(y[:, :, hs], ref["y"]), "states": relerr(saved.states_fp32()[:, :, hs], ref["states"]),
+            "dx": relerr(g["dx"][:, :, hs], ref["dx"]), "ddt": relerr(g["ddt"][:, :, hs], ref["ddt"]),
+            "dA": relerr(g["dA"][hs], ref["dA"]), "dD": relerr(g["dD"][hs], ref["dD"]),
+            "dB": relerr(g["dB"][:, :, g0:g0 + 1], ref["dB"]), "dC": relerr(g["dC"][:, :, g0:g0 + 1], ref["dC"]),
+            "dinit": relerr(g["dinit"][:, hs], ref["dinit"])}
+    bad = {k: v for k, v in errs.items() if not v < 2e-3}
+    assert not bad, (bad, errs)
+
+
 def test_bf16_varlen_T32768_sampled_sequence():
     """Packed variable-length workload: sequence 0 checked against the oracle
     (sequences never interact); dA/dD, which sum over sequences, checked as

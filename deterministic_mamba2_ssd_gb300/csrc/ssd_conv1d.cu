@@ -90,11 +90,12 @@ __device__ __forceinline__ void read_slot(uint32_t a, const __nv_bfloat16 *, flo
   v[0] = p.x, v[1] = p.y, v[2] = q.x, v[3] = q.y;
 }
 
-// logistic function, no overflow for either sign of v (the fast exponential,
-// relative error a few 1e-7, and one correctly rounded reciprocal)
+// logistic function, no overflow for either sign of v (the fast exponential
+// and the fast division, whose argument 1 + e lies in [1, 2]; relative error
+// a few 1e-7)
 __device__ __forceinline__ float sigmoid(float v) {
   const float e = __expf(-fabsf(v));
-  const float r = __frcp_rn(1.f + e);
+  const float r = __fdividef(1.f, 1.f + e);
   return v >= 0.f ? r : e * r;
 }
 
@@ -300,6 +301,134 @@ __global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
   }
 }
 
+// The same backward with the token loop unrolled by four: token u lives in
+// window slot u % 4 of xw (x) and dz (dpre), so the windows need no shifting,
+// and every slot index is a compile-time constant (the walk starts at a
+// multiple of 4, four tokens before the tile).  kSeq: seq_idx is given (a
+// sequence may start at any token); without it the only start is the row's
+// first token, whose earlier taps read zeros anyway.  Per element the
+// arithmetic is that of conv_bwd_kernel, term for term.
+template <class TIn, int K, bool kAtomic, bool kSeq>
+__global__ void conv_bwd4_kernel(ConvShape s, const TIn *__restrict__ x, const float *__restrict__ w,
+                                 const float *__restrict__ bias, const int32_t *__restrict__ seq_idx,
+                                 const TIn *__restrict__ dy, float *__restrict__ dx, float *__restrict__ part,
+                                 float *__restrict__ dw, float *__restrict__ dbias) {
+  const int64_t cv = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (cv * kVec >= s.C) return;
+  const int64_t c0 = cv * kVec;
+  const int64_t tile = blockIdx.y;
+  const int64_t bi = tile / s.tiles_per_row;
+  const int64_t t0 = int64_t(tile % s.tiles_per_row) * kTile, t1 = min(s.T, t0 + kTile);
+  float wv[K][kVec], bv[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    bv[i] = bias ? __ldg(bias + c0 + i) : 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) wv[k][i] = __ldg(w + (c0 + i) * K + k);
+  }
+  float xw[4][kVec], dz[4][kVec];   // slot u % 4: x and dpre of token u
+  bool sst[4] = {false, false, false, false};   // slot u % 4: token u starts a sequence (kSeq)
+  float dwp[K][kVec], dbp[kVec];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) xw[j][i] = dz[j][i] = 0.f;
+#pragma unroll
+  for (int k = 0; k < K; ++k)
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) dwp[k][i] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) dbp[i] = 0.f;
+  extern __shared__ __align__(16) uint8_t ring_raw[];
+  const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
+  const int64_t ub = t0 - 4, u1 = t1 + (K - 1), ue = ub + ((u1 - ub + 3) / 4) * 4;
+  const int64_t off0 = (bi * s.T + ub) * s.C + c0;   // element offset of token ub (read only where it exists)
+  auto issue = [&](int64_t u, int d, int64_t off) {
+    const bool okx = u >= 0 && u < s.T && u < u1, okg = okx && u >= t0;
+    stream_row(ring_slot(ring, d, 0), okx ? x + off : x, okx);
+    stream_row(ring_slot(ring, d, 1), okg ? dy + off : dy, okg);
+    stream_commit();
+  };
+  for (int j = 0; j < kDepth; ++j) issue(ub + j, j, off0 + j * s.C);
+  int dslot = 0;   // ring slot of token u
+  int64_t off = off0;
+  for (int64_t ug = ub; ug < ue; ug += 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // token u = ug + j, window slot j
+      const int64_t u = ug + j;
+      float g[kVec];
+      stream_wait();
+      read_slot(ring_slot(ring, dslot, 0), x, xw[j]);   // zeros outside the row
+      read_slot(ring_slot(ring, dslot, 1), dy, g);      // zeros before the tile and outside the row
+      issue(u + kDepth, dslot, off + kDepth * s.C);
+      dslot = (dslot + 1) & (kDepth - 1);
+      off += s.C;
+      if (kSeq) {
+        sst[j] = u >= 0 && u < s.T && starts_seq(seq_idx, bi, s.T, u);
+        if (sst[j]) {   // earlier taps belong to another sequence
+#pragma unroll
+          for (int k = 1; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) xw[(j - k) & 3][i] = 0.f;
+        }
+      }
+      // dpre of token u (zero before the tile and outside the row: dy is zero there)
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) {
+        float acc = bv[i];
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc = fmaf(wv[k][i], xw[(j - (K - 1) + k) & 3][i], acc);
+        if (s.silu) {
+          const float sg = sigmoid(acc);
+          dz[j][i] = g[i] * (sg * fmaf(acc, 1.f - sg, 1.f));
+        } else {
+          dz[j][i] = g[i];
+        }
+      }
+      if (u >= t0 && u < t1) {   // the tile's own tokens: partial sums of dw and dbias, in token order
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+#pragma unroll
+          for (int k = 0; k < K; ++k) dwp[k][i] = fmaf(dz[j][i], xw[(j - (K - 1) + k) & 3][i], dwp[k][i]);
+          dbp[i] += dz[j][i];
+        }
+      }
+      // dx of token sx = u-K+1 (complete now): sum_m w[K-1-m] dz[sx+m] over taps that stay in sx's sequence
+      const int64_t sx = u - (K - 1);
+      if (sx >= t0 && sx < t1) {
+        float o[kVec];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) o[i] = 0.f;
+        bool live = true;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {   // token sx + m sits in slot (j - (K-1) + m) % 4
+          const int sl = (j - (K - 1) + m) & 3;
+          if (kSeq && m > 0 && sst[sl]) live = false;
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < kVec; ++i) o[i] = fmaf(wv[K - 1 - m][i], dz[sl][i], o[i]);
+          }
+        }
+        store4(dx + off - K * s.C, o);   // token sx (off has moved on to token u + 1)
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (kAtomic) {
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) atomicAdd(dw + (c0 + i) * K + k, dwp[k][i]);
+      if (dbias) atomicAdd(dbias + c0 + i, dbp[i]);
+    }
+  } else {
+    float *p = part + tile * (K + 1) * s.C + c0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) store4(p + k * s.C, dwp[k]);
+    store4(p + K * s.C, dbp);
+  }
+}
+
 // dw[c,k] (k < K) and dbias[c] (k = K): the tiles' partial sums in ascending
 // tile order; one thread per (k, c).
 __global__ void conv_fold_kernel(int64_t C, int K, int64_t tiles, const float *__restrict__ part,
@@ -368,12 +497,23 @@ cudaError_t launch_bwd(const ConvShape &s, int K, dim3 grid, int block, const vo
                        const float *bias, const int32_t *seq_idx, const void *dy, float *dx, float *part, float *dw,
                        float *dbias, cudaStream_t st) {
   const TIn *xx = static_cast<const TIn *>(x), *gg = static_cast<const TIn *>(dy);
-  switch (K) {
-    case 1: return launch_ring(conv_bwd_kernel<TIn, 1, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
-    case 2: return launch_ring(conv_bwd_kernel<TIn, 2, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
-    case 3: return launch_ring(conv_bwd_kernel<TIn, 3, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
-    default: return launch_ring(conv_bwd_kernel<TIn, 4, kAtomic>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias);
+#define SSD_CONV_BWD(KK, SEQ) \
+  launch_ring(conv_bwd4_kernel<TIn, KK, kAtomic, SEQ>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias)
+  if (seq_idx) {
+    switch (K) {
+      case 1: return SSD_CONV_BWD(1, true);
+      case 2: return SSD_CONV_BWD(2, true);
+      case 3: return SSD_CONV_BWD(3, true);
+      default: return SSD_CONV_BWD(4, true);
+    }
   }
+  switch (K) {
+    case 1: return SSD_CONV_BWD(1, false);
+    case 2: return SSD_CONV_BWD(2, false);
+    case 3: return SSD_CONV_BWD(3, false);
+    default: return SSD_CONV_BWD(4, false);
+  }
+#undef SSD_CONV_BWD
 }
 
 }  // namespace

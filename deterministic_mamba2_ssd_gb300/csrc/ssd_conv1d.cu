@@ -175,141 +175,16 @@ __global__ void conv_fwd_kernel(ConvShape s, const TIn *__restrict__ x, const fl
 // K-1 tokens after it (for dx at the tile's end), dx of the tile's tokens,
 // and the tile's partial sums of dw and dbias in token order -- into slot
 // `tile` (part[(tile * (K + 1) + k) * C + c], k = K for dbias) or, in the
-// atomic variant, added straight into dw and dbias.
-template <class TIn, int K, bool kAtomic>
-__global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const float *__restrict__ w,
-                                const float *__restrict__ bias, const int32_t *__restrict__ seq_idx,
-                                const TIn *__restrict__ dy, float *__restrict__ dx, float *__restrict__ part,
-                                float *__restrict__ dw, float *__restrict__ dbias) {
-  const int64_t cv = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (cv * kVec >= s.C) return;
-  const int64_t c0 = cv * kVec;
-  const int64_t tile = blockIdx.y;
-  const int64_t bi = tile / s.tiles_per_row;
-  const int64_t t0 = int64_t(tile % s.tiles_per_row) * kTile, t1 = min(s.T, t0 + kTile);
-  float wv[K][kVec], bv[kVec];
-#pragma unroll
-  for (int i = 0; i < kVec; ++i) {
-    bv[i] = bias ? __ldg(bias + c0 + i) : 0.f;
-#pragma unroll
-    for (int k = 0; k < K; ++k) wv[k][i] = __ldg(w + (c0 + i) * K + k);
-  }
-  float xw[K][kVec];    // x of tokens u-K+1 .. u (taps of token u, zero across a sequence start)
-  float dz[K][kVec];    // dpre of tokens u-K+1 .. u (zero before t0)
-  uint32_t st = 0;      // bit j: token u-K+1+j starts a sequence
-  float dwp[K][kVec], dbp[kVec];
-#pragma unroll
-  for (int k = 0; k < K; ++k)
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) xw[k][i] = dz[k][i] = dwp[k][i] = 0.f;
-#pragma unroll
-  for (int i = 0; i < kVec; ++i) dbp[i] = 0.f;
-  // tokens past the row end take part as zeros, so that dx of the tile's last
-  // tokens comes out of the same loop (every window index stays static); x and
-  // dy of the next kDepth tokens stream into this thread's ring slots meanwhile
-  extern __shared__ __align__(16) uint8_t ring_raw[];
-  const uint32_t ring = uint32_t(__cvta_generic_to_shared(ring_raw));
-  const int64_t u0 = t0 - (K - 1), u1 = t1 + (K - 1);
-  const int64_t off0 = (bi * s.T + u0) * s.C + c0;   // element offset of token u0 (read only where it exists)
-  auto issue = [&](int64_t u, int d, int64_t off) {
-    const bool okx = u >= 0 && u < s.T && u < u1, okg = okx && u >= t0;
-    stream_row(ring_slot(ring, d, 0), okx ? x + off : x, okx);
-    stream_row(ring_slot(ring, d, 1), okg ? dy + off : dy, okg);
-    stream_commit();
-  };
-  for (int j = 0; j < kDepth; ++j) issue(u0 + j, j, off0 + j * s.C);
-  int dslot = 0;   // ring slot of token u
-  int64_t off = off0;
-  for (int64_t u = u0; u < u1; ++u, dslot = (dslot + 1) & (kDepth - 1), off += s.C) {
-#pragma unroll
-    for (int k = 0; k + 1 < K; ++k)
-#pragma unroll
-      for (int i = 0; i < kVec; ++i) {
-        xw[k][i] = xw[k + 1][i];
-        dz[k][i] = dz[k + 1][i];
-      }
-    st >>= 1;
-    float g[kVec];
-    stream_wait();
-    read_slot(ring_slot(ring, dslot, 0), x, xw[K - 1]);   // zeros outside the row
-    read_slot(ring_slot(ring, dslot, 1), dy, g);          // zeros before the tile and outside the row
-    issue(u + kDepth, dslot, off + kDepth * s.C);
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) dz[K - 1][i] = 0.f;
-    if (u >= 0 && u < s.T) {
-      if (starts_seq(seq_idx, bi, s.T, u)) {
-        st |= 1u << (K - 1);
-#pragma unroll
-        for (int k = 0; k + 1 < K; ++k)
-#pragma unroll
-          for (int i = 0; i < kVec; ++i) xw[k][i] = 0.f;
-      }
-      if (u >= t0) {
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-          float acc = bv[i];
-#pragma unroll
-          for (int k = 0; k < K; ++k) acc = fmaf(wv[k][i], xw[k][i], acc);
-          if (s.silu) {
-            const float sg = sigmoid(acc);
-            dz[K - 1][i] = g[i] * (sg * fmaf(acc, 1.f - sg, 1.f));
-          } else {
-            dz[K - 1][i] = g[i];
-          }
-        }
-        if (u < t1) {   // the tile's own tokens: partial sums of dw and dbias, in token order
-#pragma unroll
-          for (int i = 0; i < kVec; ++i) {
-#pragma unroll
-            for (int k = 0; k < K; ++k) dwp[k][i] = fmaf(dz[K - 1][i], xw[k][i], dwp[k][i]);
-            dbp[i] += dz[K - 1][i];
-          }
-        }
-      }
-    }
-    // dx of token s = u-K+1 (complete now): sum_k w[k] dz[s+K-1-k] over taps that stay in s's sequence
-    const int64_t sx = u - (K - 1);
-    if (sx >= t0 && sx < t1) {
-      float o[kVec];
-      bool live = true;   // no sequence start in (s, s + j]
-#pragma unroll
-      for (int i = 0; i < kVec; ++i) o[i] = 0.f;
-#pragma unroll
-      for (int j = 0; j < K; ++j) {   // dz[j] is token s + j, which reads x[s] through tap K-1-j
-        if (j > 0 && ((st >> j) & 1u)) live = false;
-        if (live) {
-#pragma unroll
-          for (int i = 0; i < kVec; ++i) o[i] = fmaf(wv[K - 1 - j][i], dz[j][i], o[i]);
-        }
-      }
-      store4(dx + off - (K - 1) * s.C, o);   // token sx = u - (K - 1)
-    }
-  }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  if (kAtomic) {
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) {
-#pragma unroll
-      for (int k = 0; k < K; ++k) atomicAdd(dw + (c0 + i) * K + k, dwp[k][i]);
-      if (dbias) atomicAdd(dbias + c0 + i, dbp[i]);
-    }
-  } else {
-    float *p = part + tile * (K + 1) * s.C + c0;
-#pragma unroll
-    for (int k = 0; k < K; ++k) store4(p + k * s.C, dwp[k]);
-    store4(p + K * s.C, dbp);
-  }
-}
-
-// The same backward with the token loop unrolled by four: token u lives in
-// window slot u % 4 of xw (x) and dz (dpre), so the windows need no shifting,
-// and every slot index is a compile-time constant (the walk starts at a
-// multiple of 4, four tokens before the tile).  kSeq: seq_idx is given (a
+// atomic variant, added straight into dw and dbias.  The token loop is
+// unrolled by four: token u lives in window slot u % 4 of xw (x) and dz
+// (dpre), so the windows need no shifting and every slot index is a
+// compile-time constant (the walk starts at a multiple of 4, four tokens
+// before the tile).  Tokens past the row end take part as zeros, so dx of the
+// tile's last tokens comes out of the same loop.  kSeq: seq_idx is given (a
 // sequence may start at any token); without it the only start is the row's
-// first token, whose earlier taps read zeros anyway.  Per element the
-// arithmetic is that of conv_bwd_kernel, term for term.
+// first token, whose earlier taps read zeros anyway.
 template <class TIn, int K, bool kAtomic, bool kSeq>
-__global__ void conv_bwd4_kernel(ConvShape s, const TIn *__restrict__ x, const float *__restrict__ w,
+__global__ void conv_bwd_kernel(ConvShape s, const TIn *__restrict__ x, const float *__restrict__ w,
                                  const float *__restrict__ bias, const int32_t *__restrict__ seq_idx,
                                  const TIn *__restrict__ dy, float *__restrict__ dx, float *__restrict__ part,
                                  float *__restrict__ dw, float *__restrict__ dbias) {
@@ -498,7 +373,7 @@ cudaError_t launch_bwd(const ConvShape &s, int K, dim3 grid, int block, const vo
                        float *dbias, cudaStream_t st) {
   const TIn *xx = static_cast<const TIn *>(x), *gg = static_cast<const TIn *>(dy);
 #define SSD_CONV_BWD(KK, SEQ) \
-  launch_ring(conv_bwd4_kernel<TIn, KK, kAtomic, SEQ>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias)
+  launch_ring(conv_bwd_kernel<TIn, KK, kAtomic, SEQ>, grid, block, st, s, xx, w, bias, seq_idx, gg, dx, part, dw, dbias)
   if (seq_idx) {
     switch (K) {
       case 1: return SSD_CONV_BWD(1, true);

@@ -76,12 +76,24 @@ def test_atomic_variant_shows_the_test_has_teeth(name):
     assert len(set(hs)) > 1
 
 
-def test_outputs_fully_written_and_guards_untouched():
+@pytest.mark.parametrize("case", [
+    dict(T=300, H=8, P=32, G=2, N=64, Q=64, path="simt"),
+    dict(T=512, H=8, P=64, G=2, N=128, Q=128, path="fused/"),
+    dict(T=512, H=8, P=64, G=1, N=256, Q=256, path="fused-split/"),
+    dict(T=500, H=4, P=64, G=1, N=128, Q=128, path="fused-padded/", lens=(100, 300, 100)),
+    dict(T=700, H=8, P=64, G=1, N=256, Q=256, path="fused-split-padded/", lens=(99, 1, 600)),
+])
+def test_outputs_fully_written_and_guards_untouched(case):
     """Every output element is written (outputs pre-filled with NaN) and no
-    byte outside the outputs or past the workspace size is touched."""
-    d = make_inputs(1, 300, 8, 32, 2, 64, dtype=torch.bfloat16, seed=6, dt_shift=4.0, with_init=True)
+    byte outside the outputs or past the workspace size is touched, on each
+    kind of path (stores, TMA stores and reduce-adds, folds, scatters)."""
+    lens = case.get("lens", ())
+    d = make_inputs(1, case["T"], case["H"], case["P"], case["G"], case["N"], dtype=torch.bfloat16, seed=6,
+                    dt_shift=4.0, with_init=True, seq_lens=lens)
     g = to_dev(d)
-    y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=64, init_states=g["init"])
+    y, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=case["Q"], seq_idx=g["seq_idx"],
+                       init_states=g["init"], any_start=bool(lens))
+    assert ssd.config_name(saved.dims, 0).startswith(case["path"]), ssd.config_name(saved.dims, 0)
     pad = 4096
     out, guards = {}, []
     shapes = dict(dx=g["x"].shape, ddt=g["dt"].shape, dA=g["A"].shape, dB=g["B"].shape, dC=g["C"].shape,

@@ -83,6 +83,8 @@ def lib():
         L.mamba2_ssd_bwd_launch_name.restype = ctypes.c_char_p
         L.mamba2_ssd_bwd_check.argtypes = [pd, ci, vp, vp]
         L.mamba2_ssd_bwd_check.restype = ci
+        L.mamba2_ssd_fwd_check.argtypes = [pd, vp, vp]
+        L.mamba2_ssd_fwd_check.restype = ci
         L.mamba2_ssd_bwd_fault_test.argtypes = [ctypes.POINTER(SavedStruct)] + [vp] * 9 + [sz, i64, ctypes.c_uint32,
                                                                                            vp]
         L.mamba2_ssd_bwd_fault_test.restype = ci
@@ -163,6 +165,11 @@ def bwd_launch_names(dims: Dims, config: int = 0, variant: int = 0):
 def bwd_check(saved: "Saved", workspace, config: int = 0, stream=None) -> int:
     """Status word the device left in ``workspace`` after a backward."""
     return lib().mamba2_ssd_bwd_check(ctypes.byref(saved.dims), config, _ptr(workspace), _stream(stream))
+
+
+def fwd_check(saved: "Saved", stream=None) -> int:
+    """Status word the device left in the forward's workspace (kept with ``saved``)."""
+    return lib().mamba2_ssd_fwd_check(ctypes.byref(saved.dims), _ptr(saved.tensors["ws"]), _stream(stream))
 
 
 def _ptr(t):

@@ -219,6 +219,25 @@ ssd_status mamba2_ssd_bwd_check(const ssd_dims *dims, int config, const void *wo
   return word ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 
+ssd_status mamba2_ssd_fwd_check(const ssd_dims *dims, const void *workspace, void *stream) {
+  if (!dims_ok(dims) || !workspace) return SSD_ERR_INVALID_ARG;
+  const ssd::Shape s = shape_of(dims);
+  void *ws = const_cast<void *>(workspace);
+  const int *status = nullptr;
+  switch (kind_of(dims)) {
+    case kFused: status = ssd::fused_fwd_status(s, ws); break;
+    case kSplit: status = ssd::fused_fwd_split_status(s, ws); break;
+    case kFusedPad: status = ssd::padded_fwd_status(s, false, ws); break;
+    case kSplitPad: status = ssd::padded_fwd_status(s, true, ws); break;
+    default: return SSD_OK;   // the general forward has no device-side waits
+  }
+  int word = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
+  return word ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
 ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, const float *A, const void *B,
                           const void *C, const float *D, const int32_t *seq_idx, const float *init_states, void *y,
                           float *states, void *workspace, size_t workspace_bytes, void *stream,

@@ -511,6 +511,11 @@ size_t fused_fwd_workspace(const Shape &s) {
   return cv.bytes();
 }
 
+int *fused_fwd_status(const Shape &s, void *ws) {
+  Carver cv(ws);
+  return carve_fwd_fused(cv, s).status;
+}
+
 cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st) {
   Carver cv(ws);
   FwdWs w = carve_fwd_fused(cv, s);
@@ -627,6 +632,11 @@ size_t fused_fwd_split_workspace(const Shape &s) {
 float *fused_split_aux(const Shape &s, void *ws) {
   Carver cv(ws);
   return carve_fwd_split(cv, s).aux;
+}
+
+int *fused_fwd_split_status(const Shape &s, void *ws) {
+  Carver cv(ws);
+  return carve_fwd_split(cv, s).k.status;
 }
 
 cudaError_t fused_fwd_split(const Shape &s, const Args &a, void *ws, cudaStream_t st) {

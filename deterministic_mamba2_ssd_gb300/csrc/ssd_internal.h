@@ -37,6 +37,11 @@ size_t fused_bwd_workspace(const Shape &s, int ring_depth);
 // chunk written directly in the packed form above.
 size_t fused_fwd_workspace(const Shape &s);
 cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st);
+// Device status word of the tensor-core forward in its workspace (error bits of
+// its bounded waits), for the plain, split and padded forms.
+int *fused_fwd_status(const Shape &s, void *ws);
+int *fused_fwd_split_status(const Shape &s, void *ws);
+int *padded_fwd_status(const Shape &s, bool split, void *ws);
 
 // dstate 256 with one group (chunk 128 or 256): the same kernels run once per
 // state half (n < 128, n >= 128) as dstate-128 problems in 128-token chunks,

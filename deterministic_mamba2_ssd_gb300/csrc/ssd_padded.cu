@@ -244,6 +244,13 @@ size_t padded_fwd_workspace(const Shape &s, bool split) {
   return cv.bytes();
 }
 
+int *padded_fwd_status(const Shape &s, bool split, void *ws) {
+  Carver cv(ws);
+  void *inner = carve_pad_fwd(cv, s, split).inner;
+  const Shape p = padded_shape(s);
+  return split ? fused_fwd_split_status(p, inner) : fused_fwd_status(p, inner);
+}
+
 size_t padded_bwd_workspace(const Shape &s, bool split, int ring_depth) {
   Carver cv(nullptr);
   carve_pad_bwd(cv, s, split, ring_depth);

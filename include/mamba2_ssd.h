@@ -59,7 +59,7 @@ typedef enum {
   SSD_ERR_UNSUPPORTED = 2,   /* valid but not supported (e.g. a sequence start inside a chunk) */
   SSD_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size query */
   SSD_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
-  SSD_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out (see mamba2_ssd_bwd_check) */
+  SSD_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out (see mamba2_ssd_bwd_check, _fwd_check) */
   SSD_ERR_HANDLE = 6         /* saved struct not produced by mamba2_ssd_fwd or dims mismatch */
 } ssd_status;
 
@@ -205,6 +205,14 @@ int64_t mamba2_ssd_padded_chunks(const ssd_dims *dims);
  * padded form, null pointers, or ids that are negative, >= nseq or
  * decreasing. */
 ssd_status mamba2_ssd_padded_piece_table(const ssd_dims *dims, const int32_t *seq_idx, int32_t *table);
+
+/* Status of the last forward that used this workspace: reads one word
+ * written by the device (synchronises `stream`).  SSD_ERR_TIMEOUT when a
+ * bounded device-side wait of the tensor-core forward ran out (its outputs
+ * are then invalid), SSD_OK otherwise (always for the general forward, which
+ * has no device-side waits); SSD_ERR_INVALID_ARG for invalid dims or a null
+ * workspace. */
+ssd_status mamba2_ssd_fwd_check(const ssd_dims *dims, const void *workspace, void *stream);
 
 /* fp32 (b,nc,H,P,N) copy of the saved chunk states (hi + lo of the packed
  * form on the fused shapes, the states themselves otherwise) into `out`

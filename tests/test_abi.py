@@ -278,3 +278,12 @@ def test_dstate_256_shapes_pick_the_split_fused_path_or_the_general_one(L):
                  ssd.make_dims(1, 512, 4, 64, 1, 256, 256, dtype=torch.float32),
                  ssd.make_dims(1, 500, 4, 64, 1, 256, 256)):
         assert ssd.config_name(dims, 0).startswith("simt"), dims
+
+
+def test_fwd_check_on_host(L):
+    FAKE = 0x7f0000000000
+    simt = ssd.make_dims(1, 256, 4, 16, 1, 16, 64, dtype=torch.float32)
+    assert L.mamba2_ssd_fwd_check(ctypes.byref(simt), ctypes.c_void_p(FAKE), None) == 0   # no device waits: nothing read
+    assert L.mamba2_ssd_fwd_check(ctypes.byref(simt), None, None) == 1
+    bad = ssd.make_dims(1, 256, 3, 16, 2, 16, 64)   # heads not a multiple of groups
+    assert L.mamba2_ssd_fwd_check(ctypes.byref(bad), ctypes.c_void_p(FAKE), None) == 1

@@ -58,3 +58,4 @@ def test_split_status_word_is_clean():
     ws = torch.empty(ssd.bwd_workspace_size(saved.dims, 0, 0), dtype=torch.uint8, device="cuda")
     ssd.bwd(saved, g["dout"], workspace=ws)
     assert ssd.bwd_check(saved, ws) == 0
+    assert ssd.fwd_check(saved) == 0

@@ -83,6 +83,10 @@ def test_bf16_mid_chunk_on_fused_shapes(lens, H, G, N, Q, init):
                          any_start=True)
     assert ssd.config_name(dims, 0) == ("fused-padded/0" if N == 128 else "fused-split-padded/0")
     check(d, Q, 2e-3)
+    g = to_dev(d)
+    _, saved = ssd.fwd(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk_size=Q, seq_idx=g["seq_idx"],
+                       init_states=g["init"], any_start=True)
+    assert ssd.fwd_check(saved) == 0
 
 
 def test_bf16_mid_chunk_ids_with_gap_on_the_padded_path():

@@ -176,3 +176,27 @@ def test_aligned_starts_same_with_and_without_flag():
     a = run_gpu(d, 32, g=g)[2]
     b = run_gpu(d, 32, g=g, any_start=True)[2]
     assert same_bits(a, b)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_bf16_padded_random_layouts(seed):
+    """Seeded random packed layouts (sequence lengths 1-300, starts anywhere,
+    dstate 128 or 256, with or without initial states) on the padded form,
+    against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    N = 128 if seed % 2 == 0 else 256
+    Q = 128 if N == 128 else int(rng.choice([128, 256]))
+    lens = []
+    while sum(lens) < 600:
+        lens.append(int(rng.integers(1, 301)))
+    T = sum(lens)
+    nseq = len(lens)
+    if nseq - 1 > (T + 127) // 128:   # more sequences than the padded form admits: merge the tail
+        lens = lens[:(T + 127) // 128] + [sum(lens[(T + 127) // 128:])]
+        nseq = len(lens)
+    init = bool(seed % 3 != 0)
+    d = make_inputs(1, T, 4, 64, 1, N, dtype=torch.bfloat16, seed=2000 + seed, dt_shift=4.0, d_mode="normal",
+                    seq_lens=tuple(lens), with_init=init)
+    dims = ssd.make_dims(1, T, 4, 64, 1, N, Q, nseq=nseq, dtype=torch.bfloat16, seq_idx=True, any_start=True)
+    assert "padded" in ssd.config_name(dims, 0), (lens, ssd.config_name(dims, 0))
+    check(d, Q, 2e-3)

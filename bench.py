@@ -222,8 +222,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "fe3c1bba83998f6729df71672304d566f5e4a9ad5ce647a26ec73f3ee6b2b017": {
-        "bytes_per_token": (2278705920 + 1246661120) / 16384,
+    "b14502f065fe29d0cf9f29d6837259a7772084a8528335dc7ca42ed5180c8009": {
+        "bytes_per_token": (2288318208 + 1256178432) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }
@@ -659,36 +659,47 @@ def main():
         atomic_ms = statistics.mean(ta)
         del ws_a, out_a
 
-    # end to end through the public API with host buffers: every step copies its inputs from
-    # pinned host memory, runs mamba2_ssd_bwd and copies every gradient back.  Steps are
-    # pipelined over two buffer sets and three streams (inputs of step k+1 travel while step k
-    # computes and its gradients travel back), as a training loop's data path would run them;
-    # the serial step time (copies, backward and copies back on one stream) is reported beside.
+    # End to end through the public API with host buffers.  The headline mode is the call
+    # sequence of a caller whose data sits in host memory: every step copies the forward's inputs
+    # and dout from pinned host memory, calls mamba2_ssd_fwd (which leaves the chunk states the
+    # backward reads in device memory; a saved handle comes only from the forward) and
+    # mamba2_ssd_bwd, and copies every gradient back.  The second mode copies the saved chunk
+    # states from the host instead of running the forward (1.07 GB more per step at T=16384) and
+    # runs the backward alone.  Steps are pipelined over two buffer sets and three streams
+    # (inputs of step k+1 travel while step k computes and its gradients travel back), as a
+    # training loop's data path would run them; the serial step time (copies, compute and copies
+    # back on one stream) is reported beside.
     e2e = None
     if not args.no_e2e:
         host = {k: v.pin_memory() for k, v in d.items() if v is not None}
-        host["states"] = saved.states.cpu().pin_memory()
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        host_states = saved.states.cpu().pin_memory()
         d2h = sum(v.numel() * v.element_size() for v in out.values())
-        sets = []
-        for _ in range(2):
-            dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
-            for k, v in host.items():   # valid contents for the set-up forward (seq_idx is checked)
-                dev_in[k].copy_(v)
-            # saved struct that points at this set's device inputs
-            _, saved_e = ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
-                                 chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"),
-                                 any_start=w.any_start)
-            saved_e.struct.states = dev_in["states"].data_ptr()
-            saved_e.tensors["states"] = dev_in["states"]
-            out_e = {k: torch.empty_like(v) for k, v in out.items()}
-            ws_e = torch.empty_like(ws)
-            host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
-            sets.append((dev_in, saved_e, out_e, ws_e, host_out))
-        torch.cuda.synchronize()
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
-        def run_steps(n, serial):
+        def fwd_on(dev_in, stream):
+            return ssd.fwd(dev_in["x"], dev_in["dt"], dev_in["A"], dev_in["B"], dev_in["C"], dev_in["D"],
+                           chunk_size=w.chunk, seq_idx=dev_in.get("seq_idx"), init_states=dev_in.get("init"),
+                           stream=stream, any_start=w.any_start)[1]
+
+        def make_sets(states_from_host):
+            src = dict(host, states=host_states) if states_from_host else host
+            sets = []
+            for _ in range(2):
+                dev_in = {k: v.to(dev) for k, v in src.items()}
+                sv = None
+                if states_from_host:
+                    # a saved handle whose chunk states are this set's copy of the host's
+                    sv = fwd_on(dev_in, None)
+                    sv.struct.states = dev_in["states"].data_ptr()
+                    sv.tensors["states"] = dev_in["states"]
+                sets.append({"in": dev_in, "saved": sv, "out": {k: torch.empty_like(v) for k, v in out.items()},
+                             "ws": torch.empty_like(ws),
+                             "host_out": {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                                          for k, v in out.items()}})
+            torch.cuda.synchronize()
+            return src, sets
+
+        def run_steps(src, sets, n, serial, with_fwd):
             """Mean ms per step over n steps, and the median interval between step completions."""
             ev_cmp = [None, None]   # compute of the step that last used each set (inputs read)
             ev_out = [None, None]   # copy-back of the step that last used each set (outputs read)
@@ -698,25 +709,29 @@ def main():
             start.record(s_in)
             for k in range(n):
                 i = k % 2
-                dev_in, saved_e, out_e, ws_e, host_out = sets[i]
+                bs = sets[i]
                 si, sc, so = (s_in, s_in, s_in) if serial else (s_in, s_cmp, s_out)
                 if ev_cmp[i] is not None:
                     si.wait_event(ev_cmp[i])
                 with torch.cuda.stream(si):
-                    for key, v in host.items():
-                        dev_in[key].copy_(v, non_blocking=True)
+                    for key, v in src.items():
+                        bs["in"][key].copy_(v, non_blocking=True)
                 e_in = torch.cuda.Event()
                 e_in.record(si)
                 sc.wait_event(e_in)
                 if ev_out[i] is not None:
                     sc.wait_event(ev_out[i])
-                ssd.bwd(saved_e, dev_in["dout"], config=args.config, out=out_e, workspace=ws_e, stream=sc)
+                with torch.cuda.stream(sc):   # the forward's buffers are allocated on this stream
+                    if with_fwd:
+                        bs["saved"] = fwd_on(bs["in"], sc)
+                    ssd.bwd(bs["saved"], bs["in"]["dout"], config=args.config, out=bs["out"], workspace=bs["ws"],
+                            stream=sc)
                 ev_cmp[i] = torch.cuda.Event()
                 ev_cmp[i].record(sc)
                 so.wait_event(ev_cmp[i])
                 with torch.cuda.stream(so):
-                    for key, v in out_e.items():
-                        host_out[key].copy_(v, non_blocking=True)
+                    for key, v in bs["out"].items():
+                        bs["host_out"][key].copy_(v, non_blocking=True)
                 ev_out[i] = torch.cuda.Event(enable_timing=True)
                 ev_out[i].record(so)
                 done.append(ev_out[i])
@@ -729,19 +744,29 @@ def main():
             gaps = [b - a for a, b in zip([0.0] + t[:-1], t)]
             return start.elapsed_time(end) / n, statistics.median(gaps)
 
-        run_steps(args.warmup, serial=False)
-        pipe_ms, pipe_med = run_steps(args.steps, serial=False)
-        pipe_ms = max_over_ranks(pipe_ms, world, dev)
-        run_steps(2, serial=True)
-        serial_ms, serial_med = run_steps(args.steps, serial=True)
-        serial_ms = max_over_ranks(serial_ms, world, dev)
-        # value from the mean over all steps; the medians show how much of it comes from
-        # occasional stalls of the host copies (steps of 80-200 ms seen on a shared machine)
-        e2e = {"value": world * tokens / (pipe_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "pipelined": True,
-               "ms_per_step_median": pipe_med, "serial_ms_per_step": serial_ms,
-               "serial_ms_per_step_median": serial_med}
-        del sets
+        def measure(states_from_host):
+            src, sets = make_sets(states_from_host)
+            with_fwd = not states_from_host
+            run_steps(src, sets, args.warmup, False, with_fwd)
+            pipe_ms, pipe_med = run_steps(src, sets, args.steps, False, with_fwd)
+            pipe_ms = max_over_ranks(pipe_ms, world, dev)
+            run_steps(src, sets, 2, True, with_fwd)
+            serial_ms, serial_med = run_steps(src, sets, args.steps, True, with_fwd)
+            serial_ms = max_over_ranks(serial_ms, world, dev)
+            h2d = sum(v.numel() * v.element_size() for v in src.values())
+            del sets
+            # value from the mean over all steps; the medians show how much of it comes from
+            # occasional stalls of the host copies (steps of 80-200 ms seen on a shared machine)
+            return {"value": world * tokens / (pipe_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "pipelined": True,
+                    "ms_per_step_median": pipe_med, "serial_ms_per_step": serial_ms,
+                    "serial_ms_per_step_median": serial_med}
+
+        e2e = measure(False)
+        e2e["calls_per_step"] = "mamba2_ssd_fwd + mamba2_ssd_bwd"
+        e2e["states_from_host"] = measure(True)
+        e2e["states_from_host"]["calls_per_step"] = "mamba2_ssd_bwd (saved chunk states copied from the host)"
+        del host, host_states
 
     # the other workload presets (the 2K and 4K rows of the pages' tables, the packed
     # variable-length batch, and fp32 inputs on the general path), timed after the headline

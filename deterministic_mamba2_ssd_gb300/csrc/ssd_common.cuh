@@ -73,4 +73,23 @@ __device__ __forceinline__ int64_t seq_of(const int32_t *seq_idx, int64_t bi, in
   return seq_idx ? int64_t(seq_idx[bi * T + t]) : bi;
 }
 
+// p[0] + p[stride] + ... + p[(n-1) stride], added one term at a time in
+// ascending order onto acc.  The loads of each batch of 32 terms are issued
+// before any of their adds, so the sum waits on one memory latency per batch
+// rather than one per term; the order of the adds, and so the bits, are those
+// of the plain loop.
+__device__ __forceinline__ float column_sum(const float *__restrict__ p, int64_t n, int64_t stride, float acc) {
+  constexpr int kBatch = 32;
+  int64_t k = 0;
+  for (; k + kBatch <= n; k += kBatch) {
+    float v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) v[j] = __ldcg(p + (k + j) * stride);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) acc += v[j];
+  }
+  for (; k < n; ++k) acc += __ldcg(p + k * stride);
+  return acc;
+}
+
 }  // namespace ssd

@@ -1023,13 +1023,8 @@ __global__ void fold_scalars_kernel(Shape s, const float *__restrict__ dA_part, 
                                     float *__restrict__ dA, float *__restrict__ dD) {
   const int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (h >= s.H) return;
-  float a = 0.f, d = 0.f;
-  for (int64_t bc = 0; bc < s.b * s.nc; ++bc) {
-    a += dA_part[bc * s.H + h];
-    d += dD_part[bc * s.H + h];
-  }
-  dA[h] = a;
-  dD[h] = d;
+  dA[h] = column_sum(dA_part + h, s.b * s.nc, s.H, 0.f);
+  dD[h] = column_sum(dD_part + h, s.b * s.nc, s.H, 0.f);
 }
 
 struct FusedWs {
@@ -1242,14 +1237,9 @@ __global__ void split_scalars_kernel(Shape h, const float *__restrict__ a0, cons
                                      const float *__restrict__ d0, float *__restrict__ dA, float *__restrict__ dD) {
   const int64_t hd = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (hd >= h.H) return;
-  float a = 0.f, d = 0.f;
-  for (int64_t bc = 0; bc < h.b * h.nc; ++bc) {
-    a += a0[bc * h.H + hd];
-    d += d0[bc * h.H + hd];
-  }
-  for (int64_t bc = 0; bc < h.b * h.nc; ++bc) a += a1[bc * h.H + hd];
-  dA[hd] = a;
-  dD[hd] = d;
+  const int64_t n = h.b * h.nc;
+  dA[hd] = column_sum(a1 + hd, n, h.H, column_sum(a0 + hd, n, h.H, 0.f));
+  dD[hd] = column_sum(d0 + hd, n, h.H, 0.f);
 }
 
 }  // namespace

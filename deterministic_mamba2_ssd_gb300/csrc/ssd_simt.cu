@@ -1057,13 +1057,8 @@ __global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ d
                                             float *__restrict__ dD) {
   const int64_t h = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (h >= s.H) return;
-  float a = 0.f, d = 0.f;
-  for (int64_t bc = 0; bc < s.b * s.nc; ++bc) {
-    a += dA_part[bc * s.H + h];
-    d += dD_part[bc * s.H + h];
-  }
-  dA[h] = a;
-  dD[h] = d;
+  dA[h] = column_sum(dA_part + h, s.b * s.nc, s.H, 0.f);
+  dD[h] = column_sum(dD_part + h, s.b * s.nc, s.H, 0.f);
 }
 
 struct BwdWs {

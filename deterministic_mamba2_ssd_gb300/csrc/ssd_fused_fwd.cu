@@ -97,6 +97,16 @@ struct FwdParams {
   int *err;
 };
 
+// Row-per-lane tiles in a warp's shared staging area: 32 rows of four 16-byte
+// chunks (64 bytes), chunk i of row l kept at slot i ^ ((l >> 1) & 3).  Lane l
+// writes its own row; after a warp barrier lane l reads chunk (l & 3) of row
+// 8 i + (l >> 2), so that the four lanes of a row hold 64 contiguous bytes of
+// it and one warp-wide store covers 8 rows.  Both access patterns are free of
+// shared-memory bank conflicts (each phase of 8 lanes touches 32 distinct banks).
+__device__ __forceinline__ uint4 *stage_slot(uint8_t *stg, int row, int chunk) {
+  return reinterpret_cast<uint4 *>(stg + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
 // =============================================== 1. chunk states (tcgen05) ==
 // One CTA of 128 threads per (batch row, chunk, group); thread t owns token t
 // (and TMEM lane t = state row n for the result).  Per head: w = exp(E - Acs)
@@ -107,7 +117,8 @@ constexpr uint32_t K1_B = 0;         // B chunk [t][n] bf16, 2 panels
 constexpr uint32_t K1_X = 32768;     // x [t][p] bf16, 2 stages of 16 KB
 constexpr uint32_t K1_WH = 65536;    // (w o x) hi [t][p]
 constexpr uint32_t K1_WL = 81920;    // (w o x) lo
-constexpr uint32_t K1_SMALL = 98304;
+constexpr uint32_t K1_STG = 98304;    // per warp: 32 rows x 16 floats, the store staging of S^T
+constexpr uint32_t K1_SMALL = 106496;
 struct K1Small {
   float wtot[2][4];
   uint64_t bfull, xfull[2], mma;
@@ -154,17 +165,29 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
                  aWl = umma::smem_u32(base + K1_WL);
   constexpr uint32_t id_mm64 = umma::idesc_bf16_f32(128, 64, 1, 1);
 
-  // S^T of head k from TMEM buffer k & 1 to ST (row n = t: 64 contiguous floats)
+  // S^T of head k from TMEM buffer k & 1 to ST (row n = t: 64 contiguous
+  // floats), 16 columns at a time through this warp's staging rows, so that
+  // each store instruction writes 8 rows x 64 contiguous bytes
+  uint8_t *const stg = base + K1_STG + warp * 2048;
+  const int lane = t & 31;
   auto store_state = [&](int k) {
     const int64_t h = int64_t(g) * hpg + k;
-    float *o = p.ST + (((int64_t(bi) * s.nc + c) * s.H + h) * kN + t) * kP;
+    float *o = p.ST + (((int64_t(bi) * s.nc + c) * s.H + h) * kN + 32 * warp) * kP;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float v[16];
       umma::tmem_ld16(tmem + lane_off + 64 * (k & 1) + 16 * j, v);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        __stcg(reinterpret_cast<float4 *>(o + 16 * j + 4 * i), make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+        *stage_slot(stg, lane, i) = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                               __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = 8 * i + (lane >> 2), ch = lane & 3;
+        __stcg(reinterpret_cast<uint4 *>(o + int64_t(row) * kP + 16 * j + 4 * ch), *stage_slot(stg, row, ch));
+      }
+      __syncwarp();
     }
   };
 
@@ -351,11 +374,15 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
   __syncwarp();
   umma::fence_after_sync();
 
-  // y of head k from TMEM buffer k & 1: this thread's row, 32 columns
+  // y of head k from TMEM buffer k & 1: this thread's row, 32 columns.  The
+  // bf16 rows go through the x stage of head k (free once head k's products
+  // are done), 2 KB per warp, so that each store instruction writes 8 rows x
+  // 64 contiguous bytes.
   auto store_y = [&](int k, float eacs) {
     const int64_t h = int64_t(g) * hpg + k;
     const uint32_t buf = 128 + 128 * uint32_t(k & 1);
     const int64_t e0 = (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
+    uint8_t *const stg = base + K3_X + (k & 1) * 16384 + warp * 2048;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float yv[16], ch[16];
@@ -384,9 +411,19 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
       __nv_bfloat162 *hb = reinterpret_cast<__nv_bfloat162 *>(u);
 #pragma unroll
       for (int i = 0; i < 8; ++i) hb[i] = __floats2bfloat162_rn(yv[2 * i], yv[2 * i + 1]);
-      *reinterpret_cast<uint4 *>(p.y + e0 + 16 * j) = u[0];
-      *reinterpret_cast<uint4 *>(p.y + e0 + 16 * j + 8) = u[1];
+      *stage_slot(stg, lane, 2 * j) = u[0];
+      *stage_slot(stg, lane, 2 * j + 1) = u[1];
     }
+    if (p.y_mode == 1) return;
+    __syncwarp();
+    __nv_bfloat16 *const yw = p.y + (int64_t(row0 + 32 * q) * s.H + h) * kP + 32 * half;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 8 * i + (lane >> 2), ch = lane & 3;
+      *reinterpret_cast<uint4 *>(yw + int64_t(row) * s.H * kP + 8 * ch) = *stage_slot(stg, row, ch);
+    }
+    // the stage is next written by the copy of head k + 2's x (async proxy)
+    umma::fence_proxy_async_smem();
   };
 
   float eacs_prev = 0.f;

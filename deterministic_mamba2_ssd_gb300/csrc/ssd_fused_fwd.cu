@@ -94,6 +94,7 @@ struct FwdParams {
   __nv_bfloat16 *y;
   float *y_acc;     // fp32 partial y (state halves of a 256-wide state, see fused_fwd_split)
   int y_mode;       // 0: y in bf16; 1: partial y to y_acc; 2: y = y_acc + this partial, in bf16
+  int slices;       // head slices per (chunk, group) unit of the state and scan kernels
   int *err;
 };
 
@@ -133,10 +134,14 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
   K1Small *sm = reinterpret_cast<K1Small *>(base + K1_SMALL);
   const Shape &s = p.s;
   const int t = threadIdx.x, warp = t >> 5;
-  const int unit = blockIdx.x;
-  const int g = unit % int(s.G), c = (unit / int(s.G)) % int(s.nc), bi = unit / int(s.G * s.nc);
+  // unit: (batch row, chunk, group, head slice); a slice's heads run in order
+  const int unit = blockIdx.x, ns = p.slices;
+  const int64_t gn = s.G * ns;
+  const int gsl = int(unit % gn), g = gsl / ns;
+  const int c = int((unit / gn) % s.nc), bi = int(unit / (gn * s.nc));
   const int row0 = bi * int(s.T) + c * kQ;
-  const int hpg = int(s.hpg);
+  const int nh = int(s.hpg) / ns;                 // heads of this unit
+  const int hb = g * int(s.hpg) + (gsl % ns) * nh;   // its first head
 
   if (warp == 0) {
     umma::tmem_alloc(&sm->tmem, 128);
@@ -151,9 +156,9 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
     umma::mbar_expect_tx(&sm->bfull, 32768);
     for (int j = 0; j < 2; ++j)
       umma::tma_load_2d(base + K1_B + j * 16384, &tm_b, g * kN + j * 64, row0, &sm->bfull);
-    for (int k = 0; k < 2 && k < hpg; ++k) {
+    for (int k = 0; k < 2 && k < nh; ++k) {
       umma::mbar_expect_tx(&sm->xfull[k], 16384);
-      umma::tma_load_2d(base + K1_X + k * 16384, &tm_x, (g * hpg + k) * kP, row0, &sm->xfull[k]);
+      umma::tma_load_2d(base + K1_X + k * 16384, &tm_x, (hb + k) * kP, row0, &sm->xfull[k]);
     }
   }
   umma::fence_before_sync();
@@ -171,7 +176,7 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
   uint8_t *const stg = base + K1_STG + warp * 2048;
   const int lane = t & 31;
   auto store_state = [&](int k) {
-    const int64_t h = int64_t(g) * hpg + k;
+    const int64_t h = int64_t(hb) + k;
     float *o = p.ST + (((int64_t(bi) * s.nc + c) * s.H + h) * kN + 32 * warp) * kP;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -191,11 +196,11 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
     }
   };
 
-  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + g * hpg);
-  for (int k = 0; k < hpg; ++k) {
-    const int64_t h = int64_t(g) * hpg + k;
+  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + hb);
+  for (int k = 0; k < nh; ++k) {
+    const int64_t h = int64_t(hb) + k;
     const float dtv = dt_next;
-    if (k + 1 < hpg) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
+    if (k + 1 < nh) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
     const float Ah = __ldg(p.A + h) * kLog2e;
     float *wt = sm->wtot[k & 1];
     const float cum = chunk_scan128(dtv, wt, t, [] { __syncthreads(); });
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
     umma::fence_before_sync();
     __syncthreads();
     if (t == 0) {
-      if (k + 2 < hpg) {   // x of head k has been read: stage k & 1 takes head k + 2
+      if (k + 2 < nh) {   // x of head k has been read: stage k & 1 takes head k + 2
         umma::mbar_expect_tx(&sm->xfull[k & 1], 16384);
         umma::tma_load_2d(base + K1_X + (k & 1) * 16384, &tm_x, int(h + 2) * kP, row0, &sm->xfull[k & 1]);
       }
@@ -238,9 +243,9 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(const FwdParams p, const
     if (k >= 1) store_state(k - 1);   // its product completed before this head's w o x was written
     umma::fence_before_sync();
   }
-  fwait(&sm->mma, uint32_t((hpg - 1) & 1), p.err);
+  fwait(&sm->mma, uint32_t((nh - 1) & 1), p.err);
   umma::fence_after_sync();
-  store_state(hpg - 1);
+  store_state(nh - 1);
   umma::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -323,11 +328,15 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = warp & 3, half = warp >> 2;
   const int r = 32 * q + lane;   // token row of this thread
-  const int unit = blockIdx.x;
-  const int g = unit % int(s.G), c = (unit / int(s.G)) % int(s.nc), bi = unit / int(s.G * s.nc);
+  // unit: (batch row, chunk, group, head slice); a slice's heads run in order
+  const int unit = blockIdx.x, ns = p.slices;
+  const int64_t gn = s.G * ns;
+  const int gsl = int(unit % gn), g = gsl / ns;
+  const int c = int((unit / gn) % s.nc), bi = int(unit / (gn * s.nc));
   const int row0 = bi * int(s.T) + c * kQ;
-  const int hpg = int(s.hpg);
-  const float *states = p.states + ((int64_t(bi) * s.nc + c) * s.H + int64_t(g) * hpg) * (kP * kN);
+  const int nh = int(s.hpg) / ns;                 // heads of this unit
+  const int hb = g * int(s.hpg) + (gsl % ns) * nh;   // its first head
+  const float *states = p.states + ((int64_t(bi) * s.nc + c) * s.H + int64_t(hb)) * (kP * kN);
 
   if (warp == 0) {
     umma::tmem_alloc(&sm->tmem, 512);
@@ -347,9 +356,9 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
       umma::tma_load_2d(base + K3_B + j * 16384, &tm_b, g * kN + j * 64, row0, &sm->bcfull);
       umma::tma_load_2d(base + K3_C + j * 16384, &tm_c, g * kN + j * 64, row0, &sm->bcfull);
     }
-    for (int k = 0; k < 2 && k < hpg; ++k) {
+    for (int k = 0; k < 2 && k < nh; ++k) {
       umma::mbar_expect_tx(&sm->xfull[k], 16384);
-      umma::tma_load_2d(base + K3_X + k * 16384, &tm_x, (g * hpg + k) * kP, row0, &sm->xfull[k]);
+      umma::tma_load_2d(base + K3_X + k * 16384, &tm_x, (hb + k) * kP, row0, &sm->xfull[k]);
       umma::mbar_expect_tx(&sm->hfull[k], kP * kN * 4);
       umma::bulk_load(base + K3_H + k * 32768, states + int64_t(k) * kP * kN, kP * kN * 4, &sm->hfull[k]);
     }
@@ -379,7 +388,7 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
   // are done), 2 KB per warp, so that each store instruction writes 8 rows x
   // 64 contiguous bytes.
   auto store_y = [&](int k, float eacs) {
-    const int64_t h = int64_t(g) * hpg + k;
+    const int64_t h = int64_t(hb) + k;
     const uint32_t buf = 128 + 128 * uint32_t(k & 1);
     const int64_t e0 = (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
     uint8_t *const stg = base + K3_X + (k & 1) * 16384 + warp * 2048;
@@ -408,9 +417,9 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
         }
       }
       uint4 u[2];
-      __nv_bfloat162 *hb = reinterpret_cast<__nv_bfloat162 *>(u);
+      __nv_bfloat162 *yb = reinterpret_cast<__nv_bfloat162 *>(u);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) hb[i] = __floats2bfloat162_rn(yv[2 * i], yv[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) yb[i] = __floats2bfloat162_rn(yv[2 * i], yv[2 * i + 1]);
       *stage_slot(stg, lane, 2 * j) = u[0];
       *stage_slot(stg, lane, 2 * j + 1) = u[1];
     }
@@ -428,11 +437,11 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
 
   float eacs_prev = 0.f;
   const int grp = tid >> 7, t = tid & 127;   // two groups of 128 threads run the same scan
-  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + g * hpg);
-  for (int k = 0; k < hpg; ++k) {
-    const int64_t h = int64_t(g) * hpg + k;
+  float dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + hb);
+  for (int k = 0; k < nh; ++k) {
+    const int64_t h = int64_t(hb) + k;
     const float dtv = dt_next;
-    if (k + 1 < hpg) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
+    if (k + 1 < nh) dt_next = __ldg(p.dt + int64_t(row0 + t) * s.H + h + 1);
     const float Ah = __ldg(p.A + h) * kLog2e, Dh = __ldg(p.D + h);
     // ---- step sizes: cumulative decay (both groups compute identical bits)
     const float cum = chunk_scan128(dtv, sm->wtot[k & 1][grp], t, [] { __syncthreads(); });
@@ -502,23 +511,23 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
     eacs_prev = eacs;
     umma::fence_before_sync();
     __syncthreads();
-    if (tid == 0 && k >= 1 && k + 1 < hpg) {
+    if (tid == 0 && k >= 1 && k + 1 < nh) {
       // head k-1's products are done (waited above): its x and H stages take head k + 1
       const int st = (k + 1) & 1;
       umma::mbar_expect_tx(&sm->xfull[st], 16384);
       umma::tma_load_2d(base + K3_X + st * 16384, &tm_x, int(h + 1) * kP, row0, &sm->xfull[st]);
       umma::mbar_expect_tx(&sm->hfull[st], kP * kN * 4);
       umma::bulk_load(base + K3_H + st * 32768, states + int64_t(k + 1) * kP * kN, kP * kN * 4, &sm->hfull[st]);
-      if (k + 2 < hpg) {
+      if (k + 2 < nh) {
         umma::tma_prefetch_2d(&tm_x, int(h + 2) * kP, row0);
         umma::prefetch_l2(states + int64_t(k + 2) * kP * kN, kP * kN * 4);
       }
     }
   }
-  if (lane == 0) fwait(&sm->mma, uint32_t((hpg - 1) & 1), p.err);
+  if (lane == 0) fwait(&sm->mma, uint32_t((nh - 1) & 1), p.err);
   __syncwarp();
   umma::fence_after_sync();
-  store_y(hpg - 1, eacs_prev);
+  store_y(nh - 1, eacs_prev);
   umma::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
@@ -538,6 +547,27 @@ FwdWs carve_fwd_fused(Carver &cv, const Shape &s) {
   w.ST = cv.take<float>(s.b * s.nc * s.H * kN * kP);
   w.decay = cv.take<float>(s.b * s.nc * s.H);
   return w;
+}
+
+// Head slices per (chunk, group) unit: the power of two (at least 16 heads a
+// slice) that minimises the heads run by the busiest SM of the scan kernel
+// (one unit per SM at a time), the smallest on a tie.  The forward's heads are
+// independent, so slicing changes which CTA runs a head and nothing else.
+int fwd_slices(const Shape &s, int64_t units) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                 cudaSuccess || sms <= 0)
+    return 1;
+  int best = 1;
+  int64_t best_load = (units + sms - 1) / sms * s.hpg;
+  for (int ns = 2; s.hpg % ns == 0 && s.hpg / ns >= 16 && units * ns <= (int64_t(1) << 30); ns *= 2) {
+    const int64_t load = (units * ns + sms - 1) / sms * (s.hpg / ns);
+    if (load < best_load) {
+      best = ns;
+      best_load = load;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -585,7 +615,8 @@ cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st) 
       (err = cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM)) !=
           cudaSuccess)
     return err;
-  const unsigned units = unsigned(s.b * s.nc * s.G);
+  p.slices = fwd_slices(s, s.b * s.nc * s.G);
+  const unsigned units = unsigned(s.b * s.nc * s.G * p.slices);
   fwd_state_kernel<<<units, 128, K1_SMEM, st>>>(p, tm_x, tm_b);
   fwd_pass_kernel<<<unsigned((s.b * s.H * kN * 8 + 255) / 256), 256, 0, st>>>(p);
   fwd_scan_kernel<<<units, 256, K3_SMEM, st>>>(p, tm_x, tm_b, tm_c);
@@ -701,11 +732,12 @@ cudaError_t fused_fwd_split(const Shape &s, const Args &a, void *ws, cudaStream_
       (err = cudaFuncSetAttribute(fwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, K3_SMEM)) !=
           cudaSuccess)
     return err;
-  const unsigned units = unsigned(h.b * h.nc);
   const int64_t tiles = h.b * h.nc * h.H * kP * kN;
   FwdParams p;
   memset(&p, 0, sizeof(p));
   p.s = h;
+  p.slices = fwd_slices(h, h.b * h.nc);
+  const unsigned units = unsigned(h.b * h.nc * p.slices);
   p.dt = a.dt;
   p.A = a.A;
   p.seq_idx = a.seq_idx;

@@ -384,14 +384,18 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
   umma::fence_after_sync();
 
   // y of head k from TMEM buffer k & 1: this thread's row, 32 columns.  The
-  // bf16 rows go through the x stage of head k (free once head k's products
-  // are done), 2 KB per warp, so that each store instruction writes 8 rows x
-  // 64 contiguous bytes.
+  // rows go to and from global memory through this warp's 2 KB of staging in
+  // the x stage (bf16 y) and the H stage (the fp32 partials of the split form)
+  // of head k, both free once head k's products are done, so that each global
+  // access instruction moves 8 rows x 64 contiguous bytes.
   auto store_y = [&](int k, float eacs) {
     const int64_t h = int64_t(hb) + k;
     const uint32_t buf = 128 + 128 * uint32_t(k & 1);
-    const int64_t e0 = (int64_t(row0 + r) * s.H + h) * kP + 32 * half;
     uint8_t *const stg = base + K3_X + (k & 1) * 16384 + warp * 2048;
+    uint8_t *const stg32 = base + K3_H + (k & 1) * 32768 + warp * 2048;
+    float *const accw = p.y_acc ? p.y_acc + (int64_t(row0 + 32 * q) * s.H + h) * kP + 32 * half : nullptr;
+    const int64_t pitch = s.H * kP;   // elements between consecutive token rows
+    const int srow = lane >> 2, sch = lane & 3;   // the row (of each 8) and chunk this lane moves
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float yv[16], ch[16];
@@ -402,19 +406,31 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
       if (p.y_mode == 1) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          __stcg(reinterpret_cast<float4 *>(p.y_acc + e0 + 16 * j + 4 * i),
-                 make_float4(yv[4 * i], yv[4 * i + 1], yv[4 * i + 2], yv[4 * i + 3]));
+          *stage_slot(stg32, lane, i) = make_uint4(__float_as_uint(yv[4 * i]), __float_as_uint(yv[4 * i + 1]),
+                                                   __float_as_uint(yv[4 * i + 2]), __float_as_uint(yv[4 * i + 3]));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          __stcg(reinterpret_cast<uint4 *>(accw + (8 * i + srow) * pitch + 16 * j + 4 * sch),
+                 *stage_slot(stg32, 8 * i + srow, sch));
+        __syncwarp();
         continue;
       }
       if (p.y_mode == 2) {   // the other state half's partial first, then this one
 #pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *stage_slot(stg32, 8 * i + srow, sch) =
+              __ldcs(reinterpret_cast<const uint4 *>(accw + (8 * i + srow) * pitch + 16 * j + 4 * sch));
+        __syncwarp();
+#pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float4 a = __ldcs(reinterpret_cast<const float4 *>(p.y_acc + e0 + 16 * j + 4 * i));
-          yv[4 * i] = a.x + yv[4 * i];
-          yv[4 * i + 1] = a.y + yv[4 * i + 1];
-          yv[4 * i + 2] = a.z + yv[4 * i + 2];
-          yv[4 * i + 3] = a.w + yv[4 * i + 3];
+          const uint4 a = *stage_slot(stg32, lane, i);
+          yv[4 * i] = __uint_as_float(a.x) + yv[4 * i];
+          yv[4 * i + 1] = __uint_as_float(a.y) + yv[4 * i + 1];
+          yv[4 * i + 2] = __uint_as_float(a.z) + yv[4 * i + 2];
+          yv[4 * i + 3] = __uint_as_float(a.w) + yv[4 * i + 3];
         }
+        __syncwarp();
       }
       uint4 u[2];
       __nv_bfloat162 *yb = reinterpret_cast<__nv_bfloat162 *>(u);
@@ -423,15 +439,14 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
       *stage_slot(stg, lane, 2 * j) = u[0];
       *stage_slot(stg, lane, 2 * j + 1) = u[1];
     }
-    if (p.y_mode == 1) return;
-    __syncwarp();
-    __nv_bfloat16 *const yw = p.y + (int64_t(row0 + 32 * q) * s.H + h) * kP + 32 * half;
+    if (p.y_mode != 1) {
+      __syncwarp();
+      __nv_bfloat16 *const yw = p.y + (int64_t(row0 + 32 * q) * s.H + h) * kP + 32 * half;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int row = 8 * i + (lane >> 2), ch = lane & 3;
-      *reinterpret_cast<uint4 *>(yw + int64_t(row) * s.H * kP + 8 * ch) = *stage_slot(stg, row, ch);
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4 *>(yw + (8 * i + srow) * pitch + 8 * sch) = *stage_slot(stg, 8 * i + srow, sch);
     }
-    // the stage is next written by the copy of head k + 2's x (async proxy)
+    // both stages are next written by the copies of head k + 2's x and H (async proxy)
     umma::fence_proxy_async_smem();
   };
 

@@ -98,16 +98,6 @@ struct FwdParams {
   int *err;
 };
 
-// Row-per-lane tiles in a warp's shared staging area: 32 rows of four 16-byte
-// chunks (64 bytes), chunk i of row l kept at slot i ^ ((l >> 1) & 3).  Lane l
-// writes its own row; after a warp barrier lane l reads chunk (l & 3) of row
-// 8 i + (l >> 2), so that the four lanes of a row hold 64 contiguous bytes of
-// it and one warp-wide store covers 8 rows.  Both access patterns are free of
-// shared-memory bank conflicts (each phase of 8 lanes touches 32 distinct banks).
-__device__ __forceinline__ uint4 *stage_slot(uint8_t *stg, int row, int chunk) {
-  return reinterpret_cast<uint4 *>(stg + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
-}
-
 // =============================================== 1. chunk states (tcgen05) ==
 // One CTA of 128 threads per (batch row, chunk, group); thread t owns token t
 // (and TMEM lane t = state row n for the result).  Per head: w = exp(E - Acs)

@@ -42,6 +42,16 @@ __device__ __forceinline__ void ld8_bf16(const uint8_t *panel, int r, int c0, fl
   bf16x8_to_f32(*reinterpret_cast<const uint4 *>(panel + r * 128 + (((c0 >> 3) ^ (r & 7)) << 4)), v);
 }
 
+// Row-per-lane tiles in a warp's shared staging area: 32 rows of four 16-byte
+// chunks (64 bytes), chunk i of row l kept at slot i ^ ((l >> 1) & 3).  Lane l
+// writes its own row; after a warp barrier lane l reads chunk (l & 3) of row
+// 8 i + (l >> 2), so that the four lanes of a row hold 64 contiguous bytes of
+// it and one warp-wide store covers 8 rows.  Both access patterns are free of
+// shared-memory bank conflicts (each phase of 8 lanes touches 32 distinct banks).
+__device__ __forceinline__ uint4 *stage_slot(uint8_t *stg, int row, int chunk) {
+  return reinterpret_cast<uint4 *>(stg + row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
 }  // namespace ssd
 
 namespace ssd {

@@ -300,12 +300,13 @@ constexpr uint32_t K3_SMALL = 229376;
 struct K3Small {
   float a2[kQ];      // Acs in log2 units, current head
   float dtv[kQ];     // step sizes, current head
+  float ecd[kQ];     // column factors exp(Acs_ref - Acs_s) dt_s, ref = s | 15, current head
   float wtot[2][2][4];
   uint64_t bcfull, cbdone, xfull[2], hfull[2], mma;
   uint32_t tmem;
 };
-constexpr uint32_t K3_SMEM = K3_SMALL + 1536 + 1024;
-static_assert(sizeof(K3Small) <= 1536, "small region");
+constexpr uint32_t K3_SMEM = K3_SMALL + 2048 + 1024;
+static_assert(sizeof(K3Small) <= 2048, "small region");
 static_assert(K3_SMEM <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tm_x,
@@ -451,9 +452,12 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
     // ---- step sizes: cumulative decay (both groups compute identical bits)
     const float cum = chunk_scan128(dtv, sm->wtot[k & 1][grp], t, [] { __syncthreads(); });
     const float a2t = cum * Ah;
+    // a2 of the last token of this token's 16-token block (the same warp)
+    const float a2ref = __shfl_sync(0xffffffffu, a2t, (t & 31) | 15);
     if (grp == 0) {
       sm->a2[t] = a2t;
       sm->dtv[t] = dtv;
+      sm->ecd[t] = umma::ex2_approx(a2ref - a2t) * dtv;
     }
     if (k >= 1 && lane == 0) fwait(&sm->mma, uint32_t((k - 1) & 1), p.err);   // head k-1 products done
     __syncwarp();
@@ -477,6 +481,23 @@ __global__ void __launch_bounds__(256, 1) fwd_scan_kernel(const FwdParams p, con
       }
       float cb[16];
       umma::tmem_ld16(tmem + lane_off + s0, cb);
+      if (s0 + 16 <= 32 * q) {
+        // every column of the block precedes every row of the quadrant: the decay
+        // exp(Acs_r - Acs_s) as the row factor exp(Acs_r - Acs_ref) (ref = the block's
+        // last column) times the column factor, both at most one, so one exp per row
+        const float er = umma::ex2_approx(a2r - sm->a2[s0 + 15]);
+#pragma unroll
+        for (int e8 = 0; e8 < 2; ++e8) {
+          const float4 c0 = *reinterpret_cast<const float4 *>(&sm->ecd[s0 + 8 * e8]);
+          const float4 c1 = *reinterpret_cast<const float4 *>(&sm->ecd[s0 + 8 * e8 + 4]);
+          const float ec[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = cb[8 * e8 + i] * er * ec[i];
+          st8_bf16_hilo(ph, pl, r, cc + 8 * e8, v);
+        }
+        continue;
+      }
 #pragma unroll
       for (int e8 = 0; e8 < 2; ++e8) {
         float v[8];

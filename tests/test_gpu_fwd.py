@@ -2,7 +2,8 @@
 the fp64 oracle: y (compared with the oracle's y rounded to bf16) and the
 saved state entering every chunk (the fp32 view of the packed pair), on
 shapes that span several chunks, heads per group (including one and an odd
-number), batch rows, initial states, packed sequences and strong decay, and
+number, and enough heads in few units that each unit's heads run as several
+slices), batch rows, initial states, packed sequences and strong decay, and
 on the 2K workload in full.  Parity bar: relL2 2e-3 per tensor (bf16 inputs,
 fp32 accumulation)."""
 import pytest
@@ -32,7 +33,8 @@ def run_fwd(d, chunk=128):
     dict(b=1, T=256, H=3, G=3),              # one head per group
     dict(b=1, T=512, H=6, G=2),              # odd heads per group
     dict(b=1, T=512, H=4, G=1, seq_lens=(128, 256, 128), with_init=True),
-    dict(b=1, T=1024, H=32, G=1, dt_shift=2.0),   # strong decay
+    dict(b=1, T=1024, H=32, G=1, dt_shift=2.0),   # strong decay; the units' heads in two slices
+    dict(b=1, T=256, H=64, G=1, with_init=True),  # two units of 64 heads: four slices of 16
 ])
 def test_forward_matches_oracle(case):
     d = make_inputs(case["b"], case["T"], case["H"], 64, case["G"], 128, dtype=torch.bfloat16,

@@ -22,6 +22,7 @@ TOL = 2e-3
     dict(b=2, T=256, H=4, Q=128, with_init=True),
     dict(b=1, T=1024, H=6, Q=256, seq_lens=(256, 512, 256), with_init=True),
     dict(b=1, T=768, H=2, Q=256, dt_shift=2.0),      # strong decay
+    dict(b=1, T=512, H=64, Q=256, with_init=True),   # 64 heads: the forward's head slices, 16 per backward slice
 ])
 def test_split_matches_oracle(case):
     d = make_inputs(case["b"], case["T"], case["H"], 64, 1, 256, dtype=torch.bfloat16, seed=case["T"] + case["H"],

@@ -99,7 +99,7 @@ struct FwdParams {
 };
 
 // =============================================== 1. chunk states (tcgen05) ==
-// One CTA of 128 threads per (batch row, chunk, group); thread t owns token t
+// One CTA of 128 threads per (batch row, chunk, group, head slice); thread t owns token t
 // (and TMEM lane t = state row n for the result).  Per head: w = exp(E - Acs)
 // dt, w o x as a bf16 hi/lo pair in shared memory, S^T = B^T (w o x) on the
 // tensor cores (M = n, N = p, K = t) into one of two TMEM buffers, and the
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(256) fwd_pass_kernel(const FwdParams p) {
 }
 
 // ================================================= 3. chunk scan (tcgen05) ==
-// One CTA of 256 threads per (batch row, chunk, group).  Warp w handles TMEM
+// One CTA of 256 threads per (batch row, chunk, group, head slice).  Warp w handles TMEM
 // lane quadrant q = w % 4 (tokens 32q..32q+31) and half w / 4 of the columns.
 // Per head: the intra-chunk matrix M'[t,s] = (C_t.B_s) exp(Acs_t - Acs_s) dt_s
 // for s <= t (plus D on the diagonal, which folds the skip term into the

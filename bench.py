@@ -222,8 +222,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "b14502f065fe29d0cf9f29d6837259a7772084a8528335dc7ca42ed5180c8009": {
-        "bytes_per_token": (2288318208 + 1256178432) / 16384,
+    "983dddb8f5311eaa2a0a36cf10b56b785d692c4532e48c4dc70c8a459835c224": {
+        "bytes_per_token": (2295961344 + 1259906304) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

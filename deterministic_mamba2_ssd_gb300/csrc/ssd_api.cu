@@ -59,24 +59,28 @@ constexpr int kFusedRings[] = {4, 2};
 constexpr int kNumFused = 2;
 
 // Which backward a shape runs.  The fused kernels reset the state at chunk
-// starts only; dstate 256 with one group runs them once per state half.
+// starts only; dstate 256 with one group runs them once per state half;
+// dstate 128 with a longer chunk (a multiple of 128) runs them in 128-token
+// chunks.
 // Sequence starts inside a chunk run them on a padded copy of the problem
 // (every piece of a sequence inside one 128-token chunk padded to a chunk of
 // its own) when the padding at most doubles the chunk count, and take the
 // general path otherwise.
-enum Kind { kSimt = 0, kFused = 1, kSplit = 2, kFusedPad = 3, kSplitPad = 4 };
+enum Kind { kSimt = 0, kFused = 1, kSplit = 2, kFusedPad = 3, kSplitPad = 4, kChunk128 = 5 };
 Kind kind_of(const ssd_dims *d) {
   const ssd::Shape s = shape_of(d);
   const bool bf16 = d->dtype == SSD_BF16;
   if (d->flags & SSD_DIMS_SEQ_ANY_START) {
     if (d->batch != 1 || !bf16 || s.nseq - 1 > (s.T + 127) / 128) return kSimt;
     const ssd::Shape p = ssd::padded_shape(s);
-    if (s.Q == 128 && ssd::fused_bwd_supported(p, bf16)) return kFusedPad;
-    if ((s.Q == 128 || s.Q == 256) && ssd::fused_split_supported(p, bf16)) return kSplitPad;
+    // (the padded problem is in 128-token chunks whatever the caller's chunk, a multiple of 128)
+    if (s.Q % 128 == 0 && ssd::fused_bwd_supported(p, bf16)) return kFusedPad;
+    if (s.Q % 128 == 0 && ssd::fused_split_supported(p, bf16)) return kSplitPad;
     return kSimt;
   }
   if (ssd::fused_bwd_supported(s, bf16)) return kFused;
   if (ssd::fused_split_supported(s, bf16)) return kSplit;
+  if (ssd::fused_chunk128_supported(s, bf16)) return kChunk128;
   return kSimt;
 }
 bool use_fused(const ssd_dims *d) { return kind_of(d) != kSimt; }
@@ -134,6 +138,7 @@ size_t mamba2_ssd_fwd_workspace_size(const ssd_dims *dims) {
   if (!dims_ok(dims)) return 0;
   switch (kind_of(dims)) {
     case kFused: return ssd::fused_fwd_workspace(shape_of(dims));
+    case kChunk128: return ssd::fused_fwd_chunk128_workspace(shape_of(dims));
     case kSplit: return ssd::fused_fwd_split_workspace(shape_of(dims));
     case kFusedPad: return ssd::padded_fwd_workspace(shape_of(dims), false);
     case kSplitPad: return ssd::padded_fwd_workspace(shape_of(dims), true);
@@ -151,6 +156,7 @@ const char *mamba2_ssd_config_name(const ssd_dims *dims, int config) {
   switch (kind_of(dims)) {
     case kSplit: return config == 0 ? "fused-split/ring4" : "fused-split/ring2";
     case kFused: return config == 0 ? "fused/ring4" : "fused/ring2";
+    case kChunk128: return config == 0 ? "fused-chunk128/ring4" : "fused-chunk128/ring2";
     // (with seq_idx every chunk has its own ring slot, so both configurations run the same launches)
     case kSplitPad: return config == 0 ? "fused-split-padded/0" : "fused-split-padded/1";
     case kFusedPad: return config == 0 ? "fused-padded/0" : "fused-padded/1";
@@ -166,6 +172,7 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
   switch (kind_of(dims)) {
     case kSplit: return ssd::fused_bwd_split_workspace(shape_of(dims), ring);
     case kFused: return ssd::fused_bwd_workspace(shape_of(dims), ring);
+    case kChunk128: return ssd::fused_bwd_workspace(ssd::fused_chunk128_shape(shape_of(dims)), ring);
     case kFusedPad: return ssd::padded_bwd_workspace(shape_of(dims), false, ring);
     case kSplitPad: return ssd::padded_bwd_workspace(shape_of(dims), true, ring);
     default: break;
@@ -226,6 +233,7 @@ ssd_status mamba2_ssd_fwd_check(const ssd_dims *dims, const void *workspace, voi
   const int *status = nullptr;
   switch (kind_of(dims)) {
     case kFused: status = ssd::fused_fwd_status(s, ws); break;
+    case kChunk128: status = ssd::fused_fwd_chunk128_status(s, ws); break;
     case kSplit: status = ssd::fused_fwd_split_status(s, ws); break;
     case kFusedPad: status = ssd::padded_fwd_status(s, false, ws); break;
     case kSplitPad: status = ssd::padded_fwd_status(s, true, ws); break;
@@ -276,20 +284,24 @@ ssd_status mamba2_ssd_fwd(const ssd_dims *dims, const void *x, const float *dt, 
   a.init = init_states; a.seq_idx = seq_idx; a.y = y; a.states_out = states;
   // The fused shape family runs the tensor-core forward, which writes each saved state as the
   // packed bf16 hi | lo operand pair the fused backward takes; dstate 256 runs it per state half
-  // (packed states of both halves kept in the workspace); every other shape the general one.
+  // (packed states of both halves kept in the workspace), dstate 128 with a longer chunk in
+  // 128-token chunks (packed states kept in the workspace); every other shape the general one.
   // Sequence starts inside a chunk run the fused kernels on a padded copy kept in the workspace.
   const Kind kind = kind_of(dims);
   cudaError_t err;
   switch (kind) {
     case kFused: err = ssd::fused_fwd(s, a, workspace, st); break;
+    case kChunk128: err = ssd::fused_fwd_chunk128(s, a, workspace, st); break;
     case kSplit: err = ssd::fused_fwd_split(s, a, workspace, st); break;
     case kFusedPad:
     case kSplitPad: err = ssd::padded_fwd(s, kind == kSplitPad, a, host_seq.data(), workspace, st); break;
     default: err = ssd::simt_fwd(s, dims->dtype == SSD_BF16, a, workspace, kSimtBlocks[0], st);
   }
   if (err != cudaSuccess) return SSD_ERR_CUDA;
-  saved_out->aux = kind == kSplit ? ssd::fused_split_aux(s, workspace) : is_padded(kind) ? static_cast<const float *>(workspace)
-                                                                         : nullptr;
+  saved_out->aux = kind == kSplit      ? ssd::fused_split_aux(s, workspace)
+                   : kind == kChunk128 ? ssd::fused_chunk128_aux(s, workspace)
+                   : is_padded(kind)   ? static_cast<const float *>(workspace)
+                                       : nullptr;
   saved_out->dims = *dims;
   saved_out->x = x; saved_out->dt = dt; saved_out->A = A; saved_out->B = B; saved_out->C = C; saved_out->D = D;
   saved_out->seq_idx = seq_idx; saved_out->init_states = init_states; saved_out->states = states;
@@ -356,7 +368,7 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   tr.count = num_events;
   cudaError_t err;
   const Kind kind = kind_of(dims);
-  if (is_padded(kind) || kind == kSplit) {
+  if (is_padded(kind) || kind == kSplit || kind == kChunk128) {
     if (!saved->aux) return SSD_ERR_HANDLE;   // the packed states live in the forward's workspace
   }
   if (is_padded(kind)) {
@@ -364,6 +376,9 @@ ssd_status mamba2_ssd_bwd_traced(const ssd_saved *saved, const void *dout, float
   } else if (kind == kSplit) {
     a.states_in = saved->aux;
     err = ssd::fused_bwd_split(s, a, workspace, fused_options(dims, config, variant), st, tr);
+  } else if (kind == kChunk128) {
+    a.states_in = saved->aux;
+    err = ssd::fused_bwd(ssd::fused_chunk128_shape(s), a, workspace, fused_options(dims, config, variant), st, tr);
   } else if (kind == kFused)
     err = ssd::fused_bwd(s, a, workspace, fused_options(dims, config, variant), st, tr);
   else

@@ -28,8 +28,10 @@
 // its index mod 4), warp 16 TMA producer, warp 17 TMEM owner and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
 // the one product whose rounding dominates the error (dx_intra = M^T g with
 // M = CB o L) runs in fp16 with exact power-of-two scaling of both operands,
-// and the head-summed intra-chunk matrix for dB/dC is split into a bf16
-// hi + lo pair.
+// and the head-summed intra-chunk matrix for dB/dC, G~, the saved state H and
+// the chained state gradient dS in Y = B dS^T are split into bf16 hi + lo
+// pairs (a single bf16 dS left dA, a sum of cancelling terms, at relL2 4.6e-3
+// on a four-head problem; with the pair 4.9e-4).
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -57,7 +59,7 @@ constexpr uint32_t OFF_C = 32768;      // C chunk  [t][n] bf16, 2 panels
 constexpr uint32_t OFF_XG = 65536;     // x [t][p] 16 KB, g 16 KB (bf16 from TMA, then scaled fp16 in place)
 constexpr uint32_t OFF_STG = 98304;    // fp32 [p][n] 32 KB: dS, the chained state gradient (bulk copy)
 constexpr uint32_t OFF_HD = 131072;    // H hi | H lo: [n][p] bf16, 16 KB each (bulk copy of the packed
-                                       // saved state); later dS [n][p] (hi half)
+                                       // saved state); later dS hi | lo [n][p]
 constexpr uint32_t OFF_GW = 163840;    // exp(Acs) o g hi | lo: [t][p] bf16; later w o x (hi half) + scratch (lo half)
 constexpr uint32_t OFF_M16 = 196608;   // scaled M: [t][s] fp16, 2 panels x 16 KB
 constexpr uint32_t OFF_SMALL = 229376;
@@ -76,7 +78,7 @@ constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
 constexpr uint32_t T_DH = T_RA, T_CH = T_RA + 64, T_Y = T_RA, T_D1 = T_RA + 64;
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, B_DBD, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sm->abort) break;
           if (publish) st_release_gpu(p.flags + ((bi * s.nc + c) * s.H + h - 1), 1);
           // the products that read head k-1's dS from the H tiles (Y, dB) are done
-          wait_bar(&bars[B_G4], uint32_t((k - 1) & 1), p.err);
+          wait_bar(&bars[B_DBD], uint32_t((k - 1) & 1), p.err);
           if (sm->abort) break;
         }
         // the state tile entering the chunk, saved by the forward as the bf16 hi | lo pair of
@@ -463,18 +465,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma::mma_commit(&bars[B_CH]);
         wait_bar(&bars[E_DS0 + st], uint32_t((k >> 1) & 1), p.err);  // dHscan read; dS and w o x in smem
         umma::fence_after_sync();
-        // Y = B dS^T  (M = t, N = p, K = n); dS stored [n][p]
-        for (int kk = 0; kk < kN; kk += 16)
-          umma::mma_bf16(tmem + T_Y, kdesc(aB, 16384, kk), mdesc(aHh, 16384, kk), id_km64, kk > 0);
-        // dB += (w o x) dS  (M = t, N = n, K = p)
-        for (int kk = 0; kk < kP; kk += 16)
-          umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), kdesc(aHh, 16384, kk), id_kk128, (k > 0) || (kk > 0));
+        // Y = B (dS_hi + dS_lo)^T  (M = t, N = p, K = n); dS stored [n][p]
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < kN; kk += 16)
+            umma::mma_bf16(tmem + T_Y, kdesc(aB, 16384, kk), mdesc(part ? aHl : aHh, 16384, kk), id_km64,
+                           (part > 0) || (kk > 0));
         wait_bar(&bars[E_CHR], par, p.err);  // CH read and g in fp16: D1 into CH's columns
         umma::fence_after_sync();
         // D1 = M^T g  (fp16 scaled operands; M = s, N = p, K = t)
         for (int kk = 0; kk < kQ; kk += 16)
           umma::mma_bf16(tmem + T_D1, mdesc(aM16, 16384, kk), mdesc(aG, 16384, kk), id_f16_mm64, kk > 0);
         umma::mma_commit(&bars[B_G4]);
+        // dB += (w o x) dS_hi  (M = t, N = n, K = p): read only at the unit's end, so issued
+        // after the products the epilogue waits for (its own barrier frees the H tiles)
+        for (int kk = 0; kk < kP; kk += 16)
+          umma::mma_bf16(tmem + T_DB, kdesc(aGh, 16384, kk), kdesc(aHh, 16384, kk), id_kk128, (k > 0) || (kk > 0));
+        umma::mma_commit(&bars[B_DBD]);
       }
       wait_bar(&bars[E_WSUM], 0, p.err);
       umma::fence_after_sync();
@@ -770,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the warps and CTAs get there
       if (p.atomic && lane == 0) atomicAdd(p.dA + h, eE * hdot * sm->red[36 + (k & 1)]);
 
-      ewait(&bars[B_CH], par, p.err);   // C H done: H (hi tile) may now give way to dS
+      ewait(&bars[B_CH], par, p.err);   // C H done: both H tiles may now give way to dS
       umma::fence_after_sync();
       {
         float d8[8];
@@ -778,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 2; ++u) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) d8[i] = ds[8 * u + i];
-          st8_bf16(sm_base + OFF_HD, n, 16 * cq + 8 * u, d8);  // dS -> bf16 [n][p]
+          st8_bf16_hilo(sm_base + OFF_HD, sm_base + OFF_HD + 16384, n, 16 * cq + 8 * u, d8);  // [n][p] hi | lo
         }
       }
       umma::fence_proxy_async_smem();

@@ -650,6 +650,81 @@ cudaError_t fused_fwd(const Shape &s, const Args &a, void *ws, cudaStream_t st) 
 }
 
 // ---------------------------------------------------------------------------
+// dstate 128, chunk length a larger multiple of 128: the kernels above in
+// 128-token chunks.  The chunked form is exact for any chunk length (the
+// state entering a chunk and every per-token result are those of the
+// token-by-token recurrence), so only the saved states differ: one per 128
+// tokens here, packed, kept in the workspace (`aux`) for the backward, and
+// the caller's buffer gets the fp32 (b, nc, H, P, N) states entering each of
+// its chunks (every ratio-th of them).
+namespace {
+
+struct Chunk128Ws {
+  float *aux;    // packed states (b, T / 128, H) tiles of P x 128
+  void *inner;   // the 128-token forward's workspace (its status word first)
+};
+
+Chunk128Ws carve_chunk128(Carver &cv, const Shape &s) {
+  const Shape h = fused_chunk128_shape(s);
+  Chunk128Ws w;
+  w.aux = cv.take<float>(h.b * h.nc * h.H * kP * kN);
+  w.inner = cv.take<char>(int64_t(fused_fwd_workspace(h)));
+  return w;
+}
+
+// fp32 state entering caller chunk c (the packed tile of 128-token chunk
+// c * ratio); one CTA per (b, caller chunk, head)
+__global__ void __launch_bounds__(256) chunk_states_view_kernel(Shape s, int ratio, const float *__restrict__ aux,
+                                                                float *__restrict__ out) {
+  __shared__ float t[64][129];
+  const int64_t tile = blockIdx.x;   // (b * nc + c) * H + h
+  const int64_t h = tile % s.H, c = tile / s.H % s.nc, bi = tile / (s.H * s.nc);
+  const int64_t nch = s.T / kQ;
+  const uint8_t *in = reinterpret_cast<const uint8_t *>(aux + ((bi * nch + c * ratio) * s.H + h) * (kP * kN));
+  unpack_state_tile(in, out + tile * (kP * kN), kN, t);
+}
+
+}  // namespace
+
+Shape fused_chunk128_shape(const Shape &s) {
+  Shape h = s;
+  h.Q = kQ;
+  h.nc = s.T / kQ;
+  return h;
+}
+
+bool fused_chunk128_supported(const Shape &s, bool bf16) {
+  return s.Q > kQ && s.Q % kQ == 0 && s.T % kQ == 0 && fused_bwd_supported(fused_chunk128_shape(s), bf16);
+}
+
+size_t fused_fwd_chunk128_workspace(const Shape &s) {
+  Carver cv(nullptr);
+  carve_chunk128(cv, s);
+  return cv.bytes();
+}
+
+float *fused_chunk128_aux(const Shape &s, void *ws) {
+  Carver cv(ws);
+  return carve_chunk128(cv, s).aux;
+}
+
+int *fused_fwd_chunk128_status(const Shape &s, void *ws) {
+  Carver cv(ws);
+  return fused_fwd_status(fused_chunk128_shape(s), carve_chunk128(cv, s).inner);
+}
+
+cudaError_t fused_fwd_chunk128(const Shape &s, const Args &a, void *ws, cudaStream_t st) {
+  Carver cv(ws);
+  const Chunk128Ws w = carve_chunk128(cv, s);
+  Args ai = a;
+  ai.states_out = w.aux;
+  cudaError_t err = fused_fwd(fused_chunk128_shape(s), ai, w.inner, st);
+  if (err != cudaSuccess || !a.states_out) return err;
+  chunk_states_view_kernel<<<unsigned(s.b * s.nc * s.H), 256, 0, st>>>(s, int(s.Q / kQ), w.aux, a.states_out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // dstate 256 (one group), chunk 128 or 256: the recurrence never mixes state
 // dimensions, so the scan is the sum of two scans over the state halves
 // n < 128 and n >= 128 (B, C split the same way), with D counted once.  Each

@@ -57,6 +57,20 @@ cudaError_t fused_bwd_split(const Shape &s, const Args &a, void *ws, const Fused
                             Trace &tr);
 cudaError_t fused_bwd(const Shape &s, const Args &a, void *ws, const FusedOptions &opt, cudaStream_t st, Trace &tr);
 
+// dstate 128 with a chunk length that is a larger multiple of 128 (the 256 of
+// Mamba2's defaults, for one): y, the gradients and the state entering each
+// chunk do not depend on the chunk length, so the kernels above run the
+// problem in 128-token chunks (fused_chunk128_shape).  The forward keeps their
+// packed states (one per 128 tokens) in its workspace (fused_chunk128_aux),
+// which the backward reads; the caller's state buffer gets the fp32 states
+// entering each of the caller's chunks.
+bool fused_chunk128_supported(const Shape &s, bool bf16);
+Shape fused_chunk128_shape(const Shape &s);
+size_t fused_fwd_chunk128_workspace(const Shape &s);
+float *fused_chunk128_aux(const Shape &s, void *ws);
+int *fused_fwd_chunk128_status(const Shape &s, void *ws);
+cudaError_t fused_fwd_chunk128(const Shape &s, const Args &a, void *ws, cudaStream_t st);
+
 // Packed batches (batch 1, seq_idx) whose sequences may start inside a chunk:
 // the token stream is cut at every sequence start and every 128 tokens, each
 // piece padded to a 128-token chunk with tokens that leave the state and all

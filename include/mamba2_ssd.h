@@ -88,9 +88,9 @@ typedef struct {
  * says; decay terms never cross a sequence start.  The fused kernels reset
  * states at chunk starts only, so these dims run them on a padded copy of the
  * problem (mamba2_ssd_padded_chunks) when they are bf16 with batch 1,
- * headdim 64, nseq - 1 <= ceil(seqlen / 128), and either chunk 128 and
- * dstate 128 ("fused-padded") or one group, an even head count, chunk 128 or
- * 256 and dstate 256 ("fused-split-padded"); seqlen need not be a multiple
+ * headdim 64, nseq - 1 <= ceil(seqlen / 128), a chunk that is a multiple of
+ * 128, and either dstate 128 ("fused-padded") or one group, an even head
+ * count and dstate 256 ("fused-split-padded"); seqlen need not be a multiple
  * of the chunk there.  Every other such shape runs the general CUDA-core
  * kernels. */
 #define SSD_DIMS_SEQ_ANY_START 2
@@ -110,7 +110,9 @@ typedef struct {
   const float *states;        /* (b,nc,H,P,N) states entering each chunk (packed on the fused shapes;
                                  see mamba2_ssd_fwd and mamba2_ssd_states_unpack) */
   const float *aux;           /* dstate-256 fused shapes: the packed states of both state halves, inside
-                                 the forward's workspace; "-padded" shapes: the forward's workspace itself
+                                 the forward's workspace; "fused-chunk128" shapes: the packed states of
+                                 every 128 tokens, inside the forward's workspace; "-padded" shapes: the
+                                 forward's workspace itself
                                  (the padded problem); either must then stay alive and unmodified until
                                  the backward has run; NULL otherwise */
   uint32_t magic;
@@ -140,8 +142,12 @@ size_t mamba2_ssd_bwd_workspace_size(const ssd_dims *dims, int config, int varia
  * fused kernels run once per 128-wide state half, in 128-token chunks, and
  * the halves' contributions are summed in a fixed order) run the fused
  * tensor-core forward and backward (with SSD_DIMS_SEQ_ANY_START set, the
- * "-padded" forms of both, see there); every other shape runs the general
- * CUDA-core ones. */
+ * "-padded" forms of both, see there).  bf16, headdim 64, dstate 128 and a
+ * chunk that is a larger multiple of 128 (256, as in Mamba2's defaults), with
+ * seqlen a multiple of 128 ("fused-chunk128/..."), run the same fused kernels
+ * in 128-token chunks: y, every gradient and the state entering each chunk
+ * are those of the recurrence whatever the chunk length.  Every other shape
+ * runs the general CUDA-core forward and backward. */
 int mamba2_ssd_num_configs(const ssd_dims *dims);
 
 /* Name of the backward algorithm a configuration selects (static string). */
@@ -172,9 +178,10 @@ const char *mamba2_ssd_bwd_launch_name(const ssd_dims *dims, int config, int var
  * swizzled tensor-core operand layout (row n at n*128 bytes, its 16-byte
  * chunk j at position j ^ (n % 8)), hi first -- the operand the fused
  * backward copies straight into shared memory.  mamba2_ssd_states_unpack
- * gives the fp32 (b,nc,H,P,N) view of either form.  On the "fused-split"
- * and "-padded" shapes `states` holds the fp32 states themselves and the
- * packed ones (and, padded, the padded copies of x, dt, B, C and seq_idx)
+ * gives the fp32 (b,nc,H,P,N) view of either form.  On the "fused-split",
+ * "fused-chunk128" and "-padded" shapes `states` holds the fp32 states
+ * themselves and the packed ones (and, padded, the padded copies of x, dt, B,
+ * C and seq_idx)
  * stay in the workspace, which must then live, unmodified, until the backward
  * (ssd_saved.aux).  *saved_out (host struct) filled for the backward.
  * workspace: >= fwd_workspace_size bytes. */

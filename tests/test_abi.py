@@ -287,3 +287,25 @@ def test_fwd_check_on_host(L):
     assert L.mamba2_ssd_fwd_check(ctypes.byref(simt), None, None) == 1
     bad = ssd.make_dims(1, 256, 3, 16, 2, 16, 64)   # heads not a multiple of groups
     assert L.mamba2_ssd_fwd_check(ctypes.byref(bad), ctypes.c_void_p(FAKE), None) == 1
+
+
+def test_longer_chunks_with_dstate_128_run_the_fused_kernels_in_128_token_chunks(L):
+    base = ssd.make_dims(1, 2048, 8, 64, 2, 128, 128)
+    for Q in (256, 512, 1024):
+        d = ssd.make_dims(1, 2048, 8, 64, 2, 128, Q)
+        assert ssd.config_name(d, 0) == "fused-chunk128/ring4" and ssd.config_name(d, 1) == "fused-chunk128/ring2"
+        assert ssd.bwd_launch_names(d) == ["fused_bwd", "fold_scalars"]
+        assert ssd.bwd_launch_names(d, 0, 1) == ["fused_bwd_atomic"]
+        # the backward is that of the same problem in 128-token chunks
+        assert ssd.bwd_workspace_size(d, 0, 0) == ssd.bwd_workspace_size(base, 0, 0)
+        # the forward keeps the packed state of every 128 tokens besides the 128-token forward's workspace
+        assert ssd.fwd_workspace_size(d) >= ssd.fwd_workspace_size(base) + 16 * 8 * 64 * 128 * 4
+        assert ssd.bwd_workspace_size(d, 0, 2) == 0   # no ordered variant on the fused kernels
+    # seqlen not a multiple of 128, a chunk that is not a multiple of 128, fp32: the general path
+    for d in (ssd.make_dims(1, 2000, 8, 64, 2, 128, 256), ssd.make_dims(1, 2048, 8, 64, 2, 128, 192),
+              ssd.make_dims(1, 2048, 8, 64, 2, 128, 256, dtype=torch.float32)):
+        assert ssd.config_name(d, 0).startswith("simt"), d
+    # sequence starts inside a chunk of 256: the padded form, whose chunks are 128 tokens anyway
+    d = ssd.make_dims(1, 2048, 8, 64, 2, 128, 256, nseq=3, seq_idx=True, any_start=True)
+    assert ssd.config_name(d, 0) == "fused-padded/0"
+    assert L.mamba2_ssd_padded_chunks(ctypes.byref(d)) == 16 + 2

@@ -79,6 +79,7 @@ def test_atomic_variant_shows_the_test_has_teeth(name):
 @pytest.mark.parametrize("case", [
     dict(T=300, H=8, P=32, G=2, N=64, Q=64, path="simt"),
     dict(T=512, H=8, P=64, G=2, N=128, Q=128, path="fused/"),
+    dict(T=640, H=8, P=64, G=2, N=128, Q=256, path="fused-chunk128/"),
     dict(T=512, H=8, P=64, G=1, N=256, Q=256, path="fused-split/"),
     dict(T=500, H=4, P=64, G=1, N=128, Q=128, path="fused-padded/", lens=(100, 300, 100)),
     dict(T=700, H=8, P=64, G=1, N=256, Q=256, path="fused-split-padded/", lens=(99, 1, 600)),

@@ -90,10 +90,15 @@ struct RowVec<2> {
 
 // fa(r, k) = A(r, k), fb(q, k) = B(q, k) (0 outside their ranges);
 // kAKFast / kBKFast: consecutive k adjacent in memory (else consecutive r, q),
-// which picks the thread order of the loads so that they coalesce.
+// which picks the thread order of the loads so that they coalesce.  Only k in
+// [kb, K) is visited: a causal product whose terms outside that window are
+// exact zeros for every row of the tile passes the window, which drops only
+// zero terms at the start or the end of each ascending chain (an accumulator
+// that starts at +0 stays +0 across them, and x + 0 = x), so the bits are those
+// of the full range.
 template <int RA, bool kAKFast, bool kBKFast, class FA, class FB>
 __device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, TileBuf<RA> &sb,
-                                        float (&acc)[RA][4]) {
+                                        float (&acc)[RA][4], int64_t kb = 0) {
   constexpr int R = 16 * RA;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
 #pragma unroll
@@ -118,8 +123,8 @@ __device__ __forceinline__ void tile_mm(int64_t K, const FA &fa, const FB &fb, T
       rb[u] = (k0 + kk < K) ? fb(q, k0 + kk) : 0.f;
     }
   };
-  if (K > 0) fetch(0);
-  for (int64_t k0 = 0; k0 < K; k0 += kTK) {
+  if (K > kb) fetch(kb);
+  for (int64_t k0 = kb; k0 < K; k0 += kTK) {
 #pragma unroll
     for (int u = 0; u < NA; ++u) {
       const int e = u * kTileThreads + tid;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kTileThreads, 3)
   const int64_t HP = s.H * s.P, GN = s.G * s.N;
   float acc[4][4], inter[4][4];
   tile_mm<4, true, false>(
-      Lc,
+      min(Lc, i0 + 64),   // (j <= i: the tile's rows see no token after its last row)
       [&](int r, int64_t j) {
         const int64_t i = i0 + r;
         if (i >= Lc || j > i || j < fr[r]) return 0.f;
@@ -619,7 +624,8 @@ __global__ void __launch_bounds__(kTileThreads, 3)
   float d1[4][4], yv[4][4];
   tile_mm<4, false, false>(
       Lc, [&](int r, int64_t j) { const int64_t i = i0 + r; return i < Lc ? M[j * s.Q + i] : 0.f; },
-      [&](int q, int64_t j) { const int64_t p = p0 + q; return p < s.P ? ld(gc + j * HP + p) : 0.f; }, sb, d1);
+      [&](int q, int64_t j) { const int64_t p = p0 + q; return p < s.P ? ld(gc + j * HP + p) : 0.f; }, sb, d1,
+      i0);   // (M[j][i] = 0 for j < i: no row of the tile takes a token before its first row)
   tile_mm<4, true, true>(
       s.N, [&](int r, int64_t n) { const int64_t i = i0 + r; return i < Lc ? ld(bc + i * GN + n) : 0.f; },
       [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? ds[p * s.N + n] : 0.f; }, sb, yv);
@@ -672,7 +678,8 @@ __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict_
     const TIn *gc = dout + ((bi * s.T + t0) * s.H + h) * s.P;
     const float *hst = states + unit * s.P * s.N;
     tile_mm<RA, true, false>(
-        Lc, [&](int r, int64_t j) { return row_ok(r) ? W[(i0 + r) * s.Q + j] : 0.f; },
+        min(Lc, i0 + 16 * RA),   // (W[i][j] = 0 for j > i)
+        [&](int r, int64_t j) { return row_ok(r) ? W[(i0 + r) * s.Q + j] : 0.f; },
         [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(bc + j * GN + n) : 0.f; }, sb, res);
     tile_mm<RA, true, false>(
         s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(gc + (i0 + r) * HP + p) : 0.f; },
@@ -705,7 +712,8 @@ __device__ __forceinline__ void dbdc_tile(const Shape &s, const TIn *__restrict_
     const float *ds = dS + unit * s.P * s.N;
     tile_mm<RA, false, false>(
         Lc, [&](int r, int64_t j) { return row_ok(r) ? W[j * s.Q + i0 + r] : 0.f; },
-        [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(cc + j * GN + n) : 0.f; }, sb, res);
+        [&](int q, int64_t j) { const int64_t n = n0 + q; return n < s.N ? ld(cc + j * GN + n) : 0.f; }, sb, res,
+        i0);   // (W[j][i] = 0 for j < i)
     tile_mm<RA, true, false>(
         s.P, [&](int r, int64_t p) { return row_ok(r) ? ld(xc + (i0 + r) * HP + p) : 0.f; },
         [&](int q, int64_t p) { const int64_t n = n0 + q; return n < s.N ? ds[p * s.N + n] : 0.f; }, sb, t1);

@@ -754,19 +754,26 @@ def main():
             serial_ms, serial_med = run_steps(src, sets, args.steps, True, with_fwd)
             serial_ms = max_over_ranks(serial_ms, world, dev)
             h2d = sum(v.numel() * v.element_size() for v in src.values())
+            # the gradients the last steps copied back to the host equal the device-timed run's,
+            # bit for bit (both buffer sets)
+            same = None if ref_host is None else all(
+                torch.equal(bs["host_out"][k].view(torch.int32), ref_host[k].view(torch.int32))
+                for bs in sets for k in ref_host)
             del sets
             # value from the mean over all steps; the medians show how much of it comes from
             # occasional stalls of the host copies (steps of 80-200 ms seen on a shared machine)
             return {"value": world * tokens / (pipe_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms, "pipelined": True,
                     "ms_per_step_median": pipe_med, "serial_ms_per_step": serial_ms,
-                    "serial_ms_per_step_median": serial_med}
+                    "serial_ms_per_step_median": serial_med, "bitwise_equal_to_device_run": same}
 
+        # (the end-to-end steps run the deterministic variant)
+        ref_host = {k: v.detach().cpu() for k, v in out.items()} if args.variant == 0 else None
         e2e = measure(False)
         e2e["calls_per_step"] = "mamba2_ssd_fwd + mamba2_ssd_bwd"
         e2e["states_from_host"] = measure(True)
         e2e["states_from_host"]["calls_per_step"] = "mamba2_ssd_bwd (saved chunk states copied from the host)"
-        del host, host_states
+        del host, host_states, ref_host
 
     # the other workload presets (the 2K and 4K rows of the pages' tables, the packed
     # variable-length batch, and fp32 inputs on the general path), timed after the headline

@@ -222,8 +222,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "983dddb8f5311eaa2a0a36cf10b56b785d692c4532e48c4dc70c8a459835c224": {
-        "bytes_per_token": (2295961344 + 1259906304) / 16384,
+    "70a433e368824871923c1a0878f064291e19e8aaf8f1abd63cb8265d1ed7f18b": {
+        "bytes_per_token": (2288158464 + 1253845760) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

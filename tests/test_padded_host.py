@@ -70,14 +70,23 @@ CASES = [
     ((1, 128, 128, 128, 127), 128),       # every start inside a chunk: the bound is reached
     ((100, 300, 1, 111), 256),
     ((300, 212, 600), 256),
+    ((100, 300, 1, 111), (256, 128)),     # chunk 256 with dstate 128
+    ((5, 600, 3, 700), (512, 128)),       # chunk 512 with dstate 128
 ]
+
+
+def q_and_n(Q):
+    """(chunk, dstate) of a case: chunk 128 with dstate 128, chunk 256 with dstate 256, or as given."""
+    return Q if isinstance(Q, tuple) else (Q, 128 if Q == 128 else 256)
 
 
 @pytest.mark.parametrize("lens,Q", CASES)
 def test_piece_table_matches_the_segmentation(L, lens, Q):
     T = sum(lens)
     seq = seq_of(lens)
-    dims = fused_dims(T, len(lens), Q=Q, N=128 if Q == 128 else 256)
+    Q, N = q_and_n(Q)
+    dims = fused_dims(T, len(lens), Q=Q, N=N)
+    assert ssd.config_name(dims, 0).startswith("fused-padded" if N == 128 else "fused-split-padded")
     npc, start, ln, ids, cmap = piece_table(L, dims, seq)
     assert npc == (T + 127) // 128 + len(lens) - 1
     ref = pieces_by_hand(seq)

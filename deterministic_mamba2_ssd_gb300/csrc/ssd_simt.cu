@@ -605,10 +605,11 @@ __global__ void dinit_mid_kernel(Shape s, const TIn *__restrict__ dout, const TI
 // of (i, p).
 template <class TIn>
 __global__ void __launch_bounds__(kTileThreads, 3)
-    dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ Bm, const float *__restrict__ dt,
-              const float *__restrict__ D, const float *__restrict__ Mm, const float *__restrict__ dS,
-              const float *__restrict__ acs_hi, const float *__restrict__ acs_lo, const int32_t *__restrict__ seq_idx,
-              const int32_t *__restrict__ first, float *__restrict__ dx) {
+    dx_kernel(Shape s, const TIn *__restrict__ dout, const TIn *__restrict__ x, const TIn *__restrict__ Bm,
+              const float *__restrict__ dt, const float *__restrict__ D, const float *__restrict__ Mm,
+              const float *__restrict__ dS, const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
+              const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first, float *__restrict__ dx,
+              float *__restrict__ sx_part) {
   __shared__ TileBuf<4> sb;
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
@@ -646,6 +647,27 @@ __global__ void __launch_bounds__(kTileThreads, 3)
       const int64_t idx = ((bi * s.T + t) * s.H + h) * s.P + p;
       dx[idx] = fmaf(dti, d1[a][b], fmaf(wi, yv[a][b], D[h] * ld(dout + idx)));
     }
+  }
+  // x . Y over this tile's head-dim columns, per token (the decay gradient's u
+  // term and ddt's state term take it): the thread's four columns in order,
+  // then a fixed xor tree over the 16 threads of the tile row; one partial per
+  // (token, column tile), summed in tile order by ddt_dacs_kernel
+  const int64_t ntp2 = cdiv(s.P, kTC);
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int64_t i = i0 + tile_row<4>(a);
+    float v = 0.f;
+    if (i < Lc) {
+      const TIn *xi = x + ((bi * s.T + t0 + i) * s.H + h) * s.P;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int64_t p = p0 + tile_col(b);
+        if (p < s.P) v = fmaf(ld(xi + p), yv[a][b], v);
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 15) == 0 && i < s.Q) sx_part[(unit * ntp2 + p0 / kTC) * s.Q + i] = v;
   }
 }
 
@@ -891,18 +913,18 @@ __global__ void __launch_bounds__(kTileThreads, 3)
                     const float *__restrict__ colp, const float *__restrict__ dg, const float *__restrict__ states,
                     const float *__restrict__ dS, const float *__restrict__ acs_hi, const float *__restrict__ acs_lo,
                     const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
-                    const float *__restrict__ init, float *__restrict__ ddt_part, float *__restrict__ dAcs,
-                    float *__restrict__ u_buf, float *__restrict__ gx_buf, float *__restrict__ vin_buf) {
+                    const float *__restrict__ init, const float *__restrict__ sx_part, float *__restrict__ ddt_part,
+                    float *__restrict__ dAcs, float *__restrict__ u_buf, float *__restrict__ gx_buf,
+                    float *__restrict__ vin_buf) {
   __shared__ TileBuf<4> sb;
-  __shared__ float chs[64][kTC + 1], ys[64][kTC + 1];
+  __shared__ float chs[64][kTC + 1];
   const int64_t unit = blockIdx.x;  // (b, c, h)
   const int64_t h = unit % s.H, c = (unit / s.H) % s.nc, bi = unit / (s.H * s.nc);
   const int64_t t0 = c * s.Q, Lc = min(s.Q, s.T - t0), g = h / s.hpg;
   const int64_t i0 = int64_t(blockIdx.y) * 64;
   const int64_t GN = s.G * s.N;
   const TIn *cc = Cm + ((bi * s.T + t0) * s.G + g) * s.N;
-  const TIn *bc = Bm + ((bi * s.T + t0) * s.G + g) * s.N;
-  const float *hst = states + unit * s.P * s.N, *ds = dS + unit * s.P * s.N;
+  const float *hst = states + unit * s.P * s.N;
   // this thread's token and quarter of the state columns
   const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
   const int64_t i = i0 + r, t = t0 + i;
@@ -924,13 +946,6 @@ __global__ void __launch_bounds__(kTileThreads, 3)
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) chs[tile_row<4>(a)][tile_col(b)] = acc[a][b];
-      tile_mm<4, true, true>(
-          s.N, [&](int rr, int64_t n) { const int64_t ii = i0 + rr; return ii < Lc ? ld(bc + ii * GN + n) : 0.f; },
-          [&](int q, int64_t n) { const int64_t p = p0 + q; return p < s.P ? ds[p * s.N + n] : 0.f; }, sb, acc);
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) ys[tile_row<4>(a)][tile_col(b)] = acc[a][b];
       __syncthreads();
       if (mine) {
         const int64_t pe = min(int64_t(kTC), s.P - p0);
@@ -944,7 +959,6 @@ __global__ void __launch_bounds__(kTileThreads, 3)
           }
           const float gp = ld(gi + p), xp = ld(xi + p);
           inter = fmaf(gp, hc, inter);
-          sx = fmaf(xp, ys[r][pp], sx);
           gx = fmaf(gp, xp, gx);
         }
       }
@@ -953,10 +967,8 @@ __global__ void __launch_bounds__(kTileThreads, 3)
   }
   // the four quarters of each token (lanes 4 r .. 4 r + 3 of one warp), fixed tree
   inter += __shfl_xor_sync(0xffffffffu, inter, 1);
-  sx += __shfl_xor_sync(0xffffffffu, sx, 1);
   gx += __shfl_xor_sync(0xffffffffu, gx, 1);
   inter += __shfl_xor_sync(0xffffffffu, inter, 2);
-  sx += __shfl_xor_sync(0xffffffffu, sx, 2);
   gx += __shfl_xor_sync(0xffffffffu, gx, 2);
   if (part != 0 || i >= s.Q) return;
   const int64_t idx = ((bi * s.H + h) * s.nc + c) * s.Q + i;
@@ -974,6 +986,9 @@ __global__ void __launch_bounds__(kTileThreads, 3)
     col += colp[(unit * nt + k) * s.Q + i];
   }
   const float diag = dg[unit * s.Q + i];
+  // x . Y: the per-column-tile partials of dx_kernel, in tile order
+  const int64_t ntp = cdiv(s.P, kTC);
+  for (int64_t k = 0; k < ntp; ++k) sx += sx_part[(unit * ntp + k) * s.Q + i];
   const float *dtc = dt + (bi * s.T + t0) * s.H + h;  // dtc[j * H]
   const float dti = dtc[i * s.H];
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
@@ -1071,7 +1086,7 @@ __global__ void reduce_heads_scalars_kernel(Shape s, const float *__restrict__ d
 
 struct BwdWs {
   int *status;   // [0] error bits (bit 1: an ordered-fold wait gave up), [1] ticket; first in the workspace
-  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *rowp, *colp, *dg, *buf, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
+  float *acs_hi, *acs_lo, *CB, *Mm, *Wm, *rowp, *colp, *dg, *sx_part, *buf, *dEpass, *dAcs, *u, *gx, *vin, *ddt_part, *dA_part,
       *dD_part, *slot_b, *slot_c;
   int32_t *first;
   int *sem;
@@ -1093,6 +1108,7 @@ BwdWs carve_bwd(Carver &cv, const Shape &s, int variant) {
   w.rowp = cv.take<float>(parts);
   w.colp = cv.take<float>(parts);
   w.dg = cv.take<float>(s.b * s.nc * s.H * s.Q);
+  w.sx_part = cv.take<float>(s.b * s.nc * s.H * cdiv(s.P, kTC) * s.Q);
   w.buf = cv.take<float>(s.b * s.nc * s.H * s.P * s.N);
   w.dEpass = cv.take<float>(s.b * s.H * s.nc * cdiv(s.P * s.N, kPassSlice));
   w.dAcs = cv.take<float>(acs);
@@ -1220,8 +1236,8 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
     tr.mark(st);
   }
   tr.mark(st);
-  dx_kernel<TIn><<<dim3(nbch, tiles_qp), kTileThreads, 0, st>>>(s, g, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi, w.acs_lo,
-                                                                a.seq_idx, first, a.dx);
+  dx_kernel<TIn><<<dim3(nbch, tiles_qp), kTileThreads, 0, st>>>(s, g, x, Bm, a.dt, a.D, w.Mm, w.buf, w.acs_hi,
+                                                                w.acs_lo, a.seq_idx, first, a.dx, w.sx_part);
   tr.mark(st);
   if (atomic) {
     tr.mark(st);
@@ -1249,8 +1265,8 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   }
   tr.mark(st);
   ddt_dacs_kernel<TIn><<<dim3(nbch, unsigned(cdiv(s.Q, 64))), kTileThreads, 0, st>>>(
-      s, x, g, Bm, Cm, a.dt, w.rowp, w.colp, w.dg, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.ddt_part,
-      w.dAcs, w.u, w.gx, w.vin);
+      s, x, g, Bm, Cm, a.dt, w.rowp, w.colp, w.dg, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init,
+      w.sx_part, w.ddt_part, w.dAcs, w.u, w.gx, w.vin);
   tr.mark(st);
   if (atomic) {
     tr.mark(st);

@@ -797,7 +797,10 @@ __global__ void __launch_bounds__(kTileThreads, 3)
     }
 }
 
-constexpr int kOrdTile = 32;   // tokens per tile of the ordered dB/dC fold
+// Tokens per tile of the ordered dB/dC fold: 64 (the slot path's tile, four
+// rows a thread) where the tile's rows of dB and dC (2 x 64 x dstate fp32) fit
+// three CTAs an SM, else 32.  The tile shape does not change any output's bits.
+inline int ord_tile(const Shape &s) { return s.N <= 128 ? 64 : 32; }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
   int v;
@@ -817,8 +820,8 @@ __device__ __forceinline__ void st_release_gpu(int *p, int v) {
 // the tile's semaphore reads k (a bounded spin: past spin_limit polls it sets
 // status bit 1 and skips its add), then stores (k = 0) or adds its rows into
 // dB/dC, and releases the semaphore to k + 1.
-template <class TIn>
-__global__ void __launch_bounds__(kTileThreads)
+template <class TIn, int OT>
+__global__ void __launch_bounds__(kTileThreads, 2)
     dbdc_ordered_kernel(Shape s, const TIn *__restrict__ x, const TIn *__restrict__ dout, const TIn *__restrict__ Bm,
                         const TIn *__restrict__ Cm, const float *__restrict__ dt, const float *__restrict__ Wm,
                         const float *__restrict__ states, const float *__restrict__ dS,
@@ -826,38 +829,38 @@ __global__ void __launch_bounds__(kTileThreads)
                         const int32_t *__restrict__ seq_idx, const int32_t *__restrict__ first,
                         const float *__restrict__ init, int *__restrict__ status, int *__restrict__ sem,
                         uint32_t spin_limit, float *__restrict__ dBo, float *__restrict__ dCo) {
-  extern __shared__ float tile[];   // [2][kOrdTile][N]: dB rows then dC rows
-  __shared__ TileBuf<kOrdTile / 16> sb;
-  __shared__ int fr[kOrdTile];
+  extern __shared__ float tile[];   // [2][OT][N]: dB rows then dC rows
+  __shared__ TileBuf<OT / 16> sb;
+  __shared__ int fr[OT];
   __shared__ int s_unit, s_go;
   if (threadIdx.x == 0) s_unit = atomicAdd(status + 1, 1);
   __syncthreads();
-  const int64_t ntt = cdiv(s.Q, kOrdTile);
+  const int64_t ntt = cdiv(s.Q, OT);
   const int64_t unit = s_unit;
   const int64_t k = unit % s.hpg, tileid = unit / s.hpg;
   const int64_t tt = tileid % ntt, g = (tileid / ntt) % s.G, c = (tileid / (ntt * s.G)) % s.nc;
   const int64_t bi = tileid / (ntt * s.G * s.nc);
   const int64_t h = g * s.hpg + k, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);
-  const int64_t i0 = tt * kOrdTile, i1 = min(Lc, i0 + kOrdTile);
-  for (int r = threadIdx.x; r < kOrdTile; r += blockDim.x)
+  const int64_t i0 = tt * OT, i1 = min(Lc, i0 + OT);
+  for (int r = threadIdx.x; r < OT; r += blockDim.x)
     fr[r] = i0 + r < Lc ? int(local_start(seq_idx, first, bi, s.T, t0 + i0 + r, t0)) : 0;
   __syncthreads();
   const int64_t fe = local_start(seq_idx, first, bi, s.T, t0 + Lc - 1, t0);
   if (i0 < Lc) {   // (the whole CTA)
     for (int64_t n0 = 0; n0 < s.N; n0 += kTC) {
-      float dcv[kOrdTile / 16][4], dbv[kOrdTile / 16][4];
-      dbdc_tile<false, kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
+      float dcv[OT / 16][4], dbv[OT / 16][4];
+      dbdc_tile<false, OT / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
                                            c, h, i0, n0, fr, fe, sb, dcv);
-      dbdc_tile<true, kOrdTile / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
+      dbdc_tile<true, OT / 16, TIn>(s, x, dout, Bm, Cm, dt, Wm, states, dS, acs_hi, acs_lo, seq_idx, init, bi,
                                           c, h, i0, n0, fr, fe, sb, dbv);
 #pragma unroll
-      for (int a = 0; a < kOrdTile / 16; ++a)
+      for (int a = 0; a < OT / 16; ++a)
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          const int64_t r = tile_row<kOrdTile / 16>(a), n = n0 + tile_col(b);
+          const int64_t r = tile_row<OT / 16>(a), n = n0 + tile_col(b);
           if (n >= s.N) continue;
           tile[r * s.N + n] = dbv[a][b];
-          tile[kOrdTile * s.N + r * s.N + n] = dcv[a][b];
+          tile[OT * s.N + r * s.N + n] = dcv[a][b];
         }
     }
   }
@@ -883,7 +886,7 @@ __global__ void __launch_bounds__(kTileThreads)
   for (int64_t e = threadIdx.x; e < (i1 - i0) * s.N; e += blockDim.x) {
     const int64_t i = i0 + e / s.N, n = e % s.N;
     const int64_t o = ((bi * s.T + t0 + i) * s.G + g) * s.N + n;
-    const float db = tile[e], dc = tile[kOrdTile * s.N + e];
+    const float db = tile[e], dc = tile[OT * s.N + e];
     dBo[o] = (k == 0 ? 0.f : dBo[o]) + db;   // 0 + s0 + s1 + ..., as the slot fold adds
     dCo[o] = (k == 0 ? 0.f : dCo[o]) + dc;
   }
@@ -1092,7 +1095,7 @@ struct BwdWs {
   int *sem;
 };
 
-int64_t ordered_tiles(const Shape &s) { return s.b * s.nc * s.G * cdiv(s.Q, kOrdTile); }
+int64_t ordered_tiles(const Shape &s) { return s.b * s.nc * s.G * cdiv(s.Q, ord_tile(s)); }
 
 BwdWs carve_bwd(Carver &cv, const Shape &s, int variant) {
   const bool atomic = variant == 1, ordered = variant == 2;
@@ -1247,14 +1250,15 @@ cudaError_t bwd_impl(const Shape &s, const Args &a, void *ws, int bs, int varian
   } else if (ordered) {
     tr.mark(st);
     const int64_t units = ordered_tiles(s) * s.hpg;
-    const size_t shm = size_t(2 * kOrdTile * s.N) * sizeof(float);
+    const int ot = ord_tile(s);
+    const size_t shm = size_t(2 * ot * s.N) * sizeof(float);
     // (the kernel's static tile buffers come on top of this)
-    if ((err = cudaFuncSetAttribute(dbdc_ordered_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(shm))) != cudaSuccess)
+    auto kern = ot == 64 ? dbdc_ordered_kernel<TIn, 64> : dbdc_ordered_kernel<TIn, 32>;
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(shm))) != cudaSuccess)
       return err;
-    dbdc_ordered_kernel<TIn><<<unsigned(units), kTileThreads, shm, st>>>(
-        s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi, w.acs_lo, a.seq_idx, first, a.init, w.status,
-        w.sem, spin_limit, a.dB, a.dC);
+    kern<<<unsigned(units), kTileThreads, shm, st>>>(s, x, g, Bm, Cm, a.dt, w.Wm, a.states_in, w.buf, w.acs_hi,
+                                                     w.acs_lo, a.seq_idx, first, a.init, w.status, w.sem,
+                                                     spin_limit, a.dB, a.dC);
     tr.mark(st);
   } else {
     tr.mark(st);

@@ -837,7 +837,10 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   __syncthreads();
   const int64_t ntt = cdiv(s.Q, OT);
   const int64_t unit = s_unit;
-  const int64_t k = unit % s.hpg, tileid = unit / s.hpg;
+  // tickets head-major over the tiles: a head's predecessor on the same tile drew its ticket one
+  // sweep of the tiles earlier, so it has usually released the tile by the time this CTA waits
+  const int64_t ntiles = s.b * s.nc * s.G * ntt;
+  const int64_t k = unit / ntiles, tileid = unit % ntiles;
   const int64_t tt = tileid % ntt, g = (tileid / ntt) % s.G, c = (tileid / (ntt * s.G)) % s.nc;
   const int64_t bi = tileid / (ntt * s.G * s.nc);
   const int64_t h = g * s.hpg + k, t0 = c * s.Q, Lc = min(s.Q, s.T - t0);

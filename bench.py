@@ -672,7 +672,8 @@ def main():
     e2e = None
     if not args.no_e2e:
         host = {k: v.pin_memory() for k, v in d.items() if v is not None}
-        host_states = saved.states.cpu().pin_memory()
+        # (the states-from-host mode runs only where the backward reads the caller's state buffer)
+        host_states = None if saved.struct.aux else saved.states.cpu().pin_memory()
         d2h = sum(v.numel() * v.element_size() for v in out.values())
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 

@@ -73,6 +73,13 @@ typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
  * exists only to measure the cost of determinism. */
 typedef enum { SSD_VARIANT_DETERMINISTIC = 0, SSD_VARIANT_ATOMIC = 1, SSD_VARIANT_ORDERED = 2 } ssd_variant;
 
+/* Valid dims (every call checks them; the size queries return 0, the counts
+ * -1 or 0, the others SSD_ERR_INVALID_ARG): every size and nseq at least 1
+ * (an empty problem is rejected, not treated as a no-op), nheads a multiple
+ * of ngroups, chunk_size at most 1024, batch * nc * nheads below 2^31, with
+ * SSD_DIMS_SEQ_IDX seqlen and nseq below 2^31, dtype an ssd_dtype, and no
+ * flag bits but the SSD_DIMS_* ones (SSD_DIMS_SEQ_ANY_START only together
+ * with SSD_DIMS_SEQ_IDX). */
 typedef struct {
   int64_t batch, seqlen, nheads, headdim, ngroups, dstate, chunk_size;
   int64_t nseq;       /* rows of init_states / dinit: number of sequences (= batch without seq_idx) */

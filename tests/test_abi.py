@@ -56,7 +56,7 @@ def test_queries(L):
     assert L.mamba2_ssd_num_chunks(ctypes.byref(ragged)) == 16
 
 
-@pytest.mark.parametrize("field,value", [("batch", 0), ("seqlen", -1), ("nheads", 0), ("ngroups", 4),
+@pytest.mark.parametrize("field,value", [("batch", 0), ("seqlen", 0), ("seqlen", -1), ("nheads", 0), ("ngroups", 4),
                                          ("chunk_size", 0), ("chunk_size", 4096), ("dtype", 7),
                                          ("flags", 2), ("flags", 4), ("nseq", 0)])
 def test_invalid_dims_rejected(L, field, value):

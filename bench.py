@@ -222,8 +222,8 @@ def kernel_bytes(name, w, es):
 # whose SHA-256 is the key (see the profiles/ summaries).  A changed kernel has
 # no entry, and the bench then reports traffic as null until it is measured.
 FUSED_TRAFFIC_PER_TOKEN = {
-    "70a433e368824871923c1a0878f064291e19e8aaf8f1abd63cb8265d1ed7f18b": {
-        "bytes_per_token": (2288158464 + 1253845760) / 16384,
+    "f14fc64d3878896514b8dcb059c560d377437f5724f802b8126fe02dd7d1c162": {
+        "bytes_per_token": (2283115776 + 1239713024) / 16384,
         "capture": "bf16_T16384, one launch, dram__bytes_read.sum + dram__bytes_write.sum (1-pass ncu)",
     },
 }

@@ -25,7 +25,10 @@
 //
 // Roles (576 threads): warps 0-15 epilogue (thread = one row of a 128-row
 // tile and one quarter of its columns; the TMEM lane quadrant of a warp is
-// its index mod 4), warp 16 TMA producer, warp 17 TMEM owner and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
+// its index mod 4; the intra-chunk phase instead gives each warp 16 x 16
+// blocks of the causal triangle, two threads a row, over rows paired so that
+// every quadrant holds the same share of it), warp 16 TMA producer, warp 17
+// TMEM owner and MMA issuer.  Operand precision: bf16 operands, fp32 accumulation;
 // the one product whose rounding dominates the error (dx_intra = M^T g with
 // M = CB o L) runs in fp16 with exact power-of-two scaling of both operands,
 // and the head-summed intra-chunk matrix for dB/dC, G~, the saved state H and
@@ -74,13 +77,30 @@ constexpr uint32_t OFF_XBUF = OFF_GW + 16384;
 constexpr uint32_t OFF_WHI = OFF_XG, OFF_WLO = OFF_STG;
 
 // TMEM columns
-// RA holds, in turn: C B^T (unit start), g x^T, then dHscan^T (cols 0-63)
-// and C H (64-127), then Y (0-63) and D1 (64-127).  WS accumulates W.
+// RA holds, in turn: C B^T (unit start), g x^T, then dHscan^T (cols 64-127,
+// the half of g x^T the epilogue reads first) and C H (0-63), then Y (64-127)
+// and D1 (0-63).  WS accumulates W.
 constexpr uint32_t T_DB = 0, T_DC = 128, T_RA = 256, T_WS = 384;
-constexpr uint32_t T_DH = T_RA, T_CH = T_RA + 64, T_Y = T_RA, T_D1 = T_RA + 64;
+constexpr uint32_t T_DH = T_RA + 64, T_CH = T_RA, T_Y = T_RA + 64, T_D1 = T_RA;
+
+// Row order of the token tiles that the intra-chunk phase reads through TMEM
+// lanes: C, g, G~, the fp16 M and W are held with the 16-token group q in
+// rows (lanes) 32q..32q+15 and the group 7-q in rows 32q+16..32q+31, so that
+// the causal triangle of g x^T and C B^T spreads evenly over the four lane
+// quadrants, i.e. over the four SM sub-partitions (the quadrant holding tokens
+// 96-127 in natural order had 8 of the 20 column blocks).  x, B, w o x, H and
+// dS stay in natural order; every product pairs rows of one order along its
+// K dimension, so C B^T, g x^T, C H and dC come out with permuted lanes and
+// Y, D1, dHscan^T and dB with natural ones.
+__device__ __forceinline__ int tok_of_row(int l) {   // token held in row (lane) l
+  return ((l & 16) ? 7 - (l >> 5) : (l >> 5)) * 16 + (l & 15);
+}
+__host__ __device__ constexpr int row_of_tok(int t) {   // row (lane) holding token t
+  return ((t >> 4) < 4 ? 32 * (t >> 4) : 32 * (7 - (t >> 4)) + 16) + (t & 15);
+}
 
 enum Bar {
-  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, B_DSL, E_X16, B_G1, B_G1R, E_GXL, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, B_DBD, E_RA, E_WSUM, B_FIN,
+  B_BC, B_CB, E_CBREAD, B_XG, E_XG, B_H, B_DSL, E_X16, B_GX1, B_GX2, E_GX1, B_DHS, B_CH, E_M16, E_CHR, E_RING, E_DS0, E_DS1, B_G4, B_DBD, E_RA, E_WSUM, B_FIN,
   NBARS
 };
 
@@ -282,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_GXL || i == E_RING || i == E_DS0 || i == E_DS1) ? kEpiWarps : 1);  // per-warp arrivals
+    for (int i = 0; i < NBARS; ++i) umma::mbar_init(&bars[i], (i == E_CHR || i == E_GX1 || i == E_RING || i == E_DS0 || i == E_DS1) ? kEpiWarps : 1);  // per-warp arrivals
     umma::fence_mbar_init();
     sm->unit = atomicAdd(p.ticket, 1);
     sm->abort = 0;
@@ -315,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 2; ++j) {
         umma::tma_load_2d(sm_base + OFF_B + j * 16384, &tm_b, int((g >> kSliceShift) * kN + j * 64), int(row0),
                           &bars[B_BC]);
-        umma::tma_load_2d(sm_base + OFF_C + j * 16384, &tm_c, int((g >> kSliceShift) * kN + j * 64), int(row0),
-                          &bars[B_BC]);
+        // C in the paired row order: one 16-row box per token group
+        for (int tg = 0; tg < 8; ++tg)
+          umma::tma_load_2d(sm_base + OFF_C + j * 16384 + row_of_tok(16 * tg) * 128, &tm_c,
+                            int((g >> kSliceShift) * kN + j * 64), int(row0 + 16 * tg), &bars[B_BC]);
       }
       const bool has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
       // this thread also publishes each head's state gradient to the chunk before
@@ -349,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma::mbar_expect_tx(&bars[B_XG], 32768);
         umma::tma_load_2d(sm_base + OFF_XG, &tm_x, int(h * kP), int(row0), &bars[B_XG]);
-        umma::tma_load_2d(sm_base + OFF_XG + 16384, &tm_g, int(h * kP), int(row0), &bars[B_XG]);
+        for (int tg = 0; tg < 8; ++tg)   // g in the paired row order
+          umma::tma_load_2d(sm_base + OFF_XG + 16384 + row_of_tok(16 * tg) * 128, &tm_g, int(h * kP),
+                            int(row0 + 16 * tg), &bars[B_XG]);
         ++n_xg;
         if (k + 1 < hpg) {
           umma::tma_prefetch_2d(&tm_x, int((h + 1) * kP), int(row0));
-          umma::tma_prefetch_2d(&tm_g, int((h + 1) * kP), int(row0));
+          for (int tg = 0; tg < 8; ++tg) umma::tma_prefetch_2d(&tm_g, int((h + 1) * kP), int(row0 + 16 * tg));
         }
         if (has_next) {
           // dS = dH of the chunk after, once its unit has published it (the staging
@@ -431,14 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k > 0) wait_bar(&bars[E_RA], par ^ 1u, p.err);
         wait_bar(&bars[B_XG], par, p.err);   // x, g landed (bf16)
         umma::fence_after_sync();
-        // Gx = g x^T (M = t, N = s, K = p), bf16 operands, in two column halves so
-        // that the epilogue can hand the left half back early
-        for (int kk = 0; kk < kP; kk += 16)
-          umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_kk64, kk > 0);
-        umma::mma_commit(&bars[B_G1]);
+        // Gx = g x^T (M = t, N = s, K = p), bf16 operands, in two column halves,
+        // the right one (s >= 64: only the later tokens' rows) first, so that the
+        // epilogue can hand it back early
         for (int kk = 0; kk < kP; kk += 16)
           umma::mma_bf16(tmem + T_RA + 64, kdesc(aG, 16384, kk), kdesc(aX + 8192, 16384, kk), id_kk64, kk > 0);
-        umma::mma_commit(&bars[B_G1R]);
+        umma::mma_commit(&bars[B_GX1]);
+        for (int kk = 0; kk < kP; kk += 16)
+          umma::mma_bf16(tmem + T_RA, kdesc(aG, 16384, kk), kdesc(aX, 16384, kk), id_kk64, kk > 0);
+        umma::mma_commit(&bars[B_GX2]);
         wait_bar(&bars[E_X16], par, p.err);  // G~ in smem
         wait_bar(&bars[B_H], par, p.err);    // H (hi, lo) landed
         umma::fence_after_sync();
@@ -449,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mma_bf16(tmem + T_DC, kdesc(aA, 16384, kk), kdesc(aBb, 16384, kk), id_kk128,
                            (k > 0) || (part > 0) || (kk > 0));
         }
-        wait_bar(&bars[E_GXL], par, p.err);  // left half of g x^T read: dHscan^T goes there
+        wait_bar(&bars[E_GX1], par, p.err);  // right half of g x^T read: dHscan^T goes there
         umma::fence_after_sync();
         // dHscan^T = C^T (G~_hi + G~_lo)  (M = n, N = p, K = t)
         for (int part = 0; part < 2; ++part)
@@ -457,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mma_bf16(tmem + T_DH, mdesc(aC, 16384, kk), mdesc(part ? aGl : aGh, 16384, kk), id_mm64,
                            (part > 0) || (kk > 0));
         umma::mma_commit(&bars[B_DHS]);
-        wait_bar(&bars[E_M16], par, p.err);  // right half read too; M16 in smem
+        wait_bar(&bars[E_M16], par, p.err);  // left half read too; M16 in smem
         umma::fence_after_sync();
         // CH = C (H_hi + H_lo)  (M = t, N = p, K = n)
         for (int part = 0; part < 2; ++part)
@@ -509,22 +534,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     XBuf *xb = reinterpret_cast<XBuf *>(sm_base + OFF_XBUF);
     constexpr float kLog2e = 1.4426950408889634f;
 
-    // C B^T rows (this thread's row, its 32 columns: 16 in each column half)
-    // into registers, pre-scaled by the power of two that brings M = CB o L
-    // into the fp16 range
-    float cbs[32];
+    // The intra-chunk phase E1 works on blocks of 16 tokens x 16 columns of
+    // the causal triangle: in quadrant q, those of token group 7-q (column
+    // blocks 0..7-q) and of group q (0..q), nine per quadrant.  Warp cq takes
+    // R: block 4+cq of group 7-q (the right half, read first) if cq < 4-q;
+    // L: block cq of group 7-q; A: block (cq+q) mod 4 of group q if that is
+    // at most q.  Two threads share a row (lanes of the 16-lane TMEM form):
+    // threads 0-15 take its columns 0-7 of the block, threads 16-31 8-15.
+    const bool hasR = cq < 4 - q;
+    const int blkA = (cq + q) & 3;
+    const bool hasA = blkA <= q;
+    const int j16 = lane & 15, hsel = lane >> 4;
+    const uint32_t lanesA = uint32_t(32 * q) << 16, lanesB = uint32_t(32 * q + 16) << 16;
+    const int tokA = 16 * q + j16, tokB = 16 * (7 - q) + j16;   // this thread's tokens in groups q, 7-q
+    // C B^T of those blocks into registers, pre-scaled by the power of two
+    // that brings M = CB o L into the fp16 range
+    float cbR[8], cbL[8], cbA[8];
     ewait(&bars[B_CB], 0, p.err);
     umma::fence_after_sync();
     float cbmax = 0.f;
+    umma::tmem_ld8_h16(tmem + lanesB + T_RA + 16 * cq, cbL);
+    if (hasR) umma::tmem_ld8_h16(tmem + lanesB + T_RA + 16 * (4 + cq), cbR);
+    if (hasA) umma::tmem_ld8_h16(tmem + lanesA + T_RA + 16 * blkA, cbA);
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float v[16];
-      umma::tmem_ld16(tmem + lane_off + T_RA + 64 * j + 16 * cq, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        cbs[16 * j + i] = v[i];
-        cbmax = fmaxf(cbmax, fabsf(v[i]));
-      }
+    for (int i = 0; i < 8; ++i) {
+      if (!hasR) cbR[i] = 0.f;
+      if (!hasA) cbA[i] = 0.f;
+      cbmax = fmaxf(cbmax, fmaxf(fabsf(cbL[i]), fmaxf(fabsf(cbR[i]), fabsf(cbA[i]))));
     }
     {
       float z[16];
@@ -543,7 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kM = fp16_scale_exp(cbmax);
     const float sM = exp2i(kM), sMinv = exp2i(-kM);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) cbs[i] *= sM;
+    for (int i = 0; i < 8; ++i) {
+      cbR[i] *= sM;
+      cbL[i] *= sM;
+      cbA[i] *= sM;
+    }
 
     if (tid == 0) {
       sm->has_next = (c + 1 < s.nc) && !is_seq_start(p.seq_idx, bi, s.T, t0 + kQ);
@@ -559,6 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ep_sync();
     const int n = r;  // for [p][n] tiles (states, state gradients): this thread's state index
+    const int tr = tok_of_row(r);   // token of row r of the paired tiles (g, G~, C B^T, C H, dC lanes)
 
     // (scalar loads and stores below bypass L1: its few KB beside the shared
     // memory carve-out are left to the register spill slots)
@@ -599,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ep_sync();
       // per-row values are re-read from shared memory in each phase that uses
       // them rather than kept in registers across phases (fewer spills)
-      const float eacs = umma::ex2_approx(sm->a2[r]);   // exp(Acs_r)
+      const float eacs = umma::ex2_approx(sm->a2[tr]);   // exp(Acs) of token tr (row r of g, G~)
       // Column factors of the decay below the diagonal blocks: within each
       // 16-column block, exp(Acs_ref - Acs_s) with ref the block's last
       // column, so that exp(Acs_r - Acs_s) = exp(Acs_r - Acs_ref) exp(Acs_ref - Acs_s)
@@ -607,13 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cq == 0) sm->dtu[r] = umma::ex2_approx(sm->a2[r | 15] - sm->a2[r]);
 
       // G~ = exp(Acs) o g as a bf16 hi + lo pair; max |g| for the fp16 scaling of g; g . x
+      // (row r of g and G~ holds token tr; x is in natural order)
       float gmax = 0.f, gx = 0.f;
 #pragma unroll
       for (int c8 = 0; c8 < 2; ++c8) {
         const int c0 = 16 * cq + 8 * c8;
         float gv[8], xv[8], t[8];
         ld8_bf16(sG, r, c0, gv);
-        ld8_bf16(sX, r, c0, xv);
+        ld8_bf16(sX, tr, c0, xv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           t[i] = eacs * gv[i];
@@ -636,74 +678,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       // both are taken from the same fp16-rounded M that the dx product
       // uses (the column sums come out of that product in E4), so their
       // difference keeps its cancellation exact up to fp32 accumulation.
-      // Two passes over the column halves of g x^T; after the left one every
-      // warp hands its columns back so that C H can be computed there while
-      // the right half is processed.
-      float rowp = 0.f;   // sum_s M16_rs Gx_rs dt_s, times sM
-      const float a2r = sm->a2[r];
+      // The right column half of g x^T comes first (block R); every warp then
+      // hands it back so that dHscan^T can be computed there while the left
+      // half (blocks L and A) is processed.
+      float rowpA = 0.f, rowpB = 0.f;   // sum_s M16_ts Gx_ts dt_s over this thread's columns, times sM
+      const float a2A = sm->a2[tokA], a2B = sm->a2[tokB];
+      // one 16 x 16 block: token group 7-q (grp 1) or q (grp 0), column block cb
+      auto e1_block = [&](int grp, int cb, const float(&cbv)[8], float &rowp) {
+        const int t = grp ? tokB : tokA;
+        const float a2t = grp ? a2B : a2A;
+        const uint32_t lanes = grp ? lanesB : lanesA;
+        const int s0 = 16 * cb + 8 * hsel;             // first of this thread's 8 columns
+        const bool diag = cb == (grp ? 7 - q : q);     // the block holds the group's diagonal (warp-uniform)
+        const float er = diag ? 0.f : umma::ex2_approx(a2t - sm->a2[16 * cb + 15]);
+        float gxv[8], ws[8];
+        uint32_t m16[4];
+        umma::tmem_ld8x2_h16(tmem + lanes + T_RA + 16 * cb, tmem + lanes + T_WS + 16 * cb, gxv, ws);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        ewait(&bars[half ? B_G1R : B_G1], par, p.err);
-        umma::fence_after_sync();
-        const int c0 = 64 * half + 16 * cq;   // this thread's 16 columns in this half
-        if (c0 < 32 * (q + 1)) {               // the block touches the causal triangle (warp-uniform)
-          const bool diag = c0 + 16 > 32 * q;  // the block may cross the diagonal for some lane
-          const float er = diag ? 0.f : umma::ex2_approx(a2r - sm->a2[c0 + 15]);
+        for (int e4 = 0; e4 < 2; ++e4) {
+          const int cb4 = s0 + 4 * e4;   // first of these 4 columns
+          const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtv[cb4]);
+          const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
+          float Lv[4];
+          if (diag) {
+            const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[cb4]);
+            const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            float gxv[8], ws[8];
-            uint32_t m16[4];
-            umma::tmem_ld8x2(tmem + lane_off + T_RA + c0 + 8 * jj, tmem + lane_off + T_WS + c0 + 8 * jj, gxv, ws);
-#pragma unroll
-            for (int e4 = 0; e4 < 2; ++e4) {
-              const int cb = c0 + 8 * jj + 4 * e4;   // first of these 4 columns
-              const float4 duv = *reinterpret_cast<const float4 *>(&sm->dtv[cb]);
-              const float dus[4] = {duv.x, duv.y, duv.z, duv.w};
-              float Lv[4];
-              if (diag) {
-                const float4 a2v = *reinterpret_cast<const float4 *>(&sm->a2[cb]);
-                const float a2s[4] = {a2v.x, a2v.y, a2v.z, a2v.w};
-#pragma unroll
-                for (int e1 = 0; e1 < 4; ++e1) Lv[e1] = (cb + e1 <= r) ? umma::ex2_approx(a2r - a2s[e1]) : 0.f;
-              } else {
-                const float4 ecv = *reinterpret_cast<const float4 *>(&sm->dtu[cb]);
-                Lv[0] = er * ecv.x;
-                Lv[1] = er * ecv.y;
-                Lv[2] = er * ecv.z;
-                Lv[3] = er * ecv.w;
-              }
-              float mv[4], gd[4];
-#pragma unroll
-              for (int e1 = 0; e1 < 4; ++e1) {
-                const int e = 4 * e4 + e1;
-                gd[e1] = gxv[e] * dus[e1];       // Gx dt (true units)
-                ws[e] = fmaf(Lv[e1], gd[e1], ws[e]);
-                mv[e1] = cbs[16 * half + 8 * jj + e] * Lv[e1];
-              }
-              const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
-              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-              rowp = fmaf(f01.x, gd[0], rowp);
-              rowp = fmaf(f01.y, gd[1], rowp);
-              rowp = fmaf(f23.x, gd[2], rowp);
-              rowp = fmaf(f23.y, gd[3], rowp);
-              m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
-              m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-            }
-            umma::tmem_st8(tmem + lane_off + T_WS + c0 + 8 * jj, ws);
-            *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
-                make_uint4(m16[0], m16[1], m16[2], m16[3]);
+            for (int e1 = 0; e1 < 4; ++e1) Lv[e1] = (cb4 + e1 <= t) ? umma::ex2_approx(a2t - a2s[e1]) : 0.f;
+          } else {
+            const float4 ecv = *reinterpret_cast<const float4 *>(&sm->dtu[cb4]);
+            Lv[0] = er * ecv.x;
+            Lv[1] = er * ecv.y;
+            Lv[2] = er * ecv.z;
+            Lv[3] = er * ecv.w;
           }
-        } else {
+          float mv[4], gd[4];
 #pragma unroll
-          for (int jj = 0; jj < 2; ++jj)
-            *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + half * 16384 + r * 128 + (((2 * cq + jj) ^ (r & 7)) << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
+          for (int e1 = 0; e1 < 4; ++e1) {
+            const int e = 4 * e4 + e1;
+            gd[e1] = gxv[e] * dus[e1];       // Gx dt (true units)
+            ws[e] = fmaf(Lv[e1], gd[e1], ws[e]);
+            mv[e1] = cbv[e] * Lv[e1];
+          }
+          const __half2 h01 = __floats2half2_rn(mv[0], mv[1]), h23 = __floats2half2_rn(mv[2], mv[3]);
+          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+          rowp = fmaf(f01.x, gd[0], rowp);
+          rowp = fmaf(f01.y, gd[1], rowp);
+          rowp = fmaf(f23.x, gd[2], rowp);
+          rowp = fmaf(f23.y, gd[3], rowp);
+          m16[2 * e4] = *reinterpret_cast<const uint32_t *>(&h01);
+          m16[2 * e4 + 1] = *reinterpret_cast<const uint32_t *>(&h23);
         }
-        if (half == 0) {
-          umma::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) umma::mbar_arrive(&bars[E_GXL]);
-        }
+        umma::tmem_st8_h16(tmem + lanes + T_WS + 16 * cb, ws);
+        const int row = 32 * q + 16 * grp + j16;   // row of the M16 tile (paired order)
+        *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + (s0 >> 6) * 16384 + row * 128 +
+                                   ((((s0 & 63) >> 3) ^ (row & 7)) << 4)) = make_uint4(m16[0], m16[1], m16[2], m16[3]);
+      };
+      ewait(&bars[B_GX1], par, p.err);   // right half of g x^T
+      umma::fence_after_sync();
+      if (hasR) e1_block(1, 4 + cq, cbR, rowpB);
+      umma::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&bars[E_GX1]);
+      ewait(&bars[B_GX2], par, p.err);  // left half
+      umma::fence_after_sync();
+      e1_block(1, cq, cbL, rowpB);
+      if (hasA) e1_block(0, blkA, cbA, rowpA);
+      // zeros in the blocks of M16 above the diagonal (group q: blocks q+1..7,
+      // group 7-q: 8-q..7; seven per quadrant, spread over its warps)
+      for (int z = cq; z < 7; z += 4) {
+        const int grp = z < 7 - q ? 0 : 1;
+        const int cb = grp ? 8 - q + (z - (7 - q)) : q + 1 + z;
+        const int s0 = 16 * cb + 8 * hsel;
+        const int row = 32 * q + 16 * grp + j16;
+        *reinterpret_cast<uint4 *>(sm_base + OFF_M16 + (s0 >> 6) * 16384 + row * 128 +
+                                   ((((s0 & 63) >> 3) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // a row's two column halves summed in a fixed order (left half first): threads 0-15
+      // hold the total of token tokA, threads 16-31 that of tokB
+      float rowp_tok;
+      {
+        const float oA = __shfl_xor_sync(0xffffffffu, rowpA, 16), oB = __shfl_xor_sync(0xffffffffu, rowpB, 16);
+        rowp_tok = hsel ? oB + rowpB : rowpA + oA;
       }
       umma::tmem_wait_st();
       umma::fence_before_sync();
@@ -718,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float wr3 = umma::ex2_approx(a2E3 - sm->a2[r]) * dtr;   // w = exp(E - Acs_r) dt_r
       const float eE = umma::ex2_approx(a2E3);                        // exp(E)
       // GW is idle from here to the next head: exchange scratch (lo half) and w o x (hi half)
-      xb->v[0][cq][r] = rowp;
-      xb->v[3][cq][r] = gx;
+      xb->v[0][cq][hsel ? tokB : tokA] = rowp_tok;
+      xb->v[3][cq][tr] = gx;
       {
 #pragma unroll
         for (int c8 = 0; c8 < 2; ++c8) {
@@ -825,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         st_row8_f16(sG, r, 16 * cq + 8, gv);
       }
-      xb->v[2][cq][r] = inter_part;
+      xb->v[2][cq][tr] = inter_part;   // (C H lane r and g row r: token tr)
       umma::fence_proxy_async_smem();   // g16 is read by the dx product issued after E_CHR
       umma::fence_before_sync();
       __syncwarp();
@@ -851,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float d1[8], y[8], xv[8], gv[8];
           umma::tmem_ld8x2(tmem + lane_off + T_D1 + 16 * cq + 8 * c8, tmem + lane_off + T_Y + 16 * cq + 8 * c8, d1, y);
           ld8_bf16(sX, r, 16 * cq + 8 * c8, xv);
-          ld8_f16(sG, r, 16 * cq + 8 * c8, gv);
+          ld8_f16(sG, row_of_tok(r), 16 * cq + 8 * c8, gv);   // g of token r (paired order)
 #pragma unroll
           for (int i4 = 0; i4 < 2; ++i4) {
             float o[4];
@@ -991,8 +1047,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
         __stcg(reinterpret_cast<float4 *>(o + 4 * i4), make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]));
-      umma::tmem_ld16(tmem + lane_off + T_DC + n0, v);
-      o = p.dC + ((row0 + r) * s.G + g) * kN + n0;
+      umma::tmem_ld16(tmem + lane_off + T_DC + n0, v);   // dC lanes: paired order
+      o = p.dC + ((row0 + tr) * s.G + g) * kN + n0;
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
         __stcg(reinterpret_cast<float4 *>(o + 4 * i4), make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]));
@@ -1087,12 +1143,13 @@ cudaError_t launch_pass(const Shape &s, const Args &a, const FusedWs &w, const F
   const uint64_t rows = uint64_t(s.b * s.T);
   if (!make_tmap_2d(&tm_x, a.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 64,
                     128, true) ||
+      // g and C are copied in 16-token boxes (the paired row order of the kernel)
       !make_tmap_2d(&tm_g, a.dout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t(s.H * kP), uint64_t(s.H * kP),
-                    64, 128, true) ||
+                    64, 16, true) ||
       !make_tmap_2d(&tm_b, a.B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((s.G >> slice_shift) * kN),
                     uint64_t(bc_pitch), 64, 128, true) ||
       !make_tmap_2d(&tm_c, a.C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows, uint64_t((s.G >> slice_shift) * kN),
-                    uint64_t(bc_pitch), 64, 128, true) ||
+                    uint64_t(bc_pitch), 64, 16, true) ||
       !make_tmap_2d(&tm_dx, a.dx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rows, uint64_t(s.H * kP), uint64_t(s.H * kP), 32,
                     128, true))
     return cudaErrorInvalidValue;
